@@ -1,0 +1,521 @@
+// api.cu -- the library's C ABI: argument checks, workspace layout and the
+// launch sequence of every entry point declared in twell.h.
+#include <cstring>
+#include <mutex>
+
+#include "gemm_tc.cuh"
+#include "internal.h"
+
+namespace tw {
+
+__device__ int g_device_status;
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+
+int current_device() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return -1;
+  return dev;
+}
+
+}  // namespace
+
+int num_sms() {
+  static int cache[kMaxDevices] = {0};
+  const int dev = current_device();
+  if (dev < 0 || dev >= kMaxDevices) return 0;
+  if (cache[dev] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    cache[dev] = n;
+  }
+  return cache[dev];
+}
+
+int* device_status_ptr() {
+  static int* cache[kMaxDevices] = {nullptr};
+  static std::mutex mu;
+  const int dev = current_device();
+  if (dev < 0 || dev >= kMaxDevices) return nullptr;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!cache[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_device_status) != cudaSuccess) return nullptr;
+    cache[dev] = reinterpret_cast<int*>(p);
+  }
+  return cache[dev];
+}
+
+}  // namespace tw
+
+using namespace tw;
+
+namespace {
+
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Every pointer given must be non-null and 16-byte aligned.
+twell_status check_ptrs(std::initializer_list<const void*> ps) {
+  for (const void* p : ps) {
+    if (!p) return TWELL_ERR_INVALID_ARG;
+    if (!aligned16(p)) return TWELL_ERR_ALIGNMENT;
+  }
+  return TWELL_OK;
+}
+
+twell_status check_shape(const twell_shape* s, bool packed) {
+  if (!s) return TWELL_ERR_INVALID_ARG;
+  if (s->M < 0 || s->d_model <= 0 || s->d_ff <= 0) return TWELL_ERR_INVALID_ARG;
+  if (s->d_model % 64 != 0 || s->d_model > 8192) return TWELL_ERR_UNSUPPORTED;
+  if (s->d_ff % 128 != 0 || s->d_ff > 65535) return TWELL_ERR_UNSUPPORTED;
+  if (packed) {
+    if (s->tile_n != 64 && s->tile_n != 128) return TWELL_ERR_UNSUPPORTED;
+    if (s->tile_cap < 1 || s->tile_cap > s->tile_n) return TWELL_ERR_UNSUPPORTED;
+  }
+  return TWELL_OK;
+}
+
+twell_status check_tiles(const twell_tiles* t) {
+  if (!t) return TWELL_ERR_INVALID_ARG;
+  return check_ptrs({t->val, t->idx, t->cnt, t->row_nnz});
+}
+
+twell_status check_route(const twell_hybrid* r) {
+  if (!r) return TWELL_ERR_INVALID_ARG;
+  if (r->ell_width < 0) return TWELL_ERR_INVALID_ARG;
+  twell_status st = check_ptrs({r->ell_nnz, r->dense_rows, r->n_dense});
+  if (st != TWELL_OK) return st;
+  if (r->ell_width > 0) return check_ptrs({r->ell_val, r->ell_col});
+  return TWELL_OK;
+}
+
+inline twell_status cuda_status(cudaError_t e) { return e == cudaSuccess ? TWELL_OK : TWELL_ERR_CUDA; }
+
+inline long long round_up(long long v, long long a) { return (v + a - 1) / a * a; }
+
+// Bump allocator over the caller's workspace (256-byte aligned slices).
+struct Carve {
+  uint8_t* base;
+  size_t off = 0;
+  explicit Carve(void* b) : base(reinterpret_cast<uint8_t*>(b)) {}
+  template <class T>
+  T* take(size_t count) {
+    off = (size_t)round_up((long long)off, 256);
+    T* p = base ? reinterpret_cast<T*>(base + off) : nullptr;
+    off += count * sizeof(T);
+    return p;
+  }
+};
+
+// Workspace of the sparse path.  Routed-row buffers are sized for every row
+// being routed; they hold whole 128-row tiles (Mp rows).  The dense backup
+// keeps its intermediates h, du, da as bf16 hi + lo pairs, so routed rows
+// are as accurate as the fp32 gather path:
+//   hr  [Mp][2f] = [h hi | h lo]
+//   ur  [Mp][f]  fp32 u
+//   ddr [Mp][4f] = [du hi | da hi | du lo | da lo]
+struct SparseWs {
+  uint16_t *xr, *hr;                    // forward fallback
+  uint16_t *dyr, *gr, *ddr;             // backward fallback
+  float* ur;
+  int *mask_off, *csc_ptr, *csc_row, *slot_pos;
+  float4* csc_vals;
+  size_t bytes;
+};
+
+SparseWs carve_sparse(void* ws, const twell_shape& s, int W, int training) {
+  const long long Mp = round_up(s.M, 128);
+  const long long d = s.d_model, f = s.d_ff;
+  Carve c(ws);
+  SparseWs w{};
+  w.xr = c.take<uint16_t>(Mp * d);
+  w.hr = c.take<uint16_t>(Mp * 2 * f);
+  if (training) {
+    const long long NB = (s.M + 31) / 32;
+    const long long E = (long long)s.M * W;
+    w.dyr = c.take<uint16_t>(Mp * d);
+    w.gr = c.take<uint16_t>(Mp * f);
+    w.ur = c.take<float>(Mp * f);
+    w.ddr = c.take<uint16_t>(Mp * 4 * f);
+    w.mask_off = c.take<int>(2 * NB * f);
+    w.csc_ptr = c.take<int>(f + 1);
+    w.csc_row = c.take<int>(E > 0 ? E : 1);
+    w.slot_pos = c.take<int>(E > 0 ? E : 1);
+    w.csc_vals = c.take<float4>(E > 0 ? E : 1);
+  }
+  w.bytes = c.off + 256;
+  return w;
+}
+
+struct DenseWs {
+  uint16_t *h, *g, *u, *dd;
+  size_t bytes;
+};
+
+DenseWs carve_dense(void* ws, const twell_shape& s, int training) {
+  const long long M = s.M, f = s.d_ff;
+  Carve c(ws);
+  DenseWs w{};
+  w.h = c.take<uint16_t>(M * f);
+  if (training) {
+    w.g = c.take<uint16_t>(M * f);
+    w.u = c.take<uint16_t>(M * f);
+    w.dd = c.take<uint16_t>(M * 2 * f);
+  }
+  w.bytes = c.off + 256;
+  return w;
+}
+
+GemmParams base_params(int M, int N, int K, int n_tile_width) {
+  GemmParams p;
+  std::memset(&p, 0, sizeof(p));
+  p.M = M;
+  p.N = N;
+  p.K = K;
+  p.n_tiles = (N + n_tile_width - 1) / n_tile_width;
+  p.k_split = 1 << 30;
+  p.status = device_status_ptr();
+  return p;
+}
+
+Mat mat(const void* p, long long rows, long long cols, long long ld) { return Mat{p, rows, cols, ld}; }
+
+// Dense gated FFN on rows [0, m_dev or M) of x_rows (a [rows][d] buffer):
+// h = bf16(ReLU(x Wg)) * (x Wu) stored bf16 (split: as hi | lo halves of a
+// [rows][2f] buffer), optional g / u copies ([rows][f]).
+cudaError_t gated_gemm(const void* x_rows, long long rows, const twell_shape& s, const void* wgT,
+                       const void* wuT, const int* m_dev, uint16_t* h, bool split, uint16_t* g,
+                       uint16_t* u, float* u32, int pad_rows, cudaStream_t st) {
+  GemmParams p = base_params((int)rows, s.d_ff, s.d_model, 128);
+  p.m_dev = m_dev;
+  p.h = h;
+  p.ldh = split ? 2LL * s.d_ff : s.d_ff;
+  p.h_lo_off = split ? s.d_ff : 0;
+  p.g_out = g;
+  p.u_out = u;
+  p.u_f32 = u32;
+  p.ldgu = s.d_ff;
+  p.pad_rows = pad_rows;
+  const Mat A = mat(x_rows, rows, s.d_model, s.d_model);
+  const Mat B = mat(wgT, s.d_ff, s.d_model, s.d_model);
+  const Mat B2 = mat(wuT, s.d_ff, s.d_model, s.d_model);
+  return gemm_launch(GK_GATED, A, B, &B2, p, st);
+}
+
+// out[row_map ? row_map[r] : r] = h[r] Wd (bf16); with split, h = hi + lo and
+// the GEMM runs over K = 2f against [Wd ; Wd].
+cudaError_t down_gemm(const uint16_t* h, long long rows, const twell_shape& s, const void* wd,
+                      bool split, const int* m_dev, const int* row_map, void* out,
+                      cudaStream_t st) {
+  const long long K = split ? 2LL * s.d_ff : s.d_ff;
+  GemmParams p = base_params((int)rows, s.d_model, (int)K, kBN);
+  p.m_dev = m_dev;
+  p.row_map = row_map;
+  p.c = out;
+  p.ldc = s.d_model;
+  p.k_split = s.d_ff / kBK;
+  const Mat A = mat(h, rows, K, K);
+  const Mat B = mat(wd, s.d_ff, s.d_model, s.d_model);  // [K = f][N = d], MN-major
+  return gemm_launch(GK_STORE_KM, A, B, &B, p, st);
+}
+
+// dd = [du | da] (split: [du | da | du lo | da lo]) from dh = dy Wd^T and g, u.
+cudaError_t dgate_gemm(const void* dy_rows, long long rows, const twell_shape& s, const void* wd,
+                       const int* m_dev, const uint16_t* g, const uint16_t* u, const float* u32,
+                       uint16_t* dd, bool split, float lambda, int pad_rows, cudaStream_t st) {
+  GemmParams p = base_params((int)rows, s.d_ff, s.d_model, kBN);
+  p.m_dev = m_dev;
+  p.g_in = g;
+  p.u_in = u;
+  p.u_f32_in = u32;
+  p.ldgu = s.d_ff;
+  p.dd = dd;
+  p.ld_dd = (split ? 4LL : 2LL) * s.d_ff;
+  p.dd_seg = s.d_ff;
+  p.dd_split = split ? 1 : 0;
+  p.lambda = lambda;
+  p.pad_rows = pad_rows;
+  const Mat A = mat(dy_rows, rows, s.d_model, s.d_model);
+  const Mat B = mat(wd, s.d_ff, s.d_model, s.d_model);  // [N = f][K = d], K-major
+  return gemm_launch(GK_BWD_GATE, A, B, nullptr, p, st);
+}
+
+// out[row_map ? row_map[r] : r] = du Wu^T + da Wg^T  (bf16): the GEMM runs over
+// K = 2f (or 4f with the lo halves) against [WuT ; WgT (; WuT ; WgT)].
+cudaError_t dx_gemm(const uint16_t* dd, long long rows, const twell_shape& s, const void* wgT,
+                    const void* wuT, bool split, const int* m_dev, const int* row_map, void* out,
+                    cudaStream_t st) {
+  const long long K = (split ? 4LL : 2LL) * s.d_ff;
+  GemmParams p = base_params((int)rows, s.d_model, (int)K, kBN);
+  p.m_dev = m_dev;
+  p.row_map = row_map;
+  p.c = out;
+  p.ldc = s.d_model;
+  p.k_split = s.d_ff / kBK;
+  const Mat A = mat(dd, rows, K, K);
+  const Mat B = mat(wuT, s.d_ff, s.d_model, s.d_model);   // [K][N], MN-major
+  const Mat B2 = mat(wgT, s.d_ff, s.d_model, s.d_model);
+  return gemm_launch(GK_STORE_KM, A, B, &B2, p, st);
+}
+
+// C[f][d] (+)= A^T B with A = [K][f] (leading dim lda) and B = [K][d], K from k_dev or K.
+cudaError_t dw_gemm(const uint16_t* a, long long lda, const void* b, long long K,
+                    const twell_shape& s, const int* k_dev, float* c, int accumulate,
+                    cudaStream_t st) {
+  GemmParams p = base_params(s.d_ff, s.d_model, (int)K, kBN);
+  p.k_dev = k_dev;
+  p.c = c;
+  p.ldc = s.d_model;
+  p.c_f32 = 1;
+  p.accumulate = accumulate;
+  const Mat A = mat(a, K, s.d_ff, lda);
+  const Mat B = mat(b, K, s.d_model, s.d_model);
+  return gemm_launch(GK_STORE_MM, A, B, nullptr, p, st);
+}
+
+}  // namespace
+
+// ============================================================== entry points
+extern "C" {
+
+const char* twell_status_string(int32_t status) {
+  switch (status) {
+    case TWELL_OK: return "ok";
+    case TWELL_ERR_INVALID_ARG: return "invalid argument";
+    case TWELL_ERR_UNSUPPORTED: return "unsupported shape";
+    case TWELL_ERR_ALIGNMENT: return "pointer not 16-byte aligned";
+    case TWELL_ERR_CAPACITY: return "packed tile overflow without a route";
+    case TWELL_ERR_CUDA: return "CUDA error";
+    case TWELL_ERR_DEVICE_TIMEOUT: return "device pipeline wait timed out";
+    case TWELL_ERR_WORKSPACE: return "workspace missing or too small";
+  }
+  return "unknown status";
+}
+
+int32_t twell_num_sms(void) { return num_sms(); }
+
+twell_status twell_get_device_status(void* stream, int32_t* out) {
+  if (!out) return TWELL_ERR_INVALID_ARG;
+  int* p = device_status_ptr();
+  if (!p) return TWELL_ERR_CUDA;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  int v = 0;
+  if (cudaMemcpyAsync(&v, p, sizeof(int), cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+      cudaMemsetAsync(p, 0, sizeof(int), s) != cudaSuccess || cudaStreamSynchronize(s) != cudaSuccess)
+    return TWELL_ERR_CUDA;
+  *out = v;
+  return TWELL_OK;
+}
+
+twell_status twell_pack(const void* x, const void* wgT, const twell_shape* shape,
+                        const twell_tiles* out, void* stream) {
+  twell_status st = check_shape(shape, true);
+  if (st != TWELL_OK) return st;
+  if ((st = check_ptrs({x, wgT})) != TWELL_OK) return st;
+  if ((st = check_tiles(out)) != TWELL_OK) return st;
+  const twell_shape& s = *shape;
+  if (s.M == 0) return TWELL_OK;
+  cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaMemsetAsync(out->row_nnz, 0, sizeof(int32_t) * (size_t)s.M, cs);
+  if (e != cudaSuccess) return TWELL_ERR_CUDA;
+  GemmParams p = base_params(s.M, s.d_ff, s.d_model, kBN);
+  p.val = reinterpret_cast<uint16_t*>(out->val);
+  p.idx = out->idx;
+  p.cnt = out->cnt;
+  p.row_nnz = out->row_nnz;
+  p.T = s.d_ff / s.tile_n;
+  p.cap = s.tile_cap;
+  p.tile_n = s.tile_n;
+  const Mat A = mat(x, s.M, s.d_model, s.d_model);
+  const Mat B = mat(wgT, s.d_ff, s.d_model, s.d_model);
+  return cuda_status(gemm_launch(GK_PACK, A, B, nullptr, p, cs));
+}
+
+twell_status twell_pack_dense(const void* a, int32_t a_dtype, const twell_shape* shape,
+                              const twell_tiles* out, void* stream) {
+  twell_status st = check_shape(shape, true);
+  if (st != TWELL_OK) return st;
+  if (a_dtype != 0 && a_dtype != 1) return TWELL_ERR_INVALID_ARG;
+  if ((st = check_ptrs({a})) != TWELL_OK) return st;
+  if ((st = check_tiles(out)) != TWELL_OK) return st;
+  const twell_shape& s = *shape;
+  return cuda_status(launch_pack_dense(a, a_dtype, s.M, s.d_ff, s.tile_n, s.tile_cap, *out,
+                                       reinterpret_cast<cudaStream_t>(stream)));
+}
+
+twell_status hybrid_route(const twell_tiles* in, const twell_shape* shape, const twell_hybrid* out,
+                          void* stream) {
+  twell_status st = check_shape(shape, true);
+  if (st != TWELL_OK) return st;
+  if ((st = check_tiles(in)) != TWELL_OK) return st;
+  if ((st = check_route(out)) != TWELL_OK) return st;
+  const twell_shape& s = *shape;
+  // the routing flags live in dense_rows until the stable list overwrites them
+  return cuda_status(launch_route(*in, s.M, s.d_ff, s.tile_n, s.tile_cap, *out, out->dense_rows,
+                                  reinterpret_cast<cudaStream_t>(stream)));
+}
+
+size_t twell_workspace_bytes(const twell_shape* shape, int32_t ell_width, int32_t training) {
+  if (check_shape(shape, true) != TWELL_OK || ell_width < 0) return 0;
+  return carve_sparse(nullptr, *shape, ell_width, training ? 1 : 0).bytes;
+}
+
+twell_status twell_ffn_fwd(const void* x, const void* wgT, const void* wuT, const void* wd,
+                           const twell_shape* shape, const twell_tiles* tiles,
+                           const twell_hybrid* route, void* y, void* ws, size_t ws_bytes,
+                           void* stream) {
+  twell_status st = check_shape(shape, true);
+  if (st != TWELL_OK) return st;
+  if ((tiles == nullptr) == (route == nullptr)) return TWELL_ERR_INVALID_ARG;
+  if ((st = check_ptrs({x, wuT, wd, y})) != TWELL_OK) return st;
+  const twell_shape& s = *shape;
+  cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  if (tiles) {
+    if ((st = check_tiles(tiles)) != TWELL_OK) return st;
+    if (s.M == 0) return TWELL_OK;
+    return cuda_status(launch_sparse_fwd(x, wuT, wd, s.M, s.d_model, s.d_ff, tiles, s.tile_n,
+                                         s.tile_cap, nullptr, y, cs));
+  }
+  if ((st = check_route(route)) != TWELL_OK) return st;
+  if ((st = check_ptrs({wgT})) != TWELL_OK) return st;
+  const SparseWs need = carve_sparse(nullptr, s, route->ell_width, 0);
+  if (!ws || ws_bytes < need.bytes) return TWELL_ERR_WORKSPACE;
+  if (!aligned16(ws)) return TWELL_ERR_ALIGNMENT;
+  if (s.M == 0) return TWELL_OK;
+  const SparseWs w = carve_sparse(ws, s, route->ell_width, 0);
+  const long long Mp = round_up(s.M, 128);
+  cudaError_t e = launch_sparse_fwd(x, wuT, wd, s.M, s.d_model, s.d_ff, nullptr, s.tile_n,
+                                    s.tile_cap, route, y, cs);
+  if (e == cudaSuccess)
+    e = launch_gather_rows(x, s.M, s.d_model, route->dense_rows, route->n_dense, w.xr, (int)Mp, cs);
+  if (e == cudaSuccess)
+    e = gated_gemm(w.xr, Mp, s, wgT, wuT, route->n_dense, w.hr, true, nullptr, nullptr,
+                   nullptr, 0, cs);
+  if (e == cudaSuccess)
+    e = down_gemm(w.hr, Mp, s, wd, true, route->n_dense, route->dense_rows, y, cs);
+  return cuda_status(e);
+}
+
+twell_status twell_ffn_bwd(const void* x, const void* wgT, const void* wuT, const void* wd,
+                           const void* dy, const twell_shape* shape, const twell_hybrid* route,
+                           float l1_coeff, void* dx, float* dwgT, float* dwuT, float* dwd,
+                           void* ws, size_t ws_bytes, void* stream) {
+  twell_status st = check_shape(shape, true);
+  if (st != TWELL_OK) return st;
+  if ((st = check_ptrs({x, wgT, wuT, wd, dy, dx, dwgT, dwuT, dwd})) != TWELL_OK) return st;
+  if ((st = check_route(route)) != TWELL_OK) return st;
+  const twell_shape& s = *shape;
+  const SparseWs need = carve_sparse(nullptr, s, route->ell_width, 1);
+  if (!ws || ws_bytes < need.bytes) return TWELL_ERR_WORKSPACE;
+  if (!aligned16(ws)) return TWELL_ERR_ALIGNMENT;
+  cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  const SparseWs w = carve_sparse(ws, s, route->ell_width, 1);
+  const long long Mp = round_up(s.M, 128);
+  const long long f = s.d_ff;
+  cudaError_t e = launch_csc_build(*route, s.M, s.d_ff, w.mask_off, w.csc_ptr, w.csc_row,
+                                   w.slot_pos, cs);
+  if (e == cudaSuccess)
+    e = launch_sparse_bwd_rows(x, dy, wgT, wuT, wd, s.M, s.d_model, *route, w.slot_pos, l1_coeff,
+                               w.csc_vals, dx, cs);
+  if (e == cudaSuccess)
+    e = launch_sparse_bwd_neurons(x, dy, s.M, s.d_model, s.d_ff, w.csc_ptr, w.csc_row, w.csc_vals,
+                                  dwgT, dwuT, dwd, cs);
+  if (s.M == 0) return cuda_status(e);
+  // routed rows: dense tensor-core backward, accumulated into the same dW
+  const int* nd = route->n_dense;
+  if (e == cudaSuccess)
+    e = launch_gather_rows(x, s.M, s.d_model, route->dense_rows, nd, w.xr, (int)Mp, cs);
+  if (e == cudaSuccess)
+    e = launch_gather_rows(dy, s.M, s.d_model, route->dense_rows, nd, w.dyr, (int)Mp, cs);
+  if (e == cudaSuccess)
+    e = gated_gemm(w.xr, Mp, s, wgT, wuT, nd, w.hr, true, w.gr, nullptr, w.ur, 1, cs);
+  if (e == cudaSuccess)
+    e = dgate_gemm(w.dyr, Mp, s, wd, nd, w.gr, nullptr, w.ur, w.ddr, true, l1_coeff, 1, cs);
+  if (e == cudaSuccess) e = dx_gemm(w.ddr, Mp, s, wgT, wuT, true, nd, route->dense_rows, dx, cs);
+  // dW += (hi + lo)^T B as two accumulating passes
+  if (e == cudaSuccess) e = dw_gemm(w.hr, 2 * f, w.dyr, Mp, s, nd, dwd, 1, cs);
+  if (e == cudaSuccess) e = dw_gemm(w.hr + f, 2 * f, w.dyr, Mp, s, nd, dwd, 1, cs);
+  if (e == cudaSuccess) e = dw_gemm(w.ddr, 4 * f, w.xr, Mp, s, nd, dwuT, 1, cs);
+  if (e == cudaSuccess) e = dw_gemm(w.ddr + 2 * f, 4 * f, w.xr, Mp, s, nd, dwuT, 1, cs);
+  if (e == cudaSuccess) e = dw_gemm(w.ddr + f, 4 * f, w.xr, Mp, s, nd, dwgT, 1, cs);
+  if (e == cudaSuccess) e = dw_gemm(w.ddr + 3 * f, 4 * f, w.xr, Mp, s, nd, dwgT, 1, cs);
+  return cuda_status(e);
+}
+
+size_t twell_dense_workspace_bytes(const twell_shape* shape, int32_t training) {
+  if (check_shape(shape, false) != TWELL_OK) return 0;
+  return carve_dense(nullptr, *shape, training ? 1 : 0).bytes;
+}
+
+twell_status twell_dense_ffn_fwd(const void* x, const void* wgT, const void* wuT, const void* wd,
+                                 const twell_shape* shape, void* y, int32_t training, void* ws,
+                                 size_t ws_bytes, void* stream) {
+  twell_status st = check_shape(shape, false);
+  if (st != TWELL_OK) return st;
+  if ((st = check_ptrs({x, wgT, wuT, wd, y})) != TWELL_OK) return st;
+  const twell_shape& s = *shape;
+  if (!ws || ws_bytes < carve_dense(nullptr, s, training ? 1 : 0).bytes) return TWELL_ERR_WORKSPACE;
+  if (!aligned16(ws)) return TWELL_ERR_ALIGNMENT;
+  if (s.M == 0) return TWELL_OK;
+  cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  const DenseWs w = carve_dense(ws, s, training ? 1 : 0);
+  cudaError_t e = gated_gemm(x, s.M, s, wgT, wuT, nullptr, w.h, false, training ? w.g : nullptr,
+                             training ? w.u : nullptr, nullptr, 0, cs);
+  if (e == cudaSuccess) e = down_gemm(w.h, s.M, s, wd, false, nullptr, nullptr, y, cs);
+  return cuda_status(e);
+}
+
+twell_status twell_dense_ffn_bwd(const void* x, const void* wgT, const void* wuT, const void* wd,
+                                 const void* dy, const twell_shape* shape, float l1_coeff,
+                                 void* dx, float* dwgT, float* dwuT, float* dwd, void* ws,
+                                 size_t ws_bytes, void* stream) {
+  twell_status st = check_shape(shape, false);
+  if (st != TWELL_OK) return st;
+  if ((st = check_ptrs({x, wgT, wuT, wd, dy, dx, dwgT, dwuT, dwd})) != TWELL_OK) return st;
+  const twell_shape& s = *shape;
+  if (!ws || ws_bytes < carve_dense(nullptr, s, 1).bytes) return TWELL_ERR_WORKSPACE;
+  if (!aligned16(ws)) return TWELL_ERR_ALIGNMENT;
+  cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  const long long f = s.d_ff;
+  if (s.M == 0) {
+    cudaError_t e = cudaMemsetAsync(dwgT, 0, sizeof(float) * f * s.d_model, cs);
+    if (e == cudaSuccess) e = cudaMemsetAsync(dwuT, 0, sizeof(float) * f * s.d_model, cs);
+    if (e == cudaSuccess) e = cudaMemsetAsync(dwd, 0, sizeof(float) * f * s.d_model, cs);
+    return cuda_status(e);
+  }
+  const DenseWs w = carve_dense(ws, s, 1);
+  cudaError_t e =
+      dgate_gemm(dy, s.M, s, wd, nullptr, w.g, w.u, nullptr, w.dd, false, l1_coeff, 0, cs);
+  if (e == cudaSuccess) e = dx_gemm(w.dd, s.M, s, wgT, wuT, false, nullptr, nullptr, dx, cs);
+  if (e == cudaSuccess) e = dw_gemm(w.h, f, dy, s.M, s, nullptr, dwd, 0, cs);
+  if (e == cudaSuccess) e = dw_gemm(w.dd, 2 * f, x, s.M, s, nullptr, dwuT, 0, cs);
+  if (e == cudaSuccess) e = dw_gemm(w.dd + f, 2 * f, x, s.M, s, nullptr, dwgT, 0, cs);
+  return cuda_status(e);
+}
+
+twell_status twell_gemm_bf16(const void* A, const void* B, void* C, int32_t M, int32_t N,
+                             int32_t K, int32_t a_mn_major, int32_t b_mn_major, int32_t c_dtype,
+                             int32_t accumulate, void* stream) {
+  if (M < 0 || N <= 0 || K <= 0) return TWELL_ERR_INVALID_ARG;
+  if (c_dtype != 0 && c_dtype != 1) return TWELL_ERR_INVALID_ARG;
+  if (accumulate && c_dtype != 1) return TWELL_ERR_INVALID_ARG;
+  twell_status st = check_ptrs({A, B, C});
+  if (st != TWELL_OK) return st;
+  if (K % 8 != 0 || N % 8 != 0) return TWELL_ERR_UNSUPPORTED;
+  if (a_mn_major && M % 8 != 0) return TWELL_ERR_UNSUPPORTED;
+  if (M == 0) return TWELL_OK;
+  GemmParams p = base_params(M, N, K, kBN);
+  p.c = C;
+  p.ldc = N;
+  p.c_f32 = c_dtype;
+  p.accumulate = accumulate;
+  const Mat a = a_mn_major ? mat(A, K, M, M) : mat(A, M, K, K);
+  const Mat b = b_mn_major ? mat(B, K, N, N) : mat(B, N, K, K);
+  const GemmKind kind = a_mn_major ? (b_mn_major ? GK_STORE_MM : GK_STORE_MK)
+                                   : (b_mn_major ? GK_STORE_KM : GK_STORE_KK);
+  return cuda_status(gemm_launch(kind, a, b, nullptr, p, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+}  // extern "C"

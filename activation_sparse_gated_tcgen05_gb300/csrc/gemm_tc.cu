@@ -1,0 +1,83 @@
+// gemm_tc.cu -- host side of the tcgen05 GEMM engine: TMA tensor maps and
+// persistent launches of the instantiated kernels.
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
+#include "gemm_tc.cuh"
+#include "internal.h"
+
+namespace tw {
+
+namespace {
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+// 2-D bf16 tensor map over a row-major [outer][inner] matrix with leading
+// dimension ld (elements), 128-byte swizzled boxes of box_inner x box_outer.
+bool make_map(CUtensorMap* m, const Mat& a, uint32_t box_inner, uint32_t box_outer) {
+  auto fn = encode_fn();
+  if (!fn || !a.ptr || a.rows <= 0 || a.cols <= 0) return false;
+  cuuint64_t dims[2] = {(cuuint64_t)a.cols, (cuuint64_t)a.rows};
+  cuuint64_t strides[1] = {(cuuint64_t)a.ld * 2};
+  cuuint32_t box[2] = {box_inner, box_outer};
+  cuuint32_t es[2] = {1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(a.ptr), dims, strides,
+                  box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+template <bool A_MN, bool B_MN, int EPI>
+cudaError_t launch_t(const Mat& A, const Mat& B, const Mat* B2, const GemmParams& p,
+                     cudaStream_t s) {
+  CUtensorMap ta, tb, tb2;
+  // A: K-major [M][K] -> box {64 (K), 128 rows}; MN-major [K][M] -> box {64 (M), 64 (K)}
+  if (!make_map(&ta, A, 64, A_MN ? 64 : kBM)) return cudaErrorInvalidValue;
+  const uint32_t b_rows = (EPI == EPI_GATED) ? 128 : kBN;
+  if (!make_map(&tb, B, 64, B_MN ? 64 : b_rows)) return cudaErrorInvalidValue;
+  if (B2) {
+    if (!make_map(&tb2, *B2, 64, B_MN ? 64 : b_rows)) return cudaErrorInvalidValue;
+  } else {
+    tb2 = tb;
+  }
+  auto kern = gemm_kernel<A_MN, B_MN, EPI>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kGemmSmem);
+  if (e != cudaSuccess) return e;
+  const long long m_tiles = (p.M + kBM - 1) / kBM;
+  const long long tiles = m_tiles * p.n_tiles;
+  if (tiles <= 0) return cudaSuccess;
+  const int grid = (int)(tiles < num_sms() ? tiles : num_sms());
+  kern<<<grid, kGemmThreads, kGemmSmem, s>>>(ta, tb, tb2, p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t gemm_launch(GemmKind kind, const Mat& A, const Mat& B, const Mat* B2,
+                        const GemmParams& p, cudaStream_t s) {
+  switch (kind) {
+    case GK_STORE_KK: return launch_t<false, false, EPI_STORE>(A, B, B2, p, s);
+    case GK_STORE_MK: return launch_t<true, false, EPI_STORE>(A, B, B2, p, s);
+    case GK_STORE_KM: return launch_t<false, true, EPI_STORE>(A, B, B2, p, s);
+    case GK_STORE_MM: return launch_t<true, true, EPI_STORE>(A, B, B2, p, s);
+    case GK_PACK: return launch_t<false, false, EPI_PACK>(A, B, B2, p, s);
+    case GK_GATED: return launch_t<false, false, EPI_GATED>(A, B, B2, p, s);
+    case GK_BWD_GATE: return launch_t<false, false, EPI_BWD_GATE>(A, B, B2, p, s);
+  }
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace tw

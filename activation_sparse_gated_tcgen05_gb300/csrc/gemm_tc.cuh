@@ -1,0 +1,483 @@
+// gemm_tc.cuh -- persistent tcgen05 GEMM engine for sm_103a with fused epilogues.
+//
+// One CTA per SM.  Warp roles (256 threads):
+//   warp 0      TMA producer: fills a STAGES-deep ring of A / B tiles in shared
+//               memory (128-byte swizzle), one elected lane
+//   warp 1      MMA issuer: tcgen05.mma 128 x 256 x 16 (bf16 in, fp32 in TMEM),
+//               one elected lane; commits free smem stages and finished tiles
+//   warp 2      TMEM owner: allocates / frees 512 columns (two accumulators)
+//   warps 4..7  epilogue: tcgen05.ld of the lane quarter each warp may touch;
+//               thread i of the 128 owns accumulator row i
+// Two 256-column accumulators let the epilogue of tile i overlap the
+// mainloop of tile i+1.  Tiles are visited in a grouped raster so CTAs that
+// run together share A rows and B columns in L2.
+//
+// Operands: A (M x K) and B (N x K), each K-major ([rows][K], K contiguous) or
+// MN-major ([K][rows]).  Epilogues:
+//   EPI_STORE     C = acc (bf16 or fp32, optional += into fp32, optional row map)
+//   EPI_PACK      ReLU + TwELL pack of the gate activation (no dense write)
+//   EPI_GATED     B = [Wg tile ; Wu tile]: h = bf16(ReLU(a)) * u, optional g, u
+//   EPI_BWD_GATE  acc = dh: du = dh * g, da = (dh * u + lambda) * 1[g > 0]
+#pragma once
+
+#include "common.cuh"
+
+namespace tw {
+
+enum EpiKind { EPI_STORE = 0, EPI_PACK = 1, EPI_GATED = 2, EPI_BWD_GATE = 3 };
+
+constexpr int kBM = 128;
+constexpr int kBN = 256;  // MMA N (for EPI_GATED: 128 gate + 128 up columns)
+constexpr int kBK = 64;   // one 128-byte swizzle row of bf16
+constexpr int kStages = 4;
+constexpr int kABytes = kBM * kBK * 2;  // 16 KB
+constexpr int kBBytes = kBN * kBK * 2;  // 32 KB
+constexpr int kGemmThreads = 256;
+constexpr int kGroupM = 16;
+constexpr uint32_t kTmemCols = 512;
+constexpr int kGemmSmem = kStages * (kABytes + kBBytes) + 1024 /*align*/ + 256 /*barriers*/;
+
+struct GemmParams {
+  int M, N, K;          // M: rows (buffer capacity), N: output columns, K: reduction
+  const int* m_dev;     // optional device row count: rows used = min(M, *m_dev)
+  const int* k_dev;     // optional device K: K used = min(K, *k_dev)
+  int n_tiles;          // tiles along N
+  int k_split;          // K segment length in k-blocks: segment s reads B (s even) or B2 (s odd)
+  int pad_rows;         // store every row of a visited tile that is < M (zero padding)
+  int* status;
+  // EPI_STORE
+  void* c;
+  long long ldc;
+  int c_f32;
+  int accumulate;
+  const int* row_map;   // destination row of output row r (scatter), or null
+  // EPI_PACK
+  uint16_t* val;
+  uint8_t* idx;
+  uint8_t* cnt;
+  int* row_nnz;
+  int T, cap, tile_n;
+  // EPI_GATED (outputs [M][N], leading dimension ldh)
+  uint16_t* h;
+  uint16_t* g_out;
+  uint16_t* u_out;
+  long long ldh;        // leading dimension of h
+  long long h_lo_off;   // if > 0: h is stored as bf16 hi at [r][j] plus bf16 lo at [r][j + h_lo_off]
+  long long ldgu;       // leading dimension of g / u (written by EPI_GATED, read by EPI_BWD_GATE)
+  float* u_f32;         // EPI_GATED: u kept in fp32 instead of u_out (bf16)
+  const float* u_f32_in;  // EPI_BWD_GATE: read u from here (fp32) instead of u_in
+  // EPI_BWD_GATE: g, u in [M][ldh]; du -> dd[r][j], da -> dd[r][dd_seg + j]; with
+  // dd_split the bf16 residuals follow: du lo at 2*dd_seg, da lo at 3*dd_seg
+  const uint16_t* g_in;
+  const uint16_t* u_in;
+  uint16_t* dd;
+  long long ld_dd;
+  long long dd_seg;
+  int dd_split;
+  float lambda;
+};
+
+__device__ __forceinline__ void tile_coords(int tile, int m_tiles, int n_tiles, int& mb, int& nb) {
+  const int per_group = kGroupM * n_tiles;
+  const int g = tile / per_group;
+  const int first = g * kGroupM;
+  const int gm = min(kGroupM, m_tiles - first);
+  const int r = tile - g * per_group;
+  mb = first + r % gm;
+  nb = r / gm;
+}
+
+// ------------------------------------------------------------------ epilogues
+template <int EPI>
+struct Epilogue;
+
+template <>
+struct Epilogue<EPI_STORE> {
+  static __device__ __forceinline__ void run(const GemmParams& p, uint32_t tacc, int row,
+                                             bool row_ok, int n0, int N) {
+    const int dst_row = (row_ok && p.row_map) ? p.row_map[row] : row;
+#pragma unroll 1
+    for (int c0 = 0; c0 < kBN; c0 += 32) {
+      uint32_t r[32];
+      tmem_ld32(tacc + c0, r);
+      tmem_wait_ld();
+      if (!row_ok) continue;
+      const int col = n0 + c0;
+      if (p.c_f32) {
+        float* dst = reinterpret_cast<float*>(p.c) + (long long)dst_row * p.ldc + col;
+#pragma unroll
+        for (int v = 0; v < 8; ++v) {
+          if (col + 4 * v + 4 <= N) {
+            float4 o = make_float4(__uint_as_float(r[4 * v]), __uint_as_float(r[4 * v + 1]),
+                                   __uint_as_float(r[4 * v + 2]), __uint_as_float(r[4 * v + 3]));
+            float4* q = reinterpret_cast<float4*>(dst + 4 * v);
+            if (p.accumulate) {
+              float4 old = *q;
+              o.x += old.x;
+              o.y += old.y;
+              o.z += old.z;
+              o.w += old.w;
+            }
+            *q = o;
+          }
+        }
+      } else {
+        uint16_t* dst = reinterpret_cast<uint16_t*>(p.c) + (long long)dst_row * p.ldc + col;
+#pragma unroll
+        for (int v = 0; v < 4; ++v) {
+          if (col + 8 * v + 8 <= N) {
+            uint4 o;
+            o.x = pack_bf16x2(__uint_as_float(r[8 * v + 0]), __uint_as_float(r[8 * v + 1]));
+            o.y = pack_bf16x2(__uint_as_float(r[8 * v + 2]), __uint_as_float(r[8 * v + 3]));
+            o.z = pack_bf16x2(__uint_as_float(r[8 * v + 4]), __uint_as_float(r[8 * v + 5]));
+            o.w = pack_bf16x2(__uint_as_float(r[8 * v + 6]), __uint_as_float(r[8 * v + 7]));
+            *reinterpret_cast<uint4*>(dst + 8 * v) = o;
+          }
+        }
+      }
+    }
+  }
+};
+
+// ReLU + TwELL pack.  The accumulator holds 256 gate columns = 256 / T_n
+// TwELL tiles; this thread owns one row, scans its columns in ascending
+// order and writes the live ones to its (row, tile) slots.
+template <>
+struct Epilogue<EPI_PACK> {
+  static __device__ __forceinline__ void run(const GemmParams& p, uint32_t tacc, int row,
+                                             bool row_ok, int n0, int /*N*/) {
+    const int tiles_here = kBN / p.tile_n;
+    const int chunks_per_tile = p.tile_n / 32;
+    int nnz = 0;
+#pragma unroll 1
+    for (int tt = 0; tt < tiles_here; ++tt) {
+      const int t = n0 / p.tile_n + tt;
+      const bool tile_ok = row_ok && t < p.T;
+      const long long slot0 = ((long long)row * p.T + t) * p.cap;
+      int c = 0;
+#pragma unroll 1
+      for (int ch = 0; ch < chunks_per_tile; ++ch) {
+        uint32_t r[32];
+        tmem_ld32(tacc + tt * p.tile_n + ch * 32, r);
+        tmem_wait_ld();
+        if (!tile_ok) continue;
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          const uint32_t g = relu_bf16_bits(__uint_as_float(r[i]));
+          if (g & 0x7FFFu) {
+            if (c < p.cap) {
+              p.val[slot0 + c] = (uint16_t)g;
+              p.idx[slot0 + c] = (uint8_t)(ch * 32 + i);
+            }
+            ++c;
+          }
+        }
+      }
+      if (tile_ok) {
+        p.cnt[(long long)row * p.T + t] = (uint8_t)c;
+        nnz += c;
+      }
+    }
+    if (row_ok && nnz) atomicAdd(p.row_nnz + row, nnz);
+  }
+};
+
+// Dense gated activation: accumulator columns [0,128) = a (gate), [128,256) =
+// u (up) of the same 128 neurons.  h = bf16(ReLU(a)) * u, stored bf16.
+template <>
+struct Epilogue<EPI_GATED> {
+  static __device__ __forceinline__ void run(const GemmParams& p, uint32_t tacc, int row,
+                                             bool row_ok, int n0, int N) {
+    // here n0 is the neuron offset (tile index * 128)
+#pragma unroll 1
+    for (int c0 = 0; c0 < 128; c0 += 32) {
+      uint32_t ra[32], ru[32];
+      tmem_ld32(tacc + c0, ra);
+      tmem_ld32(tacc + 128 + c0, ru);
+      tmem_wait_ld();
+      if (!row_ok || n0 + c0 >= N) continue;
+      const long long off = (long long)row * p.ldh + n0 + c0;
+      const long long ogu = (long long)row * p.ldgu + n0 + c0;
+#pragma unroll
+      for (int v = 0; v < 4; ++v) {
+        uint32_t hw[4], lw[4], gw[4], uw[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const int i = 8 * v + 2 * q;
+          const uint32_t g0 = relu_bf16_bits(__uint_as_float(ra[i]));
+          const uint32_t g1 = relu_bf16_bits(__uint_as_float(ra[i + 1]));
+          const float u0 = __uint_as_float(ru[i]), u1 = __uint_as_float(ru[i + 1]);
+          const float h0 = bf16_bits_to_float(g0) * u0, h1 = bf16_bits_to_float(g1) * u1;
+          hw[q] = pack_bf16x2(h0, h1);
+          const float2 hr = unpack_bf16x2(hw[q]);
+          lw[q] = pack_bf16x2(h0 - hr.x, h1 - hr.y);
+          gw[q] = g0 | (g1 << 16);
+          uw[q] = pack_bf16x2(u0, u1);
+        }
+        *reinterpret_cast<uint4*>(p.h + off + 8 * v) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+        if (p.h_lo_off)
+          *reinterpret_cast<uint4*>(p.h + off + p.h_lo_off + 8 * v) =
+              make_uint4(lw[0], lw[1], lw[2], lw[3]);
+        if (p.g_out)
+          *reinterpret_cast<uint4*>(p.g_out + ogu + 8 * v) = make_uint4(gw[0], gw[1], gw[2], gw[3]);
+        if (p.u_out)
+          *reinterpret_cast<uint4*>(p.u_out + ogu + 8 * v) = make_uint4(uw[0], uw[1], uw[2], uw[3]);
+        if (p.u_f32) {
+          float4* uo = reinterpret_cast<float4*>(p.u_f32 + ogu + 8 * v);
+          uo[0] = make_float4(__uint_as_float(ru[8 * v + 0]), __uint_as_float(ru[8 * v + 1]),
+                              __uint_as_float(ru[8 * v + 2]), __uint_as_float(ru[8 * v + 3]));
+          uo[1] = make_float4(__uint_as_float(ru[8 * v + 4]), __uint_as_float(ru[8 * v + 5]),
+                              __uint_as_float(ru[8 * v + 6]), __uint_as_float(ru[8 * v + 7]));
+        }
+      }
+    }
+  }
+};
+
+// acc = dh = dY Wd^T for 256 neurons.  du = dh * g, da = (dh * u + lambda) if
+// g > 0 else 0; both stored bf16 into dd = [du | da] (plus their bf16
+// residuals [du lo | da lo] when dd_split is set).
+template <>
+struct Epilogue<EPI_BWD_GATE> {
+  static __device__ __forceinline__ void run(const GemmParams& p, uint32_t tacc, int row,
+                                             bool row_ok, int n0, int N) {
+    const long long seg = p.dd_seg;
+#pragma unroll 1
+    for (int c0 = 0; c0 < kBN; c0 += 32) {
+      uint32_t r[32];
+      tmem_ld32(tacc + c0, r);
+      tmem_wait_ld();
+      if (!row_ok || n0 + c0 >= N) continue;
+      const long long gu = (long long)row * p.ldgu + n0 + c0;
+      const long long o = (long long)row * p.ld_dd + n0 + c0;
+#pragma unroll
+      for (int v = 0; v < 4; ++v) {
+        const uint4 g8 = *reinterpret_cast<const uint4*>(p.g_in + gu + 8 * v);
+        const uint32_t gw[4] = {g8.x, g8.y, g8.z, g8.w};
+        float uf[8];
+        if (p.u_f32_in) {
+          const float4 u0 = *reinterpret_cast<const float4*>(p.u_f32_in + gu + 8 * v);
+          const float4 u1 = *reinterpret_cast<const float4*>(p.u_f32_in + gu + 8 * v + 4);
+          uf[0] = u0.x; uf[1] = u0.y; uf[2] = u0.z; uf[3] = u0.w;
+          uf[4] = u1.x; uf[5] = u1.y; uf[6] = u1.z; uf[7] = u1.w;
+        } else {
+          const uint4 u8 = *reinterpret_cast<const uint4*>(p.u_in + gu + 8 * v);
+          const uint32_t uw[4] = {u8.x, u8.y, u8.z, u8.w};
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const float2 t = unpack_bf16x2(uw[q]);
+            uf[2 * q] = t.x;
+            uf[2 * q + 1] = t.y;
+          }
+        }
+        uint32_t duw[4], daw[4], dul[4], dal[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const float2 g = unpack_bf16x2(gw[q]);
+          const float2 u = make_float2(uf[2 * q], uf[2 * q + 1]);
+          const float dh0 = __uint_as_float(r[8 * v + 2 * q]);
+          const float dh1 = __uint_as_float(r[8 * v + 2 * q + 1]);
+          const float du0 = dh0 * g.x, du1 = dh1 * g.y;
+          const float da0 = g.x > 0.f ? fmaf(dh0, u.x, p.lambda) : 0.f;
+          const float da1 = g.y > 0.f ? fmaf(dh1, u.y, p.lambda) : 0.f;
+          duw[q] = pack_bf16x2(du0, du1);
+          daw[q] = pack_bf16x2(da0, da1);
+          const float2 duh = unpack_bf16x2(duw[q]), dah = unpack_bf16x2(daw[q]);
+          dul[q] = pack_bf16x2(du0 - duh.x, du1 - duh.y);
+          dal[q] = pack_bf16x2(da0 - dah.x, da1 - dah.y);
+        }
+        uint16_t* base = p.dd + o + 8 * v;
+        *reinterpret_cast<uint4*>(base) = make_uint4(duw[0], duw[1], duw[2], duw[3]);
+        *reinterpret_cast<uint4*>(base + seg) = make_uint4(daw[0], daw[1], daw[2], daw[3]);
+        if (p.dd_split) {
+          *reinterpret_cast<uint4*>(base + 2 * seg) = make_uint4(dul[0], dul[1], dul[2], dul[3]);
+          *reinterpret_cast<uint4*>(base + 3 * seg) = make_uint4(dal[0], dal[1], dal[2], dal[3]);
+        }
+      }
+    }
+  }
+};
+
+// ------------------------------------------------------------------ kernel
+template <bool A_MN, bool B_MN, int EPI>
+__global__ void __launch_bounds__(kGemmThreads, 1)
+    gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                const __grid_constant__ CUtensorMap tmB2, const GemmParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  uint8_t* sA = smem;
+  uint8_t* sB = smem + kStages * kABytes;
+  uint64_t* full = reinterpret_cast<uint64_t*>(sB + kStages * kBBytes);
+  uint64_t* empty = full + kStages;
+  uint64_t* tfull = empty + kStages;
+  uint64_t* tempty = tfull + 2;
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(tempty + 2);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  int M_eff = p.M;
+  if (p.m_dev) M_eff = min(M_eff, *p.m_dev);
+  int K_eff = p.K;
+  if (p.k_dev) K_eff = min(K_eff, *p.k_dev);
+  const int m_tiles = (M_eff + kBM - 1) / kBM;
+  const int num_kb = (K_eff + kBK - 1) / kBK;
+  const int total = (num_kb > 0 && M_eff > 0) ? m_tiles * p.n_tiles : 0;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(&tfull[a], 1);
+      mbar_init(&tempty[a], 128);
+    }
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 2) {
+    tmem_alloc(tmem_holder, kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_holder;
+
+  if (warp == 0) {
+    // ---------------------------------------------------------------- producer
+    if (lane == 0 && total > 0) {
+      tma_prefetch_desc(&tmA);
+      tma_prefetch_desc(&tmB);
+      tma_prefetch_desc(&tmB2);
+      int stage = 0;
+      uint32_t phase = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
+        int mb, nb;
+        tile_coords(tile, m_tiles, p.n_tiles, mb, nb);
+        for (int kb = 0; kb < num_kb; ++kb) {
+          if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(&full[stage], kABytes + kBBytes);
+          uint8_t* a_dst = sA + stage * kABytes;
+          uint8_t* b_dst = sB + stage * kBBytes;
+          if (!A_MN) {
+            tma_load_2d(a_dst, &tmA, &full[stage], kb * kBK, mb * kBM);
+          } else {
+            tma_load_2d(a_dst, &tmA, &full[stage], mb * kBM, kb * kBK);
+            tma_load_2d(a_dst + 8192, &tmA, &full[stage], mb * kBM + 64, kb * kBK);
+          }
+          if (EPI == EPI_GATED) {
+            tma_load_2d(b_dst, &tmB, &full[stage], kb * kBK, nb * 128);
+            tma_load_2d(b_dst + 16384, &tmB2, &full[stage], kb * kBK, nb * 128);
+          } else {
+            const int seg = kb / p.k_split;
+            const CUtensorMap* mp = (seg & 1) ? &tmB2 : &tmB;
+            const int kk = kb - seg * p.k_split;
+            if (!B_MN) {
+              tma_load_2d(b_dst, mp, &full[stage], kk * kBK, nb * kBN);
+            } else {
+#pragma unroll
+              for (int i = 0; i < 4; ++i)
+                tma_load_2d(b_dst + i * 8192, mp, &full[stage], nb * kBN + 64 * i, kk * kBK);
+            }
+          }
+          if (++stage == kStages) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      if (!ok) {
+        set_status(p.status, TWELL_ERR_DEVICE_TIMEOUT);
+        *abort_flag = 1;
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ---------------------------------------------------------------- MMA issuer
+    if (lane == 0 && total > 0) {
+      constexpr uint32_t idesc = idesc_bf16(kBM, kBN, A_MN, B_MN);
+      int stage = 0;
+      uint32_t phase = 0;
+      int it = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x, ++it) {
+        const int acc = it & 1;
+        const uint32_t acc_phase = (uint32_t)(it >> 1) & 1u;
+        if (!mbar_wait(&tempty[acc], acc_phase ^ 1u, abort_flag)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + (uint32_t)(acc * kBN);
+        for (int kb = 0; kb < num_kb; ++kb) {
+          if (!mbar_wait(&full[stage], phase, abort_flag)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a0 = smem_u32(sA + stage * kABytes);
+          const uint32_t b0 = smem_u32(sB + stage * kBBytes);
+#pragma unroll
+          for (int k = 0; k < kBK / 16; ++k) {
+            const uint64_t ad = A_MN ? sdesc_sw128(a0 + k * 2048, 8192, 1024)
+                                     : sdesc_sw128(a0 + k * 32, 16, 1024);
+            const uint64_t bd = B_MN ? sdesc_sw128(b0 + k * 2048, 8192, 1024)
+                                     : sdesc_sw128(b0 + k * 32, 16, 1024);
+            tc_mma_bf16(d_tmem, ad, bd, idesc, (kb | k) != 0 ? 1u : 0u);
+          }
+          tc_commit(&empty[stage]);
+          if (++stage == kStages) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (ok) tc_commit(&tfull[acc]);
+      }
+      if (!ok) {
+        set_status(p.status, TWELL_ERR_DEVICE_TIMEOUT);
+        *abort_flag = 1;
+      }
+    }
+    __syncwarp();
+  } else if (warp >= 4) {
+    // ---------------------------------------------------------------- epilogue
+    const int quarter = warp & 3;
+    const int r_local = quarter * 32 + lane;
+    int it = 0;
+    for (int tile = blockIdx.x; tile < total; tile += gridDim.x, ++it) {
+      int mb, nb;
+      tile_coords(tile, m_tiles, p.n_tiles, mb, nb);
+      const int acc = it & 1;
+      const uint32_t acc_phase = (uint32_t)(it >> 1) & 1u;
+      if (!mbar_wait(&tfull[acc], acc_phase, abort_flag)) {
+        set_status(p.status, TWELL_ERR_DEVICE_TIMEOUT);
+        *abort_flag = 1;
+        break;
+      }
+      tc_fence_after();
+      const int row = mb * kBM + r_local;
+      const bool row_ok = p.pad_rows ? (row < p.M) : (row < M_eff);
+      const uint32_t tacc = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * kBN);
+      const int n0 = (EPI == EPI_GATED) ? nb * 128 : nb * kBN;
+      Epilogue<EPI>::run(p, tacc, row, row_ok, n0, p.N);
+      tc_fence_before();
+      mbar_arrive(&tempty[acc]);
+    }
+  }
+
+  __syncthreads();
+  if (warp == 2) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, kTmemCols);
+  }
+}
+
+}  // namespace tw

@@ -1,0 +1,61 @@
+// internal.h -- host-side interfaces between the library's translation units.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "twell.h"
+
+namespace tw {
+
+struct GemmParams;
+
+// A bf16 row-major matrix view: rows x cols elements, leading dimension ld.
+struct Mat {
+  const void* ptr;
+  long long rows, cols, ld;
+};
+
+// Which epilogue / operand majorness a GEMM launch uses.
+enum GemmKind {
+  GK_STORE_KK = 0,   // A K-major, B K-major, store
+  GK_STORE_MK = 1,   // A MN-major, B K-major, store
+  GK_STORE_KM = 2,   // A K-major, B MN-major, store
+  GK_STORE_MM = 3,   // A MN-major, B MN-major, store
+  GK_PACK = 4,       // gate GEMM with the TwELL pack epilogue
+  GK_GATED = 5,      // [Wg ; Wu] GEMM with the ReLU * up epilogue
+  GK_BWD_GATE = 6,   // dh GEMM with the du / da epilogue
+};
+
+int num_sms();
+int* device_status_ptr();  // per-device status word (device address)
+
+// Launch the persistent GEMM.  A is the M-side operand, B (and B2 for a
+// second K range or the up half of EPI_GATED) the N-side one, each given in
+// its storage layout.  Returns a CUDA error or cudaSuccess; an invalid
+// tensor-map encode returns cudaErrorInvalidValue.
+cudaError_t gemm_launch(GemmKind kind, const Mat& A, const Mat& B, const Mat* B2,
+                        const GemmParams& p, cudaStream_t stream);
+
+// Non-tensor-core kernels (pack.cu, sparse_fwd.cu, sparse_bwd.cu).
+cudaError_t launch_pack_dense(const void* a, int a_f32, int M, int f, int tile_n, int cap,
+                              const twell_tiles& out, cudaStream_t s);
+cudaError_t launch_route(const twell_tiles& in, int M, int f, int tile_n, int cap,
+                         const twell_hybrid& out, int* scan_flags, cudaStream_t s);
+cudaError_t launch_gather_rows(const void* src, int M, int d, const int* rows, const int* n_rows,
+                               void* dst, int dst_rows, cudaStream_t s);
+cudaError_t launch_sparse_fwd(const void* x, const void* wuT, const void* wd, int M, int d, int f,
+                              const twell_tiles* tiles, int tile_n, int cap,
+                              const twell_hybrid* route, void* y, cudaStream_t s);
+cudaError_t launch_csc_build(const twell_hybrid& route, int M, int f, int* blk_counts,
+                             int* csc_ptr, int* csc_row, int* slot_pos, cudaStream_t s);
+cudaError_t launch_sparse_bwd_rows(const void* x, const void* dy, const void* wgT, const void* wuT,
+                                   const void* wd, int M, int d, const twell_hybrid& route,
+                                   const int* slot_pos, float lambda, float4* csc_vals, void* dx,
+                                   cudaStream_t s);
+cudaError_t launch_sparse_bwd_neurons(const void* x, const void* dy, int M, int d, int f,
+                                      const int* csc_ptr, const int* csc_row,
+                                      const float4* csc_vals, float* dwgT, float* dwuT, float* dwd,
+                                      cudaStream_t s);
+
+}  // namespace tw

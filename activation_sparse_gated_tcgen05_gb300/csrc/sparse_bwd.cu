@@ -1,0 +1,395 @@
+// sparse_bwd.cu -- backward of the sparse gated FFN over the ELL rows.
+//
+// Training path of page 2 "Sakana AI and NVIDIA introduce TwELL with CUDA
+// kernels ...", section "¿Qué hace distinto a TwELL frente a ELL clásico?"
+// (hybrid ELL rows), with the L1 term of section "Receta de entrenamiento".
+// For a live entry (m, j) with stored gate g > 0:
+//   dh = dY_m . Wd[j, :],  u = x_m . Wu[:, j],  h = g u
+//   du = dh g,  da = dh u + lambda        (ReLU' = 1 on live entries)
+//   dX_m += du Wu[:, j]^T + da Wg[:, j]^T
+//   dWd[j] += h dY_m,  dWu^T[j] += du x_m,  dWg^T[j] += da x_m
+// Dead entries contribute exactly zero, so visiting live entries only is the
+// exact gradient.
+//
+// Three phases, all deterministic (no floating-point atomics):
+//   1. csc_*: a column-major (neuron-major) index of the live entries, rows
+//      ascending inside every neuron.  Per 32-row block and neuron a bitmask
+//      of the rows that use the neuron gives every entry its rank without any
+//      ordering race: rank = prefix over blocks + popcount of lower bits.
+//   2. bwd_rows: one team of warps per row computes dh, u, du, da, h per entry
+//      (stored at the entry's neuron-major position) and dX_m.
+//   3. bwd_neurons: one team per neuron sums its entries in ascending row
+//      order into dWd[j], dWu^T[j], dWg^T[j] (fp32, written once).
+#include "common.cuh"
+#include "internal.h"
+
+namespace tw {
+
+namespace {
+
+constexpr unsigned kFull = 0xffffffffu;
+constexpr int kWarps = 8;
+
+// ---------------------------------------------------------------- CSC index
+__global__ void __launch_bounds__(kWarps * 32)
+    csc_mark_kernel(const uint16_t* __restrict__ ell_col, const int* __restrict__ ell_nnz, int M,
+                    int W, int f, unsigned* __restrict__ mask) {
+  const int lane = threadIdx.x & 31;
+  const int m = blockIdx.x * kWarps + (threadIdx.x >> 5);
+  if (m >= M) return;
+  const int n = ell_nnz[m];
+  unsigned* mrow = mask + (long long)(m >> 5) * f;
+  const unsigned bit = 1u << (m & 31);
+  for (int s = lane; s < n; s += 32) atomicOr(mrow + ell_col[(long long)m * W + s], bit);
+}
+
+// For every neuron: exclusive prefix of live rows over the 32-row blocks.
+__global__ void __launch_bounds__(256)
+    csc_colscan_kernel(const unsigned* __restrict__ mask, int NB, int f, int* __restrict__ off,
+                       int* __restrict__ tot) {
+  const int j = blockIdx.x * blockDim.x + threadIdx.x;
+  if (j >= f) return;
+  int run = 0;
+  for (int b = 0; b < NB; ++b) {
+    off[(long long)b * f + j] = run;
+    run += __popc(mask[(long long)b * f + j]);
+  }
+  tot[j] = run;
+}
+
+// csc_ptr[0..f] = exclusive prefix of tot (one block).
+__global__ void __launch_bounds__(1024)
+    csc_ptr_kernel(const int* __restrict__ tot, int f, int* __restrict__ csc_ptr) {
+  __shared__ int warp_tot[32];
+  __shared__ int carry;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  if (tid == 0) carry = 0;
+  __syncthreads();
+  for (int base = 0; base < f; base += 1024) {
+    const int j = base + tid;
+    const int c = j < f ? tot[j] : 0;
+    const int incl = warp_incl_scan(c);
+    if (lane == 31) warp_tot[warp] = incl;
+    __syncthreads();
+    if (warp == 0) {
+      const int v = warp_tot[lane];
+      warp_tot[lane] = warp_incl_scan(v) - v;
+    }
+    __syncthreads();
+    const int ex = carry + warp_tot[warp] + incl - c;
+    if (j < f) csc_ptr[j] = ex;
+    __syncthreads();
+    if (tid == 1023) carry = ex + c;
+    __syncthreads();
+  }
+  if (tid == 0) csc_ptr[f] = carry;
+}
+
+__global__ void __launch_bounds__(kWarps * 32)
+    csc_place_kernel(const uint16_t* __restrict__ ell_col, const int* __restrict__ ell_nnz, int M,
+                     int W, int f, const unsigned* __restrict__ mask, const int* __restrict__ off,
+                     const int* __restrict__ csc_ptr, int* __restrict__ csc_row,
+                     int* __restrict__ slot_pos) {
+  const int lane = threadIdx.x & 31;
+  const int m = blockIdx.x * kWarps + (threadIdx.x >> 5);
+  if (m >= M) return;
+  const int n = ell_nnz[m];
+  const long long blk = (long long)(m >> 5) * f;
+  const unsigned below = (1u << (m & 31)) - 1u;
+  for (int s = lane; s < n; s += 32) {
+    const int j = ell_col[(long long)m * W + s];
+    const int pos = csc_ptr[j] + off[blk + j] + __popc(mask[blk + j] & below);
+    csc_row[pos] = m;
+    slot_pos[(long long)m * W + s] = pos;
+  }
+}
+
+// ---------------------------------------------------------------- row phase
+template <int TEAM>
+__device__ __forceinline__ int slab(int lane, int wt, int v) {
+  return 8 * (lane + 32 * (wt + TEAM * v));
+}
+
+template <int TEAM, int VPL, int B>
+__global__ void __launch_bounds__(256)
+    bwd_rows_kernel(const uint16_t* __restrict__ x, const uint16_t* __restrict__ dy,
+                    const uint16_t* __restrict__ wgT, const uint16_t* __restrict__ wuT,
+                    const uint16_t* __restrict__ wd, int M, int d,
+                    const uint16_t* __restrict__ ell_val, const uint16_t* __restrict__ ell_col,
+                    const int* __restrict__ ell_nnz, int W, const int* __restrict__ slot_pos,
+                    float lambda, float4* __restrict__ csc_vals, uint16_t* __restrict__ dx) {
+  constexpr int ROWS = 8 / TEAM;
+  __shared__ float red[2][8][TEAM][2 * B];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int team = warp / TEAM, wt = warp % TEAM;
+  const int m = blockIdx.x * ROWS + team;
+  if (m >= M) return;
+
+  uint4 xv[VPL], dyv[VPL];
+  float acc[VPL][8];
+#pragma unroll
+  for (int v = 0; v < VPL; ++v) {
+    const int e = slab<TEAM>(lane, wt, v);
+    xv[v] = e < d ? ldg_v4(x + (long long)m * d + e) : make_uint4(0, 0, 0, 0);
+    dyv[v] = e < d ? ldg_v4(dy + (long long)m * d + e) : make_uint4(0, 0, 0, 0);
+#pragma unroll
+    for (int k = 0; k < 8; ++k) acc[v][k] = 0.f;
+  }
+  int buf = 0;
+  const int n = ell_nnz[m];
+  for (int e0 = 0; e0 < n; e0 += 32) {
+    const int count = min(32, n - e0);
+    int jl = 0, pl = 0;
+    float gl = 0.f;
+    if (lane < count) {
+      const long long s = (long long)m * W + e0 + lane;
+      jl = ell_col[s];
+      gl = bf16_bits_to_float(ell_val[s]);
+      pl = slot_pos[s];
+    }
+    for (int i = 0; i < count; i += B) {
+      int j[B], pos[B];
+      float g[B];
+#pragma unroll
+      for (int b = 0; b < B; ++b) {
+        const int src = (i + b) & 31;
+        const int jj = __shfl_sync(kFull, jl, src);
+        const int pp = __shfl_sync(kFull, pl, src);
+        const float gg = __shfl_sync(kFull, gl, src);
+        const bool ok = i + b < count;
+        j[b] = ok ? jj : -1;
+        pos[b] = pp;
+        g[b] = ok ? gg : 0.f;
+      }
+      uint4 wdv[B][VPL], wuv[B][VPL];
+#pragma unroll
+      for (int b = 0; b < B; ++b)
+#pragma unroll
+        for (int v = 0; v < VPL; ++v) {
+          const int e = slab<TEAM>(lane, wt, v);
+          const bool ok = j[b] >= 0 && e < d;
+          wdv[b][v] = ok ? ldg_v4(wd + (long long)j[b] * d + e) : make_uint4(0, 0, 0, 0);
+          wuv[b][v] = ok ? ldg_v4(wuT + (long long)j[b] * d + e) : make_uint4(0, 0, 0, 0);
+        }
+      float dh[B], u[B];
+#pragma unroll
+      for (int b = 0; b < B; ++b) {
+        dh[b] = 0.f;
+        u[b] = 0.f;
+#pragma unroll
+        for (int v = 0; v < VPL; ++v) {
+          dh[b] = dot8(dyv[v], wdv[b][v], dh[b]);
+          u[b] = dot8(xv[v], wuv[b][v], u[b]);
+        }
+        dh[b] = warp_sum(dh[b]);
+        u[b] = warp_sum(u[b]);
+      }
+      if (TEAM > 1) {
+        if (lane == 0)
+#pragma unroll
+          for (int b = 0; b < B; ++b) {
+            red[buf][team][wt][2 * b] = dh[b];
+            red[buf][team][wt][2 * b + 1] = u[b];
+          }
+        named_barrier(1 + team, 32 * TEAM);
+#pragma unroll
+        for (int b = 0; b < B; ++b) {
+          float s0 = 0.f, s1 = 0.f;
+#pragma unroll
+          for (int w = 0; w < TEAM; ++w) {
+            s0 += red[buf][team][w][2 * b];
+            s1 += red[buf][team][w][2 * b + 1];
+          }
+          dh[b] = s0;
+          u[b] = s1;
+        }
+        buf ^= 1;
+      }
+#pragma unroll
+      for (int b = 0; b < B; ++b) {
+        if (j[b] < 0) continue;
+        const float du = dh[b] * g[b];
+        const float da = fmaf(dh[b], u[b], lambda);
+        if (wt == 0 && lane == 0) csc_vals[pos[b]] = make_float4(du, da, g[b] * u[b], 0.f);
+#pragma unroll
+        for (int v = 0; v < VPL; ++v) {
+          const int e = slab<TEAM>(lane, wt, v);
+          const uint4 wg = e < d ? ldg_v4(wgT + (long long)j[b] * d + e) : make_uint4(0, 0, 0, 0);
+          axpy8(du, wuv[b][v], acc[v]);
+          axpy8(da, wg, acc[v]);
+        }
+      }
+    }
+  }
+#pragma unroll
+  for (int v = 0; v < VPL; ++v) {
+    const int e = slab<TEAM>(lane, wt, v);
+    if (e < d) {
+      uint4 o;
+      o.x = pack_bf16x2(acc[v][0], acc[v][1]);
+      o.y = pack_bf16x2(acc[v][2], acc[v][3]);
+      o.z = pack_bf16x2(acc[v][4], acc[v][5]);
+      o.w = pack_bf16x2(acc[v][6], acc[v][7]);
+      *reinterpret_cast<uint4*>(dx + (long long)m * d + e) = o;
+    }
+  }
+}
+
+// ---------------------------------------------------------------- neuron phase
+template <int TEAM, int VPL, int B>
+__global__ void __launch_bounds__(256)
+    bwd_neurons_kernel(const uint16_t* __restrict__ x, const uint16_t* __restrict__ dy, int d,
+                       int f, const int* __restrict__ csc_ptr, const int* __restrict__ csc_row,
+                       const float4* __restrict__ csc_vals, float* __restrict__ dwgT,
+                       float* __restrict__ dwuT, float* __restrict__ dwd) {
+  constexpr int ROWS = 8 / TEAM;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int team = warp / TEAM, wt = warp % TEAM;
+  const int j = blockIdx.x * ROWS + team;
+  if (j >= f) return;
+  float ad[VPL][8], au[VPL][8], ag[VPL][8];
+#pragma unroll
+  for (int v = 0; v < VPL; ++v)
+#pragma unroll
+    for (int k = 0; k < 8; ++k) ad[v][k] = au[v][k] = ag[v][k] = 0.f;
+
+  const int p0 = csc_ptr[j], p1 = csc_ptr[j + 1];
+  for (int e0 = p0; e0 < p1; e0 += 32) {
+    const int count = min(32, p1 - e0);
+    int ml = 0;
+    float4 vl = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (lane < count) {
+      ml = csc_row[e0 + lane];
+      vl = csc_vals[e0 + lane];
+    }
+    for (int i = 0; i < count; i += B) {
+      int m[B];
+      float du[B], da[B], h[B];
+#pragma unroll
+      for (int b = 0; b < B; ++b) {
+        const int src = (i + b) & 31;
+        const bool ok = i + b < count;
+        const int mm = __shfl_sync(kFull, ml, src);
+        const float a0 = __shfl_sync(kFull, vl.x, src);
+        const float a1 = __shfl_sync(kFull, vl.y, src);
+        const float a2 = __shfl_sync(kFull, vl.z, src);
+        m[b] = ok ? mm : -1;
+        du[b] = ok ? a0 : 0.f;
+        da[b] = ok ? a1 : 0.f;
+        h[b] = ok ? a2 : 0.f;
+      }
+      uint4 xv[B][VPL], dyv[B][VPL];
+#pragma unroll
+      for (int b = 0; b < B; ++b)
+#pragma unroll
+        for (int v = 0; v < VPL; ++v) {
+          const int e = slab<TEAM>(lane, wt, v);
+          const bool ok = m[b] >= 0 && e < d;
+          xv[b][v] = ok ? ldg_v4(x + (long long)m[b] * d + e) : make_uint4(0, 0, 0, 0);
+          dyv[b][v] = ok ? ldg_v4(dy + (long long)m[b] * d + e) : make_uint4(0, 0, 0, 0);
+        }
+#pragma unroll
+      for (int b = 0; b < B; ++b)
+#pragma unroll
+        for (int v = 0; v < VPL; ++v) {
+          axpy8(h[b], dyv[b][v], ad[v]);
+          axpy8(du[b], xv[b][v], au[v]);
+          axpy8(da[b], xv[b][v], ag[v]);
+        }
+    }
+  }
+  const long long row = (long long)j * d;
+#pragma unroll
+  for (int v = 0; v < VPL; ++v) {
+    const int e = slab<TEAM>(lane, wt, v);
+    if (e < d) {
+      float4* o1 = reinterpret_cast<float4*>(dwd + row + e);
+      float4* o2 = reinterpret_cast<float4*>(dwuT + row + e);
+      float4* o3 = reinterpret_cast<float4*>(dwgT + row + e);
+      o1[0] = make_float4(ad[v][0], ad[v][1], ad[v][2], ad[v][3]);
+      o1[1] = make_float4(ad[v][4], ad[v][5], ad[v][6], ad[v][7]);
+      o2[0] = make_float4(au[v][0], au[v][1], au[v][2], au[v][3]);
+      o2[1] = make_float4(au[v][4], au[v][5], au[v][6], au[v][7]);
+      o3[0] = make_float4(ag[v][0], ag[v][1], ag[v][2], ag[v][3]);
+      o3[1] = make_float4(ag[v][4], ag[v][5], ag[v][6], ag[v][7]);
+    }
+  }
+}
+
+template <int TEAM>
+cudaError_t rows_team(const void* x, const void* dy, const void* wgT, const void* wuT,
+                      const void* wd, int M, int d, const twell_hybrid& r, const int* slot_pos,
+                      float lambda, float4* csc_vals, void* dx, cudaStream_t s) {
+  constexpr int ROWS = 8 / TEAM;
+  bwd_rows_kernel<TEAM, 4, 2><<<(M + ROWS - 1) / ROWS, 256, 0, s>>>(
+      reinterpret_cast<const uint16_t*>(x), reinterpret_cast<const uint16_t*>(dy),
+      reinterpret_cast<const uint16_t*>(wgT), reinterpret_cast<const uint16_t*>(wuT),
+      reinterpret_cast<const uint16_t*>(wd), M, d, reinterpret_cast<const uint16_t*>(r.ell_val),
+      r.ell_col, r.ell_nnz, r.ell_width, slot_pos, lambda, csc_vals,
+      reinterpret_cast<uint16_t*>(dx));
+  return cudaGetLastError();
+}
+
+template <int TEAM>
+cudaError_t neurons_team(const void* x, const void* dy, int d, int f, const int* csc_ptr,
+                         const int* csc_row, const float4* csc_vals, float* dwgT, float* dwuT,
+                         float* dwd, cudaStream_t s) {
+  constexpr int ROWS = 8 / TEAM;
+  bwd_neurons_kernel<TEAM, 4, 2><<<(f + ROWS - 1) / ROWS, 256, 0, s>>>(
+      reinterpret_cast<const uint16_t*>(x), reinterpret_cast<const uint16_t*>(dy), d, f, csc_ptr,
+      csc_row, csc_vals, dwgT, dwuT, dwd);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+// blk_counts holds two [ceil(M/32)][f] int arrays (row masks, then block offsets).
+cudaError_t launch_csc_build(const twell_hybrid& r, int M, int f, int* blk_counts, int* csc_ptr,
+                             int* csc_row, int* slot_pos, cudaStream_t s) {
+  const int NB = (M + 31) / 32;
+  unsigned* mask = reinterpret_cast<unsigned*>(blk_counts);
+  int* off = blk_counts + (long long)NB * f;
+  int* tot = csc_ptr;  // totals land in csc_ptr, then the scan rewrites it in place
+  cudaError_t e = cudaMemsetAsync(mask, 0, sizeof(unsigned) * (size_t)NB * f, s);
+  if (e != cudaSuccess) return e;
+  if (M > 0) {
+    csc_mark_kernel<<<(M + kWarps - 1) / kWarps, kWarps * 32, 0, s>>>(r.ell_col, r.ell_nnz, M,
+                                                                      r.ell_width, f, mask);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  }
+  csc_colscan_kernel<<<(f + 255) / 256, 256, 0, s>>>(mask, NB, f, off, tot);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  csc_ptr_kernel<<<1, 1024, 0, s>>>(tot, f, csc_ptr);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  if (M > 0) {
+    csc_place_kernel<<<(M + kWarps - 1) / kWarps, kWarps * 32, 0, s>>>(
+        r.ell_col, r.ell_nnz, M, r.ell_width, f, mask, off, csc_ptr, csc_row, slot_pos);
+    e = cudaGetLastError();
+  }
+  return e;
+}
+
+cudaError_t launch_sparse_bwd_rows(const void* x, const void* dy, const void* wgT, const void* wuT,
+                                   const void* wd, int M, int d, const twell_hybrid& route,
+                                   const int* slot_pos, float lambda, float4* csc_vals, void* dx,
+                                   cudaStream_t s) {
+  if (M == 0) return cudaSuccess;
+  if (d <= 1024) return rows_team<1>(x, dy, wgT, wuT, wd, M, d, route, slot_pos, lambda, csc_vals, dx, s);
+  if (d <= 2048) return rows_team<2>(x, dy, wgT, wuT, wd, M, d, route, slot_pos, lambda, csc_vals, dx, s);
+  if (d <= 4096) return rows_team<4>(x, dy, wgT, wuT, wd, M, d, route, slot_pos, lambda, csc_vals, dx, s);
+  return rows_team<8>(x, dy, wgT, wuT, wd, M, d, route, slot_pos, lambda, csc_vals, dx, s);
+}
+
+cudaError_t launch_sparse_bwd_neurons(const void* x, const void* dy, int M, int d, int f,
+                                      const int* csc_ptr, const int* csc_row,
+                                      const float4* csc_vals, float* dwgT, float* dwuT, float* dwd,
+                                      cudaStream_t s) {
+  (void)M;
+  if (f == 0) return cudaSuccess;
+  if (d <= 1024) return neurons_team<1>(x, dy, d, f, csc_ptr, csc_row, csc_vals, dwgT, dwuT, dwd, s);
+  if (d <= 2048) return neurons_team<2>(x, dy, d, f, csc_ptr, csc_row, csc_vals, dwgT, dwuT, dwd, s);
+  if (d <= 4096) return neurons_team<4>(x, dy, d, f, csc_ptr, csc_row, csc_vals, dwgT, dwuT, dwd, s);
+  return neurons_team<8>(x, dy, d, f, csc_ptr, csc_row, csc_vals, dwgT, dwuT, dwd, s);
+}
+
+}  // namespace tw

@@ -1,0 +1,223 @@
+// sparse_fwd.cu -- fused sparse up + down projection over packed activations.
+//
+// Page 2 "Sakana AI and NVIDIA introduce TwELL with CUDA kernels ...", section
+// "¿Qué hace distinto a TwELL frente a ELL clásico?": one kernel reads the
+// packed gate activations and performs the up and down projections together;
+// the intermediate never reaches global memory.
+//
+// A team of TEAM warps owns one token row m; the d_model axis is split across
+// the team in 256-element (512-byte) slabs, VPL slabs per warp, so every
+// weight-row read is a run of coalesced 16-byte loads.  For each live entry
+// (j, g) of the row:
+//   u = x_m . Wu[:, j]          (x_m held in registers, WuT[j] gathered)
+//   h = g * u                   (fp32, kept in registers)
+//   y_m += h * Wd[j, :]         (fp32 accumulators in registers)
+// and y_m is written once as bf16.  Entries are processed B at a time so
+// 2*B weight rows are in flight per warp.
+#include "common.cuh"
+#include "internal.h"
+
+namespace tw {
+
+namespace {
+
+constexpr unsigned kFull = 0xffffffffu;
+
+template <int TEAM, int VPL, int B>
+struct RowCtx {
+  uint4 xv[VPL];
+  float acc[VPL][8];
+};
+
+template <int TEAM, int VPL>
+__device__ __forceinline__ int slab_elem(int lane, int wt, int v) {
+  return 8 * (lane + 32 * (wt + TEAM * v));
+}
+
+// Process `count` (<= 32) entries whose (column, gate) sit in lanes 0..count-1.
+template <int TEAM, int VPL, int B>
+__device__ __forceinline__ void process_entries(RowCtx<TEAM, VPL, B>& c, int jl, float gl,
+                                                int count, const uint16_t* __restrict__ wuT,
+                                                const uint16_t* __restrict__ wd, int d, int lane,
+                                                int wt, int team, float (*red)[8][TEAM][B],
+                                                int& buf) {
+  for (int i = 0; i < count; i += B) {
+    int j[B];
+    float g[B];
+#pragma unroll
+    for (int b = 0; b < B; ++b) {
+      const int src = (i + b) & 31;
+      const int jj = __shfl_sync(kFull, jl, src);
+      const float gg = __shfl_sync(kFull, gl, src);
+      j[b] = (i + b < count) ? jj : -1;
+      g[b] = (i + b < count) ? gg : 0.f;
+    }
+    uint4 wu[B][VPL], wdv[B][VPL];
+#pragma unroll
+    for (int b = 0; b < B; ++b)
+#pragma unroll
+      for (int v = 0; v < VPL; ++v) {
+        const int e = slab_elem<TEAM, VPL>(lane, wt, v);
+        if (j[b] >= 0 && e < d) {
+          wu[b][v] = ldg_v4(wuT + (long long)j[b] * d + e);
+          wdv[b][v] = ldg_v4(wd + (long long)j[b] * d + e);
+        } else {
+          wu[b][v] = make_uint4(0, 0, 0, 0);
+          wdv[b][v] = make_uint4(0, 0, 0, 0);
+        }
+      }
+    float p[B];
+#pragma unroll
+    for (int b = 0; b < B; ++b) {
+      p[b] = 0.f;
+#pragma unroll
+      for (int v = 0; v < VPL; ++v) p[b] = dot8(c.xv[v], wu[b][v], p[b]);
+      p[b] = warp_sum(p[b]);
+    }
+    if (TEAM > 1) {
+      if (lane == 0)
+#pragma unroll
+        for (int b = 0; b < B; ++b) red[buf][team][wt][b] = p[b];
+      named_barrier(1 + team, 32 * TEAM);
+#pragma unroll
+      for (int b = 0; b < B; ++b) {
+        float s = 0.f;
+#pragma unroll
+        for (int w = 0; w < TEAM; ++w) s += red[buf][team][w][b];
+        p[b] = s;
+      }
+      buf ^= 1;
+    }
+#pragma unroll
+    for (int b = 0; b < B; ++b) {
+      const float h = g[b] * p[b];
+#pragma unroll
+      for (int v = 0; v < VPL; ++v) axpy8(h, wdv[b][v], c.acc[v]);
+    }
+  }
+}
+
+template <int TEAM, int VPL, int B, bool ELL>
+__global__ void __launch_bounds__(256)
+    sparse_fwd_kernel(const uint16_t* __restrict__ x, const uint16_t* __restrict__ wuT,
+                      const uint16_t* __restrict__ wd, int M, int d,
+                      const uint16_t* __restrict__ val, const uint8_t* __restrict__ idx,
+                      const uint8_t* __restrict__ cnt, int T, int tile_n, int cap,
+                      const uint16_t* __restrict__ ell_val, const uint16_t* __restrict__ ell_col,
+                      const int* __restrict__ ell_nnz, int W, uint16_t* __restrict__ y,
+                      int* status) {
+  constexpr int ROWS = 8 / TEAM;
+  __shared__ float red[2][8][TEAM][B];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int team = warp / TEAM, wt = warp % TEAM;
+  const int m = blockIdx.x * ROWS + team;
+  if (m >= M) return;
+
+  RowCtx<TEAM, VPL, B> c;
+#pragma unroll
+  for (int v = 0; v < VPL; ++v) {
+    const int e = slab_elem<TEAM, VPL>(lane, wt, v);
+    c.xv[v] = e < d ? ldg_v4(x + (long long)m * d + e) : make_uint4(0, 0, 0, 0);
+#pragma unroll
+    for (int k = 0; k < 8; ++k) c.acc[v][k] = 0.f;
+  }
+  int buf = 0;
+
+  if (ELL) {
+    const int n = ell_nnz[m];
+    for (int e0 = 0; e0 < n; e0 += 32) {
+      const int count = min(32, n - e0);
+      int jl = 0;
+      float gl = 0.f;
+      if (lane < count) {
+        const long long s = (long long)m * W + e0 + lane;
+        jl = ell_col[s];
+        gl = bf16_bits_to_float(ell_val[s]);
+      }
+      process_entries<TEAM, VPL, B>(c, jl, gl, count, wuT, wd, d, lane, wt, team, red, buf);
+    }
+  } else {
+    for (int t0 = 0; t0 < T; t0 += 32) {
+      const int t = t0 + lane;
+      const int craw = t < T ? cnt[(long long)m * T + t] : 0;
+      if (craw > cap && wt == 0) set_status(status, TWELL_ERR_CAPACITY);
+      const int ct = min(craw, cap);
+      const int incl = warp_incl_scan(ct);
+      const int excl = incl - ct;
+      const int total = __shfl_sync(kFull, incl, 31);
+      for (int e0 = 0; e0 < total; e0 += 32) {
+        const int e = e0 + lane;
+        int lo = 0;  // owner lane: number of lanes whose inclusive count is <= e
+#pragma unroll
+        for (int step = 16; step >= 1; step >>= 1) {
+          const int v = __shfl_sync(kFull, incl, lo + step - 1);
+          if (v <= e) lo += step;
+        }
+        const int ex = __shfl_sync(kFull, excl, lo);
+        int jl = 0;
+        float gl = 0.f;
+        if (e < total) {
+          const int tt = t0 + lo;
+          const long long s = ((long long)m * T + tt) * cap + (e - ex);
+          jl = tt * tile_n + idx[s];
+          gl = bf16_bits_to_float(val[s]);
+        }
+        process_entries<TEAM, VPL, B>(c, jl, gl, min(32, total - e0), wuT, wd, d, lane, wt, team,
+                                      red, buf);
+      }
+    }
+  }
+
+#pragma unroll
+  for (int v = 0; v < VPL; ++v) {
+    const int e = slab_elem<TEAM, VPL>(lane, wt, v);
+    if (e < d) {
+      uint4 o;
+      o.x = pack_bf16x2(c.acc[v][0], c.acc[v][1]);
+      o.y = pack_bf16x2(c.acc[v][2], c.acc[v][3]);
+      o.z = pack_bf16x2(c.acc[v][4], c.acc[v][5]);
+      o.w = pack_bf16x2(c.acc[v][6], c.acc[v][7]);
+      *reinterpret_cast<uint4*>(y + (long long)m * d + e) = o;
+    }
+  }
+}
+
+template <int TEAM, bool ELL>
+cudaError_t launch_team(const void* x, const void* wuT, const void* wd, int M, int d,
+                        const twell_tiles* tiles, int T, int tile_n, int cap,
+                        const twell_hybrid* route, void* y, cudaStream_t s) {
+  constexpr int ROWS = 8 / TEAM;
+  const int grid = (M + ROWS - 1) / ROWS;
+  sparse_fwd_kernel<TEAM, 4, 2, ELL><<<grid, 256, 0, s>>>(
+      reinterpret_cast<const uint16_t*>(x), reinterpret_cast<const uint16_t*>(wuT),
+      reinterpret_cast<const uint16_t*>(wd), M, d,
+      tiles ? reinterpret_cast<const uint16_t*>(tiles->val) : nullptr, tiles ? tiles->idx : nullptr,
+      tiles ? tiles->cnt : nullptr, T, tile_n, cap,
+      route ? reinterpret_cast<const uint16_t*>(route->ell_val) : nullptr,
+      route ? route->ell_col : nullptr, route ? route->ell_nnz : nullptr,
+      route ? route->ell_width : 0, reinterpret_cast<uint16_t*>(y), device_status_ptr());
+  return cudaGetLastError();
+}
+
+template <bool ELL>
+cudaError_t launch_fmt(const void* x, const void* wuT, const void* wd, int M, int d,
+                       const twell_tiles* tiles, int T, int tile_n, int cap,
+                       const twell_hybrid* route, void* y, cudaStream_t s) {
+  if (d <= 1024) return launch_team<1, ELL>(x, wuT, wd, M, d, tiles, T, tile_n, cap, route, y, s);
+  if (d <= 2048) return launch_team<2, ELL>(x, wuT, wd, M, d, tiles, T, tile_n, cap, route, y, s);
+  if (d <= 4096) return launch_team<4, ELL>(x, wuT, wd, M, d, tiles, T, tile_n, cap, route, y, s);
+  return launch_team<8, ELL>(x, wuT, wd, M, d, tiles, T, tile_n, cap, route, y, s);
+}
+
+}  // namespace
+
+cudaError_t launch_sparse_fwd(const void* x, const void* wuT, const void* wd, int M, int d, int f,
+                              const twell_tiles* tiles, int tile_n, int cap,
+                              const twell_hybrid* route, void* y, cudaStream_t s) {
+  if (M == 0) return cudaSuccess;
+  const int T = f / tile_n;
+  if (route) return launch_fmt<true>(x, wuT, wd, M, d, nullptr, T, tile_n, cap, route, y, s);
+  return launch_fmt<false>(x, wuT, wd, M, d, tiles, T, tile_n, cap, nullptr, y, s);
+}
+
+}  // namespace tw

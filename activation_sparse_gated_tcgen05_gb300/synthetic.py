@@ -136,15 +136,23 @@ def make_workload(w: Workload, seed: Optional[int] = None, M: Optional[int] = No
 
 
 def make_integer_gate_inputs(M: int, d: int, f: int, density: float = DENSITY_REF,
-                             seed: int = 0) -> dict:
+                             seed: int = 0, mixed_rows: bool = False) -> dict:
     """Gate inputs whose products and partial sums are small integers, so any
     summation order in fp32 gives the same exact pre-activation.  x in
     {-2..2}, Wg in {-3..3}, constant last feature 1 with a per-neuron integer
-    offset chosen for density ``density``.  Every value is exact in bf16."""
+    offset chosen for density ``density``.  Every value is exact in bf16.
+
+    With ``mixed_rows`` the constant feature of each row is drawn from
+    {0, 1, 2} with probabilities (0.05, 0.9, 0.05): rows at ~50 %, at
+    ``density`` and at almost 0 % density, a non-uniform mix that exercises
+    the hybrid routing."""
     rng = np.random.Generator(np.random.PCG64(seed + 1000))
     x = rng.integers(-2, 3, size=(M, d)).astype(np.float32)
     wg = rng.integers(-3, 4, size=(f, d)).astype(np.float32)
     x[:, d - 1] = 1.0
+    if mixed_rows:
+        x[:, d - 1] = rng.choice(np.array([0.0, 1.0, 2.0], np.float32), size=M,
+                                 p=[0.05, 0.9, 0.05])
     sd = np.sqrt((d - 1) * 2.0 * 4.0)  # Var(x) = 2, Var(w) = 4
     off = np.round(float(z_of_density(density)) * sd)
     # keep the offset exactly representable in bf16 (8 significant bits)
@@ -152,6 +160,20 @@ def make_integer_gate_inputs(M: int, d: int, f: int, density: float = DENSITY_RE
     wg_bits = to_bf16_bits(wg)
     wg_bits[:, d - 1] = off_bits
     return {"x": to_bf16_bits(x), "wgT": wg_bits}
+
+
+def make_exact_gate_inputs(M: int, d: int, f: int, density: float = DENSITY_REF,
+                           seed: int = 0, mixed_rows: bool = False) -> dict:
+    """A full FFN workload whose gate pre-activation is exact in fp32 (see
+    make_integer_gate_inputs), with Wu, Wd, dY drawn as in make_inputs."""
+    out = make_integer_gate_inputs(M, d, f, density, seed, mixed_rows)
+    rng = np.random.Generator(np.random.PCG64(seed + 3000))
+    out["wuT"] = to_bf16_bits(rng.standard_normal((f, d), dtype=np.float32)
+                              * np.float32(1.0 / np.sqrt(d)))
+    out["wd"] = to_bf16_bits(rng.standard_normal((f, d), dtype=np.float32)
+                             * np.float32(1.0 / np.sqrt(f)))
+    out["dy"] = to_bf16_bits(rng.standard_normal((M, d), dtype=np.float32))
+    return out
 
 
 def make_sparse_preact(M: int, f: int, density: float, seed: int = 0,

@@ -1,0 +1,206 @@
+/*
+ * twell.h -- C ABI of the GB300 (sm_103a) activation-sparse gated FFN library.
+ *
+ * The method (three web pages on TwELL; page 2, "Sakana AI and NVIDIA
+ * introduce TwELL with CUDA kernels ...", is the technical one):
+ *   - "¿Cuál es el problema que TwELL resuelve?": the gated feed-forward block
+ *     y = (ReLU(x Wg) * (x Wu)) Wd of a Transformer++, whose ReLU gate output
+ *     is ~99.5 % exact zeros; classic ELLPACK needs a separate dense->sparse
+ *     conversion kernel whose cost cancels the saving.
+ *   - "¿Qué hace distinto a TwELL frente a ELL clásico?": the sparse format is
+ *     built inside the gate matmul's epilogue, with no extra launch and no
+ *     extra global write; columns are cut into tiles of the matmul's tile
+ *     width T_n and nonzeros are packed locally per tile (TwELL).  Inference
+ *     runs up and down projections in one fused kernel that never writes the
+ *     intermediate to global memory.  Training routes rows with too many
+ *     nonzeros to a dense backup, the rest to a compact ELL matrix.
+ *   - "Receta de entrenamiento": ReLU replaces SiLU as the gate activation and
+ *     an L1 term (coefficient 2e-5) is added on the hidden activations.
+ *
+ * Conventions for every entry point
+ *   - All pointers named as tensors are DEVICE pointers the caller allocated;
+ *     the library allocates no device memory and keeps no per-call state.
+ *     Structs (twell_shape, twell_tiles, twell_hybrid) are HOST structs passed
+ *     by pointer; the pointers inside them are device pointers.
+ *   - `stream` is a cudaStream_t (NULL = the legacy default stream).  All work
+ *     is asynchronous on it; no entry point synchronises the host.
+ *   - Layouts (row-major, bf16 = IEEE bfloat16 bits):
+ *       x, dy, y, dx       bf16 [M][d_model]
+ *       wgT, wuT           bf16 [d_ff][d_model]  (= Wg^T, Wu^T; nn.Linear layout)
+ *       wd                 bf16 [d_ff][d_model]  (= Wd, the down projection)
+ *       dwgT, dwuT, dwd    fp32 [d_ff][d_model]  (same layouts as the weights)
+ *     so every neuron's three weight vectors are contiguous d_model-long rows.
+ *   - Argument checks happen before any launch; a failed check returns a
+ *     non-zero status and launches nothing.  Nothing aborts or throws across
+ *     the ABI.  A CUDA launch error maps to TWELL_ERR_CUDA.
+ *   - Errors found on the device (a tile overflow with no route, a pipeline
+ *     wait that timed out) are recorded in a per-device status word that
+ *     twell_get_device_status() reads and clears.
+ *   - Supported shapes: d_model % 64 == 0 and >= 64; d_ff % tile_n == 0;
+ *     d_ff <= 65535; tile_n in {64, 128}; 1 <= tile_cap <= tile_n; M >= 0
+ *     (M == 0 is a no-op); every pointer 16-byte aligned.
+ */
+#ifndef TWELL_H
+#define TWELL_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum twell_status {
+  TWELL_OK = 0,
+  TWELL_ERR_INVALID_ARG = 1,    /* null pointer, negative size, bad enum */
+  TWELL_ERR_UNSUPPORTED = 2,    /* shape outside the supported set above */
+  TWELL_ERR_ALIGNMENT = 3,      /* a pointer is not 16-byte aligned */
+  TWELL_ERR_CAPACITY = 4,       /* a packed tile overflowed with no route */
+  TWELL_ERR_CUDA = 5,           /* a CUDA call or launch failed */
+  TWELL_ERR_DEVICE_TIMEOUT = 6, /* a device-side pipeline wait gave up */
+  TWELL_ERR_WORKSPACE = 7       /* workspace missing or smaller than required */
+} twell_status;
+
+/* Problem shape.  tile_n = T_n, the TwELL tile width (columns of the gate
+ * activation per tile); tile_cap = C, the number of stored slots per tile. */
+typedef struct twell_shape {
+  int32_t M, d_model, d_ff, tile_n, tile_cap;
+} twell_shape;
+
+/* TwELL tiles (device).  T = d_ff / tile_n tiles per row.
+ *   val      bf16 [M][T][C]  gate values g = bf16(ReLU(a)) of the live columns
+ *   idx      u8   [M][T][C]  column of each value inside its tile (0..T_n-1)
+ *   cnt      u8   [M][T]     true number of live columns in the tile (may be > C;
+ *                            then only the first C, in ascending column, are stored)
+ *   row_nnz  i32  [M]        live columns in the row (sum of cnt)
+ * Slots at or past min(cnt, C) hold unspecified bytes. */
+typedef struct twell_tiles {
+  void* val;
+  uint8_t* idx;
+  uint8_t* cnt;
+  int32_t* row_nnz;
+} twell_tiles;
+
+/* Hybrid ELL / dense-backup routing (device).
+ *   ell_val    bf16 [M][ell_width]  live gate values, ascending global column
+ *   ell_col    u16  [M][ell_width]  global column (neuron) of each value
+ *   ell_nnz    i32  [M]             entries used in the row; 0 for routed rows
+ *   dense_rows i32  [M]             routed rows, ascending, first *n_dense valid
+ *   n_dense    i32  [1]             number of routed rows (stays on the device) */
+typedef struct twell_hybrid {
+  void* ell_val;
+  uint16_t* ell_col;
+  int32_t* ell_nnz;
+  int32_t ell_width;
+  int32_t* dense_rows;
+  int32_t* n_dense;
+} twell_hybrid;
+
+/* Gate projection with the TwELL pack fused into its epilogue.
+ * Source: page 2, "¿Qué hace distinto a TwELL frente a ELL clásico?" (format
+ * built in the matmul epilogue; per-T_n-tile local packing) and "Receta de
+ * entrenamiento" (ReLU gate).
+ * Computes a = x Wg (bf16 in, fp32 accumulate on tcgen05 tensor cores), then
+ * for every (row, tile) g = bf16(ReLU(a)), keeps the live (g > 0) columns in
+ * ascending order and writes `out` (all four arrays).  No dense activation is
+ * written to global memory.
+ *   x    bf16 [M][d_model], wgT bf16 [d_ff][d_model]. */
+twell_status twell_pack(const void* x, const void* wgT, const twell_shape* shape,
+                        const twell_tiles* out, void* stream);
+
+/* Pack an already-dense pre-activation a [M][d_ff] into TwELL -- the separate
+ * conversion step of classic ELL (page 2, "¿Cuál es el problema que TwELL
+ * resuelve?").  Same output contract as twell_pack.
+ *   a_dtype: 0 = a is bf16, 1 = a is fp32. */
+twell_status twell_pack_dense(const void* a, int32_t a_dtype, const twell_shape* shape,
+                              const twell_tiles* out, void* stream);
+
+/* Hybrid routing of packed rows (training).  Source: page 2, "¿Qué hace
+ * distinto a TwELL frente a ELL clásico?" (rows with too many nonzeros go to
+ * a dense backup, the rest to a compact ELL matrix).
+ * A row is routed iff some tile has cnt > tile_cap or row_nnz > ell_width.
+ * Routed rows are listed ascending in dense_rows and get ell_nnz = 0; the other
+ * rows are compacted into ELL, ascending global column.  ell_width >= 0.
+ * The count n_dense stays on the device. */
+twell_status hybrid_route(const twell_tiles* in, const twell_shape* shape,
+                          const twell_hybrid* out, void* stream);
+
+/* Bytes of workspace twell_ffn_fwd (training = 0) or twell_ffn_fwd +
+ * twell_ffn_bwd (training = 1) need for this shape and ELL width.  The
+ * workspace is sized for the worst case (every row routed).  Returns 0 for an
+ * invalid shape. */
+size_t twell_workspace_bytes(const twell_shape* shape, int32_t ell_width, int32_t training);
+
+/* Fused sparse up + down projection.  Source: page 2, "¿Qué hace distinto a
+ * TwELL frente a ELL clásico?" (one kernel reads the packed activations and
+ * does both projections; the intermediate never reaches global memory) and,
+ * for routed rows, the dense backup of the same section.
+ * For every row m: y_m = sum over live j of g_mj * (x_m . Wu[:, j]) * Wd[j, :],
+ * fp32 accumulation, y stored as bf16.
+ * Exactly one of `tiles` (inference: reads TwELL directly; a tile with
+ * cnt > C sets TWELL_ERR_CAPACITY in the device status word and its row
+ * uses only the stored entries) and `route` (training: ELL rows by gather,
+ * routed rows by a dense tensor-core gated FFN that recomputes their gate)
+ * is non-NULL.  wgT is read only for routed rows (may be NULL with tiles).
+ * ws/ws_bytes: workspace of at least twell_workspace_bytes(shape, W, 0). */
+twell_status twell_ffn_fwd(const void* x, const void* wgT, const void* wuT, const void* wd,
+                           const twell_shape* shape, const twell_tiles* tiles,
+                           const twell_hybrid* route, void* y, void* ws, size_t ws_bytes,
+                           void* stream);
+
+/* Backward of the sparse FFN with the L1 activation term.  Source: the
+ * training path of page 2, "¿Qué hace distinto a TwELL frente a ELL
+ * clásico?" (hybrid rows) and "Receta de entrenamiento" (L1 with coefficient
+ * l1_coeff on the gate activations).  With loss = sum(y * dy) + l1_coeff *
+ * sum(g) it writes
+ *   dx  = du Wu^T + da Wg^T                     (bf16 [M][d_model])
+ *   dwd = h^T dy, dwuT = du^T x, dwgT = da^T x  (fp32 [d_ff][d_model], overwritten)
+ * where dh = dy Wd^T, du = dh * g, da = (dh * u + l1_coeff) * 1[g > 0], h = g * u,
+ * using only the live entries of ELL rows and a dense tensor-core path for the
+ * routed rows.  The route must come from hybrid_route on the same x and Wg.
+ * The reduction order is fixed, so results are bit-reproducible.
+ * ws/ws_bytes: at least twell_workspace_bytes(shape, W, 1) bytes. */
+twell_status twell_ffn_bwd(const void* x, const void* wgT, const void* wuT, const void* wd,
+                           const void* dy, const twell_shape* shape, const twell_hybrid* route,
+                           float l1_coeff, void* dx, float* dwgT, float* dwuT, float* dwd,
+                           void* ws, size_t ws_bytes, void* stream);
+
+/* The library's own dense gated FFN (the comparator), same definitions, on
+ * tcgen05 tensor cores throughout.  twell_dense_ffn_fwd writes y; with
+ * training = 1 it also keeps what the backward needs (g, u, h) in `ws`, and
+ * twell_dense_ffn_bwd must then get the same ws.  Shape fields tile_n and
+ * tile_cap are ignored. */
+size_t twell_dense_workspace_bytes(const twell_shape* shape, int32_t training);
+twell_status twell_dense_ffn_fwd(const void* x, const void* wgT, const void* wuT, const void* wd,
+                                 const twell_shape* shape, void* y, int32_t training, void* ws,
+                                 size_t ws_bytes, void* stream);
+twell_status twell_dense_ffn_bwd(const void* x, const void* wgT, const void* wuT, const void* wd,
+                                 const void* dy, const twell_shape* shape, float l1_coeff,
+                                 void* dx, float* dwgT, float* dwuT, float* dwd, void* ws,
+                                 size_t ws_bytes, void* stream);
+
+/* The tcgen05 GEMM engine the entry points above are built on, exposed for
+ * testing: C[m][n] = sum_k A(m, k) B(n, k), bf16 in, fp32 accumulate.
+ *   a_mn_major = 0: A is [M][K] (K contiguous); 1: A is [K][M] (M contiguous).
+ *   b_mn_major = 0: B is [N][K];                1: B is [K][N].
+ *   c_dtype: 0 = bf16 [M][N], 1 = fp32 [M][N]; accumulate = 1 adds into an fp32 C.
+ * Requires K % 8 == 0 and, for MN-major operands, M (or N) % 8 == 0. */
+twell_status twell_gemm_bf16(const void* A, const void* B, void* C, int32_t M, int32_t N,
+                             int32_t K, int32_t a_mn_major, int32_t b_mn_major, int32_t c_dtype,
+                             int32_t accumulate, void* stream);
+
+/* Reads and clears the device status word of the current device after
+ * synchronising `stream`.  *out receives TWELL_OK or the first error seen. */
+twell_status twell_get_device_status(void* stream, int32_t* out);
+
+/* Human-readable name of a status code (static string). */
+const char* twell_status_string(int32_t status);
+
+/* Number of SMs the library schedules persistent kernels over (0 if no device). */
+int32_t twell_num_sms(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TWELL_H */

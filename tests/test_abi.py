@@ -1,0 +1,78 @@
+"""The C-ABI library loads, exports every entry point include/twell.h declares,
+and rejects bad arguments on the host before any launch (no GPU needed)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from activation_sparse_gated_tcgen05_gb300 import _build, twell
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include",
+                      "twell.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    _build.build()
+    return twell.load()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    names = re.findall(r"^\s*(?:const\s+)?[A-Za-z_][A-Za-z0-9_]*\s*\**\s+([a-z_][a-z0-9_]*)\s*\(",
+                       text, flags=re.M)
+    return sorted(set(names))
+
+
+def test_header_lists_the_boundary():
+    names = declared_functions()
+    for n in ("twell_pack", "twell_ffn_fwd", "twell_ffn_bwd", "hybrid_route"):
+        assert n in names
+    assert set(names) == set(twell.EXPORTS)
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for n in declared_functions():
+        assert hasattr(lib, n), n
+
+
+def test_status_strings(lib):
+    for code in range(8):
+        s = lib.twell_status_string(code)
+        assert s and s != b"unknown status"
+    assert lib.twell_status_string(99) == b"unknown status"
+
+
+def test_host_validation_before_launch(lib):
+    s = twell.make_shape(256, 256, 1024, 64, 16)
+    t = twell.Tiles(16, 16, 16, 16)
+    # null inputs
+    assert lib.twell_pack(None, None, ctypes.byref(s), ctypes.byref(t), None) == 1
+    # misaligned input
+    assert lib.twell_pack(8, 16, ctypes.byref(s), ctypes.byref(t), None) == 3
+    # unsupported shapes
+    for bad in (twell.make_shape(256, 100, 1024, 64, 16), twell.make_shape(256, 256, 1000, 64, 16),
+                twell.make_shape(256, 256, 1024, 32, 16), twell.make_shape(256, 256, 1024, 64, 0),
+                twell.make_shape(256, 256, 1024, 64, 65)):
+        assert lib.twell_pack(16, 16, ctypes.byref(bad), ctypes.byref(t), None) == 2
+    assert lib.twell_pack(16, 16, ctypes.byref(twell.make_shape(-1, 256, 1024, 64, 16)),
+                          ctypes.byref(t), None) == 1
+    # exactly one of tiles / route
+    assert lib.twell_ffn_fwd(16, 16, 16, 16, ctypes.byref(s), None, None, 16, None, 0, None) == 1
+    # workspace too small
+    h = twell.Hybrid(16, 16, 16, 8, 16, 16)
+    assert lib.twell_ffn_fwd(16, 16, 16, 16, ctypes.byref(s), None, ctypes.byref(h), 16, 16, 8,
+                             None) == 7
+    assert lib.twell_pack_dense(16, 3, ctypes.byref(s), ctypes.byref(t), None) == 1
+    assert lib.twell_gemm_bf16(16, 16, 16, 10, 12, 16, 0, 0, 0, 0, None) == 2
+
+
+def test_workspace_sizes(lib):
+    s = twell.make_shape(16384, 1024, 4096, 128, 32)
+    inf = twell.twell_workspace_bytes(s, 30, False)
+    tr = twell.twell_workspace_bytes(s, 30, True)
+    assert 0 < inf < tr
+    assert twell.twell_workspace_bytes(twell.make_shape(16, 100, 1024, 64, 16), 4, True) == 0
+    assert twell.twell_dense_workspace_bytes(s, True) >= 5 * 16384 * 4096 * 2

@@ -1,0 +1,200 @@
+"""Sparse gated FFN forward / backward and the dense comparator on the GPU,
+through the C ABI, against the fp64 CPU oracle on identical seeded inputs.
+
+Tolerance (bf16 in, fp32 accumulate): relative Frobenius error <= 5e-3 and
+max |err| <= 2e-2 * rms(ref) on every float output, plus the bf16 storage
+rounding (2^-8 |ref|) for outputs stored as bf16; integer outputs exact."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from activation_sparse_gated_tcgen05_gb300 import synthetic, twell
+
+from helpers import (assert_close, bwd_allowance, dense_intermediate_allowance, dev_bf16,
+                     fwd_allowance, to_np)
+
+pytestmark = pytest.mark.gpu
+LAM = 2e-5
+
+
+class Run:
+    """Inputs on the device plus the library calls of one step."""
+
+    def __init__(self, M, d, f, tile_n, cap, density=0.005, sigma=None, seed=0, exact=False,
+                 mixed=False):
+        if exact:
+            self.w = synthetic.make_exact_gate_inputs(M, d, f, density=density, seed=seed,
+                                                      mixed_rows=mixed)
+        else:
+            self.w = synthetic.make_inputs(M, d, f, density=density, seed=seed,
+                                           lognormal_sigma=sigma)
+        self.shape = twell.make_shape(M, d, f, tile_n, cap)
+        self.x, self.wg, self.wu, self.wd, self.dy = (
+            dev_bf16(self.w[k]) for k in ("x", "wgT", "wuT", "wd", "dy"))
+        self.M, self.d, self.f = M, d, f
+
+    def pack(self):
+        t = twell.alloc_tiles(self.shape)
+        twell.twell_pack(self.x, self.wg, self.shape, t)
+        return t
+
+    def route(self, tiles, W):
+        h = twell.alloc_hybrid(self.shape, W)
+        twell.hybrid_route(tiles, self.shape, h)
+        return h
+
+    def fwd(self, tiles=None, route=None, W=0):
+        y = torch.empty(self.M, self.d, dtype=torch.bfloat16, device="cuda")
+        ws = None
+        if route is not None:
+            ws = torch.empty(twell.twell_workspace_bytes(self.shape, W, False), dtype=torch.uint8,
+                             device="cuda")
+        twell.twell_ffn_fwd(self.x, self.wg, self.wu, self.wd, self.shape, y, tiles=tiles,
+                            route=route, ws=ws)
+        return y
+
+    def bwd(self, route, W):
+        ws = torch.empty(twell.twell_workspace_bytes(self.shape, W, True), dtype=torch.uint8,
+                         device="cuda")
+        dx = torch.empty(self.M, self.d, dtype=torch.bfloat16, device="cuda")
+        dws = [torch.full((self.f, self.d), float("nan"), device="cuda") for _ in range(3)]
+        twell.twell_ffn_bwd(self.x, self.wg, self.wu, self.wd, self.dy, self.shape, route, LAM,
+                            dx, *dws, ws)
+        return dx, dws
+
+
+def _quantile_width(tiles, shape, q):
+    nnz = twell.tiles_view(tiles, shape)[3].cpu().numpy()
+    return int(np.sort(nnz)[min(len(nnz) - 1, int(q * len(nnz)))])
+
+
+def test_tiny_inference_forward_from_twell():
+    wl = synthetic.WORKLOADS["tiny_fwd"]
+    r = Run(wl.M, wl.d_model, wl.d_ff, wl.tile_n, wl.tile_cap)
+    t = r.pack()
+    y = r.fwd(tiles=t)
+    torch.cuda.synchronize()
+    assert twell.twell_get_device_status() == 0
+    ref = oracle.ffn_fwd_dense(r.w["x"], r.w["wgT"], r.w["wuT"], r.w["wd"])
+    assert_close(to_np(y), ref, "y", out_bf16=True, allowance=fwd_allowance(r.w))
+
+
+def test_tiny_inference_forward_exact_gate():
+    wl = synthetic.WORKLOADS["tiny_fwd"]
+    r = Run(wl.M, wl.d_model, wl.d_ff, wl.tile_n, wl.tile_cap, exact=True)
+    t = r.pack()
+    y = r.fwd(tiles=t)
+    torch.cuda.synchronize()
+    assert twell.twell_get_device_status() == 0
+    ref = oracle.ffn_fwd_dense(r.w["x"], r.w["wgT"], r.w["wuT"], r.w["wd"])
+    assert_close(to_np(y), ref, "y", out_bf16=True)
+
+
+def _check_step(r, y, dx, dwg, dwu, dwd, allow, dense_intermediates=False):
+    """Compare one fwd + bwd step with the oracle.  allow: add the effect of
+    gate rounding decisions (real-valued gate inputs); dense_intermediates:
+    add the bf16 rounding of h, u, du, da stored between dense GEMMs."""
+    w = r.w
+    y_ref = oracle.ffn_fwd_dense(w["x"], w["wgT"], w["wuT"], w["wd"])
+    ref = oracle.ffn_bwd_dense(w["x"], w["wgT"], w["wuT"], w["wd"], w["dy"], LAM)
+    extra = {}
+    if allow:
+        extra = dict(bwd_allowance(w, LAM), y=fwd_allowance(w))
+    if dense_intermediates:
+        for k, v in dense_intermediate_allowance(w, LAM).items():
+            extra[k] = extra.get(k, 0.0) + v
+    assert_close(to_np(y), y_ref, "y", out_bf16=True, allowance=extra.get("y"))
+    assert_close(to_np(dx), ref["dx"], "dx", out_bf16=True, allowance=extra.get("dx"))
+    assert_close(to_np(dwg), ref["dwgT"], "dwgT", allowance=extra.get("dwgT"))
+    assert_close(to_np(dwu), ref["dwuT"], "dwuT", allowance=extra.get("dwuT"))
+    assert_close(to_np(dwd), ref["dwd"], "dwd", allowance=extra.get("dwd"))
+
+
+@pytest.mark.parametrize("q", [0.0, 0.5, 0.9, 0.97, 1.0])
+@pytest.mark.parametrize("tile", [(64, 16), (128, 8)])
+def test_hybrid_step_exact_gate(q, tile):
+    # mixed per-row densities (~50 %, 2 %, ~0 %): q picks the ELL width, so the
+    # split between ELL rows and the dense tensor-core backup varies
+    r = Run(300, 256, 1024, tile[0], tile[1], density=0.02, seed=1, exact=True, mixed=True)
+    t = r.pack()
+    W = _quantile_width(t, r.shape, q) if q > 0 else 0
+    h = r.route(t, W)
+    y = r.fwd(route=h, W=W)
+    dx, (dwg, dwu, dwd) = r.bwd(h, W)
+    torch.cuda.synchronize()
+    assert twell.twell_get_device_status() == 0
+    _check_step(r, y, dx, dwg, dwu, dwd, allow=False)
+
+
+@pytest.mark.parametrize("q", [0.0, 0.9, 1.0])
+def test_hybrid_step_gaussian_inputs(q):
+    # lognormal per-row density; gate decisions near a bf16 rounding boundary
+    # may go either way, and their effect is bounded from the oracle's data
+    r = Run(256, 256, 1024, 64, 16, density=0.01, sigma=1.0, seed=1)
+    t = r.pack()
+    W = _quantile_width(t, r.shape, q) if q > 0 else 0
+    h = r.route(t, W)
+    y = r.fwd(route=h, W=W)
+    dx, (dwg, dwu, dwd) = r.bwd(h, W)
+    torch.cuda.synchronize()
+    assert twell.twell_get_device_status() == 0
+    _check_step(r, y, dx, dwg, dwu, dwd, allow=True)
+
+
+def test_backward_is_deterministic():
+    r = Run(384, 256, 1024, 64, 16, density=0.02, seed=2, exact=True, mixed=True)
+    t = r.pack()
+    W = _quantile_width(t, r.shape, 0.8)
+    h = r.route(t, W)
+    a = r.bwd(h, W)
+    b = r.bwd(h, W)
+    torch.cuda.synchronize()
+    assert torch.equal(a[0], b[0])
+    for u, v in zip(a[1], b[1]):
+        assert torch.equal(u, v)
+
+
+@pytest.mark.parametrize("M", [300, 1])
+def test_dense_comparator_matches_oracle(M):
+    r = Run(M, 256, 1024, 64, 16, density=0.05, seed=3, exact=True)
+    ws = torch.empty(twell.twell_dense_workspace_bytes(r.shape, True), dtype=torch.uint8,
+                     device="cuda")
+    y = torch.empty(r.M, r.d, dtype=torch.bfloat16, device="cuda")
+    twell.twell_dense_ffn_fwd(r.x, r.wg, r.wu, r.wd, r.shape, y, True, ws)
+    dx = torch.empty_like(y)
+    dws = [torch.empty(r.f, r.d, device="cuda") for _ in range(3)]
+    twell.twell_dense_ffn_bwd(r.x, r.wg, r.wu, r.wd, r.dy, r.shape, LAM, dx, *dws, ws)
+    torch.cuda.synchronize()
+    _check_step(r, y, dx, *dws, allow=False, dense_intermediates=True)
+
+
+def test_capacity_overflow_is_reported_without_route():
+    r = Run(64, 256, 1024, 64, 1, density=0.2, seed=4)
+    t = r.pack()
+    r.fwd(tiles=t)
+    torch.cuda.synchronize()
+    assert twell.twell_get_device_status() == 4  # TWELL_ERR_CAPACITY
+    assert twell.twell_get_device_status() == 0  # reading clears it
+
+
+def test_empty_batch_is_a_noop():
+    r = Run(1, 256, 1024, 64, 16)
+    shape = twell.make_shape(0, 256, 1024, 64, 16)
+    t = twell.alloc_tiles(shape)
+    twell.twell_pack(r.x, r.wg, shape, t)
+    y = torch.empty(1, 256, dtype=torch.bfloat16, device="cuda")
+    twell.twell_ffn_fwd(r.x, r.wg, r.wu, r.wd, shape, y, tiles=t)
+    torch.cuda.synchronize()
+    assert twell.twell_get_device_status() == 0
+
+
+@pytest.mark.parametrize("M", [1, 16, 64])
+def test_small_batch_forward(M):
+    r = Run(M, 512, 2048, 128, 32, density=0.02, seed=M, exact=True)
+    t = r.pack()
+    y = r.fwd(tiles=t)
+    torch.cuda.synchronize()
+    w = r.w
+    assert_close(to_np(y), oracle.ffn_fwd_dense(w["x"], w["wgT"], w["wuT"], w["wd"]), "y",
+                 out_bf16=True)
