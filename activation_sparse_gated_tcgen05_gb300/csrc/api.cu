@@ -1,7 +1,11 @@
 // api.cu -- the library's C ABI: argument checks, workspace layout and the
 // launch sequence of every entry point declared in twell.h.
+#include <atomic>
 #include <cstring>
+#include <map>
 #include <mutex>
+#include <string>
+#include <vector>
 
 #include "gemm_tc.cuh"
 #include "internal.h"
@@ -21,6 +25,51 @@ int current_device() {
 }
 
 }  // namespace
+
+namespace {
+std::atomic<unsigned long long> g_launches{0};
+}
+
+void count_launch(int n) { g_launches.fetch_add((unsigned long long)n, std::memory_order_relaxed); }
+
+// ---------------------------------------------------------------- profiling
+namespace {
+struct ProfRecord {
+  std::string name;
+  cudaEvent_t start, stop;
+};
+struct ProfEntry {
+  std::string name;
+  int launches;
+  double total_ms;
+};
+std::mutex g_prof_mu;
+std::atomic<bool> g_prof_on{false};
+std::string g_prof_filter;
+std::vector<ProfRecord> g_prof_records;
+std::vector<ProfEntry> g_prof_report;
+}  // namespace
+
+ProfScope::ProfScope(const char* name, cudaStream_t s) : slot(-1), stream(s) {
+  if (!g_prof_on.load(std::memory_order_relaxed)) return;
+  std::lock_guard<std::mutex> lock(g_prof_mu);
+  if (g_prof_filter != "*" && g_prof_filter != name) return;
+  ProfRecord r{name, nullptr, nullptr};
+  if (cudaEventCreate(&r.start) != cudaSuccess) return;
+  if (cudaEventCreate(&r.stop) != cudaSuccess) {
+    cudaEventDestroy(r.start);
+    return;
+  }
+  cudaEventRecord(r.start, s);
+  slot = (int)g_prof_records.size();
+  g_prof_records.push_back(r);
+}
+
+ProfScope::~ProfScope() {
+  if (slot < 0) return;
+  std::lock_guard<std::mutex> lock(g_prof_mu);
+  cudaEventRecord(g_prof_records[slot].stop, stream);
+}
 
 int num_sms() {
   static int cache[kMaxDevices] = {0};
@@ -295,6 +344,54 @@ const char* twell_status_string(int32_t status) {
 }
 
 int32_t twell_num_sms(void) { return num_sms(); }
+
+uint64_t twell_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
+
+twell_status twell_profile_begin(const char* kernel) {
+  std::lock_guard<std::mutex> lock(g_prof_mu);
+  for (auto& r : g_prof_records) {
+    cudaEventDestroy(r.start);
+    cudaEventDestroy(r.stop);
+  }
+  g_prof_records.clear();
+  g_prof_filter = kernel ? kernel : "";
+  g_prof_on.store(!g_prof_filter.empty());
+  return TWELL_OK;
+}
+
+int32_t twell_profile_end(void) {
+  std::lock_guard<std::mutex> lock(g_prof_mu);
+  g_prof_on.store(false);
+  std::map<std::string, ProfEntry> agg;
+  int bad = 0;
+  for (auto& r : g_prof_records) {
+    float ms = 0.f;
+    if (cudaEventSynchronize(r.stop) != cudaSuccess ||
+        cudaEventElapsedTime(&ms, r.start, r.stop) != cudaSuccess)
+      ++bad;
+    ProfEntry& e = agg[r.name];
+    e.name = r.name;
+    e.launches += 1;
+    e.total_ms += ms;
+    cudaEventDestroy(r.start);
+    cudaEventDestroy(r.stop);
+  }
+  g_prof_records.clear();
+  g_prof_report.clear();
+  for (auto& kv : agg) g_prof_report.push_back(kv.second);
+  return bad ? -1 : (int32_t)g_prof_report.size();
+}
+
+twell_status twell_profile_entry(int32_t i, const char** name, int32_t* launches,
+                                 double* total_ms) {
+  std::lock_guard<std::mutex> lock(g_prof_mu);
+  if (i < 0 || i >= (int32_t)g_prof_report.size() || !name || !launches || !total_ms)
+    return TWELL_ERR_INVALID_ARG;
+  *name = g_prof_report[i].name.c_str();
+  *launches = g_prof_report[i].launches;
+  *total_ms = g_prof_report[i].total_ms;
+  return TWELL_OK;
+}
 
 twell_status twell_get_device_status(void* stream, int32_t* out) {
   if (!out) return TWELL_ERR_INVALID_ARG;

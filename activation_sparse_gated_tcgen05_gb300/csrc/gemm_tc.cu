@@ -41,8 +41,8 @@ bool make_map(CUtensorMap* m, const Mat& a, uint32_t box_inner, uint32_t box_out
 }
 
 template <bool A_MN, bool B_MN, int EPI>
-cudaError_t launch_t(const Mat& A, const Mat& B, const Mat* B2, const GemmParams& p,
-                     cudaStream_t s) {
+cudaError_t launch_t(const char* name, const Mat& A, const Mat& B, const Mat* B2,
+                     const GemmParams& p, cudaStream_t s) {
   CUtensorMap ta, tb, tb2;
   // A: K-major [M][K] -> box {64 (K), 128 rows}; MN-major [K][M] -> box {64 (M), 64 (K)}
   if (!make_map(&ta, A, 64, A_MN ? 64 : kBM)) return cudaErrorInvalidValue;
@@ -60,7 +60,11 @@ cudaError_t launch_t(const Mat& A, const Mat& B, const Mat* B2, const GemmParams
   const long long tiles = m_tiles * p.n_tiles;
   if (tiles <= 0) return cudaSuccess;
   const int grid = (int)(tiles < num_sms() ? tiles : num_sms());
-  kern<<<grid, kGemmThreads, kGemmSmem, s>>>(ta, tb, tb2, p);
+  {
+    ProfScope prof(name, s);
+    kern<<<grid, kGemmThreads, kGemmSmem, s>>>(ta, tb, tb2, p);
+  }
+  count_launch();
   return cudaGetLastError();
 }
 
@@ -69,13 +73,13 @@ cudaError_t launch_t(const Mat& A, const Mat& B, const Mat* B2, const GemmParams
 cudaError_t gemm_launch(GemmKind kind, const Mat& A, const Mat& B, const Mat* B2,
                         const GemmParams& p, cudaStream_t s) {
   switch (kind) {
-    case GK_STORE_KK: return launch_t<false, false, EPI_STORE>(A, B, B2, p, s);
-    case GK_STORE_MK: return launch_t<true, false, EPI_STORE>(A, B, B2, p, s);
-    case GK_STORE_KM: return launch_t<false, true, EPI_STORE>(A, B, B2, p, s);
-    case GK_STORE_MM: return launch_t<true, true, EPI_STORE>(A, B, B2, p, s);
-    case GK_PACK: return launch_t<false, false, EPI_PACK>(A, B, B2, p, s);
-    case GK_GATED: return launch_t<false, false, EPI_GATED>(A, B, B2, p, s);
-    case GK_BWD_GATE: return launch_t<false, false, EPI_BWD_GATE>(A, B, B2, p, s);
+    case GK_STORE_KK: return launch_t<false, false, EPI_STORE>("gemm_store_kk", A, B, B2, p, s);
+    case GK_STORE_MK: return launch_t<true, false, EPI_STORE>("gemm_store_mk", A, B, B2, p, s);
+    case GK_STORE_KM: return launch_t<false, true, EPI_STORE>("gemm_store_km", A, B, B2, p, s);
+    case GK_STORE_MM: return launch_t<true, true, EPI_STORE>("gemm_store_mm", A, B, B2, p, s);
+    case GK_PACK: return launch_t<false, false, EPI_PACK>("gemm_gate_pack", A, B, B2, p, s);
+    case GK_GATED: return launch_t<false, false, EPI_GATED>("gemm_gated", A, B, B2, p, s);
+    case GK_BWD_GATE: return launch_t<false, false, EPI_BWD_GATE>("gemm_dgate", A, B, B2, p, s);
   }
   return cudaErrorInvalidValue;
 }

@@ -28,6 +28,16 @@ enum GemmKind {
 };
 
 int num_sms();
+void count_launch(int n = 1);  // kernels launched by the library (process-wide)
+
+// While profiling is on for `name` (or "*"), brackets one kernel launch with
+// CUDA events recorded on its stream; otherwise does nothing.
+struct ProfScope {
+  ProfScope(const char* name, cudaStream_t s);
+  ~ProfScope();
+  int slot;
+  cudaStream_t stream;
+};
 int* device_status_ptr();  // per-device status word (device address)
 
 // Launch the persistent GEMM.  A is the M-side operand, B (and B2 for a

@@ -202,21 +202,34 @@ cudaError_t launch_pack_dense(const void* a, int a_f32, int M, int f, int tile_n
   auto* val = reinterpret_cast<uint16_t*>(out.val);
   if (tile_n == 128) {
     if (a_f32)
-      pack_dense_kernel<4, true><<<grid, kWarpsPerBlock * 32, 0, s>>>(a, M, f, T, cap, val, out.idx,
-                                                                      out.cnt, out.row_nnz);
+      {
+        ProfScope prof("pack_dense", s);
+        pack_dense_kernel<4, true><<<grid, kWarpsPerBlock * 32, 0, s>>>(a, M, f, T, cap, val, out.idx,
+                                                                        out.cnt, out.row_nnz);
+      }
     else
-      pack_dense_kernel<4, false><<<grid, kWarpsPerBlock * 32, 0, s>>>(a, M, f, T, cap, val,
-                                                                       out.idx, out.cnt,
-                                                                       out.row_nnz);
+      {
+        ProfScope prof("pack_dense", s);
+        pack_dense_kernel<4, false><<<grid, kWarpsPerBlock * 32, 0, s>>>(a, M, f, T, cap, val,
+                                                                         out.idx, out.cnt,
+                                                                         out.row_nnz);
+      }
   } else {
     if (a_f32)
-      pack_dense_kernel<2, true><<<grid, kWarpsPerBlock * 32, 0, s>>>(a, M, f, T, cap, val, out.idx,
-                                                                      out.cnt, out.row_nnz);
+      {
+        ProfScope prof("pack_dense", s);
+        pack_dense_kernel<2, true><<<grid, kWarpsPerBlock * 32, 0, s>>>(a, M, f, T, cap, val, out.idx,
+                                                                        out.cnt, out.row_nnz);
+      }
     else
-      pack_dense_kernel<2, false><<<grid, kWarpsPerBlock * 32, 0, s>>>(a, M, f, T, cap, val,
-                                                                       out.idx, out.cnt,
-                                                                       out.row_nnz);
+      {
+        ProfScope prof("pack_dense", s);
+        pack_dense_kernel<2, false><<<grid, kWarpsPerBlock * 32, 0, s>>>(a, M, f, T, cap, val,
+                                                                         out.idx, out.cnt,
+                                                                         out.row_nnz);
+      }
   }
+  count_launch();
   return cudaGetLastError();
 }
 
@@ -225,21 +238,33 @@ cudaError_t launch_route(const twell_tiles& in, int M, int f, int tile_n, int ca
   if (M == 0) return cudaMemsetAsync(out.n_dense, 0, sizeof(int), s);
   const int T = f / tile_n;
   const int grid = (M + kWarpsPerBlock - 1) / kWarpsPerBlock;
-  route_rows_kernel<<<grid, kWarpsPerBlock * 32, 0, s>>>(
-      reinterpret_cast<const uint16_t*>(in.val), in.idx, in.cnt, in.row_nnz, M, T, tile_n, cap,
-      out.ell_width, reinterpret_cast<uint16_t*>(out.ell_val), out.ell_col, out.ell_nnz, flags);
+  {
+    ProfScope prof("route_rows", s);
+    route_rows_kernel<<<grid, kWarpsPerBlock * 32, 0, s>>>(
+        reinterpret_cast<const uint16_t*>(in.val), in.idx, in.cnt, in.row_nnz, M, T, tile_n, cap,
+        out.ell_width, reinterpret_cast<uint16_t*>(out.ell_val), out.ell_col, out.ell_nnz, flags);
+  }
+  count_launch();
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  route_list_kernel<<<1, kListThreads, 0, s>>>(flags, M, out.dense_rows, out.n_dense);
+  {
+    ProfScope prof("route_list", s);
+    route_list_kernel<<<1, kListThreads, 0, s>>>(flags, M, out.dense_rows, out.n_dense);
+  }
+  count_launch();
   return cudaGetLastError();
 }
 
 cudaError_t launch_gather_rows(const void* src, int M, int d, const int* rows, const int* n_rows,
                                void* dst, int dst_rows, cudaStream_t s) {
   if (dst_rows == 0) return cudaSuccess;
-  gather_rows_kernel<<<blocks_for(dst_rows), kWarpsPerBlock * 32, 0, s>>>(
-      reinterpret_cast<const uint16_t*>(src), M, d, rows, n_rows, reinterpret_cast<uint16_t*>(dst),
-      dst_rows);
+  {
+    ProfScope prof("gather_rows", s);
+    gather_rows_kernel<<<blocks_for(dst_rows), kWarpsPerBlock * 32, 0, s>>>(
+        reinterpret_cast<const uint16_t*>(src), M, d, rows, n_rows, reinterpret_cast<uint16_t*>(dst),
+        dst_rows);
+  }
+  count_launch();
   return cudaGetLastError();
 }
 

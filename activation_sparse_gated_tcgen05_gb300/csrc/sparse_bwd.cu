@@ -321,12 +321,16 @@ cudaError_t rows_team(const void* x, const void* dy, const void* wgT, const void
                       const void* wd, int M, int d, const twell_hybrid& r, const int* slot_pos,
                       float lambda, float4* csc_vals, void* dx, cudaStream_t s) {
   constexpr int ROWS = 8 / TEAM;
-  bwd_rows_kernel<TEAM, 4, 2><<<(M + ROWS - 1) / ROWS, 256, 0, s>>>(
-      reinterpret_cast<const uint16_t*>(x), reinterpret_cast<const uint16_t*>(dy),
-      reinterpret_cast<const uint16_t*>(wgT), reinterpret_cast<const uint16_t*>(wuT),
-      reinterpret_cast<const uint16_t*>(wd), M, d, reinterpret_cast<const uint16_t*>(r.ell_val),
-      r.ell_col, r.ell_nnz, r.ell_width, slot_pos, lambda, csc_vals,
-      reinterpret_cast<uint16_t*>(dx));
+  {
+    ProfScope prof("bwd_rows", s);
+    bwd_rows_kernel<TEAM, 4, 2><<<(M + ROWS - 1) / ROWS, 256, 0, s>>>(
+        reinterpret_cast<const uint16_t*>(x), reinterpret_cast<const uint16_t*>(dy),
+        reinterpret_cast<const uint16_t*>(wgT), reinterpret_cast<const uint16_t*>(wuT),
+        reinterpret_cast<const uint16_t*>(wd), M, d, reinterpret_cast<const uint16_t*>(r.ell_val),
+        r.ell_col, r.ell_nnz, r.ell_width, slot_pos, lambda, csc_vals,
+        reinterpret_cast<uint16_t*>(dx));
+  }
+  count_launch();
   return cudaGetLastError();
 }
 
@@ -335,9 +339,13 @@ cudaError_t neurons_team(const void* x, const void* dy, int d, int f, const int*
                          const int* csc_row, const float4* csc_vals, float* dwgT, float* dwuT,
                          float* dwd, cudaStream_t s) {
   constexpr int ROWS = 8 / TEAM;
-  bwd_neurons_kernel<TEAM, 4, 2><<<(f + ROWS - 1) / ROWS, 256, 0, s>>>(
-      reinterpret_cast<const uint16_t*>(x), reinterpret_cast<const uint16_t*>(dy), d, f, csc_ptr,
-      csc_row, csc_vals, dwgT, dwuT, dwd);
+  {
+    ProfScope prof("bwd_neurons", s);
+    bwd_neurons_kernel<TEAM, 4, 2><<<(f + ROWS - 1) / ROWS, 256, 0, s>>>(
+        reinterpret_cast<const uint16_t*>(x), reinterpret_cast<const uint16_t*>(dy), d, f, csc_ptr,
+        csc_row, csc_vals, dwgT, dwuT, dwd);
+  }
+  count_launch();
   return cudaGetLastError();
 }
 
@@ -353,17 +361,33 @@ cudaError_t launch_csc_build(const twell_hybrid& r, int M, int f, int* blk_count
   cudaError_t e = cudaMemsetAsync(mask, 0, sizeof(unsigned) * (size_t)NB * f, s);
   if (e != cudaSuccess) return e;
   if (M > 0) {
-    csc_mark_kernel<<<(M + kWarps - 1) / kWarps, kWarps * 32, 0, s>>>(r.ell_col, r.ell_nnz, M,
-                                                                      r.ell_width, f, mask);
+    {
+      ProfScope prof("csc_mark", s);
+      csc_mark_kernel<<<(M + kWarps - 1) / kWarps, kWarps * 32, 0, s>>>(r.ell_col, r.ell_nnz, M,
+                                                                        r.ell_width, f, mask);
+    }
+    count_launch();
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
-  csc_colscan_kernel<<<(f + 255) / 256, 256, 0, s>>>(mask, NB, f, off, tot);
+  {
+    ProfScope prof("csc_colscan", s);
+    csc_colscan_kernel<<<(f + 255) / 256, 256, 0, s>>>(mask, NB, f, off, tot);
+  }
+  count_launch();
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  csc_ptr_kernel<<<1, 1024, 0, s>>>(tot, f, csc_ptr);
+  {
+    ProfScope prof("csc_ptr", s);
+    csc_ptr_kernel<<<1, 1024, 0, s>>>(tot, f, csc_ptr);
+  }
+  count_launch();
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   if (M > 0) {
-    csc_place_kernel<<<(M + kWarps - 1) / kWarps, kWarps * 32, 0, s>>>(
-        r.ell_col, r.ell_nnz, M, r.ell_width, f, mask, off, csc_ptr, csc_row, slot_pos);
+    {
+      ProfScope prof("csc_place", s);
+      csc_place_kernel<<<(M + kWarps - 1) / kWarps, kWarps * 32, 0, s>>>(
+          r.ell_col, r.ell_nnz, M, r.ell_width, f, mask, off, csc_ptr, csc_row, slot_pos);
+    }
+    count_launch();
     e = cudaGetLastError();
   }
   return e;

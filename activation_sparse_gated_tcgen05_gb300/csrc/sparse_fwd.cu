@@ -188,14 +188,18 @@ cudaError_t launch_team(const void* x, const void* wuT, const void* wd, int M, i
                         const twell_hybrid* route, void* y, cudaStream_t s) {
   constexpr int ROWS = 8 / TEAM;
   const int grid = (M + ROWS - 1) / ROWS;
-  sparse_fwd_kernel<TEAM, 4, 2, ELL><<<grid, 256, 0, s>>>(
-      reinterpret_cast<const uint16_t*>(x), reinterpret_cast<const uint16_t*>(wuT),
-      reinterpret_cast<const uint16_t*>(wd), M, d,
-      tiles ? reinterpret_cast<const uint16_t*>(tiles->val) : nullptr, tiles ? tiles->idx : nullptr,
-      tiles ? tiles->cnt : nullptr, T, tile_n, cap,
-      route ? reinterpret_cast<const uint16_t*>(route->ell_val) : nullptr,
-      route ? route->ell_col : nullptr, route ? route->ell_nnz : nullptr,
-      route ? route->ell_width : 0, reinterpret_cast<uint16_t*>(y), device_status_ptr());
+  {
+    ProfScope prof("sparse_fwd", s);
+    sparse_fwd_kernel<TEAM, 4, 2, ELL><<<grid, 256, 0, s>>>(
+        reinterpret_cast<const uint16_t*>(x), reinterpret_cast<const uint16_t*>(wuT),
+        reinterpret_cast<const uint16_t*>(wd), M, d,
+        tiles ? reinterpret_cast<const uint16_t*>(tiles->val) : nullptr, tiles ? tiles->idx : nullptr,
+        tiles ? tiles->cnt : nullptr, T, tile_n, cap,
+        route ? reinterpret_cast<const uint16_t*>(route->ell_val) : nullptr,
+        route ? route->ell_col : nullptr, route ? route->ell_nnz : nullptr,
+        route ? route->ell_width : 0, reinterpret_cast<uint16_t*>(y), device_status_ptr());
+  }
+  count_launch();
   return cudaGetLastError();
 }
 

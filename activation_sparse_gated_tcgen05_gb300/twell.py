@@ -31,6 +31,7 @@ EXPORTS = (
     "twell_pack", "twell_pack_dense", "hybrid_route", "twell_workspace_bytes", "twell_ffn_fwd",
     "twell_ffn_bwd", "twell_dense_workspace_bytes", "twell_dense_ffn_fwd", "twell_dense_ffn_bwd",
     "twell_gemm_bf16", "twell_get_device_status", "twell_status_string", "twell_num_sms",
+    "twell_launch_count", "twell_profile_begin", "twell_profile_end", "twell_profile_entry",
 )
 
 
@@ -86,6 +87,11 @@ def load():
         "twell_get_device_status": (I32, [P, ctypes.POINTER(I32)]),
         "twell_status_string": (ctypes.c_char_p, [I32]),
         "twell_num_sms": (I32, []),
+        "twell_launch_count": (ctypes.c_uint64, []),
+        "twell_profile_begin": (I32, [ctypes.c_char_p]),
+        "twell_profile_end": (I32, []),
+        "twell_profile_entry": (I32, [I32, ctypes.POINTER(ctypes.c_char_p), ctypes.POINTER(I32),
+                                      ctypes.POINTER(ctypes.c_double)]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -265,3 +271,27 @@ def twell_get_device_status(stream=None) -> int:
 
 def twell_num_sms() -> int:
     return int(load().twell_num_sms())
+
+
+def twell_launch_count() -> int:
+    return int(load().twell_launch_count())
+
+
+def twell_profile_begin(kernel: Optional[str]):
+    _check("twell_profile_begin",
+           load().twell_profile_begin(kernel.encode() if kernel else None))
+
+
+def twell_profile_end() -> dict:
+    """Stop profiling; {family: (launches, total_ms)} of the recorded launches."""
+    lib = load()
+    n = lib.twell_profile_end()
+    if n < 0:
+        raise TwellError("twell_profile_end", 5)
+    out = {}
+    for i in range(n):
+        name, cnt, ms = ctypes.c_char_p(), ctypes.c_int32(), ctypes.c_double()
+        _check("twell_profile_entry", lib.twell_profile_entry(i, ctypes.byref(name),
+                                                              ctypes.byref(cnt), ctypes.byref(ms)))
+        out[name.value.decode()] = (int(cnt.value), float(ms.value))
+    return out

@@ -1,0 +1,476 @@
+#!/usr/bin/env python3
+"""Throughput of the activation-sparse gated FFN (TwELL) on one GB300.
+
+One step = the whole hot path on one batch of synthetic tokens: gate GEMM
+with the fused TwELL pack, hybrid ELL / dense routing, fused sparse up+down
+forward (routed rows on the dense tensor-core backup), and the backward
+(dX, dWg, dWu, dWd with the L1 term).  `value` is tokens/s of that
+forward+backward step over all ranks; the same JSON line also carries the
+forward-only rate, the library's own dense tcgen05 FFN at equal shapes, the
+dominant kernel's roofline, an end-to-end figure through the C ABI with host
+buffers, and the CPU oracle's rate on a bounded sample.
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl own|reference]
+Multi-GPU runs (torchrun) are independent replicas: the hot path has no
+data-path exchange, so each rank runs the full workload and only the timing
+is reduced (max over ranks).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+from activation_sparse_gated_tcgen05_gb300 import synthetic  # noqa: E402
+
+METRIC = "gated-FFN tokens/s (fwd, fwd+bwd) at 0.5% density vs own dense; % of roofline"
+UNIT = "tokens/s"
+L1 = 2e-5
+L2_FLUSH_BYTES = 256 << 20
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def parse_args():
+    ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=("own", "reference"), default="own")
+    ap.add_argument("--workload", default="fwd_0p5b", choices=sorted(synthetic.WORKLOADS))
+    ap.add_argument("--route-fraction", type=float, default=0.03,
+                    help="fraction of rows the ELL width sends to the dense backup")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0,
+                    help="target CPU time of the oracle baseline sample")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--only", choices=("sparse_step", "sparse_fwd", "dense_fwd", "dense_step"),
+                    help="time just this part (a short command for kernel profiling); prints "
+                         "a reduced JSON line")
+    return ap.parse_args()
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as fh:
+            p = json.load(fh)
+        return {k: float(p[k]) for k in FALLBACK_PEAKS}, "measured"
+    except (OSError, KeyError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def workload_config(wl, W, route_fraction):
+    dens = ("lognormal median %.2g%% sigma %.2g" % (100 * wl.density, wl.lognormal_sigma)
+            if wl.lognormal_sigma else "%.2g%% uniform" % (100 * wl.density))
+    return {
+        "workload": "%s: M=%d d_model=%d d_ff=%d T_n=%d C=%d density %s, ELL width W=%d "
+                    "(p%.0f of row_nnz)" % (wl.name, wl.M, wl.d_model, wl.d_ff, wl.tile_n,
+                                            wl.tile_cap, dens, W, 100 * (1 - route_fraction)),
+        "M": wl.M, "d_model": wl.d_model, "d_ff": wl.d_ff, "tile_n": wl.tile_n,
+        "tile_cap": wl.tile_cap, "ell_width": W, "l1_coeff": L1,
+        "l2": "flushed between timed steps (256 MiB write)",
+        "parallelism": "replicas",
+    }
+
+
+# ---------------------------------------------------------------- distributed
+class Dist:
+    def __init__(self):
+        self.world = int(os.environ.get("WORLD_SIZE", "1"))
+        self.rank = int(os.environ.get("RANK", "0"))
+        self.local = int(os.environ.get("LOCAL_RANK", "0"))
+        self.pg = None
+
+    def init(self, backend):
+        if self.world > 1:
+            import torch.distributed as dist
+
+            os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+            dist.init_process_group(backend=backend)
+            self.pg = dist
+
+    def barrier(self):
+        if self.pg:
+            self.pg.barrier()
+
+    def max(self, v: float, device) -> float:
+        if not self.pg:
+            return v
+        import torch
+
+        t = torch.tensor([v], dtype=torch.float64, device=device)
+        self.pg.all_reduce(t, op=self.pg.ReduceOp.MAX)
+        return float(t.item())
+
+    def close(self):
+        if self.pg:
+            self.pg.destroy_process_group()
+
+
+# ---------------------------------------------------------------- clocks
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.proc = None
+        self.idx = gpu_index
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "--query-gpu=" + self.FIELDS, "--format=csv,noheader,nounits",
+                 "-lms", "200", "-i", str(self.idx)],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if not self.proc:
+            return None
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, mx, reasons = [], [], set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for line in out.splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------- CPU oracle
+def oracle_step(oracle, w64, bits, rows, wl, W):
+    """The oracle's training step on the given rows: gate, pack, route,
+    sparse forward (dense formula for routed rows), hybrid backward."""
+    x = w64["x"][rows]
+    a = oracle.gate_preact(x, w64["wgT"])
+    val, idx, cnt, nnz = oracle.twell_pack(a, wl.tile_n, wl.tile_cap)
+    ev, ec, en, dr = oracle.hybrid_route(val, idx, cnt, nnz, wl.d_ff, wl.tile_n, W)
+    y = oracle.ffn_fwd_ell(x, w64["wuT"], w64["wd"], ev, ec, en)
+    if dr.size:
+        y[dr] = oracle.ffn_fwd_dense(x, w64["wgT"], w64["wuT"], w64["wd"], rows=dr)
+    g = oracle.ffn_bwd_hybrid(x, w64["wgT"], w64["wuT"], w64["wd"], w64["dy"][rows], ev, ec, en,
+                              dr, L1)
+    return y, g
+
+
+def cpu_sample_rate(wl, bits, W, seconds, step_budget=None):
+    """Time the oracle on a bounded sample of the workload's rows.  Returns
+    (tokens/s, rows per sample, threads, seconds per sample)."""
+    import oracle
+
+    threads = os.cpu_count() or 1
+    oracle.set_threads(threads)
+    w64 = {k: oracle.f64(bits[k]) for k in ("x", "wgT", "wuT", "wd", "dy")}
+    rows = np.arange(8)
+    t0 = time.perf_counter()
+    oracle_step(oracle, w64, bits, rows, wl, W)
+    dt = time.perf_counter() - t0
+    target = step_budget if step_budget is not None else seconds
+    n = int(max(8, min(wl.M, 8 * target / max(dt, 1e-3))))
+    rows = np.arange(n)
+    t0 = time.perf_counter()
+    oracle_step(oracle, w64, bits, rows, wl, W)
+    dt = time.perf_counter() - t0
+    return n / dt, n, threads, dt, w64
+
+
+# ---------------------------------------------------------------- own arm
+def algorithmic_work(family, wl, nnz_ell, n_dense):
+    """(amount, unit, bound) per launch of a kernel family, from the formulas
+    of the hot path: flops for tensor-core GEMMs, bytes for gather kernels."""
+    M, d, f = wl.M, wl.d_model, wl.d_ff
+    if family == "gemm_gate_pack":
+        return 2.0 * M * d * f, "flop", "tensor"
+    if family == "sparse_fwd":  # weight rows gathered + x read + y written + ELL entries
+        return 4.0 * d * nnz_ell + 4.0 * d * M + 4.0 * nnz_ell, "byte", "hbm"
+    if family == "bwd_rows":  # 3 weight rows per entry + x, dy, dx rows + per-entry scratch
+        return 6.0 * d * nnz_ell + 6.0 * d * M + 24.0 * nnz_ell, "byte", "hbm"
+    if family == "bwd_neurons":  # x and dy rows per entry + three fp32 dW rows per neuron
+        return 4.0 * d * nnz_ell + 12.0 * f * d + 20.0 * nnz_ell, "byte", "hbm"
+    return None
+
+
+def run_own(args, dist):
+    import torch
+
+    from activation_sparse_gated_tcgen05_gb300 import twell
+
+    dev = torch.device("cuda", dist.local)
+    torch.cuda.set_device(dev)
+    dist.init("nccl")
+    wl = synthetic.WORKLOADS[args.workload]
+    bits = synthetic.make_workload(wl)
+
+    def up(a):
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(dev).view(torch.bfloat16)
+
+    x, wg, wu, wd, dy = (up(bits[k]) for k in ("x", "wgT", "wuT", "wd", "dy"))
+    M, d, f = wl.M, wl.d_model, wl.d_ff
+    shape = twell.make_shape(M, d, f, wl.tile_n, wl.tile_cap)
+    tiles = twell.alloc_tiles(shape, dev)
+    twell.twell_pack(x, wg, shape, tiles)
+    nnz = twell.tiles_view(tiles, shape)[3].cpu().numpy()
+    W = int(np.sort(nnz)[min(M - 1, int((1.0 - args.route_fraction) * M))])
+    route = twell.alloc_hybrid(shape, W, dev)
+    ws = torch.empty(twell.twell_workspace_bytes(shape, W, True), dtype=torch.uint8, device=dev)
+    y = torch.empty(M, d, dtype=torch.bfloat16, device=dev)
+    dx = torch.empty_like(y)
+    dws = [torch.empty(f, d, dtype=torch.float32, device=dev) for _ in range(3)]
+    dws_d = [torch.empty(f, d, dtype=torch.float32, device=dev) for _ in range(3)]
+    ws_d = torch.empty(twell.twell_dense_workspace_bytes(shape, True), dtype=torch.uint8,
+                       device=dev)
+    y_d, dx_d = torch.empty_like(y), torch.empty_like(y)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def sparse_step():
+        twell.twell_pack(x, wg, shape, tiles)
+        twell.hybrid_route(tiles, shape, route)
+        twell.twell_ffn_fwd(x, wg, wu, wd, shape, y, route=route, ws=ws)
+        twell.twell_ffn_bwd(x, wg, wu, wd, dy, shape, route, L1, dx, *dws, ws)
+
+    def sparse_fwd():
+        twell.twell_pack(x, wg, shape, tiles)
+        twell.twell_ffn_fwd(x, wg, wu, wd, shape, y, tiles=tiles)
+
+    def dense_fwd():
+        twell.twell_dense_ffn_fwd(x, wg, wu, wd, shape, y_d, False, ws_d)
+
+    def dense_step():
+        twell.twell_dense_ffn_fwd(x, wg, wu, wd, shape, y_d, True, ws_d)
+        twell.twell_dense_ffn_bwd(x, wg, wu, wd, dy, shape, L1, dx_d, *dws_d, ws_d)
+
+    def timed(fn, steps, warmup, profile=None, clocks=None):
+        for _ in range(warmup):
+            flush.zero_()
+            fn()
+        torch.cuda.synchronize()
+        dist.barrier()
+        torch.cuda.synchronize()
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(steps)]
+        if clocks:
+            clocks.start()
+        if profile:
+            twell.twell_profile_begin(profile)
+        launches0 = twell.twell_launch_count()
+        for s0, s1 in ev:
+            flush.zero_()
+            s0.record(stream)
+            fn()
+            s1.record(stream)
+        launches = twell.twell_launch_count() - launches0
+        torch.cuda.synchronize()
+        prof = twell.twell_profile_end() if profile else None
+        dist.barrier()
+        torch.cuda.synchronize()
+        ck = clocks.stop() if clocks else None
+        ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
+        return dist.max(ms, dev), launches, prof, ck
+
+    if args.only:
+        fn = {"sparse_step": sparse_step, "sparse_fwd": sparse_fwd, "dense_fwd": dense_fwd,
+              "dense_step": dense_step}[args.only]
+        ms, launches, _, _ = timed(fn, args.steps, args.warmup)
+        st = twell.twell_get_device_status()
+        if dist.rank == 0:
+            print(json.dumps({"only": args.only, "workload": wl.name, "ms": ms,
+                              "tokens_per_s": dist.world * M / (ms / 1e3),
+                              "gpu_launches": launches, "device_status": st}), flush=True)
+        dist.close()
+        if st != 0:
+            raise SystemExit("device status %d" % st)
+        return
+
+    # correctness of the status word before timing anything
+    sparse_step()
+    torch.cuda.synchronize()
+    st = twell.twell_get_device_status()
+    if st != 0:
+        raise RuntimeError("device status %d after the first step" % st)
+    n_dense = int(route.n_dense[0].item())
+    nnz_ell = int(route.ell_nnz[:M].sum().item())
+    density = float(nnz.sum()) / (M * f)
+
+    # which kernel family dominates the step (untimed profiling pass)
+    twell.twell_profile_begin("*")
+    for _ in range(2):
+        flush.zero_()
+        sparse_step()
+    torch.cuda.synchronize()
+    fam = twell.twell_profile_end()
+    total = sum(v[1] for v in fam.values())
+    kernels = {k: {"launches_per_step": v[0] / 2, "ms_per_step": v[1] / 2,
+                   "share": v[1] / total if total else 0.0}
+               for k, v in sorted(fam.items(), key=lambda kv: -kv[1][1])}
+    dominant = max(fam, key=lambda k: fam[k][1])
+
+    gpu_idx = os.environ.get("CUDA_VISIBLE_DEVICES", str(dist.local)).split(",")[0]
+    clocks = ClockSampler(gpu_idx if gpu_idx.isdigit() else dist.local)
+    ms_step, launches, prof, ck = timed(sparse_step, args.steps, args.warmup, profile=dominant,
+                                        clocks=clocks)
+    ms_fwd, _, _, _ = timed(sparse_fwd, args.steps, args.warmup)
+    ms_dfwd, _, _, _ = timed(dense_fwd, args.steps, args.warmup)
+    ms_dstep, _, _, _ = timed(dense_step, args.steps, args.warmup)
+
+    # roofline of the dominant kernel, from its events inside the timed region
+    peaks, peak_src = load_peaks()
+    roof = None
+    cnt, dom_ms = prof.get(dominant, (0, 0.0)) if prof else (0, 0.0)
+    work = algorithmic_work(dominant, wl, nnz_ell, n_dense)
+    if work and cnt:
+        amount, unit, bound = work
+        per_launch_s = dom_ms / cnt / 1e3
+        if unit == "flop":
+            achieved = amount / per_launch_s / 1e12
+            peak, punit = peaks["bf16_tflops"], "TFLOP/s"
+        else:
+            achieved = amount / per_launch_s / 1e9
+            peak, punit = peaks["hbm_gbs"], "GB/s"
+        roof = {"kernel": dominant, "bound": bound, "achieved": achieved, "peak": peak,
+                "unit": punit, "frac": achieved / peak, "peak_source": peak_src,
+                "work_per_launch": amount, "work_unit": unit, "ms_per_launch": dom_ms / cnt,
+                "traffic": traffic_for(dominant, wl.name)}
+
+    # end to end through the C ABI with host buffers (H2D inputs, D2H results)
+    xh = torch.empty((M, d), dtype=torch.bfloat16).pin_memory()
+    dyh = torch.empty((M, d), dtype=torch.bfloat16).pin_memory()
+    xh.copy_(x.cpu())
+    dyh.copy_(dy.cpu())
+    yh = torch.empty((M, d), dtype=torch.bfloat16).pin_memory()
+    dxh = torch.empty((M, d), dtype=torch.bfloat16).pin_memory()
+
+    def e2e_step():
+        x.copy_(xh, non_blocking=True)
+        dy.copy_(dyh, non_blocking=True)
+        sparse_step()
+        yh.copy_(y, non_blocking=True)
+        dxh.copy_(dx, non_blocking=True)
+
+    ms_e2e, _, _, _ = timed(e2e_step, args.steps, args.warmup)
+    bi = 2 * M * d * 2
+    bo = 2 * M * d * 2
+
+    n = dist.world
+    line = {
+        "metric": METRIC, "value": n * M / (ms_step / 1e3), "unit": UNIT, "n_gpus": n,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded; gate offsets set for the target density)",
+        "config": workload_config(wl, W, args.route_fraction),
+        "fwd_tokens_per_s": n * M / (ms_fwd / 1e3),
+        "dense_fwd_tokens_per_s": n * M / (ms_dfwd / 1e3),
+        "dense_fwd_bwd_tokens_per_s": n * M / (ms_dstep / 1e3),
+        "speedup_vs_dense": {"fwd": ms_dfwd / ms_fwd, "fwd_bwd": ms_dstep / ms_step},
+        "ms": {"sparse_fwd_bwd": ms_step, "sparse_fwd": ms_fwd, "dense_fwd": ms_dfwd,
+               "dense_fwd_bwd": ms_dstep},
+        "measured_density": density, "routed_rows": n_dense, "ell_entries": nnz_ell,
+        "roofline": roof, "kernels": kernels,
+        "e2e": {"value": n * M / (ms_e2e / 1e3), "unit": UNIT, "h2d_bytes_per_step": bi,
+                "d2h_bytes_per_step": bo},
+        "gpu_launches": launches, "gpu_launches_per_step": launches / args.steps,
+        "clocks": ck,
+    }
+    if dist.rank == 0 and n == 1 and not args.no_cpu_baseline:
+        rate, rows, threads, secs, _ = cpu_sample_rate(wl, bits, W, args.cpu_seconds)
+        line["cpu_baseline"] = {
+            "value": rate, "unit": UNIT, "cores": threads, "kind": "oracle",
+            "sample": "oracle training step (gate, pack, route, sparse fwd, hybrid bwd) on "
+                      "the first %d rows of the workload, %.1f s" % (rows, secs)}
+    if dist.rank == 0:
+        print(json.dumps(line), flush=True)
+    dist.close()
+
+
+def traffic_for(kernel, workload):
+    """DRAM bytes per launch from a committed ncu capture, if one exists for
+    this kernel and workload (profiles/dram_traffic.json)."""
+    path = os.path.join(ROOT, "profiles", "dram_traffic.json")
+    try:
+        with open(path) as fh:
+            t = json.load(fh)
+        return t.get(workload, {}).get(kernel)
+    except (OSError, ValueError):
+        return None
+
+
+# ---------------------------------------------------------------- reference arm
+def run_reference(args, dist):
+    """The oracle as it stands on the host cores, same metric and workload,
+    each step a bounded sample of the workload's rows."""
+    if dist.rank != 0:
+        return
+    wl = synthetic.WORKLOADS[args.workload]
+    bits = synthetic.make_workload(wl)
+    import oracle
+
+    x64 = oracle.f64(bits["x"])
+    a = oracle.gate_preact(x64[: min(wl.M, 2048)], oracle.f64(bits["wgT"]))
+    _, _, _, nnz = oracle.twell_pack(a, wl.tile_n, wl.tile_cap)
+    W = int(np.sort(nnz)[min(nnz.size - 1, int((1.0 - args.route_fraction) * nnz.size))])
+    budget = 150.0 / max(1, args.steps + args.warmup)  # whole run within a few minutes
+    _, rows, threads, _, w64 = cpu_sample_rate(wl, bits, W, None, step_budget=budget)
+    import oracle as orc
+
+    sample = np.arange(rows)
+    for _ in range(args.warmup):
+        oracle_step(orc, w64, bits, sample, wl, W)
+    times = []
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        oracle_step(orc, w64, bits, sample, wl, W)
+        times.append(time.perf_counter() - t0)
+    sec = statistics.mean(times)
+    value = rows / sec
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": dist.world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": sec * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded; gate offsets set for the target density)",
+        "config": workload_config(wl, W, args.route_fraction),
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
+                         "sample": "first %d rows of the workload per step" % rows},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse_args()
+    dist = Dist()
+    if args.impl == "reference":
+        run_reference(args, dist)
+    else:
+        run_own(args, dist)
+
+
+if __name__ == "__main__":
+    main()

@@ -199,6 +199,25 @@ const char* twell_status_string(int32_t status);
 /* Number of SMs the library schedules persistent kernels over (0 if no device). */
 int32_t twell_num_sms(void);
 
+/* Number of CUDA kernels this library has launched in this process so far
+ * (all devices, all streams).  Lets a caller count the kernels of a region. */
+uint64_t twell_launch_count(void);
+
+/* Built-in kernel timing.  twell_profile_begin(name) makes every later launch
+ * of the kernel family `name` ("*" for all, NULL or "" to stop) record a CUDA
+ * event pair on the stream it is launched on; twell_profile_end() stops,
+ * synchronises those events and aggregates them per family, returning the
+ * number of families (or -1 if an event could not be read); entry i is then
+ * available from twell_profile_entry (name valid until the next begin/end).
+ * Families: gemm_gate_pack, gemm_gated, gemm_dgate, gemm_store_kk/mk/km/mm,
+ * pack_dense, route_rows, route_list, gather_rows, sparse_fwd, csc_mark,
+ * csc_colscan, csc_ptr, csc_place, bwd_rows, bwd_neurons.  Host-side state,
+ * process-wide; not for use while another thread launches. */
+twell_status twell_profile_begin(const char* kernel);
+int32_t twell_profile_end(void);
+twell_status twell_profile_entry(int32_t i, const char** name, int32_t* launches,
+                                 double* total_ms);
+
 #ifdef __cplusplus
 }
 #endif
