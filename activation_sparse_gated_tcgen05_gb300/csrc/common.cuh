@@ -228,6 +228,53 @@ TW_DEV int warp_incl_scan(int v) {
 
 TW_DEV uint4 ldg_v4(const void* p) { return __ldg(reinterpret_cast<const uint4*>(p)); }
 
+// ---- packed fp32 pairs (sm_100+ f32x2 arithmetic) --------------------------
+// A uint64 holds two fp32 values: low word = element 2i, high word = 2i+1.
+TW_DEV uint64_t f2_make(uint32_t lo_bits, uint32_t hi_bits) {
+  return ((uint64_t)hi_bits << 32) | (uint64_t)lo_bits;
+}
+// bf16x2 word -> two fp32 (exact)
+TW_DEV uint64_t bf2_to_f2(uint32_t v) { return f2_make(v << 16, v & 0xFFFF0000u); }
+TW_DEV uint64_t f2_splat(float s) {
+  const uint32_t b = __float_as_uint(s);
+  return f2_make(b, b);
+}
+TW_DEV uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+TW_DEV float f2_lo(uint64_t v) { return __uint_as_float((uint32_t)v); }
+TW_DEV float f2_hi(uint64_t v) { return __uint_as_float((uint32_t)(v >> 32)); }
+TW_DEV float f2_sum(uint64_t v) { return f2_lo(v) + f2_hi(v); }
+
+// 8 bf16 of a 16-byte vector as four fp32 pairs
+TW_DEV void bf8_to_f2(const uint4& w, uint64_t (&o)[4]) {
+  o[0] = bf2_to_f2(w.x);
+  o[1] = bf2_to_f2(w.y);
+  o[2] = bf2_to_f2(w.z);
+  o[3] = bf2_to_f2(w.w);
+}
+// acc += a (fp32 pairs) * w (8 bf16), pairwise
+TW_DEV uint64_t dot8_f2(const uint64_t (&a)[4], const uint4& w, uint64_t acc) {
+  acc = f2_fma(a[0], bf2_to_f2(w.x), acc);
+  acc = f2_fma(a[1], bf2_to_f2(w.y), acc);
+  acc = f2_fma(a[2], bf2_to_f2(w.z), acc);
+  acc = f2_fma(a[3], bf2_to_f2(w.w), acc);
+  return acc;
+}
+// acc (fp32 pairs) += s * w (8 bf16)
+TW_DEV void axpy8_f2(uint64_t s2, const uint4& w, uint64_t (&acc)[4]) {
+  acc[0] = f2_fma(s2, bf2_to_f2(w.x), acc[0]);
+  acc[1] = f2_fma(s2, bf2_to_f2(w.y), acc[1]);
+  acc[2] = f2_fma(s2, bf2_to_f2(w.z), acc[2]);
+  acc[3] = f2_fma(s2, bf2_to_f2(w.w), acc[3]);
+}
+TW_DEV uint4 f2x4_to_bf8(const uint64_t (&a)[4]) {
+  return make_uint4(pack_bf16x2(f2_lo(a[0]), f2_hi(a[0])), pack_bf16x2(f2_lo(a[1]), f2_hi(a[1])),
+                    pack_bf16x2(f2_lo(a[2]), f2_hi(a[2])), pack_bf16x2(f2_lo(a[3]), f2_hi(a[3])));
+}
+
 TW_DEV void named_barrier(int id, int nthreads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }

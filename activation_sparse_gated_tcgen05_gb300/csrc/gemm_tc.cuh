@@ -1,13 +1,14 @@
 // gemm_tc.cuh -- persistent tcgen05 GEMM engine for sm_103a with fused epilogues.
 //
-// One CTA per SM.  Warp roles (256 threads):
+// One CTA per SM.  Warp roles (384 threads):
 //   warp 0      TMA producer: fills a STAGES-deep ring of A / B tiles in shared
 //               memory (128-byte swizzle), one elected lane
 //   warp 1      MMA issuer: tcgen05.mma 128 x 256 x 16 (bf16 in, fp32 in TMEM),
 //               one elected lane; commits free smem stages and finished tiles
 //   warp 2      TMEM owner: allocates / frees 512 columns (two accumulators)
-//   warps 4..7  epilogue: tcgen05.ld of the lane quarter each warp may touch;
-//               thread i of the 128 owns accumulator row i
+//   warps 4..11 epilogue: warp w reads TMEM lane quarter w % 4 (the quarter a
+//               warp may touch) and column half (w - 4) / 4, so each thread
+//               owns one accumulator row and half of its 256 columns
 // Two 256-column accumulators let the epilogue of tile i overlap the
 // mainloop of tile i+1.  Tiles are visited in a grouped raster so CTAs that
 // run together share A rows and B columns in L2.
@@ -32,7 +33,8 @@ constexpr int kBK = 64;   // one 128-byte swizzle row of bf16
 constexpr int kStages = 4;
 constexpr int kABytes = kBM * kBK * 2;  // 16 KB
 constexpr int kBBytes = kBN * kBK * 2;  // 32 KB
-constexpr int kGemmThreads = 256;
+constexpr int kGemmThreads = 384;
+constexpr int kEpiThreads = 256;  // warps 4..11
 constexpr int kGroupM = 16;
 constexpr uint32_t kTmemCols = 512;
 constexpr int kGemmSmem = kStages * (kABytes + kBBytes) + 1024 /*align*/ + 256 /*barriers*/;
@@ -94,10 +96,10 @@ struct Epilogue;
 template <>
 struct Epilogue<EPI_STORE> {
   static __device__ __forceinline__ void run(const GemmParams& p, uint32_t tacc, int row,
-                                             bool row_ok, int n0, int N) {
+                                             bool row_ok, int n0, int N, int half) {
     const int dst_row = (row_ok && p.row_map) ? p.row_map[row] : row;
 #pragma unroll 1
-    for (int c0 = 0; c0 < kBN; c0 += 32) {
+    for (int c0 = half * (kBN / 2); c0 < (half + 1) * (kBN / 2); c0 += 32) {
       uint32_t r[32];
       tmem_ld32(tacc + c0, r);
       tmem_wait_ld();
@@ -139,38 +141,60 @@ struct Epilogue<EPI_STORE> {
   }
 };
 
+// Select r[i] for a runtime i in [0, 32) without indexing registers
+// dynamically (which would spill r to local memory): a 5-level select tree.
+__device__ __forceinline__ uint32_t select32(const uint32_t (&r)[32], int i) {
+  uint32_t a[16];
+#pragma unroll
+  for (int k = 0; k < 16; ++k) a[k] = (i & 16) ? r[k + 16] : r[k];
+#pragma unroll
+  for (int k = 0; k < 8; ++k) a[k] = (i & 8) ? a[k + 8] : a[k];
+#pragma unroll
+  for (int k = 0; k < 4; ++k) a[k] = (i & 4) ? a[k + 4] : a[k];
+#pragma unroll
+  for (int k = 0; k < 2; ++k) a[k] = (i & 2) ? a[k + 2] : a[k];
+  return (i & 1) ? a[1] : a[0];
+}
+
 // ReLU + TwELL pack.  The accumulator holds 256 gate columns = 256 / T_n
-// TwELL tiles; this thread owns one row, scans its columns in ascending
-// order and writes the live ones to its (row, tile) slots.
+// TwELL tiles; this thread owns one row and one column half, scans its
+// columns in ascending order and writes the live ones to its (row, tile)
+// slots.  bf16(ReLU(a)) > 0 exactly when a > 2^-134 (the largest fp32 that
+// rounds to bf16 zero is 2^-134, a tie to even; NaN compares false), so one
+// compare per column builds the live mask and values are only extracted for
+// the (rare) live columns.
 template <>
 struct Epilogue<EPI_PACK> {
   static __device__ __forceinline__ void run(const GemmParams& p, uint32_t tacc, int row,
-                                             bool row_ok, int n0, int /*N*/) {
-    const int tiles_here = kBN / p.tile_n;
+                                             bool row_ok, int n0, int /*N*/, int half) {
+    const float kLiveMin = __uint_as_float(0x00008000u);  // 2^-134
+    const int tiles_here = (kBN / 2) / p.tile_n;
     const int chunks_per_tile = p.tile_n / 32;
+    const int col0 = half * (kBN / 2);
     int nnz = 0;
 #pragma unroll 1
     for (int tt = 0; tt < tiles_here; ++tt) {
-      const int t = n0 / p.tile_n + tt;
+      const int t = (n0 + col0) / p.tile_n + tt;
       const bool tile_ok = row_ok && t < p.T;
       const long long slot0 = ((long long)row * p.T + t) * p.cap;
       int c = 0;
 #pragma unroll 1
       for (int ch = 0; ch < chunks_per_tile; ++ch) {
         uint32_t r[32];
-        tmem_ld32(tacc + tt * p.tile_n + ch * 32, r);
+        tmem_ld32(tacc + col0 + tt * p.tile_n + ch * 32, r);
         tmem_wait_ld();
         if (!tile_ok) continue;
+        uint32_t mask = 0;
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          const uint32_t g = relu_bf16_bits(__uint_as_float(r[i]));
-          if (g & 0x7FFFu) {
-            if (c < p.cap) {
-              p.val[slot0 + c] = (uint16_t)g;
-              p.idx[slot0 + c] = (uint8_t)(ch * 32 + i);
-            }
-            ++c;
+        for (int i = 0; i < 32; ++i) mask |= (__uint_as_float(r[i]) > kLiveMin ? 1u : 0u) << i;
+        while (mask) {
+          const int i = __ffs(mask) - 1;
+          mask &= mask - 1;
+          if (c < p.cap) {
+            p.val[slot0 + c] = (uint16_t)relu_bf16_bits(__uint_as_float(select32(r, i)));
+            p.idx[slot0 + c] = (uint8_t)(ch * 32 + i);
           }
+          ++c;
         }
       }
       if (tile_ok) {
@@ -187,10 +211,10 @@ struct Epilogue<EPI_PACK> {
 template <>
 struct Epilogue<EPI_GATED> {
   static __device__ __forceinline__ void run(const GemmParams& p, uint32_t tacc, int row,
-                                             bool row_ok, int n0, int N) {
-    // here n0 is the neuron offset (tile index * 128)
+                                             bool row_ok, int n0, int N, int half) {
+    // here n0 is the neuron offset (tile index * 128); this thread takes 64 neurons
 #pragma unroll 1
-    for (int c0 = 0; c0 < 128; c0 += 32) {
+    for (int c0 = half * 64; c0 < half * 64 + 64; c0 += 32) {
       uint32_t ra[32], ru[32];
       tmem_ld32(tacc + c0, ra);
       tmem_ld32(tacc + 128 + c0, ru);
@@ -240,10 +264,10 @@ struct Epilogue<EPI_GATED> {
 template <>
 struct Epilogue<EPI_BWD_GATE> {
   static __device__ __forceinline__ void run(const GemmParams& p, uint32_t tacc, int row,
-                                             bool row_ok, int n0, int N) {
+                                             bool row_ok, int n0, int N, int half) {
     const long long seg = p.dd_seg;
 #pragma unroll 1
-    for (int c0 = 0; c0 < kBN; c0 += 32) {
+    for (int c0 = half * (kBN / 2); c0 < (half + 1) * (kBN / 2); c0 += 32) {
       uint32_t r[32];
       tmem_ld32(tacc + c0, r);
       tmem_wait_ld();
@@ -333,7 +357,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(&tfull[a], 1);
-      mbar_init(&tempty[a], 128);
+      mbar_init(&tempty[a], kEpiThreads);
     }
     *abort_flag = 0;
     fence_mbar_init();
@@ -450,6 +474,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   } else if (warp >= 4) {
     // ---------------------------------------------------------------- epilogue
     const int quarter = warp & 3;
+    const int half = (warp - 4) >> 2;
     const int r_local = quarter * 32 + lane;
     int it = 0;
     for (int tile = blockIdx.x; tile < total; tile += gridDim.x, ++it) {
@@ -467,7 +492,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       const bool row_ok = p.pad_rows ? (row < p.M) : (row < M_eff);
       const uint32_t tacc = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * kBN);
       const int n0 = (EPI == EPI_GATED) ? nb * 128 : nb * kBN;
-      Epilogue<EPI>::run(p, tacc, row, row_ok, n0, p.N);
+      Epilogue<EPI>::run(p, tacc, row, row_ok, n0, p.N, half);
       tc_fence_before();
       mbar_arrive(&tempty[acc]);
     }

@@ -110,8 +110,9 @@ __device__ __forceinline__ int slab(int lane, int wt, int v) {
   return 8 * (lane + 32 * (wt + TEAM * v));
 }
 
+// One team of TEAM warps per ELL row; fp32-pair arithmetic as in the forward.
 template <int TEAM, int VPL, int B>
-__global__ void __launch_bounds__(256)
+__global__ void __launch_bounds__(256, VPL > 2 ? 1 : 2)
     bwd_rows_kernel(const uint16_t* __restrict__ x, const uint16_t* __restrict__ dy,
                     const uint16_t* __restrict__ wgT, const uint16_t* __restrict__ wuT,
                     const uint16_t* __restrict__ wd, int M, int d,
@@ -119,21 +120,21 @@ __global__ void __launch_bounds__(256)
                     const int* __restrict__ ell_nnz, int W, const int* __restrict__ slot_pos,
                     float lambda, float4* __restrict__ csc_vals, uint16_t* __restrict__ dx) {
   constexpr int ROWS = 8 / TEAM;
-  __shared__ float red[2][8][TEAM][2 * B];
+  __shared__ float red[2][ROWS][TEAM][2 * B];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int team = warp / TEAM, wt = warp % TEAM;
   const int m = blockIdx.x * ROWS + team;
   if (m >= M) return;
 
-  uint4 xv[VPL], dyv[VPL];
-  float acc[VPL][8];
+  uint64_t xf[VPL][4], dyf[VPL][4], acc[VPL][4];
 #pragma unroll
   for (int v = 0; v < VPL; ++v) {
     const int e = slab<TEAM>(lane, wt, v);
-    xv[v] = e < d ? ldg_v4(x + (long long)m * d + e) : make_uint4(0, 0, 0, 0);
-    dyv[v] = e < d ? ldg_v4(dy + (long long)m * d + e) : make_uint4(0, 0, 0, 0);
+    const bool ok = e < d;
+    bf8_to_f2(ok ? ldg_v4(x + (long long)m * d + e) : make_uint4(0, 0, 0, 0), xf[v]);
+    bf8_to_f2(ok ? ldg_v4(dy + (long long)m * d + e) : make_uint4(0, 0, 0, 0), dyf[v]);
 #pragma unroll
-    for (int k = 0; k < 8; ++k) acc[v][k] = 0.f;
+    for (int k = 0; k < 4; ++k) acc[v][k] = 0;
   }
   int buf = 0;
   const int n = ell_nnz[m];
@@ -161,28 +162,29 @@ __global__ void __launch_bounds__(256)
         pos[b] = pp;
         g[b] = ok ? gg : 0.f;
       }
-      uint4 wdv[B][VPL], wuv[B][VPL];
+      uint4 wdv[B][VPL], wuv[B][VPL], wgv[B][VPL];
 #pragma unroll
       for (int b = 0; b < B; ++b)
 #pragma unroll
         for (int v = 0; v < VPL; ++v) {
           const int e = slab<TEAM>(lane, wt, v);
           const bool ok = j[b] >= 0 && e < d;
-          wdv[b][v] = ok ? ldg_v4(wd + (long long)j[b] * d + e) : make_uint4(0, 0, 0, 0);
-          wuv[b][v] = ok ? ldg_v4(wuT + (long long)j[b] * d + e) : make_uint4(0, 0, 0, 0);
+          const long long off = (long long)j[b] * d + e;
+          wdv[b][v] = ok ? ldg_v4(wd + off) : make_uint4(0, 0, 0, 0);
+          wuv[b][v] = ok ? ldg_v4(wuT + off) : make_uint4(0, 0, 0, 0);
+          wgv[b][v] = ok ? ldg_v4(wgT + off) : make_uint4(0, 0, 0, 0);
         }
       float dh[B], u[B];
 #pragma unroll
       for (int b = 0; b < B; ++b) {
-        dh[b] = 0.f;
-        u[b] = 0.f;
+        uint64_t a = 0, c = 0;
 #pragma unroll
         for (int v = 0; v < VPL; ++v) {
-          dh[b] = dot8(dyv[v], wdv[b][v], dh[b]);
-          u[b] = dot8(xv[v], wuv[b][v], u[b]);
+          a = dot8_f2(dyf[v], wdv[b][v], a);
+          c = dot8_f2(xf[v], wuv[b][v], c);
         }
-        dh[b] = warp_sum(dh[b]);
-        u[b] = warp_sum(u[b]);
+        dh[b] = warp_sum(f2_sum(a));
+        u[b] = warp_sum(f2_sum(c));
       }
       if (TEAM > 1) {
         if (lane == 0)
@@ -211,12 +213,11 @@ __global__ void __launch_bounds__(256)
         const float du = dh[b] * g[b];
         const float da = fmaf(dh[b], u[b], lambda);
         if (wt == 0 && lane == 0) csc_vals[pos[b]] = make_float4(du, da, g[b] * u[b], 0.f);
+        const uint64_t du2 = f2_splat(du), da2 = f2_splat(da);
 #pragma unroll
         for (int v = 0; v < VPL; ++v) {
-          const int e = slab<TEAM>(lane, wt, v);
-          const uint4 wg = e < d ? ldg_v4(wgT + (long long)j[b] * d + e) : make_uint4(0, 0, 0, 0);
-          axpy8(du, wuv[b][v], acc[v]);
-          axpy8(da, wg, acc[v]);
+          axpy8_f2(du2, wuv[b][v], acc[v]);
+          axpy8_f2(da2, wgv[b][v], acc[v]);
         }
       }
     }
@@ -224,20 +225,15 @@ __global__ void __launch_bounds__(256)
 #pragma unroll
   for (int v = 0; v < VPL; ++v) {
     const int e = slab<TEAM>(lane, wt, v);
-    if (e < d) {
-      uint4 o;
-      o.x = pack_bf16x2(acc[v][0], acc[v][1]);
-      o.y = pack_bf16x2(acc[v][2], acc[v][3]);
-      o.z = pack_bf16x2(acc[v][4], acc[v][5]);
-      o.w = pack_bf16x2(acc[v][6], acc[v][7]);
-      *reinterpret_cast<uint4*>(dx + (long long)m * d + e) = o;
-    }
+    if (e < d) *reinterpret_cast<uint4*>(dx + (long long)m * d + e) = f2x4_to_bf8(acc[v]);
   }
 }
 
 // ---------------------------------------------------------------- neuron phase
+// One team per neuron; each warp owns VPL slabs of d_model and needs no
+// cross-warp communication.
 template <int TEAM, int VPL, int B>
-__global__ void __launch_bounds__(256)
+__global__ void __launch_bounds__(256, VPL > 2 ? 1 : 2)
     bwd_neurons_kernel(const uint16_t* __restrict__ x, const uint16_t* __restrict__ dy, int d,
                        int f, const int* __restrict__ csc_ptr, const int* __restrict__ csc_row,
                        const float4* __restrict__ csc_vals, float* __restrict__ dwgT,
@@ -247,11 +243,11 @@ __global__ void __launch_bounds__(256)
   const int team = warp / TEAM, wt = warp % TEAM;
   const int j = blockIdx.x * ROWS + team;
   if (j >= f) return;
-  float ad[VPL][8], au[VPL][8], ag[VPL][8];
+  uint64_t ad[VPL][4], au[VPL][4], ag[VPL][4];
 #pragma unroll
   for (int v = 0; v < VPL; ++v)
 #pragma unroll
-    for (int k = 0; k < 8; ++k) ad[v][k] = au[v][k] = ag[v][k] = 0.f;
+    for (int k = 0; k < 4; ++k) ad[v][k] = au[v][k] = ag[v][k] = 0;
 
   const int p0 = csc_ptr[j], p1 = csc_ptr[j + 1];
   for (int e0 = p0; e0 < p1; e0 += 32) {
@@ -289,13 +285,20 @@ __global__ void __launch_bounds__(256)
           dyv[b][v] = ok ? ldg_v4(dy + (long long)m[b] * d + e) : make_uint4(0, 0, 0, 0);
         }
 #pragma unroll
-      for (int b = 0; b < B; ++b)
+      for (int b = 0; b < B; ++b) {
+        const uint64_t h2 = f2_splat(h[b]), du2 = f2_splat(du[b]), da2 = f2_splat(da[b]);
 #pragma unroll
         for (int v = 0; v < VPL; ++v) {
-          axpy8(h[b], dyv[b][v], ad[v]);
-          axpy8(du[b], xv[b][v], au[v]);
-          axpy8(da[b], xv[b][v], ag[v]);
+          uint64_t xf[4];
+          bf8_to_f2(xv[b][v], xf);
+          axpy8_f2(h2, dyv[b][v], ad[v]);
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            au[v][k] = f2_fma(du2, xf[k], au[v][k]);
+            ag[v][k] = f2_fma(da2, xf[k], ag[v][k]);
+          }
         }
+      }
     }
   }
   const long long row = (long long)j * d;
@@ -306,24 +309,27 @@ __global__ void __launch_bounds__(256)
       float4* o1 = reinterpret_cast<float4*>(dwd + row + e);
       float4* o2 = reinterpret_cast<float4*>(dwuT + row + e);
       float4* o3 = reinterpret_cast<float4*>(dwgT + row + e);
-      o1[0] = make_float4(ad[v][0], ad[v][1], ad[v][2], ad[v][3]);
-      o1[1] = make_float4(ad[v][4], ad[v][5], ad[v][6], ad[v][7]);
-      o2[0] = make_float4(au[v][0], au[v][1], au[v][2], au[v][3]);
-      o2[1] = make_float4(au[v][4], au[v][5], au[v][6], au[v][7]);
-      o3[0] = make_float4(ag[v][0], ag[v][1], ag[v][2], ag[v][3]);
-      o3[1] = make_float4(ag[v][4], ag[v][5], ag[v][6], ag[v][7]);
+#pragma unroll
+      for (int q = 0; q < 2; ++q) {
+        o1[q] = make_float4(f2_lo(ad[v][2 * q]), f2_hi(ad[v][2 * q]), f2_lo(ad[v][2 * q + 1]),
+                            f2_hi(ad[v][2 * q + 1]));
+        o2[q] = make_float4(f2_lo(au[v][2 * q]), f2_hi(au[v][2 * q]), f2_lo(au[v][2 * q + 1]),
+                            f2_hi(au[v][2 * q + 1]));
+        o3[q] = make_float4(f2_lo(ag[v][2 * q]), f2_hi(ag[v][2 * q]), f2_lo(ag[v][2 * q + 1]),
+                            f2_hi(ag[v][2 * q + 1]));
+      }
     }
   }
 }
 
-template <int TEAM>
+template <int TEAM, int VPL>
 cudaError_t rows_team(const void* x, const void* dy, const void* wgT, const void* wuT,
                       const void* wd, int M, int d, const twell_hybrid& r, const int* slot_pos,
                       float lambda, float4* csc_vals, void* dx, cudaStream_t s) {
   constexpr int ROWS = 8 / TEAM;
   {
     ProfScope prof("bwd_rows", s);
-    bwd_rows_kernel<TEAM, 4, 2><<<(M + ROWS - 1) / ROWS, 256, 0, s>>>(
+    bwd_rows_kernel<TEAM, VPL, 2><<<(M + ROWS - 1) / ROWS, 256, 0, s>>>(
         reinterpret_cast<const uint16_t*>(x), reinterpret_cast<const uint16_t*>(dy),
         reinterpret_cast<const uint16_t*>(wgT), reinterpret_cast<const uint16_t*>(wuT),
         reinterpret_cast<const uint16_t*>(wd), M, d, reinterpret_cast<const uint16_t*>(r.ell_val),
@@ -334,16 +340,16 @@ cudaError_t rows_team(const void* x, const void* dy, const void* wgT, const void
   return cudaGetLastError();
 }
 
-template <int TEAM>
+template <int TEAM, int VPL>
 cudaError_t neurons_team(const void* x, const void* dy, int d, int f, const int* csc_ptr,
                          const int* csc_row, const float4* csc_vals, float* dwgT, float* dwuT,
                          float* dwd, cudaStream_t s) {
   constexpr int ROWS = 8 / TEAM;
   {
     ProfScope prof("bwd_neurons", s);
-    bwd_neurons_kernel<TEAM, 4, 2><<<(f + ROWS - 1) / ROWS, 256, 0, s>>>(
-        reinterpret_cast<const uint16_t*>(x), reinterpret_cast<const uint16_t*>(dy), d, f, csc_ptr,
-        csc_row, csc_vals, dwgT, dwuT, dwd);
+    bwd_neurons_kernel<TEAM, VPL, 2><<<(f + ROWS - 1) / ROWS, 256, 0, s>>>(
+        reinterpret_cast<const uint16_t*>(x), reinterpret_cast<const uint16_t*>(dy), d, f,
+        csc_ptr, csc_row, csc_vals, dwgT, dwuT, dwd);
   }
   count_launch();
   return cudaGetLastError();
@@ -398,10 +404,13 @@ cudaError_t launch_sparse_bwd_rows(const void* x, const void* dy, const void* wg
                                    const int* slot_pos, float lambda, float4* csc_vals, void* dx,
                                    cudaStream_t s) {
   if (M == 0) return cudaSuccess;
-  if (d <= 1024) return rows_team<1>(x, dy, wgT, wuT, wd, M, d, route, slot_pos, lambda, csc_vals, dx, s);
-  if (d <= 2048) return rows_team<2>(x, dy, wgT, wuT, wd, M, d, route, slot_pos, lambda, csc_vals, dx, s);
-  if (d <= 4096) return rows_team<4>(x, dy, wgT, wuT, wd, M, d, route, slot_pos, lambda, csc_vals, dx, s);
-  return rows_team<8>(x, dy, wgT, wuT, wd, M, d, route, slot_pos, lambda, csc_vals, dx, s);
+#define TW_ROWS(T, V) rows_team<T, V>(x, dy, wgT, wuT, wd, M, d, route, slot_pos, lambda, csc_vals, dx, s)
+  if (d <= 512) return TW_ROWS(1, 2);
+  if (d <= 1024) return TW_ROWS(2, 2);
+  if (d <= 2048) return TW_ROWS(4, 2);
+  if (d <= 4096) return TW_ROWS(8, 2);
+  return TW_ROWS(8, 4);
+#undef TW_ROWS
 }
 
 cudaError_t launch_sparse_bwd_neurons(const void* x, const void* dy, int M, int d, int f,
@@ -410,10 +419,13 @@ cudaError_t launch_sparse_bwd_neurons(const void* x, const void* dy, int M, int 
                                       cudaStream_t s) {
   (void)M;
   if (f == 0) return cudaSuccess;
-  if (d <= 1024) return neurons_team<1>(x, dy, d, f, csc_ptr, csc_row, csc_vals, dwgT, dwuT, dwd, s);
-  if (d <= 2048) return neurons_team<2>(x, dy, d, f, csc_ptr, csc_row, csc_vals, dwgT, dwuT, dwd, s);
-  if (d <= 4096) return neurons_team<4>(x, dy, d, f, csc_ptr, csc_row, csc_vals, dwgT, dwuT, dwd, s);
-  return neurons_team<8>(x, dy, d, f, csc_ptr, csc_row, csc_vals, dwgT, dwuT, dwd, s);
+#define TW_NEU(T, V) neurons_team<T, V>(x, dy, d, f, csc_ptr, csc_row, csc_vals, dwgT, dwuT, dwd, s)
+  if (d <= 512) return TW_NEU(1, 2);
+  if (d <= 1024) return TW_NEU(2, 2);
+  if (d <= 2048) return TW_NEU(4, 2);
+  if (d <= 4096) return TW_NEU(8, 2);
+  return TW_NEU(8, 4);
+#undef TW_NEU
 }
 
 }  // namespace tw

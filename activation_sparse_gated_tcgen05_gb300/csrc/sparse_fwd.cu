@@ -9,11 +9,14 @@
 // the team in 256-element (512-byte) slabs, VPL slabs per warp, so every
 // weight-row read is a run of coalesced 16-byte loads.  For each live entry
 // (j, g) of the row:
-//   u = x_m . Wu[:, j]          (x_m held in registers, WuT[j] gathered)
+//   u = x_m . Wu[:, j]          (x_m held in registers as fp32, WuT[j] gathered)
 //   h = g * u                   (fp32, kept in registers)
 //   y_m += h * Wd[j, :]         (fp32 accumulators in registers)
-// and y_m is written once as bf16.  Entries are processed B at a time so
-// 2*B weight rows are in flight per warp.
+// and y_m is written once as bf16.  Arithmetic runs on packed fp32 pairs
+// (f32x2 FMA), so each gathered bf16 costs one unpack and half an FMA; the
+// team's partial dot products meet in shared memory behind a named barrier.
+// Entries are processed B at a time, 2*B weight rows in flight per warp,
+// with registers capped so three 256-thread blocks fit on an SM.
 #include "common.cuh"
 #include "internal.h"
 
@@ -23,23 +26,25 @@ namespace {
 
 constexpr unsigned kFull = 0xffffffffu;
 
-template <int TEAM, int VPL, int B>
-struct RowCtx {
-  uint4 xv[VPL];
-  float acc[VPL][8];
-};
-
-template <int TEAM, int VPL>
+template <int TEAM>
 __device__ __forceinline__ int slab_elem(int lane, int wt, int v) {
   return 8 * (lane + 32 * (wt + TEAM * v));
 }
 
+// Row state of one warp: its share of x_m as fp32 pairs and of the fp32
+// accumulator y_m (pairs), VPL 8-element slabs each.
+template <int VPL>
+struct RowCtx {
+  uint64_t xf[VPL][4];
+  uint64_t acc[VPL][4];
+};
+
 // Process `count` (<= 32) entries whose (column, gate) sit in lanes 0..count-1.
-template <int TEAM, int VPL, int B>
-__device__ __forceinline__ void process_entries(RowCtx<TEAM, VPL, B>& c, int jl, float gl,
-                                                int count, const uint16_t* __restrict__ wuT,
+template <int TEAM, int VPL, int B, int ROWS>
+__device__ __forceinline__ void process_entries(RowCtx<VPL>& c, int jl, float gl, int count,
+                                                const uint16_t* __restrict__ wuT,
                                                 const uint16_t* __restrict__ wd, int d, int lane,
-                                                int wt, int team, float (*red)[8][TEAM][B],
+                                                int wt, int team, float (*red)[ROWS][TEAM][B],
                                                 int& buf) {
   for (int i = 0; i < count; i += B) {
     int j[B];
@@ -57,7 +62,7 @@ __device__ __forceinline__ void process_entries(RowCtx<TEAM, VPL, B>& c, int jl,
     for (int b = 0; b < B; ++b)
 #pragma unroll
       for (int v = 0; v < VPL; ++v) {
-        const int e = slab_elem<TEAM, VPL>(lane, wt, v);
+        const int e = slab_elem<TEAM>(lane, wt, v);
         if (j[b] >= 0 && e < d) {
           wu[b][v] = ldg_v4(wuT + (long long)j[b] * d + e);
           wdv[b][v] = ldg_v4(wd + (long long)j[b] * d + e);
@@ -69,10 +74,10 @@ __device__ __forceinline__ void process_entries(RowCtx<TEAM, VPL, B>& c, int jl,
     float p[B];
 #pragma unroll
     for (int b = 0; b < B; ++b) {
-      p[b] = 0.f;
+      uint64_t a2 = 0;
 #pragma unroll
-      for (int v = 0; v < VPL; ++v) p[b] = dot8(c.xv[v], wu[b][v], p[b]);
-      p[b] = warp_sum(p[b]);
+      for (int v = 0; v < VPL; ++v) a2 = dot8_f2(c.xf[v], wu[b][v], a2);
+      p[b] = warp_sum(f2_sum(a2));
     }
     if (TEAM > 1) {
       if (lane == 0)
@@ -81,24 +86,24 @@ __device__ __forceinline__ void process_entries(RowCtx<TEAM, VPL, B>& c, int jl,
       named_barrier(1 + team, 32 * TEAM);
 #pragma unroll
       for (int b = 0; b < B; ++b) {
-        float s = 0.f;
+        float sum = 0.f;
 #pragma unroll
-        for (int w = 0; w < TEAM; ++w) s += red[buf][team][w][b];
-        p[b] = s;
+        for (int w = 0; w < TEAM; ++w) sum += red[buf][team][w][b];
+        p[b] = sum;
       }
       buf ^= 1;
     }
 #pragma unroll
     for (int b = 0; b < B; ++b) {
-      const float h = g[b] * p[b];
+      const uint64_t h2 = f2_splat(g[b] * p[b]);
 #pragma unroll
-      for (int v = 0; v < VPL; ++v) axpy8(h, wdv[b][v], c.acc[v]);
+      for (int v = 0; v < VPL; ++v) axpy8_f2(h2, wdv[b][v], c.acc[v]);
     }
   }
 }
 
 template <int TEAM, int VPL, int B, bool ELL>
-__global__ void __launch_bounds__(256)
+__global__ void __launch_bounds__(256, VPL > 2 ? 1 : 3)
     sparse_fwd_kernel(const uint16_t* __restrict__ x, const uint16_t* __restrict__ wuT,
                       const uint16_t* __restrict__ wd, int M, int d,
                       const uint16_t* __restrict__ val, const uint8_t* __restrict__ idx,
@@ -107,19 +112,20 @@ __global__ void __launch_bounds__(256)
                       const int* __restrict__ ell_nnz, int W, uint16_t* __restrict__ y,
                       int* status) {
   constexpr int ROWS = 8 / TEAM;
-  __shared__ float red[2][8][TEAM][B];
+  __shared__ float red[2][ROWS][TEAM][B];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int team = warp / TEAM, wt = warp % TEAM;
   const int m = blockIdx.x * ROWS + team;
   if (m >= M) return;
 
-  RowCtx<TEAM, VPL, B> c;
+  RowCtx<VPL> c;
 #pragma unroll
   for (int v = 0; v < VPL; ++v) {
-    const int e = slab_elem<TEAM, VPL>(lane, wt, v);
-    c.xv[v] = e < d ? ldg_v4(x + (long long)m * d + e) : make_uint4(0, 0, 0, 0);
+    const int e = slab_elem<TEAM>(lane, wt, v);
+    const uint4 xv = e < d ? ldg_v4(x + (long long)m * d + e) : make_uint4(0, 0, 0, 0);
+    bf8_to_f2(xv, c.xf[v]);
 #pragma unroll
-    for (int k = 0; k < 8; ++k) c.acc[v][k] = 0.f;
+    for (int k = 0; k < 4; ++k) c.acc[v][k] = 0;
   }
   int buf = 0;
 
@@ -134,7 +140,8 @@ __global__ void __launch_bounds__(256)
         jl = ell_col[s];
         gl = bf16_bits_to_float(ell_val[s]);
       }
-      process_entries<TEAM, VPL, B>(c, jl, gl, count, wuT, wd, d, lane, wt, team, red, buf);
+      process_entries<TEAM, VPL, B, ROWS>(c, jl, gl, count, wuT, wd, d, lane, wt, team, red,
+                                          buf);
     }
   } else {
     for (int t0 = 0; t0 < T; t0 += 32) {
@@ -158,31 +165,24 @@ __global__ void __launch_bounds__(256)
         float gl = 0.f;
         if (e < total) {
           const int tt = t0 + lo;
-          const long long s = ((long long)m * T + tt) * cap + (e - ex);
-          jl = tt * tile_n + idx[s];
-          gl = bf16_bits_to_float(val[s]);
+          const long long sl = ((long long)m * T + tt) * cap + (e - ex);
+          jl = tt * tile_n + idx[sl];
+          gl = bf16_bits_to_float(val[sl]);
         }
-        process_entries<TEAM, VPL, B>(c, jl, gl, min(32, total - e0), wuT, wd, d, lane, wt, team,
-                                      red, buf);
+        process_entries<TEAM, VPL, B, ROWS>(c, jl, gl, min(32, total - e0), wuT, wd, d, lane,
+                                            wt, team, red, buf);
       }
     }
   }
 
 #pragma unroll
   for (int v = 0; v < VPL; ++v) {
-    const int e = slab_elem<TEAM, VPL>(lane, wt, v);
-    if (e < d) {
-      uint4 o;
-      o.x = pack_bf16x2(c.acc[v][0], c.acc[v][1]);
-      o.y = pack_bf16x2(c.acc[v][2], c.acc[v][3]);
-      o.z = pack_bf16x2(c.acc[v][4], c.acc[v][5]);
-      o.w = pack_bf16x2(c.acc[v][6], c.acc[v][7]);
-      *reinterpret_cast<uint4*>(y + (long long)m * d + e) = o;
-    }
+    const int e = slab_elem<TEAM>(lane, wt, v);
+    if (e < d) *reinterpret_cast<uint4*>(y + (long long)m * d + e) = f2x4_to_bf8(c.acc[v]);
   }
 }
 
-template <int TEAM, bool ELL>
+template <int TEAM, int VPL, bool ELL>
 cudaError_t launch_team(const void* x, const void* wuT, const void* wd, int M, int d,
                         const twell_tiles* tiles, int T, int tile_n, int cap,
                         const twell_hybrid* route, void* y, cudaStream_t s) {
@@ -190,11 +190,11 @@ cudaError_t launch_team(const void* x, const void* wuT, const void* wd, int M, i
   const int grid = (M + ROWS - 1) / ROWS;
   {
     ProfScope prof("sparse_fwd", s);
-    sparse_fwd_kernel<TEAM, 4, 2, ELL><<<grid, 256, 0, s>>>(
+    sparse_fwd_kernel<TEAM, VPL, 2, ELL><<<grid, 256, 0, s>>>(
         reinterpret_cast<const uint16_t*>(x), reinterpret_cast<const uint16_t*>(wuT),
         reinterpret_cast<const uint16_t*>(wd), M, d,
-        tiles ? reinterpret_cast<const uint16_t*>(tiles->val) : nullptr, tiles ? tiles->idx : nullptr,
-        tiles ? tiles->cnt : nullptr, T, tile_n, cap,
+        tiles ? reinterpret_cast<const uint16_t*>(tiles->val) : nullptr,
+        tiles ? tiles->idx : nullptr, tiles ? tiles->cnt : nullptr, T, tile_n, cap,
         route ? reinterpret_cast<const uint16_t*>(route->ell_val) : nullptr,
         route ? route->ell_col : nullptr, route ? route->ell_nnz : nullptr,
         route ? route->ell_width : 0, reinterpret_cast<uint16_t*>(y), device_status_ptr());
@@ -203,14 +203,16 @@ cudaError_t launch_team(const void* x, const void* wuT, const void* wd, int M, i
   return cudaGetLastError();
 }
 
+// A team of d/512 warps per row, two 256-element slabs per warp.
 template <bool ELL>
 cudaError_t launch_fmt(const void* x, const void* wuT, const void* wd, int M, int d,
                        const twell_tiles* tiles, int T, int tile_n, int cap,
                        const twell_hybrid* route, void* y, cudaStream_t s) {
-  if (d <= 1024) return launch_team<1, ELL>(x, wuT, wd, M, d, tiles, T, tile_n, cap, route, y, s);
-  if (d <= 2048) return launch_team<2, ELL>(x, wuT, wd, M, d, tiles, T, tile_n, cap, route, y, s);
-  if (d <= 4096) return launch_team<4, ELL>(x, wuT, wd, M, d, tiles, T, tile_n, cap, route, y, s);
-  return launch_team<8, ELL>(x, wuT, wd, M, d, tiles, T, tile_n, cap, route, y, s);
+  if (d <= 512) return launch_team<1, 2, ELL>(x, wuT, wd, M, d, tiles, T, tile_n, cap, route, y, s);
+  if (d <= 1024) return launch_team<2, 2, ELL>(x, wuT, wd, M, d, tiles, T, tile_n, cap, route, y, s);
+  if (d <= 2048) return launch_team<4, 2, ELL>(x, wuT, wd, M, d, tiles, T, tile_n, cap, route, y, s);
+  if (d <= 4096) return launch_team<8, 2, ELL>(x, wuT, wd, M, d, tiles, T, tile_n, cap, route, y, s);
+  return launch_team<8, 4, ELL>(x, wuT, wd, M, d, tiles, T, tile_n, cap, route, y, s);
 }
 
 }  // namespace

@@ -58,7 +58,9 @@ class Workload:
     density: float = DENSITY_REF          # uniform per-row target density
     lognormal_sigma: Optional[float] = None  # per-row lognormal density (median = density)
     density_cap: float = 0.30
-    route_fraction: Optional[float] = None   # ELL width = quantile of row_nnz at 1 - this
+    # ELL width W = the (1 - route_fraction) quantile of row_nnz; 0 means W = max row_nnz,
+    # so only rows with an overflowing tile go to the dense backup
+    route_fraction: float = 0.0
     seeds: tuple = (0,)
 
 
@@ -67,8 +69,7 @@ class Workload:
 # fwd+bwd with lognormal density (plus a small-M forward at that shape).
 WORKLOADS = {
     "tiny_fwd": Workload("tiny_fwd", 256, 256, 1024, 64, 16),
-    "fwd_0p5b": Workload("fwd_0p5b", 16384, 1024, 4096, 128, 32, seeds=(0, 1, 2),
-                         route_fraction=0.03),
+    "fwd_0p5b": Workload("fwd_0p5b", 16384, 1024, 4096, 128, 32, seeds=(0, 1, 2)),
     "fwd_2b": Workload("fwd_2b", 32768, 2048, 8192, 128, 32),
     "train_2b": Workload("train_2b", 16384, 2048, 8192, 128, 32, lognormal_sigma=1.0,
                          route_fraction=0.03),
@@ -77,6 +78,17 @@ WORKLOADS = {
 }
 DENSITY_SWEEP = (0.0025, 0.005, 0.01, 0.02, 0.05)
 SMALL_M = (1, 16, 64)
+
+
+def ell_width(row_nnz: np.ndarray, route_fraction: float) -> int:
+    """ELL width that sends about `route_fraction` of the rows to the dense
+    backup (0: the widest row, so none is routed for its length)."""
+    nnz = np.sort(np.asarray(row_nnz).reshape(-1))
+    if nnz.size == 0:
+        return 0
+    if route_fraction <= 0:
+        return int(nnz[-1])
+    return int(nnz[min(nnz.size - 1, int((1.0 - route_fraction) * nnz.size))])
 
 
 def row_densities(M: int, median: float, sigma: Optional[float], cap: float,

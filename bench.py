@@ -47,8 +47,9 @@ def parse_args():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=("own", "reference"), default="own")
     ap.add_argument("--workload", default="fwd_0p5b", choices=sorted(synthetic.WORKLOADS))
-    ap.add_argument("--route-fraction", type=float, default=0.03,
-                    help="fraction of rows the ELL width sends to the dense backup")
+    ap.add_argument("--route-fraction", type=float, default=None,
+                    help="fraction of rows the ELL width sends to the dense backup "
+                         "(default: the workload's; 0 routes only rows with an overflowing tile)")
     ap.add_argument("--cpu-seconds", type=float, default=15.0,
                     help="target CPU time of the oracle baseline sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -73,8 +74,9 @@ def workload_config(wl, W, route_fraction):
             if wl.lognormal_sigma else "%.2g%% uniform" % (100 * wl.density))
     return {
         "workload": "%s: M=%d d_model=%d d_ff=%d T_n=%d C=%d density %s, ELL width W=%d "
-                    "(p%.0f of row_nnz)" % (wl.name, wl.M, wl.d_model, wl.d_ff, wl.tile_n,
-                                            wl.tile_cap, dens, W, 100 * (1 - route_fraction)),
+                    "(%s)" % (wl.name, wl.M, wl.d_model, wl.d_ff, wl.tile_n, wl.tile_cap, dens, W,
+                              "p%.0f of row_nnz" % (100 * (1 - route_fraction))
+                              if route_fraction > 0 else "widest row; overflow rows routed"),
         "M": wl.M, "d_model": wl.d_model, "d_ff": wl.d_ff, "tile_n": wl.tile_n,
         "tile_cap": wl.tile_cap, "ell_width": W, "l1_coeff": L1,
         "l2": "flushed between timed steps (256 MiB write)",
@@ -238,7 +240,8 @@ def run_own(args, dist):
     tiles = twell.alloc_tiles(shape, dev)
     twell.twell_pack(x, wg, shape, tiles)
     nnz = twell.tiles_view(tiles, shape)[3].cpu().numpy()
-    W = int(np.sort(nnz)[min(M - 1, int((1.0 - args.route_fraction) * M))])
+    rf = wl.route_fraction if args.route_fraction is None else args.route_fraction
+    W = synthetic.ell_width(nnz, rf)
     route = twell.alloc_hybrid(shape, W, dev)
     ws = torch.empty(twell.twell_workspace_bytes(shape, W, True), dtype=torch.uint8, device=dev)
     y = torch.empty(M, d, dtype=torch.bfloat16, device=dev)
@@ -320,17 +323,22 @@ def run_own(args, dist):
     nnz_ell = int(route.ell_nnz[:M].sum().item())
     density = float(nnz.sum()) / (M * f)
 
-    # which kernel family dominates the step (untimed profiling pass)
-    twell.twell_profile_begin("*")
-    for _ in range(2):
-        flush.zero_()
-        sparse_step()
-    torch.cuda.synchronize()
-    fam = twell.twell_profile_end()
-    total = sum(v[1] for v in fam.values())
-    kernels = {k: {"launches_per_step": v[0] / 2, "ms_per_step": v[1] / 2,
-                   "share": v[1] / total if total else 0.0}
-               for k, v in sorted(fam.items(), key=lambda kv: -kv[1][1])}
+    # per-kernel breakdown of both steps (untimed profiling passes); the
+    # family with the largest share of the sparse step is the dominant kernel
+    def breakdown(fn):
+        twell.twell_profile_begin("*")
+        for _ in range(2):
+            flush.zero_()
+            fn()
+        torch.cuda.synchronize()
+        fam = twell.twell_profile_end()
+        total = sum(v[1] for v in fam.values())
+        return fam, {k: {"launches_per_step": v[0] / 2, "ms_per_step": v[1] / 2,
+                         "share": v[1] / total if total else 0.0}
+                     for k, v in sorted(fam.items(), key=lambda kv: -kv[1][1])}
+
+    fam, kernels = breakdown(sparse_step)
+    _, kernels_dense = breakdown(dense_step)
     dominant = max(fam, key=lambda k: fam[k][1])
 
     gpu_idx = os.environ.get("CUDA_VISIBLE_DEVICES", str(dist.local)).split(",")[0]
@@ -385,7 +393,7 @@ def run_own(args, dist):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic (seeded; gate offsets set for the target density)",
-        "config": workload_config(wl, W, args.route_fraction),
+        "config": workload_config(wl, W, rf),
         "fwd_tokens_per_s": n * M / (ms_fwd / 1e3),
         "dense_fwd_tokens_per_s": n * M / (ms_dfwd / 1e3),
         "dense_fwd_bwd_tokens_per_s": n * M / (ms_dstep / 1e3),
@@ -393,7 +401,7 @@ def run_own(args, dist):
         "ms": {"sparse_fwd_bwd": ms_step, "sparse_fwd": ms_fwd, "dense_fwd": ms_dfwd,
                "dense_fwd_bwd": ms_dstep},
         "measured_density": density, "routed_rows": n_dense, "ell_entries": nnz_ell,
-        "roofline": roof, "kernels": kernels,
+        "roofline": roof, "kernels": kernels, "kernels_dense_step": kernels_dense,
         "e2e": {"value": n * M / (ms_e2e / 1e3), "unit": UNIT, "h2d_bytes_per_step": bi,
                 "d2h_bytes_per_step": bo},
         "gpu_launches": launches, "gpu_launches_per_step": launches / args.steps,
@@ -435,7 +443,8 @@ def run_reference(args, dist):
     x64 = oracle.f64(bits["x"])
     a = oracle.gate_preact(x64[: min(wl.M, 2048)], oracle.f64(bits["wgT"]))
     _, _, _, nnz = oracle.twell_pack(a, wl.tile_n, wl.tile_cap)
-    W = int(np.sort(nnz)[min(nnz.size - 1, int((1.0 - args.route_fraction) * nnz.size))])
+    rf = wl.route_fraction if args.route_fraction is None else args.route_fraction
+    W = synthetic.ell_width(nnz, rf)
     budget = 150.0 / max(1, args.steps + args.warmup)  # whole run within a few minutes
     _, rows, threads, _, w64 = cpu_sample_rate(wl, bits, W, None, step_budget=budget)
     import oracle as orc
@@ -455,7 +464,7 @@ def run_reference(args, dist):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": sec * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic (seeded; gate offsets set for the target density)",
-        "config": workload_config(wl, W, args.route_fraction),
+        "config": workload_config(wl, W, rf),
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
                          "sample": "first %d rows of the workload per step" % rows},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
