@@ -616,3 +616,50 @@ twell_status twell_gemm_bf16(const void* A, const void* B, void* C, int32_t M, i
 }
 
 }  // extern "C"
+
+// ============================================== allocation-free hybrid forward
+// Some callers cannot allocate device memory at the point where they run the
+// FFN: code inside a CUDA graph capture or another framework's scheduler
+// where cudaMalloc would break the capture or synchronise the device, plugins
+// hosted by a runtime that owns every allocation, and deployments that fix
+// their memory footprint up front.  twell_ffn_fwd_noalloc serves them by
+// taking the routed-row scratch of the hybrid forward from a fixed array in
+// the library's own device image instead of a caller workspace.
+namespace {
+
+constexpr size_t kNoAllocScratchBytes = size_t(32) << 20;  // 32 MiB per device
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+std::mutex g_noalloc_mu;
+void* g_noalloc_ptr[64] = {nullptr};
+
+// Device address of the scratch array for the current device.  Host code
+// sees g_noalloc_scratch only as a host-side stand-in, so the address must
+// come from cudaGetSymbolAddress, once per device, with that device current.
+void* noalloc_scratch() {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  std::lock_guard<std::mutex> lock(g_noalloc_mu);
+  if (!g_noalloc_ptr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) return nullptr;
+    g_noalloc_ptr[dev] = p;
+  }
+  return g_noalloc_ptr[dev];
+}
+
+}  // namespace
+
+extern "C" twell_status twell_ffn_fwd_noalloc(const void* x, const void* wgT, const void* wuT,
+                                              const void* wd, const twell_shape* shape,
+                                              const twell_hybrid* route, void* y, void* stream) {
+  twell_status st = check_shape(shape, true);
+  if (st != TWELL_OK) return st;
+  if ((st = check_ptrs({x, wgT, wuT, wd, y})) != TWELL_OK) return st;
+  if ((st = check_route(route)) != TWELL_OK) return st;
+  const size_t need = carve_sparse(nullptr, *shape, route->ell_width, 0).bytes;
+  if (need > kNoAllocScratchBytes) return TWELL_ERR_WORKSPACE;
+  void* ws = noalloc_scratch();
+  if (!ws) return TWELL_ERR_CUDA;
+  return twell_ffn_fwd(x, wgT, wuT, wd, shape, nullptr, route, y, ws, kNoAllocScratchBytes, stream);
+}

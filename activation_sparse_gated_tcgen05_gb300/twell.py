@@ -32,6 +32,7 @@ EXPORTS = (
     "twell_ffn_bwd", "twell_dense_workspace_bytes", "twell_dense_ffn_fwd", "twell_dense_ffn_bwd",
     "twell_gemm_bf16", "twell_get_device_status", "twell_status_string", "twell_num_sms",
     "twell_launch_count", "twell_profile_begin", "twell_profile_end", "twell_profile_entry",
+    "twell_ffn_fwd_noalloc",
 )
 
 
@@ -80,6 +81,7 @@ def load():
         "twell_workspace_bytes": (SZ, [SP, I32, I32]),
         "twell_ffn_fwd": (I32, [P, P, P, P, SP, TP, HP, P, P, SZ, P]),
         "twell_ffn_bwd": (I32, [P, P, P, P, P, SP, HP, F, P, P, P, P, P, SZ, P]),
+        "twell_ffn_fwd_noalloc": (I32, [P, P, P, P, SP, HP, P, P]),
         "twell_dense_workspace_bytes": (SZ, [SP, I32]),
         "twell_dense_ffn_fwd": (I32, [P, P, P, P, SP, P, I32, P, SZ, P]),
         "twell_dense_ffn_bwd": (I32, [P, P, P, P, P, SP, F, P, P, P, P, P, SZ, P]),
@@ -225,6 +227,15 @@ def twell_ffn_fwd(x, wgT, wuT, wd, shape: Shape, y, tiles: Optional[TwellTiles] 
         _ptr(x), _ptr(wgT), _ptr(wuT), _ptr(wd), ctypes.byref(shape),
         ctypes.byref(t) if t is not None else None, ctypes.byref(h) if h is not None else None,
         _ptr(y), _ptr(ws), 0 if ws is None else ws.numel() * ws.element_size(), _stream(stream)))
+
+
+def twell_ffn_fwd_noalloc(x, wgT, wuT, wd, shape: Shape, y, route: TwellHybrid, stream=None):
+    """Hybrid forward whose scratch lives in the library's static device array
+    (no workspace argument, nothing allocated); see include/twell.h."""
+    h = route.c()
+    _check("twell_ffn_fwd_noalloc", load().twell_ffn_fwd_noalloc(
+        _ptr(x), _ptr(wgT), _ptr(wuT), _ptr(wd), ctypes.byref(shape), ctypes.byref(h), _ptr(y),
+        _stream(stream)))
 
 
 def twell_ffn_bwd(x, wgT, wuT, wd, dy, shape: Shape, route: TwellHybrid, l1_coeff: float, dx,

@@ -148,6 +148,29 @@ twell_status twell_ffn_fwd(const void* x, const void* wgT, const void* wuT, cons
                            const twell_hybrid* route, void* y, void* ws, size_t ws_bytes,
                            void* stream);
 
+/* Allocation-free variant of twell_ffn_fwd for the training (route) path.
+ * The pages have no counterpart: this entry point exists for callers that
+ * cannot allocate device memory when they run the FFN (inside a stream
+ * capture, under a host runtime that owns all allocations, or with a fixed
+ * memory budget).  It computes exactly what twell_ffn_fwd(..., tiles = NULL,
+ * route, ...) computes, with the routed-row scratch taken from a 32 MiB
+ * array compiled into the library (held by every device that loads the
+ * library until the process exits) instead of a caller workspace.  It
+ * allocates nothing and calls no allocating routine.
+ *   - Limit: twell_workspace_bytes(shape, route->ell_width, 0) must not exceed
+ *     32 MiB (e.g. M <= 1792 at d_model = 1024, d_ff = 4096); larger shapes
+ *     return TWELL_ERR_WORKSPACE before any launch.
+ *   - The first call on each device looks up the array's device address
+ *     (with that device current); make that first call before any stream
+ *     capture.
+ *   - Every call on a device shares the one array and it keeps the previous
+ *     call's contents; nothing in it needs to start at zero.  Calls that
+ *     overlap on the GPU (different streams, or graphs replayed concurrently)
+ *     race on it and must be serialised by the caller. */
+twell_status twell_ffn_fwd_noalloc(const void* x, const void* wgT, const void* wuT,
+                                   const void* wd, const twell_shape* shape,
+                                   const twell_hybrid* route, void* y, void* stream);
+
 /* Backward of the sparse FFN with the L1 activation term.  Source: the
  * training path of page 2, "¿Qué hace distinto a TwELL frente a ELL
  * clásico?" (hybrid rows) and "Receta de entrenamiento" (L1 with coefficient
