@@ -18,6 +18,7 @@ is reduced (max over ranks).
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import json
 import os
 import statistics
@@ -47,6 +48,8 @@ def parse_args():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=("own", "reference"), default="own")
     ap.add_argument("--workload", default="fwd_0p5b", choices=sorted(synthetic.WORKLOADS))
+    ap.add_argument("--density", type=float, default=None,
+                    help="override the workload's target gate density (density sweep)")
     ap.add_argument("--route-fraction", type=float, default=None,
                     help="fraction of rows the ELL width sends to the dense backup "
                          "(default: the workload's; 0 routes only rows with an overflowing tile)")
@@ -229,6 +232,8 @@ def run_own(args, dist):
     torch.cuda.set_device(dev)
     dist.init("nccl")
     wl = synthetic.WORKLOADS[args.workload]
+    if args.density is not None:
+        wl = dataclasses.replace(wl, density=args.density)
     bits = synthetic.make_workload(wl)
 
     def up(a):

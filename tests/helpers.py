@@ -130,3 +130,34 @@ def dense_intermediate_allowance(w, lam):
         "dwuT": r * np.abs(du).T @ np.abs(x),
         "dwd": r * np.abs(h).T @ np.abs(dy),
     }
+
+
+def bwd_allowance_sampled(w, lam, rows, neurons):
+    """bwd_allowance restricted to dX of `rows` and dW of `neurons` (so it
+    scales to full-size workloads)."""
+    import oracle
+
+    x, dy = oracle.f64(w["x"]), oracle.f64(w["dy"])
+    wg, wu, wd = oracle.f64(w["wgT"]), oracle.f64(w["wuT"]), oracle.f64(w["wd"])
+    d = x.shape[1]
+
+    def decisions(xs, wgs):
+        a = xs @ wgs.T
+        band = d * 2.0 ** -23 * (np.abs(xs) @ np.abs(wgs).T)
+        g_lo = oracle.f64(oracle.double_to_bf16(np.maximum(a - band, 0.0)))
+        g_hi = oracle.f64(oracle.double_to_bf16(np.maximum(a + band, 0.0)))
+        return g_hi - g_lo, (a - band <= 0.0) & (a + band > 0.0)
+
+    out = {}
+    xr = x[rows]
+    dg, flip = decisions(xr, wg)
+    u = xr @ wu.T
+    dh = dy[rows] @ wd.T
+    out["dx"] = (np.abs(dh) * dg) @ np.abs(wu) + np.where(flip, np.abs(dh * u + lam), 0.0) @ np.abs(wg)
+    dg, flip = decisions(x, wg[neurons])        # [M][n]
+    u = x @ wu[neurons].T
+    dh = dy @ wd[neurons].T
+    out["dwgT"] = np.where(flip, np.abs(dh * u + lam), 0.0).T @ np.abs(x)
+    out["dwuT"] = (np.abs(dh) * dg).T @ np.abs(x)
+    out["dwd"] = (dg * np.abs(u)).T @ np.abs(dy)
+    return out
