@@ -188,7 +188,8 @@ SparseWs carve_sparse(void* ws, const twell_shape& s, int W, int training) {
     w.gr = c.take<uint16_t>(Mp * f);
     w.ur = c.take<float>(Mp * f);
     w.ddr = c.take<uint16_t>(Mp * 4 * f);
-    w.mask_off = c.take<int>(2 * NB * f);
+    const long long NG = (NB + 31) / 32;
+    w.mask_off = c.take<int>((2 * NB + (NG > 0 ? NG : 1)) * f);
     w.csc_ptr = c.take<int>(f + 1);
     w.csc_row = c.take<int>(E > 0 ? E : 1);
     w.slot_pos = c.take<int>(E > 0 ? E : 1);
@@ -310,16 +311,19 @@ cudaError_t dx_gemm(const uint16_t* dd, long long rows, const twell_shape& s, co
 }
 
 // C[f][d] (+)= A^T B with A = [K][f] (leading dim lda) and B = [K][d], K from k_dev or K.
+// With lo_off > 0, A is a hi + lo pair (lo at column offset lo_off of the same
+// rows) and C (+)= (A_hi + A_lo)^T B in one launch.
 cudaError_t dw_gemm(const uint16_t* a, long long lda, const void* b, long long K,
                     const twell_shape& s, const int* k_dev, float* c, int accumulate,
-                    cudaStream_t st) {
+                    cudaStream_t st, long long lo_off = 0) {
   GemmParams p = base_params(s.d_ff, s.d_model, (int)K, kBN);
   p.k_dev = k_dev;
   p.c = c;
   p.ldc = s.d_model;
   p.c_f32 = 1;
   p.accumulate = accumulate;
-  const Mat A = mat(a, K, s.d_ff, lda);
+  p.a_seg_off = (int)lo_off;
+  const Mat A = mat(a, K, lo_off > 0 ? lo_off + s.d_ff : s.d_ff, lda);
   const Mat B = mat(b, K, s.d_model, s.d_model);
   return gemm_launch(GK_STORE_MM, A, B, nullptr, p, st);
 }
@@ -531,13 +535,10 @@ twell_status twell_ffn_bwd(const void* x, const void* wgT, const void* wuT, cons
   if (e == cudaSuccess)
     e = dgate_gemm(w.dyr, Mp, s, wd, nd, w.gr, nullptr, w.ur, w.ddr, true, l1_coeff, 1, cs);
   if (e == cudaSuccess) e = dx_gemm(w.ddr, Mp, s, wgT, wuT, true, nd, route->dense_rows, dx, cs);
-  // dW += (hi + lo)^T B as two accumulating passes
-  if (e == cudaSuccess) e = dw_gemm(w.hr, 2 * f, w.dyr, Mp, s, nd, dwd, 1, cs);
-  if (e == cudaSuccess) e = dw_gemm(w.hr + f, 2 * f, w.dyr, Mp, s, nd, dwd, 1, cs);
-  if (e == cudaSuccess) e = dw_gemm(w.ddr, 4 * f, w.xr, Mp, s, nd, dwuT, 1, cs);
-  if (e == cudaSuccess) e = dw_gemm(w.ddr + 2 * f, 4 * f, w.xr, Mp, s, nd, dwuT, 1, cs);
-  if (e == cudaSuccess) e = dw_gemm(w.ddr + f, 4 * f, w.xr, Mp, s, nd, dwgT, 1, cs);
-  if (e == cudaSuccess) e = dw_gemm(w.ddr + 3 * f, 4 * f, w.xr, Mp, s, nd, dwgT, 1, cs);
+  // dW += (hi + lo)^T B, both halves in one launch per weight
+  if (e == cudaSuccess) e = dw_gemm(w.hr, 2 * f, w.dyr, Mp, s, nd, dwd, 1, cs, f);
+  if (e == cudaSuccess) e = dw_gemm(w.ddr, 4 * f, w.xr, Mp, s, nd, dwuT, 1, cs, 2 * f);
+  if (e == cudaSuccess) e = dw_gemm(w.ddr + f, 4 * f, w.xr, Mp, s, nd, dwgT, 1, cs, 2 * f);
   return cuda_status(e);
 }
 

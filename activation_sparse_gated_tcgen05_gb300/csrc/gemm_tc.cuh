@@ -45,6 +45,8 @@ struct GemmParams {
   const int* k_dev;     // optional device K: K used = min(K, *k_dev)
   int n_tiles;          // tiles along N
   int k_split;          // K segment length in k-blocks: segment s reads B (s even) or B2 (s odd)
+  int a_seg_off;        // MN-major A only: if > 0, the K range is run twice, the second time
+                        // with A's M coordinate shifted by a_seg_off (B rows repeat): C += A0^T B + A1^T B
   int pad_rows;         // store every row of a visited tile that is < M (zero padding)
   int* status;
   // EPI_STORE
@@ -347,8 +349,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   int K_eff = p.K;
   if (p.k_dev) K_eff = min(K_eff, *p.k_dev);
   const int m_tiles = (M_eff + kBM - 1) / kBM;
-  const int num_kb = (K_eff + kBK - 1) / kBK;
+  const int kb_pass = (K_eff + kBK - 1) / kBK;
+  const int num_kb = (A_MN && p.a_seg_off > 0) ? 2 * kb_pass : kb_pass;
   const int total = (num_kb > 0 && M_eff > 0) ? m_tiles * p.n_tiles : 0;
+  // nothing to do (e.g. no routed rows): leave before touching TMEM or barriers
+  if (total == 0 || (int)blockIdx.x >= total) return;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
@@ -394,16 +399,20 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           if (!A_MN) {
             tma_load_2d(a_dst, &tmA, &full[stage], kb * kBK, mb * kBM);
           } else {
-            tma_load_2d(a_dst, &tmA, &full[stage], mb * kBM, kb * kBK);
-            tma_load_2d(a_dst + 8192, &tmA, &full[stage], mb * kBM + 64, kb * kBK);
+            const bool second = kb >= kb_pass;
+            const int ka = (second ? kb - kb_pass : kb) * kBK;
+            const int ma = mb * kBM + (second ? p.a_seg_off : 0);
+            tma_load_2d(a_dst, &tmA, &full[stage], ma, ka);
+            tma_load_2d(a_dst + 8192, &tmA, &full[stage], ma + 64, ka);
           }
           if (EPI == EPI_GATED) {
             tma_load_2d(b_dst, &tmB, &full[stage], kb * kBK, nb * 128);
             tma_load_2d(b_dst + 16384, &tmB2, &full[stage], kb * kBK, nb * 128);
           } else {
-            const int seg = kb / p.k_split;
+            const int kbb = (A_MN && kb >= kb_pass) ? kb - kb_pass : kb;  // B rows repeat
+            const int seg = kbb / p.k_split;
             const CUtensorMap* mp = (seg & 1) ? &tmB2 : &tmB;
-            const int kk = kb - seg * p.k_split;
+            const int kk = kbb - seg * p.k_split;
             if (!B_MN) {
               tma_load_2d(b_dst, mp, &full[stage], kk * kBK, nb * kBN);
             } else {

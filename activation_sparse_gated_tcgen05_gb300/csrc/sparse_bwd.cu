@@ -15,7 +15,8 @@
 //   1. csc_*: a column-major (neuron-major) index of the live entries, rows
 //      ascending inside every neuron.  Per 32-row block and neuron a bitmask
 //      of the rows that use the neuron gives every entry its rank without any
-//      ordering race: rank = prefix over blocks + popcount of lower bits.
+//      ordering race: rank = prefix over groups of 32 blocks + prefix over the
+//      blocks of its group + popcount of lower bits.
 //   2. bwd_rows: one team of warps per row computes dh, u, du, da, h per entry
 //      (stored at the entry's neuron-major position) and dX_m.
 //   3. bwd_neurons: one team per neuron sums its entries in ascending row
@@ -43,23 +44,40 @@ __global__ void __launch_bounds__(kWarps * 32)
   for (int s = lane; s < n; s += 32) atomicOr(mrow + ell_col[(long long)m * W + s], bit);
 }
 
-// For every neuron: exclusive prefix of live rows over the 32-row blocks.
-__global__ void __launch_bounds__(256)
+// Column scan of the row masks, in groups of 32 row blocks.  CTA (jb, g)
+// handles neurons [32 jb, 32 jb + 32) and row blocks [32 g, 32 g + 32):
+// off[b][j] = live rows of neuron j in the blocks of group g before b;
+// gtot[g][j] = live rows of neuron j in group g.
+constexpr int kScanG = 32;
+__global__ void __launch_bounds__(1024)
     csc_colscan_kernel(const unsigned* __restrict__ mask, int NB, int f, int* __restrict__ off,
-                       int* __restrict__ tot) {
-  const int j = blockIdx.x * blockDim.x + threadIdx.x;
-  if (j >= f) return;
-  int run = 0;
-  for (int b = 0; b < NB; ++b) {
-    off[(long long)b * f + j] = run;
-    run += __popc(mask[(long long)b * f + j]);
+                       int* __restrict__ gtot) {
+  __shared__ int c[kScanG][33];
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;  // w: block in group, lane: neuron
+  const int j = blockIdx.x * 32 + lane;
+  const int b = blockIdx.y * kScanG + w;
+  const bool ok = j < f && b < NB;
+  c[w][lane] = ok ? __popc(mask[(long long)b * f + j]) : 0;  // coalesced over neurons
+  __syncthreads();
+  if (w == 0) {  // warp 0: lane = neuron, serial prefix over the group's 32 blocks
+    int run = 0;
+#pragma unroll 8
+    for (int i = 0; i < kScanG; ++i) {
+      const int v = c[i][lane];
+      c[i][lane] = run;
+      run += v;
+    }
+    if (j < f) gtot[(long long)blockIdx.y * f + j] = run;
   }
-  tot[j] = run;
+  __syncthreads();
+  if (ok) off[(long long)b * f + j] = c[w][lane];
 }
 
-// csc_ptr[0..f] = exclusive prefix of tot (one block).
+// Per neuron: exclusive prefix over the groups (gpre[g][j], written over
+// gtot) and the neuron's total; then csc_ptr[0..f] = exclusive prefix of the
+// totals (one block).
 __global__ void __launch_bounds__(1024)
-    csc_ptr_kernel(const int* __restrict__ tot, int f, int* __restrict__ csc_ptr) {
+    csc_ptr_kernel(int* __restrict__ gtot, int NG, int f, int* __restrict__ csc_ptr) {
   __shared__ int warp_tot[32];
   __shared__ int carry;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -67,7 +85,14 @@ __global__ void __launch_bounds__(1024)
   __syncthreads();
   for (int base = 0; base < f; base += 1024) {
     const int j = base + tid;
-    const int c = j < f ? tot[j] : 0;
+    int c = 0;
+    if (j < f) {
+      for (int g = 0; g < NG; ++g) {
+        const int v = gtot[(long long)g * f + j];
+        gtot[(long long)g * f + j] = c;
+        c += v;
+      }
+    }
     const int incl = warp_incl_scan(c);
     if (lane == 31) warp_tot[warp] = incl;
     __syncthreads();
@@ -88,17 +113,18 @@ __global__ void __launch_bounds__(1024)
 __global__ void __launch_bounds__(kWarps * 32)
     csc_place_kernel(const uint16_t* __restrict__ ell_col, const int* __restrict__ ell_nnz, int M,
                      int W, int f, const unsigned* __restrict__ mask, const int* __restrict__ off,
-                     const int* __restrict__ csc_ptr, int* __restrict__ csc_row,
-                     int* __restrict__ slot_pos) {
+                     const int* __restrict__ gpre, const int* __restrict__ csc_ptr,
+                     int* __restrict__ csc_row, int* __restrict__ slot_pos) {
   const int lane = threadIdx.x & 31;
   const int m = blockIdx.x * kWarps + (threadIdx.x >> 5);
   if (m >= M) return;
   const int n = ell_nnz[m];
   const long long blk = (long long)(m >> 5) * f;
+  const long long grp = (long long)((m >> 5) / kScanG) * f;
   const unsigned below = (1u << (m & 31)) - 1u;
   for (int s = lane; s < n; s += 32) {
     const int j = ell_col[(long long)m * W + s];
-    const int pos = csc_ptr[j] + off[blk + j] + __popc(mask[blk + j] & below);
+    const int pos = csc_ptr[j] + gpre[grp + j] + off[blk + j] + __popc(mask[blk + j] & below);
     csc_row[pos] = m;
     slot_pos[(long long)m * W + s] = pos;
   }
@@ -357,13 +383,15 @@ cudaError_t neurons_team(const void* x, const void* dy, int d, int f, const int*
 
 }  // namespace
 
-// blk_counts holds two [ceil(M/32)][f] int arrays (row masks, then block offsets).
+// blk_counts holds the row masks and block offsets ([ceil(M/32)][f] ints each)
+// followed by the group totals / prefixes ([ceil(M/1024)][f] ints).
 cudaError_t launch_csc_build(const twell_hybrid& r, int M, int f, int* blk_counts, int* csc_ptr,
                              int* csc_row, int* slot_pos, cudaStream_t s) {
   const int NB = (M + 31) / 32;
+  const int NG = (NB + kScanG - 1) / kScanG;
   unsigned* mask = reinterpret_cast<unsigned*>(blk_counts);
   int* off = blk_counts + (long long)NB * f;
-  int* tot = csc_ptr;  // totals land in csc_ptr, then the scan rewrites it in place
+  int* gtot = off + (long long)NB * f;
   cudaError_t e = cudaMemsetAsync(mask, 0, sizeof(unsigned) * (size_t)NB * f, s);
   if (e != cudaSuccess) return e;
   if (M > 0) {
@@ -374,16 +402,18 @@ cudaError_t launch_csc_build(const twell_hybrid& r, int M, int f, int* blk_count
     }
     count_launch();
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    {
+      ProfScope prof("csc_colscan", s);
+      csc_colscan_kernel<<<dim3((f + 31) / 32, NG), 1024, 0, s>>>(mask, NB, f, off, gtot);
+    }
+    count_launch();
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  } else {
+    if ((e = cudaMemsetAsync(gtot, 0, sizeof(int) * (size_t)f, s)) != cudaSuccess) return e;
   }
-  {
-    ProfScope prof("csc_colscan", s);
-    csc_colscan_kernel<<<(f + 255) / 256, 256, 0, s>>>(mask, NB, f, off, tot);
-  }
-  count_launch();
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
   {
     ProfScope prof("csc_ptr", s);
-    csc_ptr_kernel<<<1, 1024, 0, s>>>(tot, f, csc_ptr);
+    csc_ptr_kernel<<<1, 1024, 0, s>>>(gtot, M > 0 ? NG : 1, f, csc_ptr);
   }
   count_launch();
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
@@ -391,7 +421,7 @@ cudaError_t launch_csc_build(const twell_hybrid& r, int M, int f, int* blk_count
     {
       ProfScope prof("csc_place", s);
       csc_place_kernel<<<(M + kWarps - 1) / kWarps, kWarps * 32, 0, s>>>(
-          r.ell_col, r.ell_nnz, M, r.ell_width, f, mask, off, csc_ptr, csc_row, slot_pos);
+          r.ell_col, r.ell_nnz, M, r.ell_width, f, mask, off, gtot, csc_ptr, csc_row, slot_pos);
     }
     count_launch();
     e = cudaGetLastError();

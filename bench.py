@@ -276,6 +276,17 @@ def run_own(args, dist):
         twell.twell_dense_ffn_fwd(x, wg, wu, wd, shape, y_d, True, ws_d)
         twell.twell_dense_ffn_bwd(x, wg, wu, wd, dy, shape, L1, dx_d, *dws_d, ws_d)
 
+    def graphed(fn):
+        """Capture fn (a whole step of library calls) into a CUDA graph; the
+        library is capture-safe (device-side routed-row counts, no host sync)."""
+        fn()  # eager once: function attributes and lazy module loads happen here
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            fn()
+        torch.cuda.synchronize()
+        return g.replay
+
     def timed(fn, steps, warmup, profile=None, clocks=None):
         for _ in range(warmup):
             flush.zero_()
@@ -348,11 +359,18 @@ def run_own(args, dist):
 
     gpu_idx = os.environ.get("CUDA_VISIBLE_DEVICES", str(dist.local)).split(",")[0]
     clocks = ClockSampler(gpu_idx if gpu_idx.isdigit() else dist.local)
-    ms_step, launches, prof, ck = timed(sparse_step, args.steps, args.warmup, profile=dominant,
-                                        clocks=clocks)
-    ms_fwd, _, _, _ = timed(sparse_fwd, args.steps, args.warmup)
-    ms_dfwd, _, _, _ = timed(dense_fwd, args.steps, args.warmup)
-    ms_dstep, _, _, _ = timed(dense_step, args.steps, args.warmup)
+    # headline: each step replayed from a CUDA graph (sparse and dense alike)
+    launches0 = twell.twell_launch_count()
+    step_g = graphed(sparse_step)
+    launches = twell.twell_launch_count() - launches0
+    launches_per_step = launches / 2  # the eager step and the captured one
+    ms_step, _, _, ck = timed(step_g, args.steps, args.warmup, clocks=clocks)
+    ms_fwd, _, _, _ = timed(graphed(sparse_fwd), args.steps, args.warmup)
+    ms_dfwd, _, _, _ = timed(graphed(dense_fwd), args.steps, args.warmup)
+    ms_dstep, _, _, _ = timed(graphed(dense_step), args.steps, args.warmup)
+    # eager steps with the dominant kernel's launches bracketed by CUDA events
+    ms_eager, eager_launches, prof, _ = timed(sparse_step, args.steps, args.warmup,
+                                              profile=dominant)
 
     # roofline of the dominant kernel, from its events inside the timed region
     peaks, peak_src = load_peaks()
@@ -388,7 +406,7 @@ def run_own(args, dist):
         yh.copy_(y, non_blocking=True)
         dxh.copy_(dx, non_blocking=True)
 
-    ms_e2e, _, _, _ = timed(e2e_step, args.steps, args.warmup)
+    ms_e2e, _, _, _ = timed(graphed(e2e_step), args.steps, args.warmup)
     bi = 2 * M * d * 2
     bo = 2 * M * d * 2
 
@@ -404,12 +422,15 @@ def run_own(args, dist):
         "dense_fwd_bwd_tokens_per_s": n * M / (ms_dstep / 1e3),
         "speedup_vs_dense": {"fwd": ms_dfwd / ms_fwd, "fwd_bwd": ms_dstep / ms_step},
         "ms": {"sparse_fwd_bwd": ms_step, "sparse_fwd": ms_fwd, "dense_fwd": ms_dfwd,
-               "dense_fwd_bwd": ms_dstep},
+               "dense_fwd_bwd": ms_dstep, "sparse_fwd_bwd_eager": ms_eager},
         "measured_density": density, "routed_rows": n_dense, "ell_entries": nnz_ell,
         "roofline": roof, "kernels": kernels, "kernels_dense_step": kernels_dense,
         "e2e": {"value": n * M / (ms_e2e / 1e3), "unit": UNIT, "h2d_bytes_per_step": bi,
                 "d2h_bytes_per_step": bo},
-        "gpu_launches": launches, "gpu_launches_per_step": launches / args.steps,
+        "gpu_launches": int(launches_per_step * args.steps),
+        "gpu_launches_per_step": launches_per_step,
+        "timing": "each step replayed from a CUDA graph of the library calls; "
+                  "ms.sparse_fwd_bwd_eager = the same step launched eagerly",
         "clocks": ck,
     }
     if dist.rank == 0 and n == 1 and not args.no_cpu_baseline:
