@@ -216,6 +216,44 @@ TW_DEV float warp_sum(float v) {
   return v;
 }
 
+// Sums of two values over the warp, every lane gets both (7 shuffles
+// instead of 10): the first exchange halves the work by letting lanes 0-15
+// carry a and lanes 16-31 carry b.
+TW_DEV void warp_sum2(float& a, float& b) {
+  const int lane = threadIdx.x & 31;
+  const bool lo = lane < 16;
+  float keep = lo ? a : b;
+  const float give = lo ? b : a;
+  keep += __shfl_xor_sync(0xffffffffu, give, 16);
+#pragma unroll
+  for (int o = 8; o > 0; o >>= 1) keep += __shfl_xor_sync(0xffffffffu, keep, o);
+  a = __shfl_sync(0xffffffffu, keep, 0);
+  b = __shfl_sync(0xffffffffu, keep, 16);
+}
+
+// Sums of four values over the warp, every lane gets all four (10 shuffles
+// instead of 20).
+TW_DEV void warp_sum4(float& a, float& b, float& c, float& d) {
+  const int lane = threadIdx.x & 31;
+  const bool h16 = lane & 16, h8 = lane & 8;
+  // step 1: lanes < 16 keep (a, b), lanes >= 16 keep (c, d)
+  float k0 = h16 ? c : a, k1 = h16 ? d : b;
+  const float g0 = h16 ? a : c, g1 = h16 ? b : d;
+  k0 += __shfl_xor_sync(0xffffffffu, g0, 16);
+  k1 += __shfl_xor_sync(0xffffffffu, g1, 16);
+  // step 2: within each half, lanes with bit 3 clear keep k0, set keep k1
+  float k = h8 ? k1 : k0;
+  const float g = h8 ? k0 : k1;
+  k += __shfl_xor_sync(0xffffffffu, g, 8);
+#pragma unroll
+  for (int o = 4; o > 0; o >>= 1) k += __shfl_xor_sync(0xffffffffu, k, o);
+  // totals: a at lanes 0-7, b at 8-15, c at 16-23, d at 24-31
+  a = __shfl_sync(0xffffffffu, k, 0);
+  b = __shfl_sync(0xffffffffu, k, 8);
+  c = __shfl_sync(0xffffffffu, k, 16);
+  d = __shfl_sync(0xffffffffu, k, 24);
+}
+
 TW_DEV int warp_incl_scan(int v) {
   const int lane = threadIdx.x & 31;
 #pragma unroll

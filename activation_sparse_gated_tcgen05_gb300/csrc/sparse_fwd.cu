@@ -77,7 +77,13 @@ __device__ __forceinline__ void process_entries(RowCtx<VPL>& c, int jl, float gl
       uint64_t a2 = 0;
 #pragma unroll
       for (int v = 0; v < VPL; ++v) a2 = dot8_f2(c.xf[v], wu[b][v], a2);
-      p[b] = warp_sum(f2_sum(a2));
+      p[b] = f2_sum(a2);
+    }
+    if (B == 2) {
+      warp_sum2(p[0], p[B - 1]);
+    } else {
+#pragma unroll
+      for (int b = 0; b < B; ++b) p[b] = warp_sum(p[b]);
     }
     if (TEAM > 1) {
       if (lane == 0)
