@@ -251,6 +251,13 @@ cudaError_t gated_gemm(const void* x_rows, long long rows, const twell_shape& s,
   const Mat A = mat(x_rows, rows, s.d_model, s.d_model);
   const Mat B = mat(wgT, s.d_ff, s.d_model, s.d_model);
   const Mat B2 = mat(wuT, s.d_ff, s.d_model, s.d_model);
+  if (!split && !u32) {  // dense layout: h, g, u through TMA stores
+    p.tma_out = 1;
+    const OutMat outs[3] = {{h, rows, s.d_ff, s.d_ff, 0, 32},
+                            {g ? g : h, rows, s.d_ff, s.d_ff, 0, 32},
+                            {u ? u : h, rows, s.d_ff, s.d_ff, 0, 32}};
+    return gemm_launch(GK_GATED, A, B, &B2, p, st, outs, 3);
+  }
   return gemm_launch(GK_GATED, A, B, &B2, p, st);
 }
 
@@ -268,6 +275,11 @@ cudaError_t down_gemm(const uint16_t* h, long long rows, const twell_shape& s, c
   p.k_split = s.d_ff / kBK;
   const Mat A = mat(h, rows, K, K);
   const Mat B = mat(wd, s.d_ff, s.d_model, s.d_model);  // [K = f][N = d], MN-major
+  if (!row_map && !m_dev) {
+    p.tma_out = 1;
+    const OutMat o{out, rows, s.d_model, s.d_model, 0, 32};
+    return gemm_launch(GK_STORE_KM, A, B, &B, p, st, &o, 1);
+  }
   return gemm_launch(GK_STORE_KM, A, B, &B, p, st);
 }
 
@@ -289,6 +301,11 @@ cudaError_t dgate_gemm(const void* dy_rows, long long rows, const twell_shape& s
   p.pad_rows = pad_rows;
   const Mat A = mat(dy_rows, rows, s.d_model, s.d_model);
   const Mat B = mat(wd, s.d_ff, s.d_model, s.d_model);  // [N = f][K = d], K-major
+  if (!split && !u32) {  // dense layout: du, da through TMA stores
+    p.tma_out = 1;
+    const OutMat o{dd, rows, 2LL * s.d_ff, 2LL * s.d_ff, 0, 32};
+    return gemm_launch(GK_BWD_GATE, A, B, nullptr, p, st, &o, 1);
+  }
   return gemm_launch(GK_BWD_GATE, A, B, nullptr, p, st);
 }
 
@@ -307,6 +324,11 @@ cudaError_t dx_gemm(const uint16_t* dd, long long rows, const twell_shape& s, co
   const Mat A = mat(dd, rows, K, K);
   const Mat B = mat(wuT, s.d_ff, s.d_model, s.d_model);   // [K][N], MN-major
   const Mat B2 = mat(wgT, s.d_ff, s.d_model, s.d_model);
+  if (!row_map && !m_dev) {
+    p.tma_out = 1;
+    const OutMat o{out, rows, s.d_model, s.d_model, 0, 32};
+    return gemm_launch(GK_STORE_KM, A, B, &B2, p, st, &o, 1);
+  }
   return gemm_launch(GK_STORE_KM, A, B, &B2, p, st);
 }
 
@@ -325,7 +347,9 @@ cudaError_t dw_gemm(const uint16_t* a, long long lda, const void* b, long long K
   p.a_seg_off = (int)lo_off;
   const Mat A = mat(a, K, lo_off > 0 ? lo_off + s.d_ff : s.d_ff, lda);
   const Mat B = mat(b, K, s.d_model, s.d_model);
-  return gemm_launch(GK_STORE_MM, A, B, nullptr, p, st);
+  p.tma_out = 1;  // fp32 boxes: TMA store, or TMA reduce-add when accumulating
+  const OutMat o{c, s.d_ff, s.d_model, s.d_model, 1, 32};
+  return gemm_launch(GK_STORE_MM, A, B, nullptr, p, st, &o, 1);
 }
 
 }  // namespace
@@ -613,7 +637,10 @@ twell_status twell_gemm_bf16(const void* A, const void* B, void* C, int32_t M, i
   const Mat b = b_mn_major ? mat(B, K, N, N) : mat(B, N, K, K);
   const GemmKind kind = a_mn_major ? (b_mn_major ? GK_STORE_MM : GK_STORE_MK)
                                    : (b_mn_major ? GK_STORE_KM : GK_STORE_KK);
-  return cuda_status(gemm_launch(kind, a, b, nullptr, p, reinterpret_cast<cudaStream_t>(stream)));
+  p.tma_out = 1;
+  const OutMat o{C, M, N, N, c_dtype, 32};
+  return cuda_status(
+      gemm_launch(kind, a, b, nullptr, p, reinterpret_cast<cudaStream_t>(stream), &o, 1));
 }
 
 }  // extern "C"

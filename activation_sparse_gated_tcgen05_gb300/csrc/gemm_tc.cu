@@ -40,9 +40,28 @@ bool make_map(CUtensorMap* m, const Mat& a, uint32_t box_inner, uint32_t box_out
   return r == CUDA_SUCCESS;
 }
 
+// Output map for TMA stores: box_cols x 32 rows, swizzle matching the row
+// bytes of the staging buffer (128-byte or 64-byte rows).
+bool make_out_map(CUtensorMap* m, const OutMat& o) {
+  auto fn = encode_fn();
+  if (!fn || !o.ptr || o.rows <= 0 || o.cols <= 0) return false;
+  const int esz = o.f32 ? 4 : 2;
+  const int row_bytes = o.box_cols * esz;
+  if (row_bytes != 128 && row_bytes != 64) return false;
+  cuuint64_t dims[2] = {(cuuint64_t)o.cols, (cuuint64_t)o.rows};
+  cuuint64_t strides[1] = {(cuuint64_t)o.ld * esz};
+  cuuint32_t box[2] = {(cuuint32_t)o.box_cols, 32};
+  cuuint32_t es[2] = {1, 1};
+  CUresult r = fn(m, o.f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+                  const_cast<void*>(o.ptr), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  row_bytes == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 template <bool A_MN, bool B_MN, int EPI>
 cudaError_t launch_t(const char* name, const Mat& A, const Mat& B, const Mat* B2,
-                     const GemmParams& p, cudaStream_t s) {
+                     const GemmParams& p, cudaStream_t s, const OutMat* outs, int n_outs) {
   CUtensorMap ta, tb, tb2;
   // A: K-major [M][K] -> box {64 (K), 128 rows}; MN-major [K][M] -> box {64 (M), 64 (K)}
   if (!make_map(&ta, A, 64, A_MN ? 64 : kBM)) return cudaErrorInvalidValue;
@@ -53,6 +72,14 @@ cudaError_t launch_t(const char* name, const Mat& A, const Mat& B, const Mat* B2
   } else {
     tb2 = tb;
   }
+  CUtensorMap to[3];
+  for (int i = 0; i < 3; ++i) {
+    if (i < n_outs) {
+      if (!make_out_map(&to[i], outs[i])) return cudaErrorInvalidValue;
+    } else {
+      to[i] = ta;  // unused
+    }
+  }
   auto kern = gemm_kernel<A_MN, B_MN, EPI>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kGemmSmem);
   if (e != cudaSuccess) return e;
@@ -62,7 +89,7 @@ cudaError_t launch_t(const char* name, const Mat& A, const Mat& B, const Mat* B2
   const int grid = (int)(tiles < num_sms() ? tiles : num_sms());
   {
     ProfScope prof(name, s);
-    kern<<<grid, kGemmThreads, kGemmSmem, s>>>(ta, tb, tb2, p);
+    kern<<<grid, kGemmThreads, kGemmSmem, s>>>(ta, tb, tb2, to[0], to[1], to[2], p);
   }
   count_launch();
   return cudaGetLastError();
@@ -71,15 +98,18 @@ cudaError_t launch_t(const char* name, const Mat& A, const Mat& B, const Mat* B2
 }  // namespace
 
 cudaError_t gemm_launch(GemmKind kind, const Mat& A, const Mat& B, const Mat* B2,
-                        const GemmParams& p, cudaStream_t s) {
+                        const GemmParams& p, cudaStream_t s, const OutMat* outs, int n_outs) {
   switch (kind) {
-    case GK_STORE_KK: return launch_t<false, false, EPI_STORE>("gemm_store_kk", A, B, B2, p, s);
-    case GK_STORE_MK: return launch_t<true, false, EPI_STORE>("gemm_store_mk", A, B, B2, p, s);
-    case GK_STORE_KM: return launch_t<false, true, EPI_STORE>("gemm_store_km", A, B, B2, p, s);
-    case GK_STORE_MM: return launch_t<true, true, EPI_STORE>("gemm_store_mm", A, B, B2, p, s);
-    case GK_PACK: return launch_t<false, false, EPI_PACK>("gemm_gate_pack", A, B, B2, p, s);
-    case GK_GATED: return launch_t<false, false, EPI_GATED>("gemm_gated", A, B, B2, p, s);
-    case GK_BWD_GATE: return launch_t<false, false, EPI_BWD_GATE>("gemm_dgate", A, B, B2, p, s);
+#define TW_CASE(K, AM, BM, E, NAME) \
+  case K: return launch_t<AM, BM, E>(NAME, A, B, B2, p, s, outs, n_outs);
+    TW_CASE(GK_STORE_KK, false, false, EPI_STORE, "gemm_store_kk")
+    TW_CASE(GK_STORE_MK, true, false, EPI_STORE, "gemm_store_mk")
+    TW_CASE(GK_STORE_KM, false, true, EPI_STORE, "gemm_store_km")
+    TW_CASE(GK_STORE_MM, true, true, EPI_STORE, "gemm_store_mm")
+    TW_CASE(GK_PACK, false, false, EPI_PACK, "gemm_gate_pack")
+    TW_CASE(GK_GATED, false, false, EPI_GATED, "gemm_gated")
+    TW_CASE(GK_BWD_GATE, false, false, EPI_BWD_GATE, "gemm_dgate")
+#undef TW_CASE
   }
   return cudaErrorInvalidValue;
 }

@@ -37,7 +37,9 @@ constexpr int kGemmThreads = 384;
 constexpr int kEpiThreads = 256;  // warps 4..11
 constexpr int kGroupM = 16;
 constexpr uint32_t kTmemCols = 512;
-constexpr int kGemmSmem = kStages * (kABytes + kBBytes) + 1024 /*align*/ + 256 /*barriers*/;
+constexpr int kStageBytes = 4096;  // per epilogue warp: 32 rows x 128 B output staging
+constexpr int kGemmSmem =
+    kStages * (kABytes + kBBytes) + 8 * kStageBytes + 1024 /*align*/ + 256 /*barriers*/;
 
 struct GemmParams {
   int M, N, K;          // M: rows (buffer capacity), N: output columns, K: reduction
@@ -48,6 +50,7 @@ struct GemmParams {
   int a_seg_off;        // MN-major A only: if > 0, the K range is run twice, the second time
                         // with A's M coordinate shifted by a_seg_off (B rows repeat): C += A0^T B + A1^T B
   int pad_rows;         // store every row of a visited tile that is < M (zero padding)
+  int tma_out;          // outputs go through shared memory and TMA stores (tensor maps O0..O2)
   int* status;
   // EPI_STORE
   void* c;
@@ -92,13 +95,93 @@ __device__ __forceinline__ void tile_coords(int tile, int m_tiles, int n_tiles, 
 }
 
 // ------------------------------------------------------------------ epilogues
+// Output staging: each epilogue warp owns a 4 KB shared-memory buffer; lane r
+// writes row r of a 32-row box (128-byte swizzle for 128-byte rows, 64-byte
+// swizzle for 64-byte rows, matching the tensor maps, so the 16-byte writes
+// of a warp hit distinct banks) and lane 0 sends the box with a TMA store.
+struct Stager {
+  uint8_t* buf;
+  int lane;
+  int n;  // stores issued so far
+  // 128-byte rows: the whole buffer; waits for the previous store's read
+  __device__ __forceinline__ uint8_t* full() {
+    if (lane == 0) bulk_wait_read<0>();
+    __syncwarp();
+    return buf;
+  }
+  // 64-byte rows: the two 2 KB halves in turn, one store may stay in flight
+  __device__ __forceinline__ uint8_t* half() {
+    if (lane == 0) bulk_wait_read<1>();
+    __syncwarp();
+    return buf + ((n & 1) << 11);
+  }
+  __device__ __forceinline__ void put128(uint8_t* b, int c, const uint4& v) const {
+    *reinterpret_cast<uint4*>(b + lane * 128 + ((c ^ (lane & 7)) << 4)) = v;
+  }
+  __device__ __forceinline__ void put64(uint8_t* b, int c, const uint4& v) const {
+    *reinterpret_cast<uint4*>(b + lane * 64 + ((c ^ ((lane >> 1) & 3)) << 4)) = v;
+  }
+  __device__ __forceinline__ void send(const CUtensorMap* map, const uint8_t* b, int col, int row,
+                                       bool reduce_add = false) {
+    fence_proxy_async();
+    __syncwarp();
+    if (lane == 0) {
+      if (reduce_add)
+        tma_reduce_add_2d(map, b, col, row);
+      else
+        tma_store_2d(map, b, col, row);
+      bulk_commit();
+    }
+    ++n;
+  }
+  __device__ __forceinline__ void drain() {
+    if (lane == 0) bulk_wait_all();
+    __syncwarp();
+  }
+};
+
+struct OutMaps {
+  const CUtensorMap* o0;
+  const CUtensorMap* o1;
+  const CUtensorMap* o2;
+};
+
 template <int EPI>
 struct Epilogue;
 
 template <>
 struct Epilogue<EPI_STORE> {
   static __device__ __forceinline__ void run(const GemmParams& p, uint32_t tacc, int row,
-                                             bool row_ok, int n0, int N, int half) {
+                                             bool row_ok, int n0, int N, int half, Stager& st,
+                                             const OutMaps& om, int row0) {
+    if (p.tma_out) {
+      // C through TMA: bf16 in 64-column boxes, fp32 in 32-column boxes (+= via reduce-add)
+#pragma unroll 1
+      for (int c0 = half * (kBN / 2); c0 < (half + 1) * (kBN / 2); c0 += 32) {
+        uint32_t r[32];
+        tmem_ld32(tacc + c0, r);
+        tmem_wait_ld();
+        if (n0 + c0 >= N || row0 >= p.M) continue;  // box wholly outside C (warp-uniform)
+        if (p.c_f32) {
+          uint8_t* b = st.full();
+#pragma unroll
+          for (int v = 0; v < 8; ++v)
+            st.put128(b, v, make_uint4(r[4 * v], r[4 * v + 1], r[4 * v + 2], r[4 * v + 3]));
+          st.send(om.o0, b, n0 + c0, row0, p.accumulate != 0);
+        } else {
+          uint8_t* b = st.half();
+#pragma unroll
+          for (int v = 0; v < 4; ++v)
+            st.put64(b, v,
+                     make_uint4(pack_bf16x2(__uint_as_float(r[8 * v]), __uint_as_float(r[8 * v + 1])),
+                                pack_bf16x2(__uint_as_float(r[8 * v + 2]), __uint_as_float(r[8 * v + 3])),
+                                pack_bf16x2(__uint_as_float(r[8 * v + 4]), __uint_as_float(r[8 * v + 5])),
+                                pack_bf16x2(__uint_as_float(r[8 * v + 6]), __uint_as_float(r[8 * v + 7]))));
+          st.send(om.o0, b, n0 + c0, row0);
+        }
+      }
+      return;
+    }
     const int dst_row = (row_ok && p.row_map) ? p.row_map[row] : row;
 #pragma unroll 1
     for (int c0 = half * (kBN / 2); c0 < (half + 1) * (kBN / 2); c0 += 32) {
@@ -168,7 +251,8 @@ __device__ __forceinline__ uint32_t select32(const uint32_t (&r)[32], int i) {
 template <>
 struct Epilogue<EPI_PACK> {
   static __device__ __forceinline__ void run(const GemmParams& p, uint32_t tacc, int row,
-                                             bool row_ok, int n0, int /*N*/, int half) {
+                                             bool row_ok, int n0, int /*N*/, int half, Stager&,
+                                             const OutMaps&, int) {
     const float kLiveMin = __uint_as_float(0x00008000u);  // 2^-134
     const int tiles_here = (kBN / 2) / p.tile_n;
     const int chunks_per_tile = p.tile_n / 32;
@@ -213,7 +297,8 @@ struct Epilogue<EPI_PACK> {
 template <>
 struct Epilogue<EPI_GATED> {
   static __device__ __forceinline__ void run(const GemmParams& p, uint32_t tacc, int row,
-                                             bool row_ok, int n0, int N, int half) {
+                                             bool row_ok, int n0, int N, int half, Stager& st,
+                                             const OutMaps& om, int row0) {
     // here n0 is the neuron offset (tile index * 128); this thread takes 64 neurons
 #pragma unroll 1
     for (int c0 = half * 64; c0 < half * 64 + 64; c0 += 32) {
@@ -221,6 +306,40 @@ struct Epilogue<EPI_GATED> {
       tmem_ld32(tacc + c0, ra);
       tmem_ld32(tacc + 128 + c0, ru);
       tmem_wait_ld();
+      if (p.tma_out) {
+        // h (and g, u) through TMA in 32-neuron boxes
+        if (n0 + c0 >= N || row0 >= p.M) continue;
+        uint32_t hw[16], gw[16], uw[16];
+#pragma unroll
+        for (int q = 0; q < 16; ++q) {
+          const uint32_t g0 = relu_bf16_bits(__uint_as_float(ra[2 * q]));
+          const uint32_t g1 = relu_bf16_bits(__uint_as_float(ra[2 * q + 1]));
+          const float u0 = __uint_as_float(ru[2 * q]), u1 = __uint_as_float(ru[2 * q + 1]);
+          hw[q] = pack_bf16x2(bf16_bits_to_float(g0) * u0, bf16_bits_to_float(g1) * u1);
+          gw[q] = g0 | (g1 << 16);
+          uw[q] = pack_bf16x2(u0, u1);
+        }
+        uint8_t* b = st.half();
+#pragma unroll
+        for (int v = 0; v < 4; ++v)
+          st.put64(b, v, make_uint4(hw[4 * v], hw[4 * v + 1], hw[4 * v + 2], hw[4 * v + 3]));
+        st.send(om.o0, b, n0 + c0, row0);
+        if (p.g_out) {
+          b = st.half();
+#pragma unroll
+          for (int v = 0; v < 4; ++v)
+            st.put64(b, v, make_uint4(gw[4 * v], gw[4 * v + 1], gw[4 * v + 2], gw[4 * v + 3]));
+          st.send(om.o1, b, n0 + c0, row0);
+        }
+        if (p.u_out) {
+          b = st.half();
+#pragma unroll
+          for (int v = 0; v < 4; ++v)
+            st.put64(b, v, make_uint4(uw[4 * v], uw[4 * v + 1], uw[4 * v + 2], uw[4 * v + 3]));
+          st.send(om.o2, b, n0 + c0, row0);
+        }
+        continue;
+      }
       if (!row_ok || n0 + c0 >= N) continue;
       const long long off = (long long)row * p.ldh + n0 + c0;
       const long long ogu = (long long)row * p.ldgu + n0 + c0;
@@ -266,13 +385,51 @@ struct Epilogue<EPI_GATED> {
 template <>
 struct Epilogue<EPI_BWD_GATE> {
   static __device__ __forceinline__ void run(const GemmParams& p, uint32_t tacc, int row,
-                                             bool row_ok, int n0, int N, int half) {
+                                             bool row_ok, int n0, int N, int half, Stager& st,
+                                             const OutMaps& om, int row0) {
     const long long seg = p.dd_seg;
 #pragma unroll 1
     for (int c0 = half * (kBN / 2); c0 < (half + 1) * (kBN / 2); c0 += 32) {
       uint32_t r[32];
       tmem_ld32(tacc + c0, r);
       tmem_wait_ld();
+      if (p.tma_out) {
+        // du, da through TMA in 32-column boxes; g, u read straight from global
+        if (n0 + c0 >= N || row0 >= p.M) continue;
+        uint32_t duw[16], daw[16];
+        const bool in = row < p.M;
+        const long long gu = (long long)row * p.ldgu + n0 + c0;
+#pragma unroll
+        for (int v = 0; v < 4; ++v) {
+          const uint4 g8 = in ? *reinterpret_cast<const uint4*>(p.g_in + gu + 8 * v)
+                              : make_uint4(0, 0, 0, 0);
+          const uint4 u8 = in ? *reinterpret_cast<const uint4*>(p.u_in + gu + 8 * v)
+                              : make_uint4(0, 0, 0, 0);
+          const uint32_t gw[4] = {g8.x, g8.y, g8.z, g8.w};
+          const uint32_t uw[4] = {u8.x, u8.y, u8.z, u8.w};
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const float2 g = unpack_bf16x2(gw[q]);
+            const float2 u = unpack_bf16x2(uw[q]);
+            const float dh0 = __uint_as_float(r[8 * v + 2 * q]);
+            const float dh1 = __uint_as_float(r[8 * v + 2 * q + 1]);
+            duw[4 * v + q] = pack_bf16x2(dh0 * g.x, dh1 * g.y);
+            daw[4 * v + q] = pack_bf16x2(g.x > 0.f ? fmaf(dh0, u.x, p.lambda) : 0.f,
+                                         g.y > 0.f ? fmaf(dh1, u.y, p.lambda) : 0.f);
+          }
+        }
+        uint8_t* b = st.half();
+#pragma unroll
+        for (int v = 0; v < 4; ++v)
+          st.put64(b, v, make_uint4(duw[4 * v], duw[4 * v + 1], duw[4 * v + 2], duw[4 * v + 3]));
+        st.send(om.o0, b, n0 + c0, row0);
+        b = st.half();
+#pragma unroll
+        for (int v = 0; v < 4; ++v)
+          st.put64(b, v, make_uint4(daw[4 * v], daw[4 * v + 1], daw[4 * v + 2], daw[4 * v + 3]));
+        st.send(om.o0, b, n0 + c0 + (int)seg, row0);
+        continue;
+      }
       if (!row_ok || n0 + c0 >= N) continue;
       const long long gu = (long long)row * p.ldgu + n0 + c0;
       const long long o = (long long)row * p.ld_dd + n0 + c0;
@@ -328,13 +485,16 @@ struct Epilogue<EPI_BWD_GATE> {
 template <bool A_MN, bool B_MN, int EPI>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                const __grid_constant__ CUtensorMap tmB2, const GemmParams p) {
+                const __grid_constant__ CUtensorMap tmB2, const __grid_constant__ CUtensorMap tmO0,
+                const __grid_constant__ CUtensorMap tmO1, const __grid_constant__ CUtensorMap tmO2,
+                const GemmParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
   uint8_t* sA = smem;
   uint8_t* sB = smem + kStages * kABytes;
-  uint64_t* full = reinterpret_cast<uint64_t*>(sB + kStages * kBBytes);
+  uint8_t* sOut = sB + kStages * kBBytes;  // 8 x 4 KB epilogue staging buffers
+  uint64_t* full = reinterpret_cast<uint64_t*>(sOut + 8 * kStageBytes);
   uint64_t* empty = full + kStages;
   uint64_t* tfull = empty + kStages;
   uint64_t* tempty = tfull + 2;
@@ -485,6 +645,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     const int quarter = warp & 3;
     const int half = (warp - 4) >> 2;
     const int r_local = quarter * 32 + lane;
+    Stager st{sOut + (warp - 4) * kStageBytes, lane, 0};
+    const OutMaps om{&tmO0, &tmO1, &tmO2};
     int it = 0;
     for (int tile = blockIdx.x; tile < total; tile += gridDim.x, ++it) {
       int mb, nb;
@@ -501,10 +663,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       const bool row_ok = p.pad_rows ? (row < p.M) : (row < M_eff);
       const uint32_t tacc = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * kBN);
       const int n0 = (EPI == EPI_GATED) ? nb * 128 : nb * kBN;
-      Epilogue<EPI>::run(p, tacc, row, row_ok, n0, p.N, half);
+      Epilogue<EPI>::run(p, tacc, row, row_ok, n0, p.N, half, st, om, mb * kBM + quarter * 32);
       tc_fence_before();
       mbar_arrive(&tempty[acc]);
     }
+    st.drain();  // staged stores finish reading shared memory before the CTA exits
   }
 
   __syncthreads();

@@ -16,6 +16,15 @@ struct Mat {
   long long rows, cols, ld;
 };
 
+// An output the epilogue writes through TMA: rows x cols elements (bf16 or
+// fp32), leading dimension ld, boxes of box_cols x 32 rows.
+struct OutMat {
+  const void* ptr;
+  long long rows, cols, ld;
+  int f32;
+  int box_cols;
+};
+
 // Which epilogue / operand majorness a GEMM launch uses.
 enum GemmKind {
   GK_STORE_KK = 0,   // A K-major, B K-major, store
@@ -45,7 +54,8 @@ int* device_status_ptr();  // per-device status word (device address)
 // its storage layout.  Returns a CUDA error or cudaSuccess; an invalid
 // tensor-map encode returns cudaErrorInvalidValue.
 cudaError_t gemm_launch(GemmKind kind, const Mat& A, const Mat& B, const Mat* B2,
-                        const GemmParams& p, cudaStream_t stream);
+                        const GemmParams& p, cudaStream_t stream, const OutMat* outs = nullptr,
+                        int n_outs = 0);
 
 // Non-tensor-core kernels (pack.cu, sparse_fwd.cu, sparse_bwd.cu).
 cudaError_t launch_pack_dense(const void* a, int a_f32, int M, int f, int tile_n, int cap,
