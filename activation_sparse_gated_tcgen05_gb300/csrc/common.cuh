@@ -65,7 +65,8 @@ TW_DEV bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 
 // Wait for the phase with the given parity to complete.  Gives up (returns
 // false) once the CTA-wide abort flag is raised or after kWaitLimitNs.
-TW_DEV bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag) {
+TW_DEV bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
+                      uint64_t limit_ns = kWaitLimitNs) {
   const uint32_t a = smem_u32(bar);
   if (mbar_try_wait(a, parity)) return true;
   const uint64_t t0 = globaltimer();
@@ -74,7 +75,7 @@ TW_DEV bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag) 
     for (int i = 0; i < 32; ++i)
       if (mbar_try_wait(a, parity)) return true;
     if (abort_flag && *abort_flag) return false;
-    if (globaltimer() - t0 > kWaitLimitNs) return false;
+    if (globaltimer() - t0 > limit_ns) return false;
   }
 }
 

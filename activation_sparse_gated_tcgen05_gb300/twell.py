@@ -32,7 +32,7 @@ EXPORTS = (
     "twell_ffn_bwd", "twell_dense_workspace_bytes", "twell_dense_ffn_fwd", "twell_dense_ffn_bwd",
     "twell_gemm_bf16", "twell_get_device_status", "twell_status_string", "twell_num_sms",
     "twell_launch_count", "twell_profile_begin", "twell_profile_end", "twell_profile_entry",
-    "twell_ffn_fwd_noalloc",
+    "twell_ffn_fwd_noalloc", "twell_selftest_wait_timeout", "twell_probe_gather",
 )
 
 
@@ -82,6 +82,8 @@ def load():
         "twell_ffn_fwd": (I32, [P, P, P, P, SP, TP, HP, P, P, SZ, P]),
         "twell_ffn_bwd": (I32, [P, P, P, P, P, SP, HP, F, P, P, P, P, P, SZ, P]),
         "twell_ffn_fwd_noalloc": (I32, [P, P, P, P, SP, HP, P, P]),
+        "twell_selftest_wait_timeout": (I32, [I32, P]),
+        "twell_probe_gather": (I32, [P, ctypes.c_int64, I32, P, ctypes.c_int64, P, I32, P]),
         "twell_dense_workspace_bytes": (SZ, [SP, I32]),
         "twell_dense_ffn_fwd": (I32, [P, P, P, P, SP, P, I32, P, SZ, P]),
         "twell_dense_ffn_bwd": (I32, [P, P, P, P, P, SP, F, P, P, P, P, P, SZ, P]),
@@ -282,6 +284,17 @@ def twell_get_device_status(stream=None) -> int:
 
 def twell_num_sms() -> int:
     return int(load().twell_num_sms())
+
+
+def twell_selftest_wait_timeout(limit_us: int, stream=None):
+    _check("twell_selftest_wait_timeout",
+           load().twell_selftest_wait_timeout(int(limit_us), _stream(stream)))
+
+
+def twell_probe_gather(table, row_bytes: int, idx, out, blocks: int, stream=None):
+    _check("twell_probe_gather", load().twell_probe_gather(
+        _ptr(table), table.numel() * table.element_size() // int(row_bytes), int(row_bytes),
+        _ptr(idx), idx.numel(), _ptr(out), int(blocks), _stream(stream)))
 
 
 def twell_launch_count() -> int:

@@ -372,6 +372,30 @@ def run_own(args, dist):
     ms_eager, eager_launches, prof, _ = timed(sparse_step, args.steps, args.warmup,
                                               profile=dominant)
 
+    # achievable row-gather bandwidth (the sparse kernels' access pattern):
+    # rows of 2*d_model bytes at random ids from a table that fits in L2
+    # (the weights of this workload) and from one ten times larger than L2
+    def probe(table_bytes, n_rows=1 << 20):
+        row_bytes = 2 * d
+        rows = table_bytes // row_bytes
+        table = torch.empty(rows * row_bytes // 4, dtype=torch.int32, device=dev)
+        idx = torch.randint(0, rows, (n_rows,), dtype=torch.int32, device=dev)
+        out = torch.empty(152 * 32 * 8, dtype=torch.int32, device=dev)
+        blocks = 32 * twell.twell_num_sms()
+        for _ in range(2):
+            twell.twell_probe_gather(table, row_bytes, idx, out, blocks)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(5):
+            twell.twell_probe_gather(table, row_bytes, idx, out, blocks)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        return 5 * n_rows * row_bytes / (e0.elapsed_time(e1) / 1e3) / 1e9
+
+    gather_probe = {"row_bytes": 2 * d, "l2_resident_table_bytes": 2 * f * d * 2,
+                    "l2_gbs": probe(2 * f * d * 2), "dram_table_bytes": 2 << 30,
+                    "dram_gbs": probe(2 << 30)}
+
     # roofline of the dominant kernel, from its events inside the timed region
     peaks, peak_src = load_peaks()
     roof = None
@@ -390,6 +414,11 @@ def run_own(args, dist):
                 "unit": punit, "frac": achieved / peak, "peak_source": peak_src,
                 "work_per_launch": amount, "work_unit": unit, "ms_per_launch": dom_ms / cnt,
                 "traffic": traffic_for(dominant, wl.name)}
+        if unit == "byte":
+            # the weight rows this kernel gathers are L2-resident at this size:
+            # its ceiling is the measured L2 row-gather bandwidth
+            roof["l2_gather_peak"] = gather_probe["l2_gbs"]
+            roof["frac_of_l2_gather"] = achieved / gather_probe["l2_gbs"]
 
     # end to end through the C ABI with host buffers (H2D inputs, D2H results)
     xh = torch.empty((M, d), dtype=torch.bfloat16).pin_memory()
@@ -424,7 +453,8 @@ def run_own(args, dist):
         "ms": {"sparse_fwd_bwd": ms_step, "sparse_fwd": ms_fwd, "dense_fwd": ms_dfwd,
                "dense_fwd_bwd": ms_dstep, "sparse_fwd_bwd_eager": ms_eager},
         "measured_density": density, "routed_rows": n_dense, "ell_entries": nnz_ell,
-        "roofline": roof, "kernels": kernels, "kernels_dense_step": kernels_dense,
+        "roofline": roof, "gather_probe": gather_probe, "kernels": kernels,
+        "kernels_dense_step": kernels_dense,
         "e2e": {"value": n * M / (ms_e2e / 1e3), "unit": UNIT, "h2d_bytes_per_step": bi,
                 "d2h_bytes_per_step": bo},
         "gpu_launches": int(launches_per_step * args.steps),

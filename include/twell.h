@@ -212,6 +212,23 @@ twell_status twell_gemm_bf16(const void* A, const void* B, void* C, int32_t M, i
                              int32_t K, int32_t a_mn_major, int32_t b_mn_major, int32_t c_dtype,
                              int32_t accumulate, void* stream);
 
+/* Failure-path self-test: one kernel waits on an mbarrier that nothing
+ * completes, using the same bounded wait as the GEMM pipeline but with a
+ * limit of limit_us microseconds (1 .. 10^7); when it gives up it records
+ * TWELL_ERR_DEVICE_TIMEOUT in the device status word and returns, so the
+ * error path is exercised without a fault and the context stays usable.
+ * Read the result with twell_get_device_status.  Not part of the method. */
+twell_status twell_selftest_wait_timeout(int32_t limit_us, void* stream);
+
+/* Row-gather bandwidth probe (measurement helper, not part of the method):
+ * blocks x 8 warps read n_idx whole rows table[idx[i]] (row_bytes each, a
+ * multiple of 16, 16-byte loads) -- the access pattern of the sparse gather
+ * kernels -- and write one folded word per warp to out (blocks * 8 words).
+ * Time it with the profiler family "gather_probe" or events. */
+twell_status twell_probe_gather(const void* table, int64_t table_rows, int32_t row_bytes,
+                                const int32_t* idx, int64_t n_idx, uint32_t* out, int32_t blocks,
+                                void* stream);
+
 /* Reads and clears the device status word of the current device after
  * synchronising `stream`.  *out receives TWELL_OK or the first error seen. */
 twell_status twell_get_device_status(void* stream, int32_t* out);
@@ -234,7 +251,7 @@ uint64_t twell_launch_count(void);
  * available from twell_profile_entry (name valid until the next begin/end).
  * Families: gemm_gate_pack, gemm_gated, gemm_dgate, gemm_store_kk/mk/km/mm,
  * pack_dense, route_rows, route_list, gather_rows, sparse_fwd, csc_mark,
- * csc_colscan, csc_ptr, csc_place, bwd_rows, bwd_neurons.  Host-side state,
+ * csc_colscan, csc_ptr, csc_place, bwd_rows, bwd_neurons, gather_probe.  Host-side state,
  * process-wide; not for use while another thread launches. */
 twell_status twell_profile_begin(const char* kernel);
 int32_t twell_profile_end(void);
