@@ -325,6 +325,31 @@ TW_DEV uint64_t dot8_f2(const uint64_t (&a)[4], const uint4& w, uint64_t acc) {
   acc = f2_fma(a[3], bf2_to_f2(w.w), acc);
   return acc;
 }
+// Mixed-precision dot of 8 bf16 x 8 bf16 with fp32 accumulation: the bf16
+// halves feed the FMA directly (fma.rn.f32.bf16), no unpacking; two partial
+// sums keep the dependency chains short.
+TW_DEV void bf16_fma(float& acc, uint32_t a_word, uint32_t b_word, bool hi) {
+  uint16_t a16, b16;
+  if (hi) {
+    asm("{ .reg .b16 t; mov.b32 {t, %0}, %1; }" : "=h"(a16) : "r"(a_word));
+    asm("{ .reg .b16 t; mov.b32 {t, %0}, %1; }" : "=h"(b16) : "r"(b_word));
+  } else {
+    asm("{ .reg .b16 t; mov.b32 {%0, t}, %1; }" : "=h"(a16) : "r"(a_word));
+    asm("{ .reg .b16 t; mov.b32 {%0, t}, %1; }" : "=h"(b16) : "r"(b_word));
+  }
+  asm("fma.rn.f32.bf16 %0, %1, %2, %0;" : "+f"(acc) : "h"(a16), "h"(b16));
+}
+TW_DEV void dot8_bf16(const uint4& a, const uint4& b, float& acc0, float& acc1) {
+  bf16_fma(acc0, a.x, b.x, false);
+  bf16_fma(acc1, a.x, b.x, true);
+  bf16_fma(acc0, a.y, b.y, false);
+  bf16_fma(acc1, a.y, b.y, true);
+  bf16_fma(acc0, a.z, b.z, false);
+  bf16_fma(acc1, a.z, b.z, true);
+  bf16_fma(acc0, a.w, b.w, false);
+  bf16_fma(acc1, a.w, b.w, true);
+}
+
 // acc (fp32 pairs) += s * w (8 bf16)
 TW_DEV void axpy8_f2(uint64_t s2, const uint4& w, uint64_t (&acc)[4]) {
   acc[0] = f2_fma(s2, bf2_to_f2(w.x), acc[0]);

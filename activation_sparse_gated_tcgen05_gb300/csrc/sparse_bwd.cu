@@ -152,13 +152,14 @@ __global__ void __launch_bounds__(256, VPL > 2 ? 1 : 2)
   const int m = blockIdx.x * ROWS + team;
   if (m >= M) return;
 
-  uint64_t xf[VPL][4], dyf[VPL][4], acc[VPL][4];
+  uint4 xp[VPL], dyp[VPL];  // x_m, dY_m slabs, packed bf16
+  uint64_t acc[VPL][4];
 #pragma unroll
   for (int v = 0; v < VPL; ++v) {
     const int e = slab<TEAM>(lane, wt, v);
     const bool ok = e < d;
-    bf8_to_f2(ok ? ldg_v4(x + (long long)m * d + e) : make_uint4(0, 0, 0, 0), xf[v]);
-    bf8_to_f2(ok ? ldg_v4(dy + (long long)m * d + e) : make_uint4(0, 0, 0, 0), dyf[v]);
+    xp[v] = ok ? ldg_v4(x + (long long)m * d + e) : make_uint4(0, 0, 0, 0);
+    dyp[v] = ok ? ldg_v4(dy + (long long)m * d + e) : make_uint4(0, 0, 0, 0);
 #pragma unroll
     for (int k = 0; k < 4; ++k) acc[v][k] = 0;
   }
@@ -203,14 +204,14 @@ __global__ void __launch_bounds__(256, VPL > 2 ? 1 : 2)
       float dh[B], u[B];
 #pragma unroll
       for (int b = 0; b < B; ++b) {
-        uint64_t a = 0, c = 0;
+        float a0 = 0.f, a1 = 0.f, c0 = 0.f, c1 = 0.f;
 #pragma unroll
         for (int v = 0; v < VPL; ++v) {
-          a = dot8_f2(dyf[v], wdv[b][v], a);
-          c = dot8_f2(xf[v], wuv[b][v], c);
+          dot8_bf16(dyp[v], wdv[b][v], a0, a1);
+          dot8_bf16(xp[v], wuv[b][v], c0, c1);
         }
-        dh[b] = warp_sum(f2_sum(a));
-        u[b] = warp_sum(f2_sum(c));
+        dh[b] = warp_sum(a0 + a1);
+        u[b] = warp_sum(c0 + c1);
       }
       if (TEAM > 1) {
         if (lane == 0)

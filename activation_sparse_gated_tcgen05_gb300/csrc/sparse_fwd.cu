@@ -35,7 +35,7 @@ __device__ __forceinline__ int slab_elem(int lane, int wt, int v) {
 // accumulator y_m (pairs), VPL 8-element slabs each.
 template <int VPL>
 struct RowCtx {
-  uint64_t xf[VPL][4];
+  uint4 xv[VPL];  // x_m slabs, packed bf16
   uint64_t acc[VPL][4];
 };
 
@@ -74,10 +74,10 @@ __device__ __forceinline__ void process_entries(RowCtx<VPL>& c, int jl, float gl
     float p[B];
 #pragma unroll
     for (int b = 0; b < B; ++b) {
-      uint64_t a2 = 0;
+      float a0 = 0.f, a1 = 0.f;
 #pragma unroll
-      for (int v = 0; v < VPL; ++v) a2 = dot8_f2(c.xf[v], wu[b][v], a2);
-      p[b] = f2_sum(a2);
+      for (int v = 0; v < VPL; ++v) dot8_bf16(c.xv[v], wu[b][v], a0, a1);
+      p[b] = a0 + a1;
     }
     if (B == 2) {
       warp_sum2(p[0], p[B - 1]);
@@ -128,8 +128,7 @@ __global__ void __launch_bounds__(256, VPL > 2 ? 1 : 3)
 #pragma unroll
   for (int v = 0; v < VPL; ++v) {
     const int e = slab_elem<TEAM>(lane, wt, v);
-    const uint4 xv = e < d ? ldg_v4(x + (long long)m * d + e) : make_uint4(0, 0, 0, 0);
-    bf8_to_f2(xv, c.xf[v]);
+    c.xv[v] = e < d ? ldg_v4(x + (long long)m * d + e) : make_uint4(0, 0, 0, 0);
 #pragma unroll
     for (int k = 0; k < 4; ++k) c.acc[v][k] = 0;
   }
