@@ -163,10 +163,12 @@ struct Carve {
 // keeps its intermediates h, du, da as bf16 hi + lo pairs, so routed rows
 // are as accurate as the fp32 gather path:
 //   hr  [Mp][2f] = [h hi | h lo]
+//   part [Mp][d] fp32: split-K partials of the routed rows' y and dX GEMMs
 //   ur  [Mp][f]  fp32 u
 //   ddr [Mp][4f] = [du hi | da hi | du lo | da lo]
 struct SparseWs {
   uint16_t *xr, *hr;                    // forward fallback
+  float* part;
   uint16_t *dyr, *gr, *ddr;             // backward fallback
   float* ur;
   int *mask_off, *csc_ptr, *csc_row, *slot_pos;
@@ -181,6 +183,7 @@ SparseWs carve_sparse(void* ws, const twell_shape& s, int W, int training) {
   SparseWs w{};
   w.xr = c.take<uint16_t>(Mp * d);
   w.hr = c.take<uint16_t>(Mp * 2 * f);
+  w.part = c.take<float>(Mp * d);
   if (training) {
     const long long NB = (s.M + 31) / 32;
     const long long E = (long long)s.M * W;
@@ -261,11 +264,32 @@ cudaError_t gated_gemm(const void* x_rows, long long rows, const twell_shape& s,
   return gemm_launch(GK_GATED, A, B, &B2, p, st);
 }
 
+// Routed rows: out[row_map[r]] = A[r] B with the K range split across CTAs
+// (the few routed rows give too few output tiles to fill the GPU); each split
+// stores an fp32 partial in `part` and a reduction kernel sums them in fixed
+// order and scatters the bf16 rows.
+constexpr int kSplitKMax = 8;
+cudaError_t routed_gemm(const Mat& A, const Mat& B, const Mat* B2, long long rows, int K,
+                        const twell_shape& s, int k_split, const int* m_dev, const int* row_map,
+                        float* part, void* out, cudaStream_t st) {
+  GemmParams p = base_params((int)rows, s.d_model, K, kBN);
+  p.m_dev = m_dev;
+  p.k_split = k_split;
+  p.c_f32 = 1;
+  p.tma_out = 1;
+  p.split_k_max = kSplitKMax;
+  const OutMat o{part, rows, s.d_model, s.d_model, 1, 32};
+  cudaError_t e = gemm_launch(GK_STORE_KM, A, B, B2, p, st, &o, 1);
+  if (e != cudaSuccess) return e;
+  return launch_splitk_scatter(part, (int)rows, (K + kBK - 1) / kBK, kSplitKMax, m_dev, row_map,
+                               s.M, s.d_model, out, st);
+}
+
 // out[row_map ? row_map[r] : r] = h[r] Wd (bf16); with split, h = hi + lo and
 // the GEMM runs over K = 2f against [Wd ; Wd].
 cudaError_t down_gemm(const uint16_t* h, long long rows, const twell_shape& s, const void* wd,
                       bool split, const int* m_dev, const int* row_map, void* out,
-                      cudaStream_t st) {
+                      cudaStream_t st, float* part = nullptr) {
   const long long K = split ? 2LL * s.d_ff : s.d_ff;
   GemmParams p = base_params((int)rows, s.d_model, (int)K, kBN);
   p.m_dev = m_dev;
@@ -275,6 +299,8 @@ cudaError_t down_gemm(const uint16_t* h, long long rows, const twell_shape& s, c
   p.k_split = s.d_ff / kBK;
   const Mat A = mat(h, rows, K, K);
   const Mat B = mat(wd, s.d_ff, s.d_model, s.d_model);  // [K = f][N = d], MN-major
+  if (row_map && part)
+    return routed_gemm(A, B, &B, rows, (int)K, s, s.d_ff / kBK, m_dev, row_map, part, out, st);
   if (!row_map && !m_dev) {
     p.tma_out = 1;
     const OutMat o{out, rows, s.d_model, s.d_model, 0, 32};
@@ -313,7 +339,7 @@ cudaError_t dgate_gemm(const void* dy_rows, long long rows, const twell_shape& s
 // K = 2f (or 4f with the lo halves) against [WuT ; WgT (; WuT ; WgT)].
 cudaError_t dx_gemm(const uint16_t* dd, long long rows, const twell_shape& s, const void* wgT,
                     const void* wuT, bool split, const int* m_dev, const int* row_map, void* out,
-                    cudaStream_t st) {
+                    cudaStream_t st, float* part = nullptr) {
   const long long K = (split ? 4LL : 2LL) * s.d_ff;
   GemmParams p = base_params((int)rows, s.d_model, (int)K, kBN);
   p.m_dev = m_dev;
@@ -324,6 +350,8 @@ cudaError_t dx_gemm(const uint16_t* dd, long long rows, const twell_shape& s, co
   const Mat A = mat(dd, rows, K, K);
   const Mat B = mat(wuT, s.d_ff, s.d_model, s.d_model);   // [K][N], MN-major
   const Mat B2 = mat(wgT, s.d_ff, s.d_model, s.d_model);
+  if (row_map && part)
+    return routed_gemm(A, B, &B2, rows, (int)K, s, s.d_ff / kBK, m_dev, row_map, part, out, st);
   if (!row_map && !m_dev) {
     p.tma_out = 1;
     const OutMat o{out, rows, s.d_model, s.d_model, 0, 32};
@@ -519,7 +547,7 @@ twell_status twell_ffn_fwd(const void* x, const void* wgT, const void* wuT, cons
     e = gated_gemm(w.xr, Mp, s, wgT, wuT, route->n_dense, w.hr, true, nullptr, nullptr,
                    nullptr, 0, cs);
   if (e == cudaSuccess)
-    e = down_gemm(w.hr, Mp, s, wd, true, route->n_dense, route->dense_rows, y, cs);
+    e = down_gemm(w.hr, Mp, s, wd, true, route->n_dense, route->dense_rows, y, cs, w.part);
   return cuda_status(e);
 }
 
@@ -558,7 +586,8 @@ twell_status twell_ffn_bwd(const void* x, const void* wgT, const void* wuT, cons
     e = gated_gemm(w.xr, Mp, s, wgT, wuT, nd, w.hr, true, w.gr, nullptr, w.ur, 1, cs);
   if (e == cudaSuccess)
     e = dgate_gemm(w.dyr, Mp, s, wd, nd, w.gr, nullptr, w.ur, w.ddr, true, l1_coeff, 1, cs);
-  if (e == cudaSuccess) e = dx_gemm(w.ddr, Mp, s, wgT, wuT, true, nd, route->dense_rows, dx, cs);
+  if (e == cudaSuccess)
+    e = dx_gemm(w.ddr, Mp, s, wgT, wuT, true, nd, route->dense_rows, dx, cs, w.part);
   // dW += (hi + lo)^T B, both halves in one launch per weight
   if (e == cudaSuccess) e = dw_gemm(w.hr, 2 * f, w.dyr, Mp, s, nd, dwd, 1, cs, f);
   if (e == cudaSuccess) e = dw_gemm(w.ddr, 4 * f, w.xr, Mp, s, nd, dwuT, 1, cs, 2 * f);

@@ -186,6 +186,20 @@ __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, bool a_mn, bool 
          ((b_mn ? 1u : 0u) << 16) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
 
+// Split-K plan shared by the GEMM and the kernel that reduces its partials:
+// as many K splits (at most s_max) as fit when each split writes rows_eff
+// (= the used rows rounded up to 128) rows of a buffer with buf_rows rows;
+// kps k-blocks per split, splits = the number of non-empty splits.
+__host__ __device__ inline void splitk_plan(int rows_eff, int buf_rows, int num_kb, int s_max,
+                                            int& splits, int& kps) {
+  int sp = rows_eff > 0 ? buf_rows / rows_eff : 1;
+  sp = sp < s_max ? sp : s_max;
+  sp = sp < num_kb ? sp : num_kb;
+  sp = sp < 1 ? 1 : sp;
+  kps = (num_kb + sp - 1) / sp;
+  splits = kps > 0 ? (num_kb + kps - 1) / kps : 1;
+}
+
 // ------------------------------------------------------------------ numerics
 TW_DEV float bf16_bits_to_float(uint32_t b) { return __uint_as_float(b << 16); }
 

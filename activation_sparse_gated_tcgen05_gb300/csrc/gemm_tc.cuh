@@ -51,6 +51,8 @@ struct GemmParams {
                         // with A's M coordinate shifted by a_seg_off (B rows repeat): C += A0^T B + A1^T B
   int pad_rows;         // store every row of a visited tile that is < M (zero padding)
   int tma_out;          // outputs go through shared memory and TMA stores (tensor maps O0..O2)
+  int split_k_max;      // > 1: split K (plan from splitk_plan); split s stores its fp32 partial
+                        // at rows [s * rows_eff, (s + 1) * rows_eff) of the output map
   int* status;
   // EPI_STORE
   void* c;
@@ -511,7 +513,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   const int m_tiles = (M_eff + kBM - 1) / kBM;
   const int kb_pass = (K_eff + kBK - 1) / kBK;
   const int num_kb = (A_MN && p.a_seg_off > 0) ? 2 * kb_pass : kb_pass;
-  const int total = (num_kb > 0 && M_eff > 0) ? m_tiles * p.n_tiles : 0;
+  const int tiles = m_tiles * p.n_tiles;
+  int splits = 1, kps = num_kb;
+  if (p.split_k_max > 1 && num_kb > 0 && M_eff > 0)
+    splitk_plan(m_tiles * kBM, p.M, num_kb, p.split_k_max, splits, kps);
+  const int total = (num_kb > 0 && M_eff > 0) ? tiles * splits : 0;
   // nothing to do (e.g. no routed rows): leave before touching TMEM or barriers
   if (total == 0 || (int)blockIdx.x >= total) return;
 
@@ -545,10 +551,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       int stage = 0;
       uint32_t phase = 0;
       bool ok = true;
-      for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
+      for (int unit = blockIdx.x; unit < total && ok; unit += gridDim.x) {
         int mb, nb;
-        tile_coords(tile, m_tiles, p.n_tiles, mb, nb);
-        for (int kb = 0; kb < num_kb; ++kb) {
+        const int ks = unit / tiles;
+        tile_coords(unit - ks * tiles, m_tiles, p.n_tiles, mb, nb);
+        const int kb1 = min(num_kb, (ks + 1) * kps);
+        for (int kb = ks * kps; kb < kb1; ++kb) {
           if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag)) {
             ok = false;
             break;
@@ -601,7 +609,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       uint32_t phase = 0;
       int it = 0;
       bool ok = true;
-      for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x, ++it) {
+      for (int unit = blockIdx.x; unit < total && ok; unit += gridDim.x, ++it) {
         const int acc = it & 1;
         const uint32_t acc_phase = (uint32_t)(it >> 1) & 1u;
         if (!mbar_wait(&tempty[acc], acc_phase ^ 1u, abort_flag)) {
@@ -610,7 +618,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         }
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + (uint32_t)(acc * kBN);
-        for (int kb = 0; kb < num_kb; ++kb) {
+        const int ks = unit / tiles;
+        const int kb0 = ks * kps, kb1 = min(num_kb, (ks + 1) * kps);
+        for (int kb = kb0; kb < kb1; ++kb) {
           if (!mbar_wait(&full[stage], phase, abort_flag)) {
             ok = false;
             break;
@@ -624,7 +634,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                                      : sdesc_sw128(a0 + k * 32, 16, 1024);
             const uint64_t bd = B_MN ? sdesc_sw128(b0 + k * 2048, 8192, 1024)
                                      : sdesc_sw128(b0 + k * 32, 16, 1024);
-            tc_mma_bf16(d_tmem, ad, bd, idesc, (kb | k) != 0 ? 1u : 0u);
+            tc_mma_bf16(d_tmem, ad, bd, idesc, (kb != kb0 || k != 0) ? 1u : 0u);
           }
           tc_commit(&empty[stage]);
           if (++stage == kStages) {
@@ -648,9 +658,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     Stager st{sOut + (warp - 4) * kStageBytes, lane, 0};
     const OutMaps om{&tmO0, &tmO1, &tmO2};
     int it = 0;
-    for (int tile = blockIdx.x; tile < total; tile += gridDim.x, ++it) {
+    for (int unit = blockIdx.x; unit < total; unit += gridDim.x, ++it) {
       int mb, nb;
-      tile_coords(tile, m_tiles, p.n_tiles, mb, nb);
+      const int ks = unit / tiles;
+      tile_coords(unit - ks * tiles, m_tiles, p.n_tiles, mb, nb);
+      const int row_off = ks * m_tiles * kBM;  // split-K partial of split ks
       const int acc = it & 1;
       const uint32_t acc_phase = (uint32_t)(it >> 1) & 1u;
       if (!mbar_wait(&tfull[acc], acc_phase, abort_flag)) {
@@ -663,7 +675,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       const bool row_ok = p.pad_rows ? (row < p.M) : (row < M_eff);
       const uint32_t tacc = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * kBN);
       const int n0 = (EPI == EPI_GATED) ? nb * 128 : nb * kBN;
-      Epilogue<EPI>::run(p, tacc, row, row_ok, n0, p.N, half, st, om, mb * kBM + quarter * 32);
+      Epilogue<EPI>::run(p, tacc, row, row_ok, n0, p.N, half, st, om,
+                         row_off + mb * kBM + quarter * 32);
       tc_fence_before();
       mbar_arrive(&tempty[acc]);
     }

@@ -62,6 +62,9 @@ cudaError_t launch_pack_dense(const void* a, int a_f32, int M, int f, int tile_n
                               const twell_tiles& out, cudaStream_t s);
 cudaError_t launch_route(const twell_tiles& in, int M, int f, int tile_n, int cap,
                          const twell_hybrid& out, int* scan_flags, cudaStream_t s);
+cudaError_t launch_splitk_scatter(const float* part, int buf_rows, int num_kb, int s_max,
+                                  const int* n_rows, const int* rows, int M, int N, void* out,
+                                  cudaStream_t s);
 cudaError_t launch_gather_rows(const void* src, int M, int d, const int* rows, const int* n_rows,
                                void* dst, int dst_rows, cudaStream_t s);
 cudaError_t launch_sparse_fwd(const void* x, const void* wuT, const void* wd, int M, int d, int f,

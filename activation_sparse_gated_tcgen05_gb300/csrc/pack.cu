@@ -185,6 +185,38 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32)
   }
 }
 
+// Sum the split-K partials of the routed rows in fixed order (split 0, 1, ...)
+// and scatter the bf16 result to out[rows[r]] -- deterministic, no atomics.
+__global__ void __launch_bounds__(256)
+    splitk_scatter_kernel(const float* __restrict__ part, int buf_rows, int num_kb, int s_max,
+                          const int* __restrict__ n_rows, const int* __restrict__ rows, int M, int N,
+                          uint16_t* __restrict__ out) {
+  const int n = min(*n_rows, buf_rows);
+  if (n <= 0) return;
+  const int rows_eff = ((n + 127) / 128) * 128;
+  int splits, kps;
+  splitk_plan(rows_eff, buf_rows, num_kb, s_max, splits, kps);
+  const int vecs = N / 8;
+  const long long total = (long long)n * vecs;
+  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < total;
+       i += (long long)gridDim.x * blockDim.x) {
+    const int r = (int)(i / vecs), c = (int)(i % vecs) * 8;
+    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    for (int sp = 0; sp < splits; ++sp) {
+      const float4* src =
+          reinterpret_cast<const float4*>(part + ((long long)sp * rows_eff + r) * N + c);
+      const float4 a = src[0], b = src[1];
+      acc[0] += a.x; acc[1] += a.y; acc[2] += a.z; acc[3] += a.w;
+      acc[4] += b.x; acc[5] += b.y; acc[6] += b.z; acc[7] += b.w;
+    }
+    const int dst = rows[r];
+    if (dst < 0 || dst >= M) continue;
+    *reinterpret_cast<uint4*>(out + (long long)dst * N + c) =
+        make_uint4(pack_bf16x2(acc[0], acc[1]), pack_bf16x2(acc[2], acc[3]),
+                   pack_bf16x2(acc[4], acc[5]), pack_bf16x2(acc[6], acc[7]));
+  }
+}
+
 int blocks_for(long long warps_needed) {
   long long b = (warps_needed + kWarpsPerBlock - 1) / kWarpsPerBlock;
   const long long cap = (long long)num_sms() * 16;
@@ -193,6 +225,18 @@ int blocks_for(long long warps_needed) {
 }
 
 }  // namespace
+
+cudaError_t launch_splitk_scatter(const float* part, int buf_rows, int num_kb, int s_max,
+                                  const int* n_rows, const int* rows, int M, int N, void* out,
+                                  cudaStream_t s) {
+  {
+    ProfScope prof("splitk_scatter", s);
+    splitk_scatter_kernel<<<num_sms() * 4, 256, 0, s>>>(part, buf_rows, num_kb, s_max, n_rows,
+                                                        rows, M, N, reinterpret_cast<uint16_t*>(out));
+  }
+  count_launch();
+  return cudaGetLastError();
+}
 
 cudaError_t launch_pack_dense(const void* a, int a_f32, int M, int f, int tile_n, int cap,
                               const twell_tiles& out, cudaStream_t s) {

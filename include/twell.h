@@ -158,7 +158,7 @@ twell_status twell_ffn_fwd(const void* x, const void* wgT, const void* wuT, cons
  * library until the process exits) instead of a caller workspace.  It
  * allocates nothing and calls no allocating routine.
  *   - Limit: twell_workspace_bytes(shape, route->ell_width, 0) must not exceed
- *     32 MiB (e.g. M <= 1792 at d_model = 1024, d_ff = 4096); larger shapes
+ *     32 MiB (e.g. M <= 1408 at d_model = 1024, d_ff = 4096); larger shapes
  *     return TWELL_ERR_WORKSPACE before any launch.
  *   - The first call on each device looks up the array's device address
  *     (with that device current); make that first call before any stream
