@@ -19,6 +19,10 @@
 //      blocks of its group + popcount of lower bits.
 //   2. bwd_rows: one team of warps per row computes dh, u, du, da, h per entry
 //      (stored at the entry's neuron-major position) and dX_m.
+// Gathered rows are loaded without predicates: a batch slot past the last
+// entry reads neuron (or row) 0 with zero coefficients, and lanes past
+// d_model read the first slab against zero x / dY, so no zero-fill selects
+// sit between the loads and the arithmetic.
 //   3. bwd_neurons: one team per neuron sums its entries in ascending row
 //      order into dWd[j], dWu^T[j], dWg^T[j] (fp32, written once).
 #include "common.cuh"
@@ -154,10 +158,12 @@ __global__ void __launch_bounds__(256, VPL > 2 ? 1 : 2)
 
   uint4 xp[VPL], dyp[VPL];  // x_m, dY_m slabs, packed bf16
   uint64_t acc[VPL][4];
+  int eoff[VPL];  // slab offsets, lanes past d_model read the first slab
 #pragma unroll
   for (int v = 0; v < VPL; ++v) {
     const int e = slab<TEAM>(lane, wt, v);
     const bool ok = e < d;
+    eoff[v] = ok ? e : 0;
     xp[v] = ok ? ldg_v4(x + (long long)m * d + e) : make_uint4(0, 0, 0, 0);
     dyp[v] = ok ? ldg_v4(dy + (long long)m * d + e) : make_uint4(0, 0, 0, 0);
 #pragma unroll
@@ -167,7 +173,7 @@ __global__ void __launch_bounds__(256, VPL > 2 ? 1 : 2)
   const int n = ell_nnz[m];
   for (int e0 = 0; e0 < n; e0 += 32) {
     const int count = min(32, n - e0);
-    int jl = 0, pl = 0;
+    int jl = 0, pl = 0;  // slots past the row's end: neuron 0, gate 0
     float gl = 0.f;
     if (lane < count) {
       const long long s = (long long)m * W + e0 + lane;
@@ -181,26 +187,22 @@ __global__ void __launch_bounds__(256, VPL > 2 ? 1 : 2)
 #pragma unroll
       for (int b = 0; b < B; ++b) {
         const int src = (i + b) & 31;
-        const int jj = __shfl_sync(kFull, jl, src);
-        const int pp = __shfl_sync(kFull, pl, src);
-        const float gg = __shfl_sync(kFull, gl, src);
-        const bool ok = i + b < count;
-        j[b] = ok ? jj : -1;
-        pos[b] = pp;
-        g[b] = ok ? gg : 0.f;
+        j[b] = __shfl_sync(kFull, jl, src);
+        pos[b] = __shfl_sync(kFull, pl, src);
+        g[b] = __shfl_sync(kFull, gl, src);
       }
+      // unpredicated loads: a slot past the end reads neuron 0's rows
       uint4 wdv[B][VPL], wuv[B][VPL], wgv[B][VPL];
 #pragma unroll
-      for (int b = 0; b < B; ++b)
+      for (int b = 0; b < B; ++b) {
+        const long long row = (long long)j[b] * d;
 #pragma unroll
         for (int v = 0; v < VPL; ++v) {
-          const int e = slab<TEAM>(lane, wt, v);
-          const bool ok = j[b] >= 0 && e < d;
-          const long long off = (long long)j[b] * d + e;
-          wdv[b][v] = ok ? ldg_v4(wd + off) : make_uint4(0, 0, 0, 0);
-          wuv[b][v] = ok ? ldg_v4(wuT + off) : make_uint4(0, 0, 0, 0);
-          wgv[b][v] = ok ? ldg_v4(wgT + off) : make_uint4(0, 0, 0, 0);
+          wdv[b][v] = ldg_v4(wd + row + eoff[v]);
+          wuv[b][v] = ldg_v4(wuT + row + eoff[v]);
+          wgv[b][v] = ldg_v4(wgT + row + eoff[v]);
         }
+      }
       float dh[B], u[B];
 #pragma unroll
       for (int b = 0; b < B; ++b) {
@@ -236,10 +238,11 @@ __global__ void __launch_bounds__(256, VPL > 2 ? 1 : 2)
       }
 #pragma unroll
       for (int b = 0; b < B; ++b) {
-        if (j[b] < 0) continue;
+        // a slot past the end has g = 0 (du = 0) and must add no da either
+        const bool live = i + b < count;
         const float du = dh[b] * g[b];
-        const float da = fmaf(dh[b], u[b], lambda);
-        if (wt == 0 && lane == 0) csc_vals[pos[b]] = make_float4(du, da, g[b] * u[b], 0.f);
+        const float da = live ? fmaf(dh[b], u[b], lambda) : 0.f;
+        if (live && wt == 0 && lane == 0) csc_vals[pos[b]] = make_float4(du, da, g[b] * u[b], 0.f);
         const uint64_t du2 = f2_splat(du), da2 = f2_splat(da);
 #pragma unroll
         for (int v = 0; v < VPL; ++v) {
@@ -276,10 +279,16 @@ __global__ void __launch_bounds__(256, VPL > 2 ? 1 : 2)
 #pragma unroll
     for (int k = 0; k < 4; ++k) ad[v][k] = au[v][k] = ag[v][k] = 0;
 
+  int eoff[VPL];  // slab offsets, lanes past d_model read the first slab
+#pragma unroll
+  for (int v = 0; v < VPL; ++v) {
+    const int e = slab<TEAM>(lane, wt, v);
+    eoff[v] = e < d ? e : 0;
+  }
   const int p0 = csc_ptr[j], p1 = csc_ptr[j + 1];
   for (int e0 = p0; e0 < p1; e0 += 32) {
     const int count = min(32, p1 - e0);
-    int ml = 0;
+    int ml = 0;  // slots past the neuron's end: row 0 with zero coefficients
     float4 vl = make_float4(0.f, 0.f, 0.f, 0.f);
     if (lane < count) {
       ml = csc_row[e0 + lane];
@@ -291,26 +300,21 @@ __global__ void __launch_bounds__(256, VPL > 2 ? 1 : 2)
 #pragma unroll
       for (int b = 0; b < B; ++b) {
         const int src = (i + b) & 31;
-        const bool ok = i + b < count;
-        const int mm = __shfl_sync(kFull, ml, src);
-        const float a0 = __shfl_sync(kFull, vl.x, src);
-        const float a1 = __shfl_sync(kFull, vl.y, src);
-        const float a2 = __shfl_sync(kFull, vl.z, src);
-        m[b] = ok ? mm : -1;
-        du[b] = ok ? a0 : 0.f;
-        da[b] = ok ? a1 : 0.f;
-        h[b] = ok ? a2 : 0.f;
+        m[b] = __shfl_sync(kFull, ml, src);
+        du[b] = __shfl_sync(kFull, vl.x, src);
+        da[b] = __shfl_sync(kFull, vl.y, src);
+        h[b] = __shfl_sync(kFull, vl.z, src);
       }
       uint4 xv[B][VPL], dyv[B][VPL];
 #pragma unroll
-      for (int b = 0; b < B; ++b)
+      for (int b = 0; b < B; ++b) {
+        const long long row = (long long)m[b] * d;
 #pragma unroll
         for (int v = 0; v < VPL; ++v) {
-          const int e = slab<TEAM>(lane, wt, v);
-          const bool ok = m[b] >= 0 && e < d;
-          xv[b][v] = ok ? ldg_v4(x + (long long)m[b] * d + e) : make_uint4(0, 0, 0, 0);
-          dyv[b][v] = ok ? ldg_v4(dy + (long long)m[b] * d + e) : make_uint4(0, 0, 0, 0);
+          xv[b][v] = ldg_v4(x + row + eoff[v]);
+          dyv[b][v] = ldg_v4(dy + row + eoff[v]);
         }
+      }
 #pragma unroll
       for (int b = 0; b < B; ++b) {
         const uint64_t h2 = f2_splat(h[b]), du2 = f2_splat(du[b]), da2 = f2_splat(da[b]);

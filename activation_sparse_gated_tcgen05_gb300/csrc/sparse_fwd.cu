@@ -9,14 +9,17 @@
 // the team in 256-element (512-byte) slabs, VPL slabs per warp, so every
 // weight-row read is a run of coalesced 16-byte loads.  For each live entry
 // (j, g) of the row:
-//   u = x_m . Wu[:, j]          (x_m held in registers as fp32, WuT[j] gathered)
+//   u = x_m . Wu[:, j]          (x_m held in registers as packed bf16, WuT[j]
+//                                gathered; bf16 x bf16 -> fp32 FMA)
 //   h = g * u                   (fp32, kept in registers)
-//   y_m += h * Wd[j, :]         (fp32 accumulators in registers)
-// and y_m is written once as bf16.  Arithmetic runs on packed fp32 pairs
-// (f32x2 FMA), so each gathered bf16 costs one unpack and half an FMA; the
-// team's partial dot products meet in shared memory behind a named barrier.
-// Entries are processed B at a time, 2*B weight rows in flight per warp,
-// with registers capped so three 256-thread blocks fit on an SM.
+//   y_m += h * Wd[j, :]         (fp32-pair accumulators in registers)
+// and y_m is written once as bf16.  Entries are processed B at a time, 2*B
+// weight rows in flight per warp.  Loads are never predicated: slots past
+// the row's last entry read neuron 0 with gate 0 (their h is exactly 0), and
+// lanes past d_model read the row's first slab against a zero x, so the load
+// sequence has no zero-fill selects.  Up to d_model = 1024 a single warp owns
+// the row (no cross-warp reduction); wider rows split it over a team whose
+// partial dot products meet in shared memory behind a named barrier.
 #include "common.cuh"
 #include "internal.h"
 
@@ -31,12 +34,14 @@ __device__ __forceinline__ int slab_elem(int lane, int wt, int v) {
   return 8 * (lane + 32 * (wt + TEAM * v));
 }
 
-// Row state of one warp: its share of x_m as fp32 pairs and of the fp32
-// accumulator y_m (pairs), VPL 8-element slabs each.
+// Row state of one warp: its share of x_m (packed bf16), of the fp32
+// accumulator y_m (pairs), and the in-row offsets of its VPL slabs (clamped
+// to the first slab past d_model).
 template <int VPL>
 struct RowCtx {
-  uint4 xv[VPL];  // x_m slabs, packed bf16
+  uint4 xv[VPL];
   uint64_t acc[VPL][4];
+  int eoff[VPL];
 };
 
 // Process `count` (<= 32) entries whose (column, gate) sit in lanes 0..count-1.
@@ -47,30 +52,25 @@ __device__ __forceinline__ void process_entries(RowCtx<VPL>& c, int jl, float gl
                                                 int wt, int team, float (*red)[ROWS][TEAM][B],
                                                 int& buf) {
   for (int i = 0; i < count; i += B) {
+    // lanes >= count hold (0, 0): a valid row with a zero gate
     int j[B];
     float g[B];
 #pragma unroll
     for (int b = 0; b < B; ++b) {
-      const int src = (i + b) & 31;
-      const int jj = __shfl_sync(kFull, jl, src);
-      const float gg = __shfl_sync(kFull, gl, src);
-      j[b] = (i + b < count) ? jj : -1;
-      g[b] = (i + b < count) ? gg : 0.f;
+      j[b] = __shfl_sync(kFull, jl, (i + b) & 31);
+      g[b] = __shfl_sync(kFull, gl, (i + b) & 31);
     }
     uint4 wu[B][VPL], wdv[B][VPL];
 #pragma unroll
-    for (int b = 0; b < B; ++b)
+    for (int b = 0; b < B; ++b) {
+      const uint16_t* pu = wuT + (long long)j[b] * d;
+      const uint16_t* pd = wd + (long long)j[b] * d;
 #pragma unroll
       for (int v = 0; v < VPL; ++v) {
-        const int e = slab_elem<TEAM>(lane, wt, v);
-        if (j[b] >= 0 && e < d) {
-          wu[b][v] = ldg_v4(wuT + (long long)j[b] * d + e);
-          wdv[b][v] = ldg_v4(wd + (long long)j[b] * d + e);
-        } else {
-          wu[b][v] = make_uint4(0, 0, 0, 0);
-          wdv[b][v] = make_uint4(0, 0, 0, 0);
-        }
+        wu[b][v] = ldg_v4(pu + c.eoff[v]);
+        wdv[b][v] = ldg_v4(pd + c.eoff[v]);
       }
+    }
     float p[B];
 #pragma unroll
     for (int b = 0; b < B; ++b) {
@@ -79,13 +79,13 @@ __device__ __forceinline__ void process_entries(RowCtx<VPL>& c, int jl, float gl
       for (int v = 0; v < VPL; ++v) dot8_bf16(c.xv[v], wu[b][v], a0, a1);
       p[b] = a0 + a1;
     }
-    if (B == 2) {
+    if constexpr (B == 2) {
       warp_sum2(p[0], p[B - 1]);
     } else {
 #pragma unroll
       for (int b = 0; b < B; ++b) p[b] = warp_sum(p[b]);
     }
-    if (TEAM > 1) {
+    if constexpr (TEAM > 1) {
       if (lane == 0)
 #pragma unroll
         for (int b = 0; b < B; ++b) red[buf][team][wt][b] = p[b];
@@ -109,7 +109,7 @@ __device__ __forceinline__ void process_entries(RowCtx<VPL>& c, int jl, float gl
 }
 
 template <int TEAM, int VPL, int B, bool ELL>
-__global__ void __launch_bounds__(256, VPL > 2 ? 1 : 3)
+__global__ void __launch_bounds__(256, VPL > 2 ? 2 : 3)
     sparse_fwd_kernel(const uint16_t* __restrict__ x, const uint16_t* __restrict__ wuT,
                       const uint16_t* __restrict__ wd, int M, int d,
                       const uint16_t* __restrict__ val, const uint8_t* __restrict__ idx,
@@ -128,6 +128,7 @@ __global__ void __launch_bounds__(256, VPL > 2 ? 1 : 3)
 #pragma unroll
   for (int v = 0; v < VPL; ++v) {
     const int e = slab_elem<TEAM>(lane, wt, v);
+    c.eoff[v] = e < d ? e : 0;
     c.xv[v] = e < d ? ldg_v4(x + (long long)m * d + e) : make_uint4(0, 0, 0, 0);
 #pragma unroll
     for (int k = 0; k < 4; ++k) c.acc[v][k] = 0;
@@ -208,13 +209,14 @@ cudaError_t launch_team(const void* x, const void* wuT, const void* wd, int M, i
   return cudaGetLastError();
 }
 
-// A team of d/512 warps per row, two 256-element slabs per warp.
+// One warp per row up to d_model = 1024 (four 256-element slabs), then teams
+// of d/512 warps with two slabs each.
 template <bool ELL>
 cudaError_t launch_fmt(const void* x, const void* wuT, const void* wd, int M, int d,
                        const twell_tiles* tiles, int T, int tile_n, int cap,
                        const twell_hybrid* route, void* y, cudaStream_t s) {
   if (d <= 512) return launch_team<1, 2, ELL>(x, wuT, wd, M, d, tiles, T, tile_n, cap, route, y, s);
-  if (d <= 1024) return launch_team<2, 2, ELL>(x, wuT, wd, M, d, tiles, T, tile_n, cap, route, y, s);
+  if (d <= 1024) return launch_team<1, 4, ELL>(x, wuT, wd, M, d, tiles, T, tile_n, cap, route, y, s);
   if (d <= 2048) return launch_team<4, 2, ELL>(x, wuT, wd, M, d, tiles, T, tile_n, cap, route, y, s);
   if (d <= 4096) return launch_team<8, 2, ELL>(x, wuT, wd, M, d, tiles, T, tile_n, cap, route, y, s);
   return launch_team<8, 4, ELL>(x, wuT, wd, M, d, tiles, T, tile_n, cap, route, y, s);
