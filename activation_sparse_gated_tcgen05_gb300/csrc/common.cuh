@@ -304,6 +304,20 @@ TW_DEV int warp_incl_scan(int v) {
 
 TW_DEV uint4 ldg_v4(const void* p) { return __ldg(reinterpret_cast<const uint4*>(p)); }
 
+// L2 policy that marks lines for early eviction: for results written once
+// and not read again by the same kernel, so they do not push gathered
+// operands out of L2.
+TW_DEV uint64_t l2_evict_first_policy() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+TW_DEV void st_v4_hint(void* p, const uint4& v, uint64_t pol) {
+  asm volatile("st.global.L2::cache_hint.v4.u32 [%0], {%1, %2, %3, %4}, %5;" ::"l"(p), "r"(v.x),
+               "r"(v.y), "r"(v.z), "r"(v.w), "l"(pol)
+               : "memory");
+}
+
 // ---- packed fp32 pairs (sm_100+ f32x2 arithmetic) --------------------------
 // A uint64 holds two fp32 values: low word = element 2i, high word = 2i+1.
 TW_DEV uint64_t f2_make(uint32_t lo_bits, uint32_t hi_bits) {

@@ -141,8 +141,8 @@ __device__ __forceinline__ int slab(int lane, int wt, int v) {
 }
 
 // One team of TEAM warps per ELL row; fp32-pair arithmetic as in the forward.
-template <int TEAM, int VPL, int B>
-__global__ void __launch_bounds__(256, VPL > 2 ? 1 : 2)
+template <int TEAM, int VPL, int B, int MINB>
+__global__ void __launch_bounds__(256, MINB)
     bwd_rows_kernel(const uint16_t* __restrict__ x, const uint16_t* __restrict__ dy,
                     const uint16_t* __restrict__ wgT, const uint16_t* __restrict__ wuT,
                     const uint16_t* __restrict__ wd, int M, int d,
@@ -212,10 +212,21 @@ __global__ void __launch_bounds__(256, VPL > 2 ? 1 : 2)
           dot8_bf16(dyp[v], wdv[b][v], a0, a1);
           dot8_bf16(xp[v], wuv[b][v], c0, c1);
         }
-        dh[b] = warp_sum(a0 + a1);
-        u[b] = warp_sum(c0 + c1);
+        dh[b] = a0 + a1;
+        u[b] = c0 + c1;
       }
-      if (TEAM > 1) {
+      if constexpr (B == 1) {
+        warp_sum2(dh[0], u[0]);
+      } else if constexpr (B == 2) {
+        warp_sum4(dh[0], u[0], dh[B - 1], u[B - 1]);
+      } else {
+#pragma unroll
+        for (int b = 0; b < B; ++b) {
+          dh[b] = warp_sum(dh[b]);
+          u[b] = warp_sum(u[b]);
+        }
+      }
+      if constexpr (TEAM > 1) {
         if (lane == 0)
 #pragma unroll
           for (int b = 0; b < B; ++b) {
@@ -261,9 +272,10 @@ __global__ void __launch_bounds__(256, VPL > 2 ? 1 : 2)
 
 // ---------------------------------------------------------------- neuron phase
 // One team per neuron; each warp owns VPL slabs of d_model and needs no
-// cross-warp communication.
-template <int TEAM, int VPL, int B>
-__global__ void __launch_bounds__(256, VPL > 2 ? 1 : 2)
+// cross-warp communication, so narrow slabs (VPL = 1) buy occupancy and
+// more gathered rows in flight per SM.
+template <int TEAM, int VPL, int B, int MINB>
+__global__ void __launch_bounds__(256, MINB)
     bwd_neurons_kernel(const uint16_t* __restrict__ x, const uint16_t* __restrict__ dy, int d,
                        int f, const int* __restrict__ csc_ptr, const int* __restrict__ csc_row,
                        const float4* __restrict__ csc_vals, float* __restrict__ dwgT,
@@ -332,35 +344,37 @@ __global__ void __launch_bounds__(256, VPL > 2 ? 1 : 2)
       }
     }
   }
+  // dW rows are written once: evict-first so they do not displace x / dY
+  const uint64_t pol = l2_evict_first_policy();
   const long long row = (long long)j * d;
 #pragma unroll
   for (int v = 0; v < VPL; ++v) {
     const int e = slab<TEAM>(lane, wt, v);
     if (e < d) {
-      float4* o1 = reinterpret_cast<float4*>(dwd + row + e);
-      float4* o2 = reinterpret_cast<float4*>(dwuT + row + e);
-      float4* o3 = reinterpret_cast<float4*>(dwgT + row + e);
 #pragma unroll
       for (int q = 0; q < 2; ++q) {
-        o1[q] = make_float4(f2_lo(ad[v][2 * q]), f2_hi(ad[v][2 * q]), f2_lo(ad[v][2 * q + 1]),
-                            f2_hi(ad[v][2 * q + 1]));
-        o2[q] = make_float4(f2_lo(au[v][2 * q]), f2_hi(au[v][2 * q]), f2_lo(au[v][2 * q + 1]),
-                            f2_hi(au[v][2 * q + 1]));
-        o3[q] = make_float4(f2_lo(ag[v][2 * q]), f2_hi(ag[v][2 * q]), f2_lo(ag[v][2 * q + 1]),
-                            f2_hi(ag[v][2 * q + 1]));
+        const uint64_t d0 = ad[v][2 * q], d1 = ad[v][2 * q + 1];
+        const uint64_t u0 = au[v][2 * q], u1 = au[v][2 * q + 1];
+        const uint64_t g0 = ag[v][2 * q], g1 = ag[v][2 * q + 1];
+        st_v4_hint(dwd + row + e + 4 * q,
+                   make_uint4((uint32_t)d0, (uint32_t)(d0 >> 32), (uint32_t)d1, (uint32_t)(d1 >> 32)), pol);
+        st_v4_hint(dwuT + row + e + 4 * q,
+                   make_uint4((uint32_t)u0, (uint32_t)(u0 >> 32), (uint32_t)u1, (uint32_t)(u1 >> 32)), pol);
+        st_v4_hint(dwgT + row + e + 4 * q,
+                   make_uint4((uint32_t)g0, (uint32_t)(g0 >> 32), (uint32_t)g1, (uint32_t)(g1 >> 32)), pol);
       }
     }
   }
 }
 
-template <int TEAM, int VPL>
+template <int TEAM, int VPL, int B, int MINB>
 cudaError_t rows_team(const void* x, const void* dy, const void* wgT, const void* wuT,
                       const void* wd, int M, int d, const twell_hybrid& r, const int* slot_pos,
                       float lambda, float4* csc_vals, void* dx, cudaStream_t s) {
   constexpr int ROWS = 8 / TEAM;
   {
     ProfScope prof("bwd_rows", s);
-    bwd_rows_kernel<TEAM, VPL, 2><<<(M + ROWS - 1) / ROWS, 256, 0, s>>>(
+    bwd_rows_kernel<TEAM, VPL, B, MINB><<<(M + ROWS - 1) / ROWS, 256, 0, s>>>(
         reinterpret_cast<const uint16_t*>(x), reinterpret_cast<const uint16_t*>(dy),
         reinterpret_cast<const uint16_t*>(wgT), reinterpret_cast<const uint16_t*>(wuT),
         reinterpret_cast<const uint16_t*>(wd), M, d, reinterpret_cast<const uint16_t*>(r.ell_val),
@@ -371,14 +385,14 @@ cudaError_t rows_team(const void* x, const void* dy, const void* wgT, const void
   return cudaGetLastError();
 }
 
-template <int TEAM, int VPL>
+template <int TEAM, int VPL, int B, int MINB>
 cudaError_t neurons_team(const void* x, const void* dy, int d, int f, const int* csc_ptr,
                          const int* csc_row, const float4* csc_vals, float* dwgT, float* dwuT,
                          float* dwd, cudaStream_t s) {
   constexpr int ROWS = 8 / TEAM;
   {
     ProfScope prof("bwd_neurons", s);
-    bwd_neurons_kernel<TEAM, VPL, 2><<<(f + ROWS - 1) / ROWS, 256, 0, s>>>(
+    bwd_neurons_kernel<TEAM, VPL, B, MINB><<<(f + ROWS - 1) / ROWS, 256, 0, s>>>(
         reinterpret_cast<const uint16_t*>(x), reinterpret_cast<const uint16_t*>(dy), d, f,
         csc_ptr, csc_row, csc_vals, dwgT, dwuT, dwd);
   }
@@ -439,12 +453,13 @@ cudaError_t launch_sparse_bwd_rows(const void* x, const void* dy, const void* wg
                                    const int* slot_pos, float lambda, float4* csc_vals, void* dx,
                                    cudaStream_t s) {
   if (M == 0) return cudaSuccess;
-#define TW_ROWS(T, V) rows_team<T, V>(x, dy, wgT, wuT, wd, M, d, route, slot_pos, lambda, csc_vals, dx, s)
-  if (d <= 512) return TW_ROWS(1, 2);
-  if (d <= 1024) return TW_ROWS(2, 2);
-  if (d <= 2048) return TW_ROWS(4, 2);
-  if (d <= 4096) return TW_ROWS(8, 2);
-  return TW_ROWS(8, 4);
+#define TW_ROWS(T, V, B, MINB) \
+  rows_team<T, V, B, MINB>(x, dy, wgT, wuT, wd, M, d, route, slot_pos, lambda, csc_vals, dx, s)
+  if (d <= 512) return TW_ROWS(1, 2, 2, 2);
+  if (d <= 1024) return TW_ROWS(1, 4, 1, 2);
+  if (d <= 2048) return TW_ROWS(4, 2, 2, 2);
+  if (d <= 4096) return TW_ROWS(8, 2, 2, 2);
+  return TW_ROWS(8, 4, 2, 1);
 #undef TW_ROWS
 }
 
@@ -454,12 +469,16 @@ cudaError_t launch_sparse_bwd_neurons(const void* x, const void* dy, int M, int 
                                       cudaStream_t s) {
   (void)M;
   if (f == 0) return cudaSuccess;
-#define TW_NEU(T, V) neurons_team<T, V>(x, dy, d, f, csc_ptr, csc_row, csc_vals, dwgT, dwuT, dwd, s)
-  if (d <= 512) return TW_NEU(1, 2);
-  if (d <= 1024) return TW_NEU(2, 2);
-  if (d <= 2048) return TW_NEU(4, 2);
-  if (d <= 4096) return TW_NEU(8, 2);
-  return TW_NEU(8, 4);
+#define TW_NEU(T, V, B, MINB) \
+  neurons_team<T, V, B, MINB>(x, dy, d, f, csc_ptr, csc_row, csc_vals, dwgT, dwuT, dwd, s)
+  // one 256-element slab per warp (short accumulators, 3-4 blocks per SM)
+  // while a block's 8 warps cover d_model
+  if (d <= 256) return TW_NEU(1, 1, 2, 4);
+  if (d <= 512) return TW_NEU(2, 1, 2, 4);
+  if (d <= 1024) return TW_NEU(4, 1, 2, 4);
+  if (d <= 2048) return TW_NEU(8, 1, 4, 3);
+  if (d <= 4096) return TW_NEU(8, 2, 2, 2);
+  return TW_NEU(8, 4, 2, 1);
 #undef TW_NEU
 }
 
