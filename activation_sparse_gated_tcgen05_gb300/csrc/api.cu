@@ -3,6 +3,7 @@
 #include <atomic>
 #include <cstring>
 #include <map>
+#include <cmath>
 #include <mutex>
 #include <string>
 #include <vector>
@@ -81,6 +82,20 @@ int num_sms() {
     cache[dev] = n;
   }
   return cache[dev];
+}
+
+int l2_chunks(double gathered_bytes) {
+  static int cache[kMaxDevices] = {0};
+  const int dev = current_device();
+  if (dev < 0 || dev >= kMaxDevices) return 1;
+  if (cache[dev] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrL2CacheSize, dev) != cudaSuccess || n <= 0) return 1;
+    cache[dev] = n;
+  }
+  const double l2 = (double)cache[dev];
+  if (gathered_bytes <= 0.75 * l2) return 1;
+  return (int)std::ceil(gathered_bytes / (0.5 * l2));
 }
 
 int* device_status_ptr() {
@@ -529,7 +544,7 @@ twell_status twell_ffn_fwd(const void* x, const void* wgT, const void* wuT, cons
     if ((st = check_tiles(tiles)) != TWELL_OK) return st;
     if (s.M == 0) return TWELL_OK;
     return cuda_status(launch_sparse_fwd(x, wuT, wd, s.M, s.d_model, s.d_ff, tiles, s.tile_n,
-                                         s.tile_cap, nullptr, y, cs));
+                                         s.tile_cap, nullptr, y, nullptr, cs));
   }
   if ((st = check_route(route)) != TWELL_OK) return st;
   if ((st = check_ptrs({wgT})) != TWELL_OK) return st;
@@ -539,8 +554,10 @@ twell_status twell_ffn_fwd(const void* x, const void* wgT, const void* wuT, cons
   if (s.M == 0) return TWELL_OK;
   const SparseWs w = carve_sparse(ws, s, route->ell_width, 0);
   const long long Mp = round_up(s.M, 128);
+  // w.part carries y between L2-sized passes; the routed rows' split-K GEMM
+  // reuses it afterwards on the same stream
   cudaError_t e = launch_sparse_fwd(x, wuT, wd, s.M, s.d_model, s.d_ff, nullptr, s.tile_n,
-                                    s.tile_cap, route, y, cs);
+                                    s.tile_cap, route, y, w.part, cs);
   if (e == cudaSuccess)
     e = launch_gather_rows(x, s.M, s.d_model, route->dense_rows, route->n_dense, w.xr, (int)Mp, cs);
   if (e == cudaSuccess)

@@ -37,6 +37,10 @@ enum GemmKind {
 };
 
 int num_sms();
+// Passes over the neuron axis for a gather whose weight rows total
+// `gathered_bytes`: 1 while they fit comfortably in L2 (3/4 of it), else
+// enough chunks of about half of L2 each.
+int l2_chunks(double gathered_bytes);
 void count_launch(int n = 1);  // kernels launched by the library (process-wide)
 
 // While profiling is on for `name` (or "*"), brackets one kernel launch with
@@ -67,9 +71,11 @@ cudaError_t launch_splitk_scatter(const float* part, int buf_rows, int num_kb, i
                                   cudaStream_t s);
 cudaError_t launch_gather_rows(const void* src, int M, int d, const int* rows, const int* n_rows,
                                void* dst, int dst_rows, cudaStream_t s);
+// `part` ([M][d] fp32) carries y between the passes of an ELL gather split
+// into L2-sized neuron chunks; it may be null when one pass suffices.
 cudaError_t launch_sparse_fwd(const void* x, const void* wuT, const void* wd, int M, int d, int f,
                               const twell_tiles* tiles, int tile_n, int cap,
-                              const twell_hybrid* route, void* y, cudaStream_t s);
+                              const twell_hybrid* route, void* y, float* part, cudaStream_t s);
 cudaError_t launch_csc_build(const twell_hybrid& route, int M, int f, int* blk_counts,
                              int* csc_ptr, int* csc_row, int* slot_pos, cudaStream_t s);
 cudaError_t launch_sparse_bwd_rows(const void* x, const void* dy, const void* wgT, const void* wuT,

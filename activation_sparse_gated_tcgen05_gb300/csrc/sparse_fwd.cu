@@ -28,6 +28,7 @@ namespace tw {
 namespace {
 
 constexpr unsigned kFull = 0xffffffffu;
+constexpr int kPassFirst = 1, kPassLast = 2;
 
 template <int TEAM>
 __device__ __forceinline__ int slab_elem(int lane, int wt, int v) {
@@ -116,7 +117,7 @@ __global__ void __launch_bounds__(256, VPL > 2 ? 2 : 3)
                       const uint8_t* __restrict__ cnt, int T, int tile_n, int cap,
                       const uint16_t* __restrict__ ell_val, const uint16_t* __restrict__ ell_col,
                       const int* __restrict__ ell_nnz, int W, uint16_t* __restrict__ y,
-                      int* status) {
+                      float* __restrict__ part, int j_lo, int j_hi, int pass, int* status) {
   constexpr int ROWS = 8 / TEAM;
   __shared__ float red[2][ROWS][TEAM][B];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -124,21 +125,41 @@ __global__ void __launch_bounds__(256, VPL > 2 ? 2 : 3)
   const int m = blockIdx.x * ROWS + team;
   if (m >= M) return;
 
+  const bool first = pass & kPassFirst, last = pass & kPassLast;
   RowCtx<VPL> c;
 #pragma unroll
   for (int v = 0; v < VPL; ++v) {
     const int e = slab_elem<TEAM>(lane, wt, v);
     c.eoff[v] = e < d ? e : 0;
     c.xv[v] = e < d ? ldg_v4(x + (long long)m * d + e) : make_uint4(0, 0, 0, 0);
+    if (first || e >= d) {
 #pragma unroll
-    for (int k = 0; k < 4; ++k) c.acc[v][k] = 0;
+      for (int k = 0; k < 4; ++k) c.acc[v][k] = 0;
+    } else {  // running sum of the earlier neuron chunks
+      const uint4* pp = reinterpret_cast<const uint4*>(part + (long long)m * d + e);
+      const uint4 q0 = pp[0], q1 = pp[1];
+      c.acc[v][0] = f2_make(q0.x, q0.y);
+      c.acc[v][1] = f2_make(q0.z, q0.w);
+      c.acc[v][2] = f2_make(q1.x, q1.y);
+      c.acc[v][3] = f2_make(q1.z, q1.w);
+    }
   }
   int buf = 0;
 
   if (ELL) {
     const int n = ell_nnz[m];
-    for (int e0 = 0; e0 < n; e0 += 32) {
-      const int count = min(32, n - e0);
+    // a row's columns ascend: the chunk [j_lo, j_hi) is the slice [a, b)
+    int a = 0, b = n;
+    if (!(first && last)) {
+      a = b = 0;
+      for (int s0 = 0; s0 < n; s0 += 32) {
+        const int jc = s0 + lane < n ? (int)ell_col[(long long)m * W + s0 + lane] : 0x7fffffff;
+        a += __popc(__ballot_sync(kFull, jc < j_lo));
+        b += __popc(__ballot_sync(kFull, jc < j_hi));
+      }
+    }
+    for (int e0 = a; e0 < b; e0 += 32) {
+      const int count = min(32, b - e0);
       int jl = 0;
       float gl = 0.f;
       if (lane < count) {
@@ -184,53 +205,80 @@ __global__ void __launch_bounds__(256, VPL > 2 ? 2 : 3)
 #pragma unroll
   for (int v = 0; v < VPL; ++v) {
     const int e = slab_elem<TEAM>(lane, wt, v);
-    if (e < d) *reinterpret_cast<uint4*>(y + (long long)m * d + e) = f2x4_to_bf8(c.acc[v]);
+    if (e >= d) continue;
+    if (last) {
+      *reinterpret_cast<uint4*>(y + (long long)m * d + e) = f2x4_to_bf8(c.acc[v]);
+    } else {
+      uint4* pp = reinterpret_cast<uint4*>(part + (long long)m * d + e);
+      pp[0] = make_uint4((uint32_t)c.acc[v][0], (uint32_t)(c.acc[v][0] >> 32),
+                         (uint32_t)c.acc[v][1], (uint32_t)(c.acc[v][1] >> 32));
+      pp[1] = make_uint4((uint32_t)c.acc[v][2], (uint32_t)(c.acc[v][2] >> 32),
+                         (uint32_t)c.acc[v][3], (uint32_t)(c.acc[v][3] >> 32));
+    }
   }
 }
 
 template <int TEAM, int VPL, bool ELL>
-cudaError_t launch_team(const void* x, const void* wuT, const void* wd, int M, int d,
+cudaError_t launch_team(const void* x, const void* wuT, const void* wd, int M, int d, int f,
                         const twell_tiles* tiles, int T, int tile_n, int cap,
-                        const twell_hybrid* route, void* y, cudaStream_t s) {
+                        const twell_hybrid* route, void* y, float* part, int chunks,
+                        cudaStream_t s) {
   constexpr int ROWS = 8 / TEAM;
   const int grid = (M + ROWS - 1) / ROWS;
-  {
-    ProfScope prof("sparse_fwd", s);
-    sparse_fwd_kernel<TEAM, VPL, 2, ELL><<<grid, 256, 0, s>>>(
-        reinterpret_cast<const uint16_t*>(x), reinterpret_cast<const uint16_t*>(wuT),
-        reinterpret_cast<const uint16_t*>(wd), M, d,
-        tiles ? reinterpret_cast<const uint16_t*>(tiles->val) : nullptr,
-        tiles ? tiles->idx : nullptr, tiles ? tiles->cnt : nullptr, T, tile_n, cap,
-        route ? reinterpret_cast<const uint16_t*>(route->ell_val) : nullptr,
-        route ? route->ell_col : nullptr, route ? route->ell_nnz : nullptr,
-        route ? route->ell_width : 0, reinterpret_cast<uint16_t*>(y), device_status_ptr());
+  for (int c = 0; c < chunks; ++c) {
+    const int j_lo = (int)((long long)f * c / chunks), j_hi = (int)((long long)f * (c + 1) / chunks);
+    const int pass = (c == 0 ? kPassFirst : 0) | (c == chunks - 1 ? kPassLast : 0);
+    {
+      ProfScope prof("sparse_fwd", s);
+      sparse_fwd_kernel<TEAM, VPL, 2, ELL><<<grid, 256, 0, s>>>(
+          reinterpret_cast<const uint16_t*>(x), reinterpret_cast<const uint16_t*>(wuT),
+          reinterpret_cast<const uint16_t*>(wd), M, d,
+          tiles ? reinterpret_cast<const uint16_t*>(tiles->val) : nullptr,
+          tiles ? tiles->idx : nullptr, tiles ? tiles->cnt : nullptr, T, tile_n, cap,
+          route ? reinterpret_cast<const uint16_t*>(route->ell_val) : nullptr,
+          route ? route->ell_col : nullptr, route ? route->ell_nnz : nullptr,
+          route ? route->ell_width : 0, reinterpret_cast<uint16_t*>(y), part, j_lo, j_hi, pass,
+          device_status_ptr());
+    }
+    count_launch();
+    const cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
   }
-  count_launch();
-  return cudaGetLastError();
+  return cudaSuccess;
 }
 
 // One warp per row up to d_model = 1024 (four 256-element slabs), then teams
 // of d/512 warps with two slabs each.
 template <bool ELL>
-cudaError_t launch_fmt(const void* x, const void* wuT, const void* wd, int M, int d,
+cudaError_t launch_fmt(const void* x, const void* wuT, const void* wd, int M, int d, int f,
                        const twell_tiles* tiles, int T, int tile_n, int cap,
-                       const twell_hybrid* route, void* y, cudaStream_t s) {
-  if (d <= 512) return launch_team<1, 2, ELL>(x, wuT, wd, M, d, tiles, T, tile_n, cap, route, y, s);
-  if (d <= 1024) return launch_team<1, 4, ELL>(x, wuT, wd, M, d, tiles, T, tile_n, cap, route, y, s);
-  if (d <= 2048) return launch_team<4, 2, ELL>(x, wuT, wd, M, d, tiles, T, tile_n, cap, route, y, s);
-  if (d <= 4096) return launch_team<8, 2, ELL>(x, wuT, wd, M, d, tiles, T, tile_n, cap, route, y, s);
-  return launch_team<8, 4, ELL>(x, wuT, wd, M, d, tiles, T, tile_n, cap, route, y, s);
+                       const twell_hybrid* route, void* y, float* part, int chunks,
+                       cudaStream_t s) {
+#define TW_FWD(TEAM, VPL) \
+  launch_team<TEAM, VPL, ELL>(x, wuT, wd, M, d, f, tiles, T, tile_n, cap, route, y, part, chunks, s)
+  if (d <= 512) return TW_FWD(1, 2);
+  if (d <= 1024) return TW_FWD(1, 4);
+  if (d <= 2048) return TW_FWD(4, 2);
+  if (d <= 4096) return TW_FWD(8, 2);
+  return TW_FWD(8, 4);
+#undef TW_FWD
 }
 
 }  // namespace
 
 cudaError_t launch_sparse_fwd(const void* x, const void* wuT, const void* wd, int M, int d, int f,
                               const twell_tiles* tiles, int tile_n, int cap,
-                              const twell_hybrid* route, void* y, cudaStream_t s) {
+                              const twell_hybrid* route, void* y, float* part, cudaStream_t s) {
   if (M == 0) return cudaSuccess;
   const int T = f / tile_n;
-  if (route) return launch_fmt<true>(x, wuT, wd, M, d, nullptr, T, tile_n, cap, route, y, s);
-  return launch_fmt<false>(x, wuT, wd, M, d, tiles, T, tile_n, cap, nullptr, y, s);
+  if (route) {
+    // Wu^T and Wd rows: split the neuron axis into L2-sized passes when they
+    // do not fit (partial sums in `part`, same accumulation order)
+    const int chunks = part ? l2_chunks(2.0 * 2.0 * (double)f * d) : 1;
+    return launch_fmt<true>(x, wuT, wd, M, d, f, nullptr, T, tile_n, cap, route, y, part,
+                            chunks, s);
+  }
+  return launch_fmt<false>(x, wuT, wd, M, d, f, tiles, T, tile_n, cap, nullptr, y, nullptr, 1, s);
 }
 
 }  // namespace tw

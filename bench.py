@@ -265,9 +265,18 @@ def run_own(args, dist):
         twell.twell_ffn_fwd(x, wg, wu, wd, shape, y, route=route, ws=ws)
         twell.twell_ffn_bwd(x, wg, wu, wd, dy, shape, route, L1, dx, *dws, ws)
 
+    # inference workloads (uniform density, no routing) run the TwELL forward;
+    # training workloads run the forward of their training step: pack, hybrid
+    # route, ELL gather plus the dense fallback for the routed rows
+    fwd_path = "hybrid" if rf > 0 else "twell"
+
     def sparse_fwd():
         twell.twell_pack(x, wg, shape, tiles)
-        twell.twell_ffn_fwd(x, wg, wu, wd, shape, y, tiles=tiles)
+        if fwd_path == "hybrid":
+            twell.hybrid_route(tiles, shape, route)
+            twell.twell_ffn_fwd(x, wg, wu, wd, shape, y, route=route, ws=ws)
+        else:
+            twell.twell_ffn_fwd(x, wg, wu, wd, shape, y, tiles=tiles)
 
     def dense_fwd():
         twell.twell_dense_ffn_fwd(x, wg, wu, wd, shape, y_d, False, ws_d)
@@ -313,6 +322,9 @@ def run_own(args, dist):
         torch.cuda.synchronize()
         ck = clocks.stop() if clocks else None
         ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
+        st = twell.twell_get_device_status()
+        if st != 0:  # a capacity overflow or timeout voids the number
+            raise RuntimeError("device status %d after timing" % st)
         return dist.max(ms, dev), launches, prof, ck
 
     if args.only:
@@ -354,6 +366,7 @@ def run_own(args, dist):
                      for k, v in sorted(fam.items(), key=lambda kv: -kv[1][1])}
 
     fam, kernels = breakdown(sparse_step)
+    _, kernels_fwd = breakdown(sparse_fwd)
     _, kernels_dense = breakdown(dense_step)
     dominant = max(fam, key=lambda k: fam[k][1])
 
@@ -450,11 +463,12 @@ def run_own(args, dist):
         "dense_fwd_tokens_per_s": n * M / (ms_dfwd / 1e3),
         "dense_fwd_bwd_tokens_per_s": n * M / (ms_dstep / 1e3),
         "speedup_vs_dense": {"fwd": ms_dfwd / ms_fwd, "fwd_bwd": ms_dstep / ms_step},
+        "fwd_path": fwd_path,
         "ms": {"sparse_fwd_bwd": ms_step, "sparse_fwd": ms_fwd, "dense_fwd": ms_dfwd,
                "dense_fwd_bwd": ms_dstep, "sparse_fwd_bwd_eager": ms_eager},
         "measured_density": density, "routed_rows": n_dense, "ell_entries": nnz_ell,
         "roofline": roof, "gather_probe": gather_probe, "kernels": kernels,
-        "kernels_dense_step": kernels_dense,
+        "kernels_fwd": kernels_fwd, "kernels_dense_step": kernels_dense,
         "e2e": {"value": n * M / (ms_e2e / 1e3), "unit": UNIT, "h2d_bytes_per_step": bi,
                 "d2h_bytes_per_step": bo},
         "gpu_launches": int(launches_per_step * args.steps),

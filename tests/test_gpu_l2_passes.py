@@ -1,0 +1,65 @@
+"""The ELL forward gather split into L2-sized neuron passes.
+
+When the gathered weight rows (Wu^T and Wd, 4 * d_ff * d_model bytes) exceed
+about 3/4 of L2, the fused up+down kernel of page 2 "Sakana AI and NVIDIA
+introduce TwELL with CUDA kernels ...", section "¿Qué hace distinto a TwELL
+frente a ELL clásico?" runs once per neuron chunk and carries y_m between
+passes in fp32.  A row's ELL columns ascend, every chunk is a contiguous slice
+of it and the per-entry arithmetic and accumulation order are unchanged, so
+the result must equal the single-pass TwELL forward bit for bit; sampled
+rows are also checked against the oracle."""
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from activation_sparse_gated_tcgen05_gb300 import synthetic, twell
+
+from helpers import assert_close, dev_bf16, fwd_allowance, to_np
+
+pytestmark = pytest.mark.gpu
+
+
+def _expected_passes(d, f):
+    l2 = torch.cuda.get_device_properties(0).L2_cache_size
+    gathered = 4.0 * f * d
+    return 1 if gathered <= 0.75 * l2 else math.ceil(gathered / (0.5 * l2))
+
+
+@pytest.mark.parametrize("M,d,f", [(384, 4096, 8192), (130, 2048, 16384)])
+def test_multi_pass_forward_matches_single_pass(M, d, f):
+    passes = _expected_passes(d, f)
+    assert passes > 1, "shape no longer exceeds L2; pick a larger one"
+    w = synthetic.make_inputs(M, d, f, seed=11, with_dy=False)
+    x, wg, wu, wd = (dev_bf16(w[k]) for k in ("x", "wgT", "wuT", "wd"))
+    shape = twell.make_shape(M, d, f, 128, 32)
+    tiles = twell.alloc_tiles(shape)
+    twell.twell_pack(x, wg, shape, tiles)
+    nnz = twell.tiles_view(tiles, shape)[3].cpu().numpy()
+    W = int(nnz.max())  # no row routed: every row goes through the gather
+    route = twell.alloc_hybrid(shape, W)
+    twell.hybrid_route(tiles, shape, route)
+    ws = torch.empty(twell.twell_workspace_bytes(shape, W, False), dtype=torch.uint8,
+                     device="cuda")
+    y_single = torch.empty(M, d, dtype=torch.bfloat16, device="cuda")
+    twell.twell_ffn_fwd(x, wg, wu, wd, shape, y_single, tiles=tiles)
+    y_multi = torch.full((M, d), float("nan"), dtype=torch.bfloat16, device="cuda")
+    twell.twell_profile_begin("sparse_fwd")
+    twell.twell_ffn_fwd(x, wg, wu, wd, shape, y_multi, route=route, ws=ws)
+    torch.cuda.synchronize()
+    prof = twell.twell_profile_end()
+    assert twell.twell_get_device_status() == 0
+    assert int(twell.hybrid_view(route, shape)[4].item()) == 0
+    assert prof["sparse_fwd"][0] == passes
+    # same bytes: entries in the same order, fp32 carried exactly between passes
+    assert torch.equal(y_multi.view(torch.int16), y_single.view(torch.int16))
+    rows = np.array([0, 1, M // 2, M - 1], dtype=np.int64)
+    oracle.set_threads(os.cpu_count() or 1)
+    try:
+        ref = oracle.ffn_fwd_dense(w["x"], w["wgT"], w["wuT"], w["wd"], rows=rows)
+    finally:
+        oracle.set_threads(1)
+    assert_close(to_np(y_multi)[rows], ref, "y", out_bf16=True, allowance=fwd_allowance(w, rows))
