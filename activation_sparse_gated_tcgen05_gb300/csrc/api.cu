@@ -587,8 +587,8 @@ twell_status twell_ffn_bwd(const void* x, const void* wgT, const void* wuT, cons
   cudaError_t e = launch_csc_build(*route, s.M, s.d_ff, w.mask_off, w.csc_ptr, w.csc_row,
                                    w.slot_pos, cs);
   if (e == cudaSuccess)
-    e = launch_sparse_bwd_rows(x, dy, wgT, wuT, wd, s.M, s.d_model, *route, w.slot_pos, l1_coeff,
-                               w.csc_vals, dx, cs);
+    e = launch_sparse_bwd_rows(x, dy, wgT, wuT, wd, s.M, s.d_model, s.d_ff, *route, w.slot_pos,
+                               l1_coeff, w.csc_vals, dx, w.part, cs);
   if (e == cudaSuccess)
     e = launch_sparse_bwd_neurons(x, dy, s.M, s.d_model, s.d_ff, w.csc_ptr, w.csc_row, w.csc_vals,
                                   dwgT, dwuT, dwd, cs);

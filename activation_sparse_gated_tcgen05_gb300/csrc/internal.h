@@ -78,10 +78,11 @@ cudaError_t launch_sparse_fwd(const void* x, const void* wuT, const void* wd, in
                               const twell_hybrid* route, void* y, float* part, cudaStream_t s);
 cudaError_t launch_csc_build(const twell_hybrid& route, int M, int f, int* blk_counts,
                              int* csc_ptr, int* csc_row, int* slot_pos, cudaStream_t s);
+// `part` ([M][d] fp32) carries dX between L2-sized neuron passes (may be null).
 cudaError_t launch_sparse_bwd_rows(const void* x, const void* dy, const void* wgT, const void* wuT,
-                                   const void* wd, int M, int d, const twell_hybrid& route,
+                                   const void* wd, int M, int d, int f, const twell_hybrid& route,
                                    const int* slot_pos, float lambda, float4* csc_vals, void* dx,
-                                   cudaStream_t s);
+                                   float* part, cudaStream_t s);
 cudaError_t launch_sparse_bwd_neurons(const void* x, const void* dy, int M, int d, int f,
                                       const int* csc_ptr, const int* csc_row,
                                       const float4* csc_vals, float* dwgT, float* dwuT, float* dwd,

@@ -34,6 +34,7 @@ namespace {
 
 constexpr unsigned kFull = 0xffffffffu;
 constexpr int kWarps = 8;
+constexpr int kPassFirst = 1, kPassLast = 2;
 
 // ---------------------------------------------------------------- CSC index
 __global__ void __launch_bounds__(kWarps * 32)
@@ -148,7 +149,8 @@ __global__ void __launch_bounds__(256, MINB)
                     const uint16_t* __restrict__ wd, int M, int d,
                     const uint16_t* __restrict__ ell_val, const uint16_t* __restrict__ ell_col,
                     const int* __restrict__ ell_nnz, int W, const int* __restrict__ slot_pos,
-                    float lambda, float4* __restrict__ csc_vals, uint16_t* __restrict__ dx) {
+                    float lambda, float4* __restrict__ csc_vals, uint16_t* __restrict__ dx,
+                    float* __restrict__ part, int j_lo, int j_hi, int pass) {
   constexpr int ROWS = 8 / TEAM;
   __shared__ float red[2][ROWS][TEAM][2 * B];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -156,6 +158,7 @@ __global__ void __launch_bounds__(256, MINB)
   const int m = blockIdx.x * ROWS + team;
   if (m >= M) return;
 
+  const bool first = pass & kPassFirst, last = pass & kPassLast;
   uint4 xp[VPL], dyp[VPL];  // x_m, dY_m slabs, packed bf16
   uint64_t acc[VPL][4];
   int eoff[VPL];  // slab offsets, lanes past d_model read the first slab
@@ -166,13 +169,32 @@ __global__ void __launch_bounds__(256, MINB)
     eoff[v] = ok ? e : 0;
     xp[v] = ok ? ldg_v4(x + (long long)m * d + e) : make_uint4(0, 0, 0, 0);
     dyp[v] = ok ? ldg_v4(dy + (long long)m * d + e) : make_uint4(0, 0, 0, 0);
+    if (first || !ok) {
 #pragma unroll
-    for (int k = 0; k < 4; ++k) acc[v][k] = 0;
+      for (int k = 0; k < 4; ++k) acc[v][k] = 0;
+    } else {  // dX_m of the earlier neuron chunks
+      const uint4* pp = reinterpret_cast<const uint4*>(part + (long long)m * d + e);
+      const uint4 q0 = pp[0], q1 = pp[1];
+      acc[v][0] = f2_make(q0.x, q0.y);
+      acc[v][1] = f2_make(q0.z, q0.w);
+      acc[v][2] = f2_make(q1.x, q1.y);
+      acc[v][3] = f2_make(q1.z, q1.w);
+    }
   }
   int buf = 0;
   const int n = ell_nnz[m];
-  for (int e0 = 0; e0 < n; e0 += 32) {
-    const int count = min(32, n - e0);
+  // a row's columns ascend: the neuron chunk [j_lo, j_hi) is the slice [a, b)
+  int a = 0, bnd = n;
+  if (!(first && last)) {
+    a = bnd = 0;
+    for (int s0 = 0; s0 < n; s0 += 32) {
+      const int jc = s0 + lane < n ? (int)ell_col[(long long)m * W + s0 + lane] : 0x7fffffff;
+      a += __popc(__ballot_sync(kFull, jc < j_lo));
+      bnd += __popc(__ballot_sync(kFull, jc < j_hi));
+    }
+  }
+  for (int e0 = a; e0 < bnd; e0 += 32) {
+    const int count = min(32, bnd - e0);
     int jl = 0, pl = 0;  // slots past the row's end: neuron 0, gate 0
     float gl = 0.f;
     if (lane < count) {
@@ -266,7 +288,16 @@ __global__ void __launch_bounds__(256, MINB)
 #pragma unroll
   for (int v = 0; v < VPL; ++v) {
     const int e = slab<TEAM>(lane, wt, v);
-    if (e < d) *reinterpret_cast<uint4*>(dx + (long long)m * d + e) = f2x4_to_bf8(acc[v]);
+    if (e >= d) continue;
+    if (last) {
+      *reinterpret_cast<uint4*>(dx + (long long)m * d + e) = f2x4_to_bf8(acc[v]);
+    } else {
+      uint4* pp = reinterpret_cast<uint4*>(part + (long long)m * d + e);
+      pp[0] = make_uint4((uint32_t)acc[v][0], (uint32_t)(acc[v][0] >> 32), (uint32_t)acc[v][1],
+                         (uint32_t)(acc[v][1] >> 32));
+      pp[1] = make_uint4((uint32_t)acc[v][2], (uint32_t)(acc[v][2] >> 32), (uint32_t)acc[v][3],
+                         (uint32_t)(acc[v][3] >> 32));
+    }
   }
 }
 
@@ -369,20 +400,27 @@ __global__ void __launch_bounds__(256, MINB)
 
 template <int TEAM, int VPL, int B, int MINB>
 cudaError_t rows_team(const void* x, const void* dy, const void* wgT, const void* wuT,
-                      const void* wd, int M, int d, const twell_hybrid& r, const int* slot_pos,
-                      float lambda, float4* csc_vals, void* dx, cudaStream_t s) {
+                      const void* wd, int M, int d, int f, const twell_hybrid& r,
+                      const int* slot_pos, float lambda, float4* csc_vals, void* dx, float* part,
+                      int chunks, cudaStream_t s) {
   constexpr int ROWS = 8 / TEAM;
-  {
-    ProfScope prof("bwd_rows", s);
-    bwd_rows_kernel<TEAM, VPL, B, MINB><<<(M + ROWS - 1) / ROWS, 256, 0, s>>>(
-        reinterpret_cast<const uint16_t*>(x), reinterpret_cast<const uint16_t*>(dy),
-        reinterpret_cast<const uint16_t*>(wgT), reinterpret_cast<const uint16_t*>(wuT),
-        reinterpret_cast<const uint16_t*>(wd), M, d, reinterpret_cast<const uint16_t*>(r.ell_val),
-        r.ell_col, r.ell_nnz, r.ell_width, slot_pos, lambda, csc_vals,
-        reinterpret_cast<uint16_t*>(dx));
+  for (int c = 0; c < chunks; ++c) {
+    const int j_lo = (int)((long long)f * c / chunks), j_hi = (int)((long long)f * (c + 1) / chunks);
+    const int pass = (c == 0 ? kPassFirst : 0) | (c == chunks - 1 ? kPassLast : 0);
+    {
+      ProfScope prof("bwd_rows", s);
+      bwd_rows_kernel<TEAM, VPL, B, MINB><<<(M + ROWS - 1) / ROWS, 256, 0, s>>>(
+          reinterpret_cast<const uint16_t*>(x), reinterpret_cast<const uint16_t*>(dy),
+          reinterpret_cast<const uint16_t*>(wgT), reinterpret_cast<const uint16_t*>(wuT),
+          reinterpret_cast<const uint16_t*>(wd), M, d,
+          reinterpret_cast<const uint16_t*>(r.ell_val), r.ell_col, r.ell_nnz, r.ell_width,
+          slot_pos, lambda, csc_vals, reinterpret_cast<uint16_t*>(dx), part, j_lo, j_hi, pass);
+    }
+    count_launch();
+    const cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
   }
-  count_launch();
-  return cudaGetLastError();
+  return cudaSuccess;
 }
 
 template <int TEAM, int VPL, int B, int MINB>
@@ -449,12 +487,16 @@ cudaError_t launch_csc_build(const twell_hybrid& r, int M, int f, int* blk_count
 }
 
 cudaError_t launch_sparse_bwd_rows(const void* x, const void* dy, const void* wgT, const void* wuT,
-                                   const void* wd, int M, int d, const twell_hybrid& route,
+                                   const void* wd, int M, int d, int f, const twell_hybrid& route,
                                    const int* slot_pos, float lambda, float4* csc_vals, void* dx,
-                                   cudaStream_t s) {
+                                   float* part, cudaStream_t s) {
   if (M == 0) return cudaSuccess;
-#define TW_ROWS(T, V, B, MINB) \
-  rows_team<T, V, B, MINB>(x, dy, wgT, wuT, wd, M, d, route, slot_pos, lambda, csc_vals, dx, s)
+  // Wd, Wu^T and Wg^T rows: L2-sized neuron passes when they do not fit,
+  // dX_m carried in `part` (fp32) with the accumulation order unchanged
+  const int chunks = part ? l2_chunks(3.0 * 2.0 * (double)f * d) : 1;
+#define TW_ROWS(T, V, B, MINB)                                                                 \
+  rows_team<T, V, B, MINB>(x, dy, wgT, wuT, wd, M, d, f, route, slot_pos, lambda, csc_vals, dx, \
+                           part, chunks, s)
   if (d <= 512) return TW_ROWS(1, 2, 2, 2);
   if (d <= 1024) return TW_ROWS(1, 4, 1, 2);
   if (d <= 2048) return TW_ROWS(4, 2, 2, 2);

@@ -63,3 +63,48 @@ def test_multi_pass_forward_matches_single_pass(M, d, f):
     finally:
         oracle.set_threads(1)
     assert_close(to_np(y_multi)[rows], ref, "y", out_bf16=True, allowance=fwd_allowance(w, rows))
+
+
+def test_multi_pass_backward_rows():
+    """dX over ELL rows in L2-sized passes (Wd, Wu^T, Wg^T rows exceed L2):
+    sampled rows of dX and sampled neurons of the weight gradients against
+    the oracle, and the pass count seen by the profiler."""
+    from helpers import bwd_allowance_sampled
+
+    M, d, f, lam = 256, 4096, 8192, 2e-5
+    l2 = torch.cuda.get_device_properties(0).L2_cache_size
+    gathered = 6.0 * f * d
+    passes = 1 if gathered <= 0.75 * l2 else math.ceil(gathered / (0.5 * l2))
+    assert passes > 1, "shape no longer exceeds L2; pick a larger one"
+    w = synthetic.make_inputs(M, d, f, seed=12)
+    x, wg, wu, wd, dy = (dev_bf16(w[k]) for k in ("x", "wgT", "wuT", "wd", "dy"))
+    shape = twell.make_shape(M, d, f, 128, 32)
+    tiles = twell.alloc_tiles(shape)
+    twell.twell_pack(x, wg, shape, tiles)
+    W = int(twell.tiles_view(tiles, shape)[3].max().item())
+    route = twell.alloc_hybrid(shape, W)
+    twell.hybrid_route(tiles, shape, route)
+    ws = torch.empty(twell.twell_workspace_bytes(shape, W, True), dtype=torch.uint8,
+                     device="cuda")
+    dx = torch.full((M, d), float("nan"), dtype=torch.bfloat16, device="cuda")
+    dws = [torch.full((f, d), float("nan"), device="cuda") for _ in range(3)]
+    twell.twell_profile_begin("bwd_rows")
+    twell.twell_ffn_bwd(x, wg, wu, wd, dy, shape, route, lam, dx, *dws, ws)
+    torch.cuda.synchronize()
+    prof = twell.twell_profile_end()
+    assert twell.twell_get_device_status() == 0
+    assert prof["bwd_rows"][0] == passes
+    rows = np.array([0, 7, M // 2, M - 1], dtype=np.int64)
+    neurons = np.array([0, 5, f // 3, f - 1], dtype=np.int64)
+    oracle.set_threads(os.cpu_count() or 1)
+    try:
+        al = bwd_allowance_sampled(w, lam, rows, neurons)
+        dx_ref = oracle.ffn_bwd_dx_rows(w["x"], w["wgT"], w["wuT"], w["wd"], w["dy"], lam, rows)
+        og, ou, od = oracle.ffn_bwd_dw_neurons(w["x"], w["wgT"], w["wuT"], w["wd"], w["dy"], lam,
+                                               neurons)
+    finally:
+        oracle.set_threads(1)
+    assert_close(to_np(dx)[rows], dx_ref, "dx", out_bf16=True, allowance=al["dx"])
+    assert_close(dws[0].cpu().numpy()[neurons], og, "dwgT", allowance=al["dwgT"])
+    assert_close(dws[1].cpu().numpy()[neurons], ou, "dwuT", allowance=al["dwuT"])
+    assert_close(dws[2].cpu().numpy()[neurons], od, "dwd", allowance=al["dwd"])
