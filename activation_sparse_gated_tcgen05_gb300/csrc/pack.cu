@@ -109,12 +109,25 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32)
     const int t = t0 + lane;
     const int c = t < T ? crow[t] : 0;
     const int incl = warp_incl_scan(c);
+    const int excl = incl - c;
     const int total = __shfl_sync(0xffffffffu, incl, 31);
-    const long long src = ((long long)m * T + t) * cap;
-    const long long dst = (long long)m * W + base + incl - c;
-    for (int s = 0; s < c; ++s) {
-      ell_val[dst + s] = val[src + s];
-      ell_col[dst + s] = (uint16_t)(t * tile_n + idx[src + s]);
+    // the group's entries are spread over the lanes: entry e belongs to the
+    // tile whose inclusive count first exceeds e (binary search over lanes)
+    for (int e = lane; e - lane < total; e += 32) {
+      int lo = 0;
+#pragma unroll
+      for (int step = 16; step >= 1; step >>= 1) {
+        const int v = __shfl_sync(0xffffffffu, incl, lo + step - 1);
+        if (v <= e) lo += step;
+      }
+      const int ex = __shfl_sync(0xffffffffu, excl, lo);
+      if (e < total) {
+        const int tt = t0 + lo;
+        const long long src = ((long long)m * T + tt) * cap + (e - ex);
+        const long long dst = (long long)m * W + base + e;
+        ell_val[dst] = val[src];
+        ell_col[dst] = (uint16_t)(tt * tile_n + idx[src]);
+      }
     }
     base += total;
   }

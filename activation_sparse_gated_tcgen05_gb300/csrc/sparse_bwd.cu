@@ -92,10 +92,17 @@ __global__ void __launch_bounds__(1024)
     const int j = base + tid;
     int c = 0;
     if (j < f) {
-      for (int g = 0; g < NG; ++g) {
-        const int v = gtot[(long long)g * f + j];
-        gtot[(long long)g * f + j] = c;
-        c += v;
+      // eight group totals are loaded before any is overwritten, so the
+      // loads overlap instead of alternating with the stores
+      for (int g0 = 0; g0 < NG; g0 += 8) {
+        int v[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) v[k] = g0 + k < NG ? gtot[(long long)(g0 + k) * f + j] : 0;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          if (g0 + k < NG) gtot[(long long)(g0 + k) * f + j] = c;
+          c += v[k];
+        }
       }
     }
     const int incl = warp_incl_scan(c);
