@@ -300,9 +300,12 @@ def run_own(args, dist):
         torch.cuda.synchronize()
         return g.replay
 
-    def timed(fn, steps, warmup, profile=None, clocks=None):
+    medians = {}
+
+    def timed(fn, steps, warmup, profile=None, clocks=None, l2_flush=True, key=None):
         for _ in range(warmup):
-            flush.zero_()
+            if l2_flush:
+                flush.zero_()
             fn()
         torch.cuda.synchronize()
         dist.barrier()
@@ -315,7 +318,8 @@ def run_own(args, dist):
             twell.twell_profile_begin(profile)
         launches0 = twell.twell_launch_count()
         for s0, s1 in ev:
-            flush.zero_()
+            if l2_flush:
+                flush.zero_()
             s0.record(stream)
             fn()
             s1.record(stream)
@@ -326,6 +330,8 @@ def run_own(args, dist):
         torch.cuda.synchronize()
         ck = clocks.stop() if clocks else None
         ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
+        if key:
+            medians[key] = dist.max(statistics.median(a.elapsed_time(b) for a, b in ev), dev)
         st = twell.twell_get_device_status()
         if st != 0:  # a capacity overflow or timeout voids the number
             raise RuntimeError("device status %d after timing" % st)
@@ -381,10 +387,27 @@ def run_own(args, dist):
     step_g = graphed(sparse_step)
     launches = twell.twell_launch_count() - launches0
     launches_per_step = launches / 2  # the eager step and the captured one
-    ms_step, _, _, ck = timed(step_g, args.steps, args.warmup, clocks=clocks)
-    ms_fwd, _, _, _ = timed(graphed(sparse_fwd), args.steps, args.warmup)
+    ms_step, _, _, ck = timed(step_g, args.steps, args.warmup, clocks=clocks, key="sparse_fwd_bwd")
+    fwd_g = graphed(sparse_fwd)
+    ms_fwd, _, _, _ = timed(fwd_g, args.steps, args.warmup, key="sparse_fwd")
+    # the same steps without the L2 flush (weights warm, as in back-to-back layers of one shape)
+    ms_step_warm, _, _, _ = timed(step_g, args.steps, args.warmup, l2_flush=False)
+    ms_fwd_warm, _, _, _ = timed(fwd_g, args.steps, args.warmup, l2_flush=False)
+    # classic-ELL ablation (inference path): the dense gate written to HBM in
+    # bf16, converted by a separate pack kernel, then the same fused forward
+    ms_classic = None
+    if fwd_path == "twell":
+        a_dense = torch.empty(M, f, dtype=torch.bfloat16, device=dev)
+
+        def classic_fwd():
+            twell.twell_gemm_bf16(x, wg, a_dense, M, f, d, False, False)
+            twell.twell_pack_dense(a_dense, shape, tiles)
+            twell.twell_ffn_fwd(x, wg, wu, wd, shape, y, tiles=tiles)
+
+        ms_classic, _, _, _ = timed(graphed(classic_fwd), args.steps, args.warmup)
+        del a_dense
     ms_dfwd, _, _, _ = timed(graphed(dense_fwd), args.steps, args.warmup)
-    ms_dstep, _, _, _ = timed(graphed(dense_step), args.steps, args.warmup)
+    ms_dstep, _, _, _ = timed(graphed(dense_step), args.steps, args.warmup, key="dense_fwd_bwd")
     # eager steps with the dominant kernel's launches bracketed by CUDA events
     ms_eager, eager_launches, prof, _ = timed(sparse_step, args.steps, args.warmup,
                                               profile=dominant)
@@ -469,7 +492,12 @@ def run_own(args, dist):
         "speedup_vs_dense": {"fwd": ms_dfwd / ms_fwd, "fwd_bwd": ms_dstep / ms_step},
         "fwd_path": fwd_path,
         "ms": {"sparse_fwd_bwd": ms_step, "sparse_fwd": ms_fwd, "dense_fwd": ms_dfwd,
-               "dense_fwd_bwd": ms_dstep, "sparse_fwd_bwd_eager": ms_eager},
+               "dense_fwd_bwd": ms_dstep, "sparse_fwd_bwd_eager": ms_eager,
+               "sparse_fwd_bwd_warm_l2": ms_step_warm, "sparse_fwd_warm_l2": ms_fwd_warm,
+               "classic_ell_fwd": ms_classic},
+        "ms_median": medians,
+        "ms_per_step_median": medians.get("sparse_fwd_bwd"),
+        "saved_for_backward_bytes": saved_bytes(shape, W, M, f, d),
         "measured_density": density, "routed_rows": n_dense, "ell_entries": nnz_ell,
         "roofline": roof, "gather_probe": gather_probe, "kernels": kernels,
         "kernels_fwd": kernels_fwd, "kernels_dense_step": kernels_dense,
@@ -490,6 +518,18 @@ def run_own(args, dist):
     if dist.rank == 0:
         print(json.dumps(line), flush=True)
     dist.close()
+
+
+def saved_bytes(shape, W, M, f, d):
+    """Activation memory kept from the forward for the backward: the sparse
+    path keeps the hybrid ELL arrays (the TwELL tiles are transient: routing
+    reads them once), the dense path keeps g, u and h (bf16 [M][d_ff] each)."""
+    T, C = f // shape.tile_n, shape.tile_cap
+    ell = M * W * (2 + 2) + M * 4 + M * 4 + 4
+    tiles = M * T * C * (2 + 1) + M * T + M * 4
+    dense = 3 * M * f * 2
+    return {"sparse_ell": ell, "sparse_twell_tiles_transient": tiles, "dense_g_u_h": dense,
+            "dense_over_sparse": dense / ell}
 
 
 def traffic_for(kernel, workload):
