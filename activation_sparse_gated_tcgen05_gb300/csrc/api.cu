@@ -84,7 +84,7 @@ int num_sms() {
   return cache[dev];
 }
 
-int l2_chunks(double gathered_bytes) {
+int l2_chunks(double gathered_bytes, double fit) {
   static int cache[kMaxDevices] = {0};
   const int dev = current_device();
   if (dev < 0 || dev >= kMaxDevices) return 1;
@@ -94,7 +94,7 @@ int l2_chunks(double gathered_bytes) {
     cache[dev] = n;
   }
   const double l2 = (double)cache[dev];
-  if (gathered_bytes <= 0.75 * l2) return 1;
+  if (gathered_bytes <= fit * l2) return 1;
   return (int)std::ceil(gathered_bytes / (0.5 * l2));
 }
 

@@ -272,9 +272,10 @@ cudaError_t launch_sparse_fwd(const void* x, const void* wuT, const void* wd, in
   if (M == 0) return cudaSuccess;
   const int T = f / tile_n;
   if (route) {
-    // Wu^T and Wd rows: split the neuron axis into L2-sized passes when they
-    // do not fit (partial sums in `part`, same accumulation order)
-    const int chunks = part ? l2_chunks(2.0 * 2.0 * (double)f * d) : 1;
+    // Wu^T and Wd rows: split the neuron axis into L2-sized passes once they
+    // exceed 3/4 of L2 (partial sums in `part`, same accumulation order; on
+    // the 2B-class shape, 67 MB of weights, two passes were slower than one)
+    const int chunks = part ? l2_chunks(2.0 * 2.0 * (double)f * d, 0.75) : 1;
     return launch_fmt<true>(x, wuT, wd, M, d, f, nullptr, T, tile_n, cap, route, y, part,
                             chunks, s);
   }

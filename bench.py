@@ -56,6 +56,8 @@ def parse_args():
     ap.add_argument("--cpu-seconds", type=float, default=15.0,
                     help="target CPU time of the oracle baseline sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-torch-dense", action="store_true",
+                    help="skip the PyTorch (cuBLAS) dense FFN reference timing")
     ap.add_argument("--only", choices=("sparse_step", "sparse_fwd", "dense_fwd", "dense_step"),
                     help="time just this part (a short command for kernel profiling); prints "
                          "a reduced JSON line")
@@ -408,6 +410,31 @@ def run_own(args, dist):
         del a_dense
     ms_dfwd, _, _, _ = timed(graphed(dense_fwd), args.steps, args.warmup)
     ms_dstep, _, _, _ = timed(graphed(dense_step), args.steps, args.warmup, key="dense_fwd_bwd")
+    # a second dense reference outside this library: the same ReLU-gated FFN
+    # composed of PyTorch ops (cuBLAS GEMMs, autograd backward; no L1 term),
+    # CUDA-graphed and timed the same way
+    torch_dense = {}
+    if not args.no_torch_dense:
+        xt_ = x.detach().clone().requires_grad_()
+        wgt_, wut_ = wg.detach().clone().requires_grad_(), wu.detach().clone().requires_grad_()
+        wdt_ = wd.detach().t().contiguous().requires_grad_()  # [d][f], nn.Linear layout
+
+        def torch_fwd():
+            with torch.no_grad():
+                y_t = (torch.relu(xt_ @ wgt_.T) * (xt_ @ wut_.T)) @ wdt_.T
+            return y_t
+
+        def torch_step():
+            y_t = (torch.relu(xt_ @ wgt_.T) * (xt_ @ wut_.T)) @ wdt_.T
+            return torch.autograd.grad(y_t, (xt_, wgt_, wut_, wdt_), dy)
+
+        torch_step()
+        torch_dense["fwd_ms"] = timed(graphed(torch_fwd), args.steps, args.warmup)[0]
+        torch_dense["fwd_bwd_ms"] = timed(graphed(torch_step), args.steps, args.warmup)[0]
+        torch_dense["sparse_speedup"] = {"fwd": torch_dense["fwd_ms"] / ms_fwd,
+                                         "fwd_bwd": torch_dense["fwd_bwd_ms"] / ms_step}
+        del xt_, wgt_, wut_, wdt_
+
     # eager steps with the dominant kernel's launches bracketed by CUDA events
     ms_eager, eager_launches, prof, _ = timed(sparse_step, args.steps, args.warmup,
                                               profile=dominant)
@@ -501,6 +528,7 @@ def run_own(args, dist):
         "measured_density": density, "routed_rows": n_dense, "ell_entries": nnz_ell,
         "roofline": roof, "gather_probe": gather_probe, "kernels": kernels,
         "kernels_fwd": kernels_fwd, "kernels_dense_step": kernels_dense,
+        "torch_cublas_dense": torch_dense or None,
         "e2e": {"value": n * M / (ms_e2e / 1e3), "unit": UNIT, "h2d_bytes_per_step": bi,
                 "d2h_bytes_per_step": bo},
         "gpu_launches": int(launches_per_step * args.steps),
