@@ -386,48 +386,27 @@ struct Epilogue<EPI_GATED> {
 // residuals [du lo | da lo] when dd_split is set).
 template <>
 struct Epilogue<EPI_BWD_GATE> {
-  // g, u of one 32-column chunk of this thread's row (TMA-output path): the
-  // loads of chunk k+1 are in flight while chunk k is computed, and the first
-  // chunk of the next tile is requested before its accumulator is waited for
-  struct Chunk {
-    uint4 g[4], u[4];
-  };
-  static __device__ __forceinline__ void load(const GemmParams& p, int row, int n0, int N, int c0,
-                                              Chunk& ch) {
-    const bool in = row < p.M && n0 + c0 < N;
-    const long long gu = (long long)row * p.ldgu + n0 + c0;
-#pragma unroll
-    for (int v = 0; v < 4; ++v) {
-      ch.g[v] = in ? ldg_v4(p.g_in + gu + 8 * v) : make_uint4(0, 0, 0, 0);
-      ch.u[v] = in ? ldg_v4(p.u_in + gu + 8 * v) : make_uint4(0, 0, 0, 0);
-    }
-  }
-  static __device__ __forceinline__ void prefetch(const GemmParams& p, int row, int n0, int N,
-                                                  int half, Chunk& ch) {
-    if (p.tma_out) load(p, row, n0, N, half * (kBN / 2), ch);
-  }
   static __device__ __forceinline__ void run(const GemmParams& p, uint32_t tacc, int row,
                                              bool row_ok, int n0, int N, int half, Stager& st,
-                                             const OutMaps& om, int row0, Chunk& cur) {
+                                             const OutMaps& om, int row0) {
     const long long seg = p.dd_seg;
 #pragma unroll 1
     for (int c0 = half * (kBN / 2); c0 < (half + 1) * (kBN / 2); c0 += 32) {
-      Chunk nxt;
-      if (p.tma_out && c0 + 32 < (half + 1) * (kBN / 2)) load(p, row, n0, N, c0 + 32, nxt);
       uint32_t r[32];
       tmem_ld32(tacc + c0, r);
       tmem_wait_ld();
       if (p.tma_out) {
-        // du, da through TMA in 32-column boxes; g, u prefetched from global
-        if (n0 + c0 >= N || row0 >= p.M) {
-          cur = nxt;
-          continue;
-        }
+        // du, da through TMA in 32-column boxes; g, u read straight from global
+        if (n0 + c0 >= N || row0 >= p.M) continue;
         uint32_t duw[16], daw[16];
+        const bool in = row < p.M;
+        const long long gu = (long long)row * p.ldgu + n0 + c0;
 #pragma unroll
         for (int v = 0; v < 4; ++v) {
-          const uint4 g8 = cur.g[v];
-          const uint4 u8 = cur.u[v];
+          const uint4 g8 = in ? *reinterpret_cast<const uint4*>(p.g_in + gu + 8 * v)
+                              : make_uint4(0, 0, 0, 0);
+          const uint4 u8 = in ? *reinterpret_cast<const uint4*>(p.u_in + gu + 8 * v)
+                              : make_uint4(0, 0, 0, 0);
           const uint32_t gw[4] = {g8.x, g8.y, g8.z, g8.w};
           const uint32_t uw[4] = {u8.x, u8.y, u8.z, u8.w};
 #pragma unroll
@@ -451,7 +430,6 @@ struct Epilogue<EPI_BWD_GATE> {
         for (int v = 0; v < 4; ++v)
           st.put64(b, v, make_uint4(daw[4 * v], daw[4 * v + 1], daw[4 * v + 2], daw[4 * v + 3]));
         st.send(om.o0, b, n0 + c0 + (int)seg, row0);
-        cur = nxt;
         continue;
       }
       if (!row_ok || n0 + c0 >= N) continue;
@@ -506,17 +484,6 @@ struct Epilogue<EPI_BWD_GATE> {
 };
 
 // ------------------------------------------------------------------ kernel
-// per-thread operand registers an epilogue keeps across tiles (none but the
-// backward gate's prefetched g / u chunk)
-template <int EPI>
-struct EpiChunk {
-  struct type {};
-};
-template <>
-struct EpiChunk<EPI_BWD_GATE> {
-  using type = Epilogue<EPI_BWD_GATE>::Chunk;
-};
-
 template <bool A_MN, bool B_MN, int EPI>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
@@ -691,7 +658,6 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     Stager st{sOut + (warp - 4) * kStageBytes, lane, 0};
     const OutMaps om{&tmO0, &tmO1, &tmO2};
     int it = 0;
-    typename EpiChunk<EPI>::type chunk;
     for (int unit = blockIdx.x; unit < total; unit += gridDim.x, ++it) {
       int mb, nb;
       const int ks = unit / tiles;
@@ -699,8 +665,6 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       const int row_off = ks * m_tiles * kBM;  // split-K partial of split ks
       const int acc = it & 1;
       const uint32_t acc_phase = (uint32_t)(it >> 1) & 1u;
-      if constexpr (EPI == EPI_BWD_GATE)  // operand loads overlap the tile's MMA
-        Epilogue<EPI>::prefetch(p, mb * kBM + r_local, nb * kBN, p.N, half, chunk);
       if (!mbar_wait(&tfull[acc], acc_phase, abort_flag)) {
         set_status(p.status, TWELL_ERR_DEVICE_TIMEOUT);
         *abort_flag = 1;
@@ -711,12 +675,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       const bool row_ok = p.pad_rows ? (row < p.M) : (row < M_eff);
       const uint32_t tacc = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * kBN);
       const int n0 = (EPI == EPI_GATED) ? nb * 128 : nb * kBN;
-      if constexpr (EPI == EPI_BWD_GATE)
-        Epilogue<EPI>::run(p, tacc, row, row_ok, n0, p.N, half, st, om,
-                           row_off + mb * kBM + quarter * 32, chunk);
-      else
-        Epilogue<EPI>::run(p, tacc, row, row_ok, n0, p.N, half, st, om,
-                           row_off + mb * kBM + quarter * 32);
+      Epilogue<EPI>::run(p, tacc, row, row_ok, n0, p.N, half, st, om,
+                         row_off + mb * kBM + quarter * 32);
       tc_fence_before();
       mbar_arrive(&tempty[acc]);
     }
