@@ -47,6 +47,9 @@ def _load():
         "orc_hybrid_route": (None, [_U16, _U8, _U8, _I32, _i64, _i64, _int, _int, ctypes.c_int32,
                                     _U16, _U16, _I32, _I32, _I32]),
         "orc_ffn_fwd_dense": (None, [_D, _D, _D, _D, _i64, _i64, _int, _I64, _i64, _D]),
+        "orc_ffn_fwd_dense_silu": (None, [_D, _D, _D, _D, _i64, _i64, _I64, _i64, _D]),
+        "orc_ffn_bwd_dense_silu": (None, [_D, _D, _D, _D, _D, _i64, _i64, _i64, _D, _D, _D,
+                                          _D]),
         "orc_ffn_fwd_twell": (None, [_D, _D, _D, _i64, _i64, _int, _int, _U16, _U8, _U8,
                                      _I64, _i64, _D]),
         "orc_ffn_fwd_ell": (None, [_D, _D, _D, _i64, ctypes.c_int32, _U16, _U16, _I32, _I64,
@@ -170,6 +173,33 @@ def ffn_fwd_dense(x, wgT, wuT, wd, rows=None, round_g: bool = True) -> np.ndarra
     _load().orc_ffn_fwd_dense(_p(x, _D), _p(wg, _D), _p(wu, _D), _p(wdd, _D), d, f,
                               int(round_g), _p(r, _I64), r.size, _p(y, _D))
     return y
+
+
+def ffn_fwd_dense_silu(x, wgT, wuT, wd, rows=None) -> np.ndarray:
+    """y = (SiLU(x Wg) * (x Wu)) Wd in fp64 (the unmodified gated FFN)."""
+    x, wg, wu, wdd = f64(x), f64(wgT), f64(wuT), f64(wd)
+    M, d = x.shape
+    f = wg.shape[0]
+    r = _rows(rows, M)
+    y = np.empty((r.size, d), np.float64)
+    _load().orc_ffn_fwd_dense_silu(_p(x, _D), _p(wg, _D), _p(wu, _D), _p(wdd, _D), d, f,
+                                   _p(r, _I64), r.size, _p(y, _D))
+    return y
+
+
+def ffn_bwd_dense_silu(x, wgT, wuT, wd, dy):
+    """Whole-batch backward of the SiLU-gated FFN (no L1 term; small shapes).
+    Returns dict dx, dwgT, dwuT, dwd."""
+    x, wg, wu, wdd, dyy = f64(x), f64(wgT), f64(wuT), f64(wd), f64(dy)
+    M, d = x.shape
+    f = wg.shape[0]
+    dx = np.empty((M, d))
+    dwg = np.empty((f, d))
+    dwu = np.empty((f, d))
+    dwd = np.empty((f, d))
+    _load().orc_ffn_bwd_dense_silu(_p(x, _D), _p(wg, _D), _p(wu, _D), _p(wdd, _D), _p(dyy, _D),
+                                   M, d, f, _p(dx, _D), _p(dwg, _D), _p(dwu, _D), _p(dwd, _D))
+    return {"dx": dx, "dwgT": dwg, "dwuT": dwu, "dwd": dwd}
 
 
 def ffn_fwd_twell(x, wuT, wd, val, idx, cnt, tile_n: int, rows=None) -> np.ndarray:

@@ -444,4 +444,77 @@ void orc_ffn_bwd_hybrid(const double* x, const double* wgT, const double* wuT,
   }
 }
 
+// ---- SiLU-gated dense FFN (comparator only)  [P2-recipe] ----------------------
+// The unmodified gated FFN the recipe starts from: the gate activation is SiLU
+// instead of ReLU, and there is no L1 term.
+//   s_j = silu(a_j) = a_j * sigmoid(a_j),  h_j = s_j u_j,  y_m = sum_j h_j Wd[j,:]
+// Backward, by the chain rule:
+//   dh = dY Wd^T,  du = dh s,  da = dh u silu'(a),
+//   silu'(a) = sigmoid(a) (1 + a (1 - sigmoid(a))),
+//   dWd = h^T dY, dWu = x^T du, dWg = x^T da, dx = du Wu^T + da Wg^T.
+static double sigmoid(double a) { return 1.0 / (1.0 + std::exp(-a)); }
+
+void orc_ffn_fwd_dense_silu(const double* x, const double* wgT, const double* wuT,
+                            const double* wd, int64_t d, int64_t f, const int64_t* rows,
+                            int64_t nrows, double* y) {
+  parallel_for(nrows, [&](int64_t lo, int64_t hi) {
+    for (int64_t r = lo; r < hi; ++r) {
+      const double* xm = x + rows[r] * d;
+      double* yr = y + r * d;
+      for (int64_t k = 0; k < d; ++k) yr[k] = 0.0;
+      for (int64_t j = 0; j < f; ++j) {
+        double a = dot(xm, wgT + j * d, d);
+        double s = a * sigmoid(a);
+        double u = dot(xm, wuT + j * d, d);
+        double h = s * u;
+        for (int64_t k = 0; k < d; ++k) yr[k] += h * wd[j * d + k];
+      }
+    }
+  });
+}
+
+// Whole-batch SiLU backward (small shapes: it holds [M][f] arrays).
+void orc_ffn_bwd_dense_silu(const double* x, const double* wgT, const double* wuT,
+                            const double* wd, const double* dy, int64_t M, int64_t d,
+                            int64_t f, double* dx, double* dwgT, double* dwuT, double* dwd) {
+  std::vector<double> h(M * f), du(M * f), da(M * f);
+  parallel_for(M, [&](int64_t lo, int64_t hi) {
+    for (int64_t m = lo; m < hi; ++m)
+      for (int64_t j = 0; j < f; ++j) {
+        double a = dot(x + m * d, wgT + j * d, d);
+        double sg = sigmoid(a);
+        double s = a * sg;
+        double ds = sg * (1.0 + a * (1.0 - sg));
+        double uj = dot(x + m * d, wuT + j * d, d);
+        double dh = dot(dy + m * d, wd + j * d, d);
+        h[m * f + j] = s * uj;
+        du[m * f + j] = dh * s;
+        da[m * f + j] = dh * uj * ds;
+      }
+  });
+  parallel_for(f, [&](int64_t lo, int64_t hi) {
+    for (int64_t j = lo; j < hi; ++j)
+      for (int64_t k = 0; k < d; ++k) {
+        double sd = 0.0, su = 0.0, sg = 0.0;
+        for (int64_t m = 0; m < M; ++m) {
+          sd += h[m * f + j] * dy[m * d + k];
+          su += du[m * f + j] * x[m * d + k];
+          sg += da[m * f + j] * x[m * d + k];
+        }
+        dwd[j * d + k] = sd;
+        dwuT[j * d + k] = su;
+        dwgT[j * d + k] = sg;
+      }
+  });
+  parallel_for(M, [&](int64_t lo, int64_t hi) {
+    for (int64_t m = lo; m < hi; ++m)
+      for (int64_t k = 0; k < d; ++k) {
+        double s = 0.0;
+        for (int64_t j = 0; j < f; ++j)
+          s += du[m * f + j] * wuT[j * d + k] + da[m * f + j] * wgT[j * d + k];
+        dx[m * d + k] = s;
+      }
+  });
+}
+
 }  // extern "C"

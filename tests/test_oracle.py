@@ -333,3 +333,62 @@ def test_threads_do_not_change_results():
     y5 = oracle.ffn_fwd_dense(w["x"], w["wgT"], w["wuT"], w["wd"], rows=rows)
     oracle.set_threads(1)
     np.testing.assert_array_equal(y1, y5)
+
+
+# ------------------------------------------- SiLU-gated comparator (dense only)
+def test_silu_fwd_bwd_match_torch_autograd():
+    """The SiLU-gated FFN against torch's own silu and autograd in fp64."""
+    rng = np.random.default_rng(21)
+    M, d, f = 6, 16, 24
+    x = rng.standard_normal((M, d))
+    wgT, wuT, wd = (rng.standard_normal((f, d)) / 3 for _ in range(3))
+    dy = rng.standard_normal((M, d))
+    X = torch.tensor(x, requires_grad=True)
+    Wg = torch.tensor(wgT.T.copy(), requires_grad=True)
+    Wu = torch.tensor(wuT.T.copy(), requires_grad=True)
+    Wd = torch.tensor(wd, requires_grad=True)
+    y_t = (torch.nn.functional.silu(X @ Wg) * (X @ Wu)) @ Wd
+    (y_t * torch.tensor(dy)).sum().backward()
+    y = oracle.ffn_fwd_dense_silu(x, wgT, wuT, wd)
+    b = oracle.ffn_bwd_dense_silu(x, wgT, wuT, wd, dy)
+    np.testing.assert_allclose(y, y_t.detach().numpy(), rtol=1e-12, atol=1e-13)
+    np.testing.assert_allclose(b["dx"], X.grad.numpy(), rtol=1e-12, atol=1e-13)
+    np.testing.assert_allclose(b["dwgT"], Wg.grad.numpy().T, rtol=1e-12, atol=1e-13)
+    np.testing.assert_allclose(b["dwuT"], Wu.grad.numpy().T, rtol=1e-12, atol=1e-13)
+    np.testing.assert_allclose(b["dwd"], Wd.grad.numpy(), rtol=1e-12, atol=1e-13)
+
+
+def test_silu_backward_matches_finite_differences():
+    rng = np.random.default_rng(12)
+    M, d, f = 3, 8, 12
+    x = rng.standard_normal((M, d))
+    wgT, wuT, wd = (rng.standard_normal((f, d)) / 2 for _ in range(3))
+    dy = rng.standard_normal((M, d))
+    b = oracle.ffn_bwd_dense_silu(x, wgT, wuT, wd, dy)
+    h = 1e-6
+    for gname, arr in {"dx": x, "dwgT": wgT, "dwuT": wuT, "dwd": wd}.items():
+        for flat in range(arr.size):
+            i = np.unravel_index(flat, arr.shape)
+            old = arr[i]
+            arr[i] = old + h
+            lp = float((oracle.ffn_fwd_dense_silu(x, wgT, wuT, wd) * dy).sum())
+            arr[i] = old - h
+            lm = float((oracle.ffn_fwd_dense_silu(x, wgT, wuT, wd) * dy).sum())
+            arr[i] = old
+            fd = (lp - lm) / (2 * h)
+            assert abs(fd - b[gname][i]) <= 1e-6 * max(1.0, abs(b[gname][i])), (gname, i)
+
+
+def test_silu_equals_relu_when_every_gate_is_large():
+    """sigmoid(a) = 1 to fp64 precision for a >= 40: SiLU and ReLU gates agree."""
+    rng = np.random.default_rng(13)
+    M, d, f = 5, 10, 16
+    x = rng.standard_normal((M, d))
+    x[:, -1] = 1.0
+    wgT = rng.standard_normal((f, d)) / 4
+    wgT[:, -1] = 60.0  # a = x . Wg >= 60 - |rest| > 40
+    wuT, wd = rng.standard_normal((f, d)), rng.standard_normal((f, d))
+    assert oracle.gate_preact(x, wgT).min() > 40
+    np.testing.assert_allclose(oracle.ffn_fwd_dense_silu(x, wgT, wuT, wd),
+                               oracle.ffn_fwd_dense(x, wgT, wuT, wd, round_g=False),
+                               rtol=1e-13, atol=1e-12)
