@@ -255,8 +255,10 @@ Mat mat(const void* p, long long rows, long long cols, long long ld) { return Ma
 // [rows][2f] buffer), optional g / u copies ([rows][f]).
 cudaError_t gated_gemm(const void* x_rows, long long rows, const twell_shape& s, const void* wgT,
                        const void* wuT, const int* m_dev, uint16_t* h, bool split, uint16_t* g,
-                       uint16_t* u, float* u32, int pad_rows, cudaStream_t st) {
+                       uint16_t* u, float* u32, int pad_rows, cudaStream_t st,
+                       int act = kActRelu) {
   GemmParams p = base_params((int)rows, s.d_ff, s.d_model, 128);
+  p.act = act;
   p.m_dev = m_dev;
   p.h = h;
   p.ldh = split ? 2LL * s.d_ff : s.d_ff;
@@ -327,8 +329,10 @@ cudaError_t down_gemm(const uint16_t* h, long long rows, const twell_shape& s, c
 // dd = [du | da] (split: [du | da | du lo | da lo]) from dh = dy Wd^T and g, u.
 cudaError_t dgate_gemm(const void* dy_rows, long long rows, const twell_shape& s, const void* wd,
                        const int* m_dev, const uint16_t* g, const uint16_t* u, const float* u32,
-                       uint16_t* dd, bool split, float lambda, int pad_rows, cudaStream_t st) {
+                       uint16_t* dd, bool split, float lambda, int pad_rows, cudaStream_t st,
+                       int act = kActRelu) {
   GemmParams p = base_params((int)rows, s.d_ff, s.d_model, kBN);
+  p.act = act;
   p.m_dev = m_dev;
   p.g_in = g;
   p.u_in = u;
@@ -617,11 +621,13 @@ size_t twell_dense_workspace_bytes(const twell_shape* shape, int32_t training) {
   return carve_dense(nullptr, *shape, training ? 1 : 0).bytes;
 }
 
-twell_status twell_dense_ffn_fwd(const void* x, const void* wgT, const void* wuT, const void* wd,
-                                 const twell_shape* shape, void* y, int32_t training, void* ws,
-                                 size_t ws_bytes, void* stream) {
+twell_status twell_dense_ffn_fwd_act(const void* x, const void* wgT, const void* wuT,
+                                     const void* wd, const twell_shape* shape,
+                                     int32_t activation, void* y, int32_t training, void* ws,
+                                     size_t ws_bytes, void* stream) {
   twell_status st = check_shape(shape, false);
   if (st != TWELL_OK) return st;
+  if (activation != TWELL_ACT_RELU && activation != TWELL_ACT_SILU) return TWELL_ERR_INVALID_ARG;
   if ((st = check_ptrs({x, wgT, wuT, wd, y})) != TWELL_OK) return st;
   const twell_shape& s = *shape;
   if (!ws || ws_bytes < carve_dense(nullptr, s, training ? 1 : 0).bytes) return TWELL_ERR_WORKSPACE;
@@ -630,17 +636,28 @@ twell_status twell_dense_ffn_fwd(const void* x, const void* wgT, const void* wuT
   cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
   const DenseWs w = carve_dense(ws, s, training ? 1 : 0);
   cudaError_t e = gated_gemm(x, s.M, s, wgT, wuT, nullptr, w.h, false, training ? w.g : nullptr,
-                             training ? w.u : nullptr, nullptr, 0, cs);
+                             training ? w.u : nullptr, nullptr, 0, cs,
+                             activation == TWELL_ACT_SILU ? kActSilu : kActRelu);
   if (e == cudaSuccess) e = down_gemm(w.h, s.M, s, wd, false, nullptr, nullptr, y, cs);
   return cuda_status(e);
 }
 
-twell_status twell_dense_ffn_bwd(const void* x, const void* wgT, const void* wuT, const void* wd,
-                                 const void* dy, const twell_shape* shape, float l1_coeff,
-                                 void* dx, float* dwgT, float* dwuT, float* dwd, void* ws,
+twell_status twell_dense_ffn_fwd(const void* x, const void* wgT, const void* wuT, const void* wd,
+                                 const twell_shape* shape, void* y, int32_t training, void* ws,
                                  size_t ws_bytes, void* stream) {
+  return twell_dense_ffn_fwd_act(x, wgT, wuT, wd, shape, TWELL_ACT_RELU, y, training, ws,
+                                 ws_bytes, stream);
+}
+
+twell_status twell_dense_ffn_bwd_act(const void* x, const void* wgT, const void* wuT,
+                                     const void* wd, const void* dy, const twell_shape* shape,
+                                     int32_t activation, float l1_coeff, void* dx, float* dwgT,
+                                     float* dwuT, float* dwd, void* ws, size_t ws_bytes,
+                                     void* stream) {
   twell_status st = check_shape(shape, false);
   if (st != TWELL_OK) return st;
+  if (activation != TWELL_ACT_RELU && activation != TWELL_ACT_SILU) return TWELL_ERR_INVALID_ARG;
+  if (activation == TWELL_ACT_SILU && l1_coeff != 0.0f) return TWELL_ERR_INVALID_ARG;
   if ((st = check_ptrs({x, wgT, wuT, wd, dy, dx, dwgT, dwuT, dwd})) != TWELL_OK) return st;
   const twell_shape& s = *shape;
   if (!ws || ws_bytes < carve_dense(nullptr, s, 1).bytes) return TWELL_ERR_WORKSPACE;
@@ -654,13 +671,21 @@ twell_status twell_dense_ffn_bwd(const void* x, const void* wgT, const void* wuT
     return cuda_status(e);
   }
   const DenseWs w = carve_dense(ws, s, 1);
-  cudaError_t e =
-      dgate_gemm(dy, s.M, s, wd, nullptr, w.g, w.u, nullptr, w.dd, false, l1_coeff, 0, cs);
+  cudaError_t e = dgate_gemm(dy, s.M, s, wd, nullptr, w.g, w.u, nullptr, w.dd, false, l1_coeff, 0,
+                             cs, activation == TWELL_ACT_SILU ? kActSilu : kActRelu);
   if (e == cudaSuccess) e = dx_gemm(w.dd, s.M, s, wgT, wuT, false, nullptr, nullptr, dx, cs);
   if (e == cudaSuccess) e = dw_gemm(w.h, f, dy, s.M, s, nullptr, dwd, 0, cs);
   if (e == cudaSuccess) e = dw_gemm(w.dd, 2 * f, x, s.M, s, nullptr, dwuT, 0, cs);
   if (e == cudaSuccess) e = dw_gemm(w.dd + f, 2 * f, x, s.M, s, nullptr, dwgT, 0, cs);
   return cuda_status(e);
+}
+
+twell_status twell_dense_ffn_bwd(const void* x, const void* wgT, const void* wuT, const void* wd,
+                                 const void* dy, const twell_shape* shape, float l1_coeff,
+                                 void* dx, float* dwgT, float* dwuT, float* dwd, void* ws,
+                                 size_t ws_bytes, void* stream) {
+  return twell_dense_ffn_bwd_act(x, wgT, wuT, wd, dy, shape, TWELL_ACT_RELU, l1_coeff, dx, dwgT,
+                                 dwuT, dwd, ws, ws_bytes, stream);
 }
 
 twell_status twell_gemm_bf16(const void* A, const void* B, void* C, int32_t M, int32_t N,

@@ -41,6 +41,11 @@ constexpr int kStageBytes = 4096;  // per epilogue warp: 32 rows x 128 B output 
 constexpr int kGemmSmem =
     kStages * (kABytes + kBBytes) + 8 * kStageBytes + 1024 /*align*/ + 256 /*barriers*/;
 
+// Gate activations.  ReLU is the sparse path's gate; SiLU serves only the
+// dense comparator (the unmodified gated FFN) and only on the TMA-store path,
+// where the saved "g" holds bf16(a) so the backward can recompute SiLU.
+constexpr int kActRelu = 0, kActSilu = 1;
+
 struct GemmParams {
   int M, N, K;          // M: rows (buffer capacity), N: output columns, K: reduction
   const int* m_dev;     // optional device row count: rows used = min(M, *m_dev)
@@ -51,6 +56,7 @@ struct GemmParams {
                         // with A's M coordinate shifted by a_seg_off (B rows repeat): C += A0^T B + A1^T B
   int pad_rows;         // store every row of a visited tile that is < M (zero padding)
   int tma_out;          // outputs go through shared memory and TMA stores (tensor maps O0..O2)
+  int act;              // gate activation of EPI_GATED / EPI_BWD_GATE: kActRelu or kActSilu
   int split_k_max;      // > 1: split K (plan from splitk_plan); split s stores its fp32 partial
                         // at rows [s * rows_eff, (s + 1) * rows_eff) of the output map
   int* status;
@@ -312,14 +318,26 @@ struct Epilogue<EPI_GATED> {
         // h (and g, u) through TMA in 32-neuron boxes
         if (n0 + c0 >= N || row0 >= p.M) continue;
         uint32_t hw[16], gw[16], uw[16];
+        if (p.act == kActSilu) {
 #pragma unroll
-        for (int q = 0; q < 16; ++q) {
-          const uint32_t g0 = relu_bf16_bits(__uint_as_float(ra[2 * q]));
-          const uint32_t g1 = relu_bf16_bits(__uint_as_float(ra[2 * q + 1]));
-          const float u0 = __uint_as_float(ru[2 * q]), u1 = __uint_as_float(ru[2 * q + 1]);
-          hw[q] = pack_bf16x2(bf16_bits_to_float(g0) * u0, bf16_bits_to_float(g1) * u1);
-          gw[q] = g0 | (g1 << 16);
-          uw[q] = pack_bf16x2(u0, u1);
+          for (int q = 0; q < 16; ++q) {
+            const float a0 = __uint_as_float(ra[2 * q]), a1 = __uint_as_float(ra[2 * q + 1]);
+            const float u0 = __uint_as_float(ru[2 * q]), u1 = __uint_as_float(ru[2 * q + 1]);
+            const float s0 = a0 / (1.0f + __expf(-a0)), s1 = a1 / (1.0f + __expf(-a1));
+            hw[q] = pack_bf16x2(s0 * u0, s1 * u1);
+            gw[q] = pack_bf16x2(a0, a1);  // pre-activation, for the backward
+            uw[q] = pack_bf16x2(u0, u1);
+          }
+        } else {
+#pragma unroll
+          for (int q = 0; q < 16; ++q) {
+            const uint32_t g0 = relu_bf16_bits(__uint_as_float(ra[2 * q]));
+            const uint32_t g1 = relu_bf16_bits(__uint_as_float(ra[2 * q + 1]));
+            const float u0 = __uint_as_float(ru[2 * q]), u1 = __uint_as_float(ru[2 * q + 1]);
+            hw[q] = pack_bf16x2(bf16_bits_to_float(g0) * u0, bf16_bits_to_float(g1) * u1);
+            gw[q] = g0 | (g1 << 16);
+            uw[q] = pack_bf16x2(u0, u1);
+          }
         }
         uint8_t* b = st.half();
 #pragma unroll
@@ -415,9 +433,16 @@ struct Epilogue<EPI_BWD_GATE> {
             const float2 u = unpack_bf16x2(uw[q]);
             const float dh0 = __uint_as_float(r[8 * v + 2 * q]);
             const float dh1 = __uint_as_float(r[8 * v + 2 * q + 1]);
-            duw[4 * v + q] = pack_bf16x2(dh0 * g.x, dh1 * g.y);
-            daw[4 * v + q] = pack_bf16x2(g.x > 0.f ? fmaf(dh0, u.x, p.lambda) : 0.f,
-                                         g.y > 0.f ? fmaf(dh1, u.y, p.lambda) : 0.f);
+            if (p.act == kActSilu) {  // g holds a: du = dh silu(a), da = dh u silu'(a)
+              const float sg0 = 1.0f / (1.0f + __expf(-g.x)), sg1 = 1.0f / (1.0f + __expf(-g.y));
+              duw[4 * v + q] = pack_bf16x2(dh0 * (g.x * sg0), dh1 * (g.y * sg1));
+              daw[4 * v + q] = pack_bf16x2(dh0 * u.x * (sg0 * (1.0f + g.x * (1.0f - sg0))),
+                                           dh1 * u.y * (sg1 * (1.0f + g.y * (1.0f - sg1))));
+            } else {
+              duw[4 * v + q] = pack_bf16x2(dh0 * g.x, dh1 * g.y);
+              daw[4 * v + q] = pack_bf16x2(g.x > 0.f ? fmaf(dh0, u.x, p.lambda) : 0.f,
+                                           g.y > 0.f ? fmaf(dh1, u.y, p.lambda) : 0.f);
+            }
           }
         }
         uint8_t* b = st.half();

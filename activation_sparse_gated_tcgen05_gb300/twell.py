@@ -30,6 +30,7 @@ STATUS = {
 EXPORTS = (
     "twell_pack", "twell_pack_dense", "hybrid_route", "twell_workspace_bytes", "twell_ffn_fwd",
     "twell_ffn_bwd", "twell_dense_workspace_bytes", "twell_dense_ffn_fwd", "twell_dense_ffn_bwd",
+    "twell_dense_ffn_fwd_act", "twell_dense_ffn_bwd_act",
     "twell_gemm_bf16", "twell_get_device_status", "twell_status_string", "twell_num_sms",
     "twell_launch_count", "twell_profile_begin", "twell_profile_end", "twell_profile_entry",
     "twell_ffn_fwd_noalloc", "twell_selftest_wait_timeout", "twell_probe_gather",
@@ -87,6 +88,8 @@ def load():
         "twell_dense_workspace_bytes": (SZ, [SP, I32]),
         "twell_dense_ffn_fwd": (I32, [P, P, P, P, SP, P, I32, P, SZ, P]),
         "twell_dense_ffn_bwd": (I32, [P, P, P, P, P, SP, F, P, P, P, P, P, SZ, P]),
+        "twell_dense_ffn_fwd_act": (I32, [P, P, P, P, SP, I32, P, I32, P, SZ, P]),
+        "twell_dense_ffn_bwd_act": (I32, [P, P, P, P, P, SP, I32, F, P, P, P, P, P, SZ, P]),
         "twell_gemm_bf16": (I32, [P, P, P, I32, I32, I32, I32, I32, I32, I32, P]),
         "twell_get_device_status": (I32, [P, ctypes.POINTER(I32)]),
         "twell_status_string": (ctypes.c_char_p, [I32]),
@@ -265,6 +268,24 @@ def twell_dense_ffn_bwd(x, wgT, wuT, wd, dy, shape: Shape, l1_coeff: float, dx, 
         _ptr(x), _ptr(wgT), _ptr(wuT), _ptr(wd), _ptr(dy), ctypes.byref(shape), float(l1_coeff),
         _ptr(dx), _ptr(dwgT), _ptr(dwuT), _ptr(dwd), _ptr(ws), ws.numel() * ws.element_size(),
         _stream(stream)))
+
+
+ACT_RELU, ACT_SILU = 0, 1
+
+
+def twell_dense_ffn_fwd_act(x, wgT, wuT, wd, shape: Shape, activation: int, y, training: bool, ws,
+                            stream=None):
+    _check("twell_dense_ffn_fwd_act", load().twell_dense_ffn_fwd_act(
+        _ptr(x), _ptr(wgT), _ptr(wuT), _ptr(wd), ctypes.byref(shape), int(activation), _ptr(y),
+        int(training), _ptr(ws), ws.numel() * ws.element_size(), _stream(stream)))
+
+
+def twell_dense_ffn_bwd_act(x, wgT, wuT, wd, dy, shape: Shape, activation: int, l1_coeff: float,
+                            dx, dwgT, dwuT, dwd, ws, stream=None):
+    _check("twell_dense_ffn_bwd_act", load().twell_dense_ffn_bwd_act(
+        _ptr(x), _ptr(wgT), _ptr(wuT), _ptr(wd), _ptr(dy), ctypes.byref(shape), int(activation),
+        float(l1_coeff), _ptr(dx), _ptr(dwgT), _ptr(dwuT), _ptr(dwd), _ptr(ws),
+        ws.numel() * ws.element_size(), _stream(stream)))
 
 
 def twell_gemm_bf16(A, B, C, M: int, N: int, K: int, a_mn_major: bool, b_mn_major: bool,

@@ -291,6 +291,15 @@ def run_own(args, dist):
         twell.twell_dense_ffn_fwd(x, wg, wu, wd, shape, y_d, True, ws_d)
         twell.twell_dense_ffn_bwd(x, wg, wu, wd, dy, shape, L1, dx_d, *dws_d, ws_d)
 
+    # the unmodified SiLU-gated FFN that the ReLU recipe replaces (no L1 term)
+    def dense_silu_fwd():
+        twell.twell_dense_ffn_fwd_act(x, wg, wu, wd, shape, twell.ACT_SILU, y_d, False, ws_d)
+
+    def dense_silu_step():
+        twell.twell_dense_ffn_fwd_act(x, wg, wu, wd, shape, twell.ACT_SILU, y_d, True, ws_d)
+        twell.twell_dense_ffn_bwd_act(x, wg, wu, wd, dy, shape, twell.ACT_SILU, 0.0, dx_d, *dws_d,
+                                      ws_d)
+
     def graphed(fn):
         """Capture fn (a whole step of library calls) into a CUDA graph; the
         library is capture-safe (device-side routed-row counts, no host sync)."""
@@ -410,6 +419,8 @@ def run_own(args, dist):
         del a_dense
     ms_dfwd, _, _, _ = timed(graphed(dense_fwd), args.steps, args.warmup)
     ms_dstep, _, _, _ = timed(graphed(dense_step), args.steps, args.warmup, key="dense_fwd_bwd")
+    ms_sfwd, _, _, _ = timed(graphed(dense_silu_fwd), args.steps, args.warmup)
+    ms_sstep, _, _, _ = timed(graphed(dense_silu_step), args.steps, args.warmup)
     # a second dense reference outside this library: the same ReLU-gated FFN
     # composed of PyTorch ops (cuBLAS GEMMs, autograd backward; no L1 term),
     # CUDA-graphed and timed the same way
@@ -517,11 +528,13 @@ def run_own(args, dist):
         "dense_fwd_tokens_per_s": n * M / (ms_dfwd / 1e3),
         "dense_fwd_bwd_tokens_per_s": n * M / (ms_dstep / 1e3),
         "speedup_vs_dense": {"fwd": ms_dfwd / ms_fwd, "fwd_bwd": ms_dstep / ms_step},
+        "speedup_vs_dense_silu": {"fwd": ms_sfwd / ms_fwd, "fwd_bwd": ms_sstep / ms_step},
         "fwd_path": fwd_path,
         "ms": {"sparse_fwd_bwd": ms_step, "sparse_fwd": ms_fwd, "dense_fwd": ms_dfwd,
                "dense_fwd_bwd": ms_dstep, "sparse_fwd_bwd_eager": ms_eager,
                "sparse_fwd_bwd_warm_l2": ms_step_warm, "sparse_fwd_warm_l2": ms_fwd_warm,
-               "classic_ell_fwd": ms_classic},
+               "classic_ell_fwd": ms_classic, "dense_silu_fwd": ms_sfwd,
+               "dense_silu_fwd_bwd": ms_sstep},
         "ms_median": medians,
         "ms_per_step_median": medians.get("sparse_fwd_bwd"),
         "saved_for_backward_bytes": saved_bytes(shape, W, M, f, d),

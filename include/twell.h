@@ -202,6 +202,27 @@ twell_status twell_dense_ffn_bwd(const void* x, const void* wgT, const void* wuT
                                  void* dx, float* dwgT, float* dwuT, float* dwd, void* ws,
                                  size_t ws_bytes, void* stream);
 
+/* The dense comparator with a choice of gate activation.  TWELL_ACT_RELU is
+ * exactly twell_dense_ffn_fwd / _bwd.  TWELL_ACT_SILU is the unmodified
+ * gated FFN that page 2's "Receta de entrenamiento" replaces (its gate is
+ * SiLU, s = a * sigmoid(a), before the switch to ReLU): h = s * u, and the
+ * backward is du = dh * s, da = dh * u * s'(a) with s'(a) = sigmoid(a) *
+ * (1 + a * (1 - sigmoid(a))); there is no L1 term, so l1_coeff must be 0
+ * (else TWELL_ERR_INVALID_ARG).  With training = 1 the workspace keeps
+ * bf16(a) in place of g.  Any other activation value is
+ * TWELL_ERR_INVALID_ARG.  The fwd and bwd of one step must use the same
+ * activation and workspace. */
+enum { TWELL_ACT_RELU = 0, TWELL_ACT_SILU = 1 };
+twell_status twell_dense_ffn_fwd_act(const void* x, const void* wgT, const void* wuT,
+                                     const void* wd, const twell_shape* shape,
+                                     int32_t activation, void* y, int32_t training, void* ws,
+                                     size_t ws_bytes, void* stream);
+twell_status twell_dense_ffn_bwd_act(const void* x, const void* wgT, const void* wuT,
+                                     const void* wd, const void* dy, const twell_shape* shape,
+                                     int32_t activation, float l1_coeff, void* dx, float* dwgT,
+                                     float* dwuT, float* dwd, void* ws, size_t ws_bytes,
+                                     void* stream);
+
 /* The tcgen05 GEMM engine the entry points above are built on, exposed for
  * testing: C[m][n] = sum_k A(m, k) B(n, k), bf16 in, fp32 accumulate.
  *   a_mn_major = 0: A is [M][K] (K contiguous); 1: A is [K][M] (M contiguous).

@@ -132,6 +132,38 @@ def dense_intermediate_allowance(w, lam):
     }
 
 
+def dense_silu_intermediate_allowance(w):
+    """dense_intermediate_allowance for the SiLU-gated comparator, which keeps
+    bf16(a), u, h, du, da between its GEMMs.  Each stored value carries a
+    relative rounding error of at most 2^-8; the backward recomputes
+    s = silu(a) and s'(a) from the rounded a, so a's error enters du through
+    s'(a) and da through s''(a).  First order, propagated through |weights|."""
+    import oracle
+
+    x, dy = oracle.f64(w["x"]), oracle.f64(w["dy"])
+    wg, wu, wd = oracle.f64(w["wgT"]), oracle.f64(w["wuT"]), oracle.f64(w["wd"])
+    a = x @ wg.T
+    sg = 1.0 / (1.0 + np.exp(-a))
+    s = a * sg
+    ds = sg * (1.0 + a * (1.0 - sg))
+    d2s = sg * (1.0 - sg) * (2.0 + a * (1.0 - 2.0 * sg))
+    u = x @ wu.T
+    h = s * u
+    dh = dy @ wd.T
+    du = dh * s
+    da = dh * u * ds
+    r = 2.0 ** -8
+    du_err = r * (np.abs(du) + np.abs(dh * ds * a))
+    da_err = r * (np.abs(da) + np.abs(dh * u * d2s * a) + np.abs(dh * ds * u))
+    return {
+        "y": r * np.abs(h) @ np.abs(wd),
+        "dx": du_err @ np.abs(wu) + da_err @ np.abs(wg),
+        "dwgT": da_err.T @ np.abs(x),
+        "dwuT": du_err.T @ np.abs(x),
+        "dwd": r * np.abs(h).T @ np.abs(dy),
+    }
+
+
 def bwd_allowance_sampled(w, lam, rows, neurons):
     """bwd_allowance restricted to dX of `rows` and dW of `neurons` (so it
     scales to full-size workloads)."""

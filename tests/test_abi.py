@@ -67,6 +67,13 @@ def test_host_validation_before_launch(lib):
                              None) == 7
     assert lib.twell_pack_dense(16, 3, ctypes.byref(s), ctypes.byref(t), None) == 1
     assert lib.twell_gemm_bf16(16, 16, 16, 10, 12, 16, 0, 0, 0, 0, None) == 2
+    # dense comparator: unknown activation; SiLU has no L1 term
+    assert lib.twell_dense_ffn_fwd_act(16, 16, 16, 16, ctypes.byref(s), 2, 16, 1, 16, 1 << 30,
+                                       None) == 1
+    assert lib.twell_dense_ffn_bwd_act(16, 16, 16, 16, 16, ctypes.byref(s), 1, 2e-5, 16, 16, 16,
+                                       16, 16, 1 << 30, None) == 1
+    assert lib.twell_dense_ffn_bwd_act(16, 16, 16, 16, 16, ctypes.byref(s), 1, 0.0, 16, 16, 16,
+                                       16, 16, 8, None) == 7
 
 
 def test_workspace_sizes(lib):

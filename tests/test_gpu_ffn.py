@@ -11,8 +11,8 @@ import torch
 import oracle
 from activation_sparse_gated_tcgen05_gb300 import synthetic, twell
 
-from helpers import (assert_close, bwd_allowance, dense_intermediate_allowance, dev_bf16,
-                     fwd_allowance, to_np)
+from helpers import (assert_close, bwd_allowance, dense_intermediate_allowance,
+                     dense_silu_intermediate_allowance, dev_bf16, fwd_allowance, to_np)
 
 pytestmark = pytest.mark.gpu
 LAM = 2e-5
@@ -167,6 +167,33 @@ def test_dense_comparator_matches_oracle(M):
     twell.twell_dense_ffn_bwd(r.x, r.wg, r.wu, r.wd, r.dy, r.shape, LAM, dx, *dws, ws)
     torch.cuda.synchronize()
     _check_step(r, y, dx, *dws, allow=False, dense_intermediates=True)
+
+
+@pytest.mark.parametrize("M", [300, 1])
+def test_dense_silu_comparator_matches_oracle(M):
+    """The unmodified SiLU-gated FFN (the comparator the recipe starts from):
+    smooth gate, so no gate-decision allowance; h, bf16(a), u, du, da are kept
+    in bf16 between the GEMMs like the ReLU comparator's intermediates."""
+    w = synthetic.make_inputs(M, 256, 1024, density=0.2, seed=6)
+    x, wg, wu, wd, dy = (dev_bf16(w[k]) for k in ("x", "wgT", "wuT", "wd", "dy"))
+    shape = twell.make_shape(M, 256, 1024, 64, 16)
+    ws = torch.empty(twell.twell_dense_workspace_bytes(shape, True), dtype=torch.uint8,
+                     device="cuda")
+    y = torch.empty(M, 256, dtype=torch.bfloat16, device="cuda")
+    twell.twell_dense_ffn_fwd_act(x, wg, wu, wd, shape, twell.ACT_SILU, y, True, ws)
+    dx = torch.empty_like(y)
+    dws = [torch.full((1024, 256), float("nan"), device="cuda") for _ in range(3)]
+    twell.twell_dense_ffn_bwd_act(x, wg, wu, wd, dy, shape, twell.ACT_SILU, 0.0, dx, *dws, ws)
+    torch.cuda.synchronize()
+    assert twell.twell_get_device_status() == 0
+    y_ref = oracle.ffn_fwd_dense_silu(w["x"], w["wgT"], w["wuT"], w["wd"])
+    ref = oracle.ffn_bwd_dense_silu(w["x"], w["wgT"], w["wuT"], w["wd"], w["dy"])
+    al = dense_silu_intermediate_allowance(w)
+    assert_close(to_np(y), y_ref, "y", out_bf16=True, allowance=al["y"])
+    assert_close(to_np(dx), ref["dx"], "dx", out_bf16=True, allowance=al["dx"])
+    assert_close(dws[0].cpu().numpy(), ref["dwgT"], "dwgT", allowance=al["dwgT"])
+    assert_close(dws[1].cpu().numpy(), ref["dwuT"], "dwuT", allowance=al["dwuT"])
+    assert_close(dws[2].cpu().numpy(), ref["dwd"], "dwd", allowance=al["dwd"])
 
 
 def test_capacity_overflow_is_reported_without_route():
