@@ -20,6 +20,8 @@
 // sequence has no zero-fill selects.  Up to d_model = 1024 a single warp owns
 // the row (no cross-warp reduction); wider rows split it over a team whose
 // partial dot products meet in shared memory behind a named barrier.
+#include <cooperative_groups.h>
+
 #include "common.cuh"
 #include "internal.h"
 
@@ -218,6 +220,140 @@ __global__ void __launch_bounds__(256, VPL > 2 ? 2 : 3)
   }
 }
 
+// Small batches (TwELL rows): too few rows to fill the GPU one team per row,
+// so each row's tiles are split over the CL blocks of a thread-block cluster.
+// Block `rank` accumulates the entries of tiles [T rank / CL, T (rank+1) / CL)
+// in registers and stages its partial y_m in shared memory; after a cluster
+// barrier, block `rank` sums columns [rank d / CL, (rank+1) d / CL) of every
+// row over the cluster's blocks in rank order (distributed shared memory)
+// and writes y.  Deterministic; no global scratch.
+template <int TEAM, int VPL, int B>
+__global__ void __launch_bounds__(256, VPL > 2 ? 2 : 3)
+    sparse_fwd_cluster_kernel(const uint16_t* __restrict__ x, const uint16_t* __restrict__ wuT,
+                              const uint16_t* __restrict__ wd, int M, int d,
+                              const uint16_t* __restrict__ val, const uint8_t* __restrict__ idx,
+                              const uint8_t* __restrict__ cnt, int T, int tile_n, int cap,
+                              uint16_t* __restrict__ y, int* status) {
+  namespace cg = cooperative_groups;
+  cg::cluster_group cluster = cg::this_cluster();
+  const int CL = (int)cluster.num_blocks();
+  const int rank = (int)cluster.block_rank();
+  constexpr int ROWS = 8 / TEAM;
+  extern __shared__ __align__(16) float part[];  // [ROWS][d] partial y of this block
+  __shared__ float red[2][ROWS][TEAM][B];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int team = warp / TEAM, wt = warp % TEAM;
+  const int m0 = (int)(blockIdx.x / CL) * ROWS;  // the cluster's first row
+  const int m = m0 + team;
+  const bool row_ok = m < M;  // no early exit: every block reaches the cluster barriers
+
+  RowCtx<VPL> c;
+#pragma unroll
+  for (int v = 0; v < VPL; ++v) {
+    const int e = slab_elem<TEAM>(lane, wt, v);
+    c.eoff[v] = e < d ? e : 0;
+    c.xv[v] = (e < d && row_ok) ? ldg_v4(x + (long long)m * d + e) : make_uint4(0, 0, 0, 0);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) c.acc[v][k] = 0;
+  }
+  int buf = 0;
+  if (row_ok) {
+    const int t_lo = (int)((long long)T * rank / CL), t_hi = (int)((long long)T * (rank + 1) / CL);
+    for (int t0 = t_lo; t0 < t_hi; t0 += 32) {
+      const int t = t0 + lane;
+      const int craw = t < t_hi ? cnt[(long long)m * T + t] : 0;
+      if (craw > cap && wt == 0) set_status(status, TWELL_ERR_CAPACITY);
+      const int ct = min(craw, cap);
+      const int incl = warp_incl_scan(ct);
+      const int excl = incl - ct;
+      const int total = __shfl_sync(kFull, incl, 31);
+      for (int e0 = 0; e0 < total; e0 += 32) {
+        const int e = e0 + lane;
+        int lo = 0;
+#pragma unroll
+        for (int step = 16; step >= 1; step >>= 1) {
+          const int v = __shfl_sync(kFull, incl, lo + step - 1);
+          if (v <= e) lo += step;
+        }
+        const int ex = __shfl_sync(kFull, excl, lo);
+        int jl = 0;
+        float gl = 0.f;
+        if (e < total) {
+          const int tt = t0 + lo;
+          const long long sl = ((long long)m * T + tt) * cap + (e - ex);
+          jl = tt * tile_n + idx[sl];
+          gl = bf16_bits_to_float(val[sl]);
+        }
+        process_entries<TEAM, VPL, B, ROWS>(c, jl, gl, min(32, total - e0), wuT, wd, d, lane,
+                                            wt, team, red, buf);
+      }
+    }
+  }
+#pragma unroll
+  for (int v = 0; v < VPL; ++v) {
+    const int e = slab_elem<TEAM>(lane, wt, v);
+    if (e < d) {
+      float4* pp = reinterpret_cast<float4*>(part + team * d + e);
+      pp[0] = make_float4(f2_lo(c.acc[v][0]), f2_hi(c.acc[v][0]), f2_lo(c.acc[v][1]),
+                          f2_hi(c.acc[v][1]));
+      pp[1] = make_float4(f2_lo(c.acc[v][2]), f2_hi(c.acc[v][2]), f2_lo(c.acc[v][3]),
+                          f2_hi(c.acc[v][3]));
+    }
+  }
+  cluster.sync();
+  // columns [rank * cols, (rank + 1) * cols) of the cluster's rows, 8 per thread
+  const int cols = d / CL;
+  for (int i = threadIdx.x * 8; i < ROWS * cols; i += 256 * 8) {
+    const int r = i / cols, col = rank * cols + (i - r * cols);
+    float s[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    for (int q = 0; q < CL; ++q) {
+      const float4* src = reinterpret_cast<const float4*>(
+          cluster.map_shared_rank(part + r * d + col, (unsigned)q));
+      const float4 a = src[0], b = src[1];
+      s[0] += a.x; s[1] += a.y; s[2] += a.z; s[3] += a.w;
+      s[4] += b.x; s[5] += b.y; s[6] += b.z; s[7] += b.w;
+    }
+    if (m0 + r < M)
+      *reinterpret_cast<uint4*>(y + (long long)(m0 + r) * d + col) =
+          make_uint4(pack_bf16x2(s[0], s[1]), pack_bf16x2(s[2], s[3]), pack_bf16x2(s[4], s[5]),
+                     pack_bf16x2(s[6], s[7]));
+  }
+  cluster.sync();  // no block leaves while another still reads its shared memory
+}
+
+template <int TEAM, int VPL>
+cudaError_t launch_cluster(const void* x, const void* wuT, const void* wd, int M, int d,
+                           const twell_tiles* tiles, int T, int tile_n, int cap, int CL, void* y,
+                           cudaStream_t s) {
+  constexpr int ROWS = 8 / TEAM;
+  const int groups = (M + ROWS - 1) / ROWS;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)(groups * CL));
+  cfg.blockDim = dim3(256);
+  cfg.dynamicSmemBytes = (size_t)ROWS * d * sizeof(float);
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = (unsigned)CL;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cudaError_t e;
+  {
+    ProfScope prof("sparse_fwd", s);
+    e = cudaLaunchKernelEx(&cfg, sparse_fwd_cluster_kernel<TEAM, VPL, 2>,
+                           reinterpret_cast<const uint16_t*>(x),
+                           reinterpret_cast<const uint16_t*>(wuT),
+                           reinterpret_cast<const uint16_t*>(wd), M, d,
+                           reinterpret_cast<const uint16_t*>(tiles->val), tiles->idx, tiles->cnt, T,
+                           tile_n, cap, reinterpret_cast<uint16_t*>(y), device_status_ptr());
+  }
+  count_launch();
+  if (e != cudaSuccess) return e;
+  return cudaGetLastError();
+}
+
 template <int TEAM, int VPL, bool ELL>
 cudaError_t launch_team(const void* x, const void* wuT, const void* wd, int M, int d, int f,
                         const twell_tiles* tiles, int T, int tile_n, int cap,
@@ -254,8 +390,22 @@ cudaError_t launch_fmt(const void* x, const void* wuT, const void* wd, int M, in
                        const twell_tiles* tiles, int T, int tile_n, int cap,
                        const twell_hybrid* route, void* y, float* part, int chunks,
                        cudaStream_t s) {
-#define TW_FWD(TEAM, VPL) \
-  launch_team<TEAM, VPL, ELL>(x, wuT, wd, M, d, f, tiles, T, tile_n, cap, route, y, part, chunks, s)
+#define TW_FWD(TEAM, VPL)                                                                      \
+  (cl > 1 ? launch_cluster<TEAM, VPL>(x, wuT, wd, M, d, tiles, T, tile_n, cap, cl, y, s)        \
+          : launch_team<TEAM, VPL, ELL>(x, wuT, wd, M, d, f, tiles, T, tile_n, cap, route, y, part, \
+                                        chunks, s))
+  // TwELL rows too few to give every SM two blocks: split each row over a
+  // cluster of up to 8 blocks, widening while the grid stays within four
+  // blocks per SM (a row's slices then stay short even for the heaviest rows)
+  int cl = 1;
+  if (!ELL) {
+    const int team = d <= 1024 ? 1 : d <= 2048 ? 4 : 8;
+    const int groups = (M + 8 / team - 1) / (8 / team);
+    if (groups < 2 * num_sms())
+      while (cl < 8 && groups * cl * 2 <= 4 * num_sms() && 2 * cl <= T &&
+             d % (64 * 2 * cl) == 0)
+        cl *= 2;
+  }
   if (d <= 512) return TW_FWD(1, 2);
   if (d <= 1024) return TW_FWD(1, 4);
   if (d <= 2048) return TW_FWD(4, 2);

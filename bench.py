@@ -56,6 +56,8 @@ def parse_args():
     ap.add_argument("--cpu-seconds", type=float, default=15.0,
                     help="target CPU time of the oracle baseline sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-small-m", action="store_true",
+                    help="skip the M = 1, 16, 64 forward timings at the workload's shape")
     ap.add_argument("--no-torch-dense", action="store_true",
                     help="skip the PyTorch (cuBLAS) dense FFN reference timing")
     ap.add_argument("--only", choices=("sparse_step", "sparse_fwd", "dense_fwd", "dense_step"),
@@ -446,6 +448,42 @@ def run_own(args, dist):
                                          "fwd_bwd": torch_dense["fwd_bwd_ms"] / ms_step}
         del xt_, wgt_, wut_, wdt_
 
+    # small batches at this shape (M = 1, 16, 64): the TwELL forward reads all
+    # of Wg once plus the distinct live rows of Wu and Wd, so it is HBM-bound;
+    # the dense forward reads all three weight matrices
+    small_m = {}
+    if not args.no_small_m:
+        peaks_, _ = load_peaks()
+        for Ms in synthetic.SMALL_M:
+            if Ms > M:
+                continue
+            xs = x[:Ms].contiguous()
+            shp = twell.make_shape(Ms, d, f, wl.tile_n, wl.tile_cap)
+            tl = twell.alloc_tiles(shp, dev)
+            ys = torch.empty(Ms, d, dtype=torch.bfloat16, device=dev)
+            wsd = torch.empty(twell.twell_dense_workspace_bytes(shp, False), dtype=torch.uint8,
+                              device=dev)
+
+            def small_sparse():
+                twell.twell_pack(xs, wg, shp, tl)
+                twell.twell_ffn_fwd(xs, wg, wu, wd, shp, ys, tiles=tl)
+
+            def small_dense():
+                twell.twell_dense_ffn_fwd(xs, wg, wu, wd, shp, ys, False, wsd)
+
+            t_sp = timed(graphed(small_sparse), args.steps, args.warmup)[0]
+            t_de = timed(graphed(small_dense), args.steps, args.warmup)[0]
+            vt, it_, ct, _ = twell.tiles_view(tl, shp)
+            T_, C_ = f // wl.tile_n, wl.tile_cap
+            cols = (torch.arange(T_, device=dev).view(1, T_, 1) * wl.tile_n
+                    + it_.long())[torch.arange(C_, device=dev).view(1, 1, C_)
+                                  < ct.long().clamp(max=C_).unsqueeze(2)]
+            n_unique = int(torch.unique(cols).numel())
+            byts = 2 * f * d + 2 * 2 * n_unique * d + 2 * 2 * Ms * d
+            small_m[str(Ms)] = {"sparse_fwd_us": t_sp * 1e3, "dense_fwd_us": t_de * 1e3,
+                                "distinct_live_neurons": n_unique, "hbm_bytes": byts,
+                                "frac_of_hbm": byts / (t_sp / 1e3) / 1e9 / peaks_["hbm_gbs"]}
+
     # eager steps with the dominant kernel's launches bracketed by CUDA events
     ms_eager, eager_launches, prof, _ = timed(sparse_step, args.steps, args.warmup,
                                               profile=dominant)
@@ -542,6 +580,7 @@ def run_own(args, dist):
         "roofline": roof, "gather_probe": gather_probe, "kernels": kernels,
         "kernels_fwd": kernels_fwd, "kernels_dense_step": kernels_dense,
         "torch_cublas_dense": torch_dense or None,
+        "small_m": small_m or None,
         "e2e": {"value": n * M / (ms_e2e / 1e3), "unit": UNIT, "h2d_bytes_per_step": bi,
                 "d2h_bytes_per_step": bo},
         "gpu_launches": int(launches_per_step * args.steps),

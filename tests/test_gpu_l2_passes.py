@@ -29,8 +29,13 @@ def _expected_passes(d, f):
     return 1 if gathered <= 0.75 * l2 else math.ceil(gathered / (0.5 * l2))
 
 
-@pytest.mark.parametrize("M,d,f", [(384, 4096, 8192), (130, 2048, 16384)])
-def test_multi_pass_forward_matches_single_pass(M, d, f):
+# M large enough that the TwELL forward runs one team per row (batches of
+# fewer than two row groups per SM split rows over clusters, which sums in
+# another order): d = 4096 has one row per group, d = 2048 two
+@pytest.mark.parametrize("rows_per_group,d,f", [(1, 4096, 8192), (2, 2048, 16384)])
+def test_multi_pass_forward_matches_single_pass(rows_per_group, d, f):
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    M = 2 * sms * rows_per_group + 37
     passes = _expected_passes(d, f)
     assert passes > 1, "shape no longer exceeds L2; pick a larger one"
     w = synthetic.make_inputs(M, d, f, seed=11, with_dy=False)
