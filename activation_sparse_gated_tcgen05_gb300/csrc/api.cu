@@ -500,6 +500,14 @@ twell_status twell_pack(const void* x, const void* wgT, const twell_shape* shape
   p.T = s.d_ff / s.tile_n;
   p.cap = s.tile_cap;
   p.tile_n = s.tile_n;
+  // Small batches give fewer output tiles than half the SMs: split K over the
+  // blocks of a cluster (up to 8, each with at least two K blocks), so more
+  // SMs stream Wg; the leader block sums the partials in rank order.
+  const long long tiles = (long long)((s.M + kBM - 1) / kBM) * p.n_tiles;
+  const int num_kb = (s.d_model + kBK - 1) / kBK;
+  while (p.cluster_k < 8 && tiles * 2 * (p.cluster_k ? 2 * p.cluster_k : 2) <= 2LL * num_sms() &&
+         (p.cluster_k ? 2 * p.cluster_k : 2) * 2 <= num_kb)
+    p.cluster_k = p.cluster_k ? 2 * p.cluster_k : 2;
   const Mat A = mat(x, s.M, s.d_model, s.d_model);
   const Mat B = mat(wgT, s.d_ff, s.d_model, s.d_model);
   return cuda_status(gemm_launch(GK_PACK, A, B, nullptr, p, cs));

@@ -86,6 +86,30 @@ cudaError_t launch_t(const char* name, const Mat& A, const Mat& B, const Mat* B2
   const long long m_tiles = (p.M + kBM - 1) / kBM;
   const long long tiles = m_tiles * p.n_tiles;
   if (tiles <= 0) return cudaSuccess;
+  if (EPI == EPI_PACK && p.cluster_k > 1) {
+    // cluster split-K: one (tile, K split) per block, the splits of a tile in
+    // one cluster
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(tiles * p.cluster_k));
+    cfg.blockDim = dim3(kGemmThreads);
+    cfg.dynamicSmemBytes = kGemmSmem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = (unsigned)p.cluster_k;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaError_t le;
+    {
+      ProfScope prof(name, s);
+      le = cudaLaunchKernelEx(&cfg, kern, ta, tb, tb2, to[0], to[1], to[2], p);
+    }
+    count_launch();
+    if (le != cudaSuccess) return le;
+    return cudaGetLastError();
+  }
   const int grid = (int)(tiles < num_sms() ? tiles : num_sms());
   {
     ProfScope prof(name, s);

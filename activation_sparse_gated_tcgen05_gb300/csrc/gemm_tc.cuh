@@ -21,6 +21,8 @@
 //   EPI_BWD_GATE  acc = dh: du = dh * g, da = (dh * u + lambda) * 1[g > 0]
 #pragma once
 
+#include <cooperative_groups.h>
+
 #include "common.cuh"
 
 namespace tw {
@@ -57,6 +59,7 @@ struct GemmParams {
   int pad_rows;         // store every row of a visited tile that is < M (zero padding)
   int tma_out;          // outputs go through shared memory and TMA stores (tensor maps O0..O2)
   int act;              // gate activation of EPI_GATED / EPI_BWD_GATE: kActRelu or kActSilu
+  int cluster_k;        // EPI_PACK only: > 1 = split K over the blocks of a cluster (see kernel)
   int split_k_max;      // > 1: split K (plan from splitk_plan); split s stores its fp32 partial
                         // at rows [s * rows_eff, (s + 1) * rows_eff) of the output map
   int* status;
@@ -100,6 +103,20 @@ __device__ __forceinline__ void tile_coords(int tile, int m_tiles, int n_tiles, 
   const int r = tile - g * per_group;
   mb = first + r % gm;
   nb = r / gm;
+}
+
+// unit -> (tile index, K split): split-major for split-K partials written to
+// global memory; with cluster split-K the splits of one tile are the blocks
+// of one cluster, so they are adjacent in the grid
+__device__ __forceinline__ void unit_coords(int unit, int tiles, int cluster_k, int& tile,
+                                            int& ks) {
+  if (cluster_k > 1) {
+    tile = unit / cluster_k;
+    ks = unit - tile * cluster_k;
+  } else {
+    ks = unit / tiles;
+    tile = unit - ks * tiles;
+  }
 }
 
 // ------------------------------------------------------------------ epilogues
@@ -258,9 +275,23 @@ __device__ __forceinline__ uint32_t select32(const uint32_t (&r)[32], int i) {
 // the (rare) live columns.
 template <>
 struct Epilogue<EPI_PACK> {
+  // With cluster split-K the leader block adds the other blocks' partial
+  // accumulators, staged [column][row] in their shared memory, in rank order.
+  static __device__ __forceinline__ void add_remote(const GemmParams& p, float* part, int r_local,
+                                                    int col, uint32_t (&r)[32]) {
+    namespace cg = cooperative_groups;
+    cg::cluster_group cluster = cg::this_cluster();
+    for (int q = 1; q < p.cluster_k; ++q) {
+      const float* src = cluster.map_shared_rank(part, (unsigned)q);
+#pragma unroll
+      for (int i = 0; i < 32; ++i)
+        r[i] = __float_as_uint(__uint_as_float(r[i]) + src[(col + i) * kBM + r_local]);
+    }
+  }
   static __device__ __forceinline__ void run(const GemmParams& p, uint32_t tacc, int row,
                                              bool row_ok, int n0, int /*N*/, int half, Stager&,
-                                             const OutMaps&, int) {
+                                             const OutMaps&, int, float* part = nullptr,
+                                             int r_local = 0) {
     const float kLiveMin = __uint_as_float(0x00008000u);  // 2^-134
     const int tiles_here = (kBN / 2) / p.tile_n;
     const int chunks_per_tile = p.tile_n / 32;
@@ -278,6 +309,7 @@ struct Epilogue<EPI_PACK> {
         tmem_ld32(tacc + col0 + tt * p.tile_n + ch * 32, r);
         tmem_wait_ld();
         if (!tile_ok) continue;
+        if (part) add_remote(p, part, r_local, col0 + tt * p.tile_n + ch * 32, r);
         uint32_t mask = 0;
 #pragma unroll
         for (int i = 0; i < 32; ++i) mask |= (__uint_as_float(r[i]) > kLiveMin ? 1u : 0u) << i;
@@ -540,8 +572,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   const int num_kb = (A_MN && p.a_seg_off > 0) ? 2 * kb_pass : kb_pass;
   const int tiles = m_tiles * p.n_tiles;
   int splits = 1, kps = num_kb;
-  if (p.split_k_max > 1 && num_kb > 0 && M_eff > 0)
+  const int cluster_k = (EPI == EPI_PACK && p.cluster_k > 1) ? p.cluster_k : 1;
+  if (cluster_k > 1) {
+    splits = cluster_k;
+    kps = (num_kb + cluster_k - 1) / cluster_k;
+  } else if (p.split_k_max > 1 && num_kb > 0 && M_eff > 0) {
     splitk_plan(m_tiles * kBM, p.M, num_kb, p.split_k_max, splits, kps);
+  }
   const int total = (num_kb > 0 && M_eff > 0) ? tiles * splits : 0;
   // nothing to do (e.g. no routed rows): leave before touching TMEM or barriers
   if (total == 0 || (int)blockIdx.x >= total) return;
@@ -577,9 +614,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       uint32_t phase = 0;
       bool ok = true;
       for (int unit = blockIdx.x; unit < total && ok; unit += gridDim.x) {
-        int mb, nb;
-        const int ks = unit / tiles;
-        tile_coords(unit - ks * tiles, m_tiles, p.n_tiles, mb, nb);
+        int mb, nb, tile, ks;
+        unit_coords(unit, tiles, cluster_k, tile, ks);
+        tile_coords(tile, m_tiles, p.n_tiles, mb, nb);
         const int kb1 = min(num_kb, (ks + 1) * kps);
         for (int kb = ks * kps; kb < kb1; ++kb) {
           if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag)) {
@@ -643,7 +680,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         }
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + (uint32_t)(acc * kBN);
-        const int ks = unit / tiles;
+        int tile, ks;
+        unit_coords(unit, tiles, cluster_k, tile, ks);
         const int kb0 = ks * kps, kb1 = min(num_kb, (ks + 1) * kps);
         for (int kb = kb0; kb < kb1; ++kb) {
           if (!mbar_wait(&full[stage], phase, abort_flag)) {
@@ -684,10 +722,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     const OutMaps om{&tmO0, &tmO1, &tmO2};
     int it = 0;
     for (int unit = blockIdx.x; unit < total; unit += gridDim.x, ++it) {
-      int mb, nb;
-      const int ks = unit / tiles;
-      tile_coords(unit - ks * tiles, m_tiles, p.n_tiles, mb, nb);
-      const int row_off = ks * m_tiles * kBM;  // split-K partial of split ks
+      int mb, nb, tile, ks;
+      unit_coords(unit, tiles, cluster_k, tile, ks);
+      tile_coords(tile, m_tiles, p.n_tiles, mb, nb);
+      const int row_off = cluster_k > 1 ? 0 : ks * m_tiles * kBM;  // split-K partial rows
       const int acc = it & 1;
       const uint32_t acc_phase = (uint32_t)(it >> 1) & 1u;
       if (!mbar_wait(&tfull[acc], acc_phase, abort_flag)) {
@@ -700,12 +738,56 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       const bool row_ok = p.pad_rows ? (row < p.M) : (row < M_eff);
       const uint32_t tacc = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * kBN);
       const int n0 = (EPI == EPI_GATED) ? nb * 128 : nb * kBN;
+      if (cluster_k > 1) {
+        // one unit per block: split 0 packs after the cluster barrier below;
+        // the other splits stage their accumulator [column][row] in the
+        // operand buffers, idle now that every MMA of the tile has completed
+        if (ks > 0) {
+          float* part = reinterpret_cast<float*>(sA);
+#pragma unroll 1
+          for (int c0 = half * (kBN / 2); c0 < (half + 1) * (kBN / 2); c0 += 32) {
+            uint32_t r[32];
+            tmem_ld32(tacc + c0, r);
+            tmem_wait_ld();
+#pragma unroll
+            for (int i = 0; i < 32; ++i) part[(c0 + i) * kBM + r_local] = __uint_as_float(r[i]);
+          }
+        }
+        continue;
+      }
       Epilogue<EPI>::run(p, tacc, row, row_ok, n0, p.N, half, st, om,
                          row_off + mb * kBM + quarter * 32);
       tc_fence_before();
       mbar_arrive(&tempty[acc]);
     }
     st.drain();  // staged stores finish reading shared memory before the CTA exits
+  }
+
+  if constexpr (EPI == EPI_PACK) {
+    if (cluster_k > 1) {
+      // every thread of every block of the cluster passes both barriers (all
+      // waits above are bounded, so a block that gave up still arrives)
+      namespace cg = cooperative_groups;
+      cg::cluster_group cluster = cg::this_cluster();
+      cluster.sync();  // partials staged
+      if (warp >= 4 && total > 0 && !*abort_flag) {
+        int mb, nb, tile, ks;
+        unit_coords(blockIdx.x, tiles, cluster_k, tile, ks);
+        tile_coords(tile, m_tiles, p.n_tiles, mb, nb);
+        if (ks == 0) {
+          const int quarter = warp & 3;
+          const int half = (warp - 4) >> 2;
+          const int r_local = quarter * 32 + lane;
+          const int row = mb * kBM + r_local;
+          const uint32_t tacc = tmem_base + ((uint32_t)(quarter * 32) << 16);
+          Stager st{sOut + (warp - 4) * kStageBytes, lane, 0};
+          const OutMaps om{&tmO0, &tmO1, &tmO2};
+          Epilogue<EPI>::run(p, tacc, row, row < M_eff, nb * kBN, p.N, half, st, om, 0,
+                             reinterpret_cast<float*>(sA), r_local);
+        }
+      }
+      cluster.sync();  // no block leaves while the leader still reads its partial
+    }
   }
 
   __syncthreads();
