@@ -501,13 +501,15 @@ twell_status twell_pack(const void* x, const void* wgT, const twell_shape* shape
   p.cap = s.tile_cap;
   p.tile_n = s.tile_n;
   // Small batches give fewer output tiles than half the SMs: split K over the
-  // blocks of a cluster (up to 8, each with at least two K blocks), so more
-  // SMs stream Wg; the leader block sums the partials in rank order.
+  // blocks of a cluster (up to 8, within one wave, each split at least 8 K
+  // blocks so streaming Wg still outweighs summing the partials), so more SMs
+  // stream Wg; the leader block sums the partials in rank order.
   const long long tiles = (long long)((s.M + kBM - 1) / kBM) * p.n_tiles;
   const int num_kb = (s.d_model + kBK - 1) / kBK;
-  while (p.cluster_k < 8 && tiles * 2 * (p.cluster_k ? 2 * p.cluster_k : 2) <= 2LL * num_sms() &&
-         (p.cluster_k ? 2 * p.cluster_k : 2) * 2 <= num_kb)
-    p.cluster_k = p.cluster_k ? 2 * p.cluster_k : 2;
+  for (int next = 2; next <= 8; next *= 2) {
+    if (tiles * next > num_sms() || next * 8 > num_kb) break;
+    p.cluster_k = next;
+  }
   const Mat A = mat(x, s.M, s.d_model, s.d_model);
   const Mat B = mat(wgT, s.d_ff, s.d_model, s.d_model);
   return cuda_status(gemm_launch(GK_PACK, A, B, nullptr, p, cs));

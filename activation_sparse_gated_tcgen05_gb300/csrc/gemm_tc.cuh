@@ -275,18 +275,13 @@ __device__ __forceinline__ uint32_t select32(const uint32_t (&r)[32], int i) {
 // the (rare) live columns.
 template <>
 struct Epilogue<EPI_PACK> {
-  // With cluster split-K the leader block adds the other blocks' partial
-  // accumulators, staged [column][row] in their shared memory, in rank order.
-  static __device__ __forceinline__ void add_remote(const GemmParams& p, float* part, int r_local,
-                                                    int col, uint32_t (&r)[32]) {
-    namespace cg = cooperative_groups;
-    cg::cluster_group cluster = cg::this_cluster();
-    for (int q = 1; q < p.cluster_k; ++q) {
-      const float* src = cluster.map_shared_rank(part, (unsigned)q);
+  // With cluster split-K the leader block adds `part`, the sum of the other
+  // blocks' partial accumulators staged [column][row] in its shared memory.
+  static __device__ __forceinline__ void add_partial(const float* part, int r_local, int col,
+                                                     uint32_t (&r)[32]) {
 #pragma unroll
-      for (int i = 0; i < 32; ++i)
-        r[i] = __float_as_uint(__uint_as_float(r[i]) + src[(col + i) * kBM + r_local]);
-    }
+    for (int i = 0; i < 32; ++i)
+      r[i] = __float_as_uint(__uint_as_float(r[i]) + part[(col + i) * kBM + r_local]);
   }
   static __device__ __forceinline__ void run(const GemmParams& p, uint32_t tacc, int row,
                                              bool row_ok, int n0, int /*N*/, int half, Stager&,
@@ -309,7 +304,7 @@ struct Epilogue<EPI_PACK> {
         tmem_ld32(tacc + col0 + tt * p.tile_n + ch * 32, r);
         tmem_wait_ld();
         if (!tile_ok) continue;
-        if (part) add_remote(p, part, r_local, col0 + tt * p.tile_n + ch * 32, r);
+        if (part) add_partial(part, r_local, col0 + tt * p.tile_n + ch * 32, r);
         uint32_t mask = 0;
 #pragma unroll
         for (int i = 0; i < 32; ++i) mask |= (__uint_as_float(r[i]) > kLiveMin ? 1u : 0u) << i;
@@ -770,11 +765,44 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       namespace cg = cooperative_groups;
       cg::cluster_group cluster = cg::this_cluster();
       cluster.sync();  // partials staged
-      if (warp >= 4 && total > 0 && !*abort_flag) {
-        int mb, nb, tile, ks;
+      int mb = 0, nb = 0, tile = 0, ks = 1;
+      if (total > 0) {
         unit_coords(blockIdx.x, tiles, cluster_k, tile, ks);
         tile_coords(tile, m_tiles, p.n_tiles, mb, nb);
-        if (ks == 0) {
+      }
+      if (ks == 0 && !*abort_flag) {  // uniform over the leader block
+        // the whole block sums the other splits' partials of the tile's valid
+        // rows into its own shared memory, rank order, every remote value of
+        // an element requested before any is added
+        float* rsum = reinterpret_cast<float*>(sA);
+        const float* src[7];
+#pragma unroll
+        for (int q = 1; q < 8; ++q)
+          src[q - 1] = q < cluster_k ? cluster.map_shared_rank(rsum, (unsigned)q) : rsum;
+        const int vrows = min(kBM, M_eff - mb * kBM);
+        const int n_el = vrows * kBN;
+        // four elements per pass: their remote values are all in flight together
+        for (int e0 = threadIdx.x; e0 < n_el; e0 += 4 * kGemmThreads) {
+          int o[4];
+          float v[4][7];
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const int e = min(e0 + k * kGemmThreads, n_el - 1);
+            const int col = e / vrows;
+            o[k] = col * kBM + (e - col * vrows);
+#pragma unroll
+            for (int q = 1; q < 8; ++q) v[k][q - 1] = q < cluster_k ? src[q - 1][o[k]] : 0.f;
+          }
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            float acc = 0.f;
+#pragma unroll
+            for (int q = 0; q < 7; ++q) acc += v[k][q];
+            if (e0 + k * kGemmThreads < n_el) rsum[o[k]] = acc;
+          }
+        }
+        __syncthreads();
+        if (warp >= 4) {
           const int quarter = warp & 3;
           const int half = (warp - 4) >> 2;
           const int r_local = quarter * 32 + lane;
@@ -782,8 +810,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           const uint32_t tacc = tmem_base + ((uint32_t)(quarter * 32) << 16);
           Stager st{sOut + (warp - 4) * kStageBytes, lane, 0};
           const OutMaps om{&tmO0, &tmO1, &tmO2};
-          Epilogue<EPI>::run(p, tacc, row, row < M_eff, nb * kBN, p.N, half, st, om, 0,
-                             reinterpret_cast<float*>(sA), r_local);
+          Epilogue<EPI>::run(p, tacc, row, row < M_eff, nb * kBN, p.N, half, st, om, 0, rsum,
+                             r_local);
         }
       }
       cluster.sync();  // no block leaves while the leader still reads its partial

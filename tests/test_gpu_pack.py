@@ -66,6 +66,12 @@ def test_pack_dense_bit_exact(dtype, M, f, tile_n, cap, p):
     (300, 512, 2048, 128, 32, 0.02),     # ragged M, several N tiles
     (1000, 1024, 4096, 128, 4, 0.05),    # overflowing tiles (cnt > C)
     (5, 128, 384, 128, 32, 0.3),         # d_ff not a multiple of 256
+    # small batches with K split over a thread-block cluster (the leader sums
+    # the other blocks' partials): 2, 8 and 4 splits, the last over two row
+    # tiles with a 2-row ragged second tile
+    (5, 1024, 1024, 128, 32, 0.05),
+    (64, 4096, 2048, 128, 32, 0.02),
+    (130, 2048, 1024, 64, 8, 0.1),
 ])
 def test_fused_pack_bit_exact_on_exact_inputs(M, d, f, tile_n, cap, p):
     w = synthetic.make_integer_gate_inputs(M, d, f, density=p, seed=M)
