@@ -84,7 +84,7 @@ int num_sms() {
   return cache[dev];
 }
 
-int l2_chunks(double gathered_bytes, double fit) {
+int l2_chunks(double gathered_bytes, double fit, double chunk) {
   static int cache[kMaxDevices] = {0};
   const int dev = current_device();
   if (dev < 0 || dev >= kMaxDevices) return 1;
@@ -95,7 +95,7 @@ int l2_chunks(double gathered_bytes, double fit) {
   }
   const double l2 = (double)cache[dev];
   if (gathered_bytes <= fit * l2) return 1;
-  return (int)std::ceil(gathered_bytes / (0.5 * l2));
+  return (int)std::ceil(gathered_bytes / (chunk * l2));
 }
 
 int* device_status_ptr() {

@@ -39,8 +39,8 @@ enum GemmKind {
 int num_sms();
 // Passes over the neuron axis for a gather whose weight rows total
 // `gathered_bytes`: 1 while they fit in the fraction `fit` of L2, else
-// enough chunks of about half of L2 each.
-int l2_chunks(double gathered_bytes, double fit);
+// enough chunks of at most the fraction `chunk` of L2 each.
+int l2_chunks(double gathered_bytes, double fit, double chunk);
 void count_launch(int n = 1);  // kernels launched by the library (process-wide)
 
 // While profiling is on for `name` (or "*"), brackets one kernel launch with

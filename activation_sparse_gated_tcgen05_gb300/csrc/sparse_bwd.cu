@@ -166,6 +166,9 @@ __global__ void __launch_bounds__(256, MINB)
   if (m >= M) return;
 
   const bool first = pass & kPassFirst, last = pass & kPassLast;
+  // x, dY and the dX carry stream through once per pass: evict-first, so the
+  // pass's weight rows keep L2
+  const uint64_t pol = l2_evict_first_policy();
   uint4 xp[VPL], dyp[VPL];  // x_m, dY_m slabs, packed bf16
   uint64_t acc[VPL][4];
   int eoff[VPL];  // slab offsets, lanes past d_model read the first slab
@@ -174,14 +177,14 @@ __global__ void __launch_bounds__(256, MINB)
     const int e = slab<TEAM>(lane, wt, v);
     const bool ok = e < d;
     eoff[v] = ok ? e : 0;
-    xp[v] = ok ? ldg_v4(x + (long long)m * d + e) : make_uint4(0, 0, 0, 0);
-    dyp[v] = ok ? ldg_v4(dy + (long long)m * d + e) : make_uint4(0, 0, 0, 0);
+    xp[v] = ok ? ldg_v4_hint(x + (long long)m * d + e, pol) : make_uint4(0, 0, 0, 0);
+    dyp[v] = ok ? ldg_v4_hint(dy + (long long)m * d + e, pol) : make_uint4(0, 0, 0, 0);
     if (first || !ok) {
 #pragma unroll
       for (int k = 0; k < 4; ++k) acc[v][k] = 0;
     } else {  // dX_m of the earlier neuron chunks
-      const uint4* pp = reinterpret_cast<const uint4*>(part + (long long)m * d + e);
-      const uint4 q0 = pp[0], q1 = pp[1];
+      const float* pp = part + (long long)m * d + e;
+      const uint4 q0 = ldg_v4_hint(pp, pol), q1 = ldg_v4_hint(pp + 4, pol);
       acc[v][0] = f2_make(q0.x, q0.y);
       acc[v][1] = f2_make(q0.z, q0.w);
       acc[v][2] = f2_make(q1.x, q1.y);
@@ -299,11 +302,11 @@ __global__ void __launch_bounds__(256, MINB)
     if (last) {
       *reinterpret_cast<uint4*>(dx + (long long)m * d + e) = f2x4_to_bf8(acc[v]);
     } else {
-      uint4* pp = reinterpret_cast<uint4*>(part + (long long)m * d + e);
-      pp[0] = make_uint4((uint32_t)acc[v][0], (uint32_t)(acc[v][0] >> 32), (uint32_t)acc[v][1],
-                         (uint32_t)(acc[v][1] >> 32));
-      pp[1] = make_uint4((uint32_t)acc[v][2], (uint32_t)(acc[v][2] >> 32), (uint32_t)acc[v][3],
-                         (uint32_t)(acc[v][3] >> 32));
+      float* pp = part + (long long)m * d + e;
+      st_v4_hint(pp, make_uint4((uint32_t)acc[v][0], (uint32_t)(acc[v][0] >> 32),
+                                (uint32_t)acc[v][1], (uint32_t)(acc[v][1] >> 32)), pol);
+      st_v4_hint(pp + 4, make_uint4((uint32_t)acc[v][2], (uint32_t)(acc[v][2] >> 32),
+                                    (uint32_t)acc[v][3], (uint32_t)(acc[v][3] >> 32)), pol);
     }
   }
 }
@@ -500,9 +503,10 @@ cudaError_t launch_sparse_bwd_rows(const void* x, const void* dy, const void* wg
   if (M == 0) return cudaSuccess;
   // Wd, Wu^T and Wg^T rows: L2-sized neuron passes once they exceed half of
   // L2 (x, dY and dX stream through L2 beside them; on the 2B-class shape,
-  // 101 MB of weights, two passes beat one by 7 %), dX_m carried in `part`
+  // 101 MB of weights, two passes beat one by 7 %), chunks of at most 0.65 of
+  // L2 (on the 8B-class shape 4 passes beat 6 and 8), dX_m carried in `part`
   // (fp32) with the accumulation order unchanged
-  const int chunks = part ? l2_chunks(3.0 * 2.0 * (double)f * d, 0.5) : 1;
+  const int chunks = part ? l2_chunks(3.0 * 2.0 * (double)f * d, 0.5, 0.65) : 1;
 #define TW_ROWS(T, V, B, MINB)                                                                 \
   rows_team<T, V, B, MINB>(x, dy, wgT, wuT, wd, M, d, f, route, slot_pos, lambda, csc_vals, dx, \
                            part, chunks, s)

@@ -128,18 +128,21 @@ __global__ void __launch_bounds__(256, VPL > 2 ? 2 : 3)
   if (m >= M) return;
 
   const bool first = pass & kPassFirst, last = pass & kPassLast;
+  // x, y and the y carry stream through once per pass: evict-first, so the
+  // gathered weight rows keep L2
+  const uint64_t pol = l2_evict_first_policy();
   RowCtx<VPL> c;
 #pragma unroll
   for (int v = 0; v < VPL; ++v) {
     const int e = slab_elem<TEAM>(lane, wt, v);
     c.eoff[v] = e < d ? e : 0;
-    c.xv[v] = e < d ? ldg_v4(x + (long long)m * d + e) : make_uint4(0, 0, 0, 0);
+    c.xv[v] = e < d ? ldg_v4_hint(x + (long long)m * d + e, pol) : make_uint4(0, 0, 0, 0);
     if (first || e >= d) {
 #pragma unroll
       for (int k = 0; k < 4; ++k) c.acc[v][k] = 0;
     } else {  // running sum of the earlier neuron chunks
-      const uint4* pp = reinterpret_cast<const uint4*>(part + (long long)m * d + e);
-      const uint4 q0 = pp[0], q1 = pp[1];
+      const float* pp = part + (long long)m * d + e;
+      const uint4 q0 = ldg_v4_hint(pp, pol), q1 = ldg_v4_hint(pp + 4, pol);
       c.acc[v][0] = f2_make(q0.x, q0.y);
       c.acc[v][1] = f2_make(q0.z, q0.w);
       c.acc[v][2] = f2_make(q1.x, q1.y);
@@ -209,13 +212,13 @@ __global__ void __launch_bounds__(256, VPL > 2 ? 2 : 3)
     const int e = slab_elem<TEAM>(lane, wt, v);
     if (e >= d) continue;
     if (last) {
-      *reinterpret_cast<uint4*>(y + (long long)m * d + e) = f2x4_to_bf8(c.acc[v]);
+      st_v4_hint(y + (long long)m * d + e, f2x4_to_bf8(c.acc[v]), pol);
     } else {
-      uint4* pp = reinterpret_cast<uint4*>(part + (long long)m * d + e);
-      pp[0] = make_uint4((uint32_t)c.acc[v][0], (uint32_t)(c.acc[v][0] >> 32),
-                         (uint32_t)c.acc[v][1], (uint32_t)(c.acc[v][1] >> 32));
-      pp[1] = make_uint4((uint32_t)c.acc[v][2], (uint32_t)(c.acc[v][2] >> 32),
-                         (uint32_t)c.acc[v][3], (uint32_t)(c.acc[v][3] >> 32));
+      float* pp = part + (long long)m * d + e;
+      st_v4_hint(pp, make_uint4((uint32_t)c.acc[v][0], (uint32_t)(c.acc[v][0] >> 32),
+                                (uint32_t)c.acc[v][1], (uint32_t)(c.acc[v][1] >> 32)), pol);
+      st_v4_hint(pp + 4, make_uint4((uint32_t)c.acc[v][2], (uint32_t)(c.acc[v][2] >> 32),
+                                    (uint32_t)c.acc[v][3], (uint32_t)(c.acc[v][3] >> 32)), pol);
     }
   }
 }
@@ -425,7 +428,7 @@ cudaError_t launch_sparse_fwd(const void* x, const void* wuT, const void* wd, in
     // Wu^T and Wd rows: split the neuron axis into L2-sized passes once they
     // exceed 3/4 of L2 (partial sums in `part`, same accumulation order; on
     // the 2B-class shape, 67 MB of weights, two passes were slower than one)
-    const int chunks = part ? l2_chunks(2.0 * 2.0 * (double)f * d, 0.75) : 1;
+    const int chunks = part ? l2_chunks(2.0 * 2.0 * (double)f * d, 0.75, 0.5) : 1;
     return launch_fmt<true>(x, wuT, wd, M, d, f, nullptr, T, tile_n, cap, route, y, part,
                             chunks, s);
   }

@@ -79,7 +79,7 @@ def test_multi_pass_backward_rows():
     M, d, f, lam = 256, 4096, 8192, 2e-5
     l2 = torch.cuda.get_device_properties(0).L2_cache_size
     gathered = 6.0 * f * d
-    passes = 1 if gathered <= 0.5 * l2 else math.ceil(gathered / (0.5 * l2))
+    passes = 1 if gathered <= 0.5 * l2 else math.ceil(gathered / (0.65 * l2))
     assert passes > 1, "shape no longer exceeds L2; pick a larger one"
     w = synthetic.make_inputs(M, d, f, seed=12)
     x, wg, wu, wd, dy = (dev_bf16(w[k]) for k in ("x", "wgT", "wuT", "wd", "dy"))
