@@ -142,7 +142,13 @@ size_t twell_workspace_bytes(const twell_shape* shape, int32_t ell_width, int32_
  * uses only the stored entries) and `route` (training: ELL rows by gather,
  * routed rows by a dense tensor-core gated FFN that recomputes their gate)
  * is non-NULL.  wgT is read only for routed rows (may be NULL with tiles).
- * ws/ws_bytes: workspace of at least twell_workspace_bytes(shape, W, 0). */
+ * ws/ws_bytes: with `route`, a workspace of at least
+ * twell_workspace_bytes(shape, W, 0) bytes (16-byte aligned); besides the
+ * routed rows' buffers it carries the fp32 running y between passes when
+ * the gathered Wu / Wd rows exceed L2 and the ELL gather is split into
+ * L2-sized neuron passes (same result, bit for bit).  With `tiles` the
+ * workspace is not used (may be NULL); batches too small to fill the GPU
+ * split each row over a thread-block cluster, which sums in another order. */
 twell_status twell_ffn_fwd(const void* x, const void* wgT, const void* wuT, const void* wd,
                            const twell_shape* shape, const twell_tiles* tiles,
                            const twell_hybrid* route, void* y, void* ws, size_t ws_bytes,
@@ -182,7 +188,9 @@ twell_status twell_ffn_fwd_noalloc(const void* x, const void* wgT, const void* w
  * using only the live entries of ELL rows and a dense tensor-core path for the
  * routed rows.  The route must come from hybrid_route on the same x and Wg.
  * The reduction order is fixed, so results are bit-reproducible.
- * ws/ws_bytes: at least twell_workspace_bytes(shape, W, 1) bytes. */
+ * ws/ws_bytes: at least twell_workspace_bytes(shape, W, 1) bytes (16-byte
+ * aligned); it also carries the fp32 running dX when the row phase is split
+ * into L2-sized neuron passes (Wd, Wu and Wg rows beyond half of L2). */
 twell_status twell_ffn_bwd(const void* x, const void* wgT, const void* wuT, const void* wd,
                            const void* dy, const twell_shape* shape, const twell_hybrid* route,
                            float l1_coeff, void* dx, float* dwgT, float* dwuT, float* dwd,
