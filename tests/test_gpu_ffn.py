@@ -225,3 +225,27 @@ def test_small_batch_forward(M):
     w = r.w
     assert_close(to_np(y), oracle.ffn_fwd_dense(w["x"], w["wgT"], w["wuT"], w["wd"]), "y",
                  out_bf16=True)
+
+
+@pytest.mark.parametrize("M,d", [(200, 320), (200, 704), (160, 1088), (64, 4160)])
+def test_d_model_leaving_partial_slabs(M, d):
+    """The gathers load without predicates: lanes past d_model read the row's
+    first slab against a zero x / dY and their sums are never stored.  These
+    d_model values leave partial slabs in the one-warp (d <= 1024), four-warp
+    (d <= 2048) and eight-warp four-slab (d > 4096) team shapes of the
+    forward, row and neuron phases."""
+    r = Run(M, d, 1024, 64, 16, density=0.02, seed=8, exact=True)
+    y = r.fwd(tiles=r.pack())
+    torch.cuda.synchronize()
+    assert twell.twell_get_device_status() == 0
+    y_ref = oracle.ffn_fwd_dense(r.w["x"], r.w["wgT"], r.w["wuT"], r.w["wd"])
+    assert_close(to_np(y), y_ref, "y (TwELL)", out_bf16=True)
+    r = Run(M, d, 1024, 64, 16, density=0.02, seed=9, exact=True, mixed=True)
+    t = r.pack()
+    W = _quantile_width(t, r.shape, 0.9)
+    h = r.route(t, W)
+    y = r.fwd(route=h, W=W)
+    dx, (dwg, dwu, dwd) = r.bwd(h, W)
+    torch.cuda.synchronize()
+    assert twell.twell_get_device_status() == 0
+    _check_step(r, y, dx, dwg, dwu, dwd, allow=False)
