@@ -271,14 +271,15 @@ cudaError_t gated_gemm(const void* x_rows, long long rows, const twell_shape& s,
   const Mat A = mat(x_rows, rows, s.d_model, s.d_model);
   const Mat B = mat(wgT, s.d_ff, s.d_model, s.d_model);
   const Mat B2 = mat(wuT, s.d_ff, s.d_model, s.d_model);
-  if (!split && !u32) {  // dense layout: h, g, u through TMA stores
-    p.tma_out = 1;
-    const OutMat outs[3] = {{h, rows, s.d_ff, s.d_ff, 0, 32},
-                            {g ? g : h, rows, s.d_ff, s.d_ff, 0, 32},
-                            {u ? u : h, rows, s.d_ff, s.d_ff, 0, 32}};
-    return gemm_launch(GK_GATED, A, B, &B2, p, st, outs, 3);
-  }
-  return gemm_launch(GK_GATED, A, B, &B2, p, st);
+  // h (with its lo half h_lo_off columns on), g and u through TMA stores
+  p.tma_out = 1;
+  const long long hcols = split ? 2LL * s.d_ff : s.d_ff;
+  OutMat outs[3];
+  outs[0] = OutMat{h, rows, hcols, p.ldh, 0, 32};
+  outs[1] = OutMat{g ? g : h, rows, s.d_ff, s.d_ff, 0, 32};
+  outs[2] = OutMat{u ? u : h, rows, s.d_ff, s.d_ff, 0, 32};
+  if (u32) outs[2] = OutMat{u32, rows, s.d_ff, s.d_ff, 1, 32};
+  return gemm_launch(GK_GATED, A, B, &B2, p, st, outs, 3);
 }
 
 // Routed rows: out[row_map[r]] = A[r] B with the K range split across CTAs
@@ -346,12 +347,10 @@ cudaError_t dgate_gemm(const void* dy_rows, long long rows, const twell_shape& s
   p.pad_rows = pad_rows;
   const Mat A = mat(dy_rows, rows, s.d_model, s.d_model);
   const Mat B = mat(wd, s.d_ff, s.d_model, s.d_model);  // [N = f][K = d], K-major
-  if (!split && !u32) {  // dense layout: du, da through TMA stores
-    p.tma_out = 1;
-    const OutMat o{dd, rows, 2LL * s.d_ff, 2LL * s.d_ff, 0, 32};
-    return gemm_launch(GK_BWD_GATE, A, B, nullptr, p, st, &o, 1);
-  }
-  return gemm_launch(GK_BWD_GATE, A, B, nullptr, p, st);
+  // du, da (and their lo halves) through TMA stores into dd [rows][2f or 4f]
+  p.tma_out = 1;
+  const OutMat o{dd, rows, p.ld_dd, p.ld_dd, 0, 32};
+  return gemm_launch(split ? GK_BWD_GATE_RT : GK_BWD_GATE, A, B, nullptr, p, st, &o, 1);
 }
 
 // out[row_map ? row_map[r] : r] = du Wu^T + da Wg^T  (bf16): the GEMM runs over

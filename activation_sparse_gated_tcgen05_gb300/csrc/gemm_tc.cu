@@ -133,6 +133,7 @@ cudaError_t gemm_launch(GemmKind kind, const Mat& A, const Mat& B, const Mat* B2
     TW_CASE(GK_PACK, false, false, EPI_PACK, "gemm_gate_pack")
     TW_CASE(GK_GATED, false, false, EPI_GATED, "gemm_gated")
     TW_CASE(GK_BWD_GATE, false, false, EPI_BWD_GATE, "gemm_dgate")
+    TW_CASE(GK_BWD_GATE_RT, false, false, EPI_BWD_GATE_RT, "gemm_dgate")
 #undef TW_CASE
   }
   return cudaErrorInvalidValue;

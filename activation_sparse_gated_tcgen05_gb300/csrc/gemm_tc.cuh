@@ -27,7 +27,7 @@
 
 namespace tw {
 
-enum EpiKind { EPI_STORE = 0, EPI_PACK = 1, EPI_GATED = 2, EPI_BWD_GATE = 3 };
+enum EpiKind { EPI_STORE = 0, EPI_PACK = 1, EPI_GATED = 2, EPI_BWD_GATE = 3, EPI_BWD_GATE_RT = 4 };
 
 constexpr int kBM = 128;
 constexpr int kBN = 256;  // MMA N (for EPI_GATED: 128 gate + 128 up columns)
@@ -127,17 +127,26 @@ __device__ __forceinline__ void unit_coords(int unit, int tiles, int cluster_k, 
 struct Stager {
   uint8_t* buf;
   int lane;
-  int n;  // stores issued so far
-  // 128-byte rows: the whole buffer; waits for the previous store's read
+  int n;          // stores issued so far
+  bool whole;     // the last buffer handed out was the whole 4 KB
+  // 128-byte rows: the whole buffer; waits until no store still reads it
   __device__ __forceinline__ uint8_t* full() {
     if (lane == 0) bulk_wait_read<0>();
     __syncwarp();
+    whole = true;
     return buf;
   }
   // 64-byte rows: the two 2 KB halves in turn, one store may stay in flight
+  // (none if that store read the whole buffer)
   __device__ __forceinline__ uint8_t* half() {
-    if (lane == 0) bulk_wait_read<1>();
+    if (lane == 0) {
+      if (whole)
+        bulk_wait_read<0>();
+      else
+        bulk_wait_read<1>();
+    }
     __syncwarp();
+    whole = false;
     return buf + ((n & 1) << 11);
   }
   __device__ __forceinline__ void put128(uint8_t* b, int c, const uint4& v) const {
@@ -341,8 +350,7 @@ struct Epilogue<EPI_GATED> {
       tmem_ld32(tacc + c0, ra);
       tmem_ld32(tacc + 128 + c0, ru);
       tmem_wait_ld();
-      if (p.tma_out) {
-        // h (and g, u) through TMA in 32-neuron boxes
+      {  // h (its lo half, g, u) through shared memory and TMA stores, 32 neurons a box
         if (n0 + c0 >= N || row0 >= p.M) continue;
         uint32_t hw[16], gw[16], uw[16];
         if (p.act == kActSilu) {
@@ -371,6 +379,30 @@ struct Epilogue<EPI_GATED> {
         for (int v = 0; v < 4; ++v)
           st.put64(b, v, make_uint4(hw[4 * v], hw[4 * v + 1], hw[4 * v + 2], hw[4 * v + 3]));
         st.send(om.o0, b, n0 + c0, row0);
+        if (p.h_lo_off) {  // h - bf16(h) in the same map, h_lo_off columns on
+          uint32_t lw[16];
+#pragma unroll
+          for (int q = 0; q < 16; ++q) {
+            const float2 hr = unpack_bf16x2(hw[q]);
+            float h0, h1;
+            if (p.act == kActSilu) {
+              const float a0 = __uint_as_float(ra[2 * q]), a1 = __uint_as_float(ra[2 * q + 1]);
+              h0 = a0 / (1.0f + __expf(-a0)) * __uint_as_float(ru[2 * q]);
+              h1 = a1 / (1.0f + __expf(-a1)) * __uint_as_float(ru[2 * q + 1]);
+            } else {
+              h0 = bf16_bits_to_float(relu_bf16_bits(__uint_as_float(ra[2 * q]))) *
+                   __uint_as_float(ru[2 * q]);
+              h1 = bf16_bits_to_float(relu_bf16_bits(__uint_as_float(ra[2 * q + 1]))) *
+                   __uint_as_float(ru[2 * q + 1]);
+            }
+            lw[q] = pack_bf16x2(h0 - hr.x, h1 - hr.y);
+          }
+          b = st.half();
+#pragma unroll
+          for (int v = 0; v < 4; ++v)
+            st.put64(b, v, make_uint4(lw[4 * v], lw[4 * v + 1], lw[4 * v + 2], lw[4 * v + 3]));
+          st.send(om.o0, b, n0 + c0 + (int)p.h_lo_off, row0);
+        }
         if (p.g_out) {
           b = st.half();
 #pragma unroll
@@ -378,48 +410,18 @@ struct Epilogue<EPI_GATED> {
             st.put64(b, v, make_uint4(gw[4 * v], gw[4 * v + 1], gw[4 * v + 2], gw[4 * v + 3]));
           st.send(om.o1, b, n0 + c0, row0);
         }
-        if (p.u_out) {
+        if (p.u_f32) {  // u kept in fp32: 32 columns are a 128-byte row
+          b = st.full();
+#pragma unroll
+          for (int v = 0; v < 8; ++v)
+            st.put128(b, v, make_uint4(ru[4 * v], ru[4 * v + 1], ru[4 * v + 2], ru[4 * v + 3]));
+          st.send(om.o2, b, n0 + c0, row0);
+        } else if (p.u_out) {
           b = st.half();
 #pragma unroll
           for (int v = 0; v < 4; ++v)
             st.put64(b, v, make_uint4(uw[4 * v], uw[4 * v + 1], uw[4 * v + 2], uw[4 * v + 3]));
           st.send(om.o2, b, n0 + c0, row0);
-        }
-        continue;
-      }
-      if (!row_ok || n0 + c0 >= N) continue;
-      const long long off = (long long)row * p.ldh + n0 + c0;
-      const long long ogu = (long long)row * p.ldgu + n0 + c0;
-#pragma unroll
-      for (int v = 0; v < 4; ++v) {
-        uint32_t hw[4], lw[4], gw[4], uw[4];
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const int i = 8 * v + 2 * q;
-          const uint32_t g0 = relu_bf16_bits(__uint_as_float(ra[i]));
-          const uint32_t g1 = relu_bf16_bits(__uint_as_float(ra[i + 1]));
-          const float u0 = __uint_as_float(ru[i]), u1 = __uint_as_float(ru[i + 1]);
-          const float h0 = bf16_bits_to_float(g0) * u0, h1 = bf16_bits_to_float(g1) * u1;
-          hw[q] = pack_bf16x2(h0, h1);
-          const float2 hr = unpack_bf16x2(hw[q]);
-          lw[q] = pack_bf16x2(h0 - hr.x, h1 - hr.y);
-          gw[q] = g0 | (g1 << 16);
-          uw[q] = pack_bf16x2(u0, u1);
-        }
-        *reinterpret_cast<uint4*>(p.h + off + 8 * v) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
-        if (p.h_lo_off)
-          *reinterpret_cast<uint4*>(p.h + off + p.h_lo_off + 8 * v) =
-              make_uint4(lw[0], lw[1], lw[2], lw[3]);
-        if (p.g_out)
-          *reinterpret_cast<uint4*>(p.g_out + ogu + 8 * v) = make_uint4(gw[0], gw[1], gw[2], gw[3]);
-        if (p.u_out)
-          *reinterpret_cast<uint4*>(p.u_out + ogu + 8 * v) = make_uint4(uw[0], uw[1], uw[2], uw[3]);
-        if (p.u_f32) {
-          float4* uo = reinterpret_cast<float4*>(p.u_f32 + ogu + 8 * v);
-          uo[0] = make_float4(__uint_as_float(ru[8 * v + 0]), __uint_as_float(ru[8 * v + 1]),
-                              __uint_as_float(ru[8 * v + 2]), __uint_as_float(ru[8 * v + 3]));
-          uo[1] = make_float4(__uint_as_float(ru[8 * v + 4]), __uint_as_float(ru[8 * v + 5]),
-                              __uint_as_float(ru[8 * v + 6]), __uint_as_float(ru[8 * v + 7]));
         }
       }
     }
@@ -427,8 +429,7 @@ struct Epilogue<EPI_GATED> {
 };
 
 // acc = dh = dY Wd^T for 256 neurons.  du = dh * g, da = (dh * u + lambda) if
-// g > 0 else 0; both stored bf16 into dd = [du | da] (plus their bf16
-// residuals [du lo | da lo] when dd_split is set).
+// g > 0 else 0 (SiLU: see below); both stored bf16 into dd = [du | da].
 template <>
 struct Epilogue<EPI_BWD_GATE> {
   static __device__ __forceinline__ void run(const GemmParams& p, uint32_t tacc, int row,
@@ -440,8 +441,7 @@ struct Epilogue<EPI_BWD_GATE> {
       uint32_t r[32];
       tmem_ld32(tacc + c0, r);
       tmem_wait_ld();
-      if (p.tma_out) {
-        // du, da through TMA in 32-column boxes; g, u read straight from global
+      {  // du, da through shared memory and TMA stores, 32 columns a box
         if (n0 + c0 >= N || row0 >= p.M) continue;
         uint32_t duw[16], daw[16];
         const bool in = row < p.M;
@@ -482,54 +482,80 @@ struct Epilogue<EPI_BWD_GATE> {
         for (int v = 0; v < 4; ++v)
           st.put64(b, v, make_uint4(daw[4 * v], daw[4 * v + 1], daw[4 * v + 2], daw[4 * v + 3]));
         st.send(om.o0, b, n0 + c0 + (int)seg, row0);
-        continue;
       }
-      if (!row_ok || n0 + c0 >= N) continue;
-      const long long gu = (long long)row * p.ldgu + n0 + c0;
-      const long long o = (long long)row * p.ld_dd + n0 + c0;
+    }
+  }
+};
+
+
+// Routed rows' variant (its own instantiation, so the dense comparator's
+// epilogue stays lean): g bf16, u fp32, and dd = [du | da | du lo | da lo].
+template <>
+struct Epilogue<EPI_BWD_GATE_RT> {
+  // du, da from dh and the saved g, u (ReLU: da = dh u + lambda on live
+  // entries; SiLU: g holds a, du = dh silu(a), da = dh u silu'(a))
+  static __device__ __forceinline__ void grads(const GemmParams& p, float dh, float g, float u,
+                                               float& du, float& da) {
+    if (p.act == kActSilu) {
+      const float sg = 1.0f / (1.0f + __expf(-g));
+      du = dh * (g * sg);
+      da = dh * u * (sg * (1.0f + g * (1.0f - sg)));
+    } else {
+      du = dh * g;
+      da = g > 0.f ? fmaf(dh, u, p.lambda) : 0.f;
+    }
+  }
+  static __device__ __forceinline__ void send16(Stager& st, const CUtensorMap* m,
+                                                const uint32_t (&w)[16], int col, int row0) {
+    uint8_t* b = st.half();
 #pragma unroll
-      for (int v = 0; v < 4; ++v) {
-        const uint4 g8 = *reinterpret_cast<const uint4*>(p.g_in + gu + 8 * v);
-        const uint32_t gw[4] = {g8.x, g8.y, g8.z, g8.w};
-        float uf[8];
-        if (p.u_f32_in) {
-          const float4 u0 = *reinterpret_cast<const float4*>(p.u_f32_in + gu + 8 * v);
-          const float4 u1 = *reinterpret_cast<const float4*>(p.u_f32_in + gu + 8 * v + 4);
-          uf[0] = u0.x; uf[1] = u0.y; uf[2] = u0.z; uf[3] = u0.w;
-          uf[4] = u1.x; uf[5] = u1.y; uf[6] = u1.z; uf[7] = u1.w;
-        } else {
-          const uint4 u8 = *reinterpret_cast<const uint4*>(p.u_in + gu + 8 * v);
-          const uint32_t uw[4] = {u8.x, u8.y, u8.z, u8.w};
+    for (int v = 0; v < 4; ++v) st.put64(b, v, make_uint4(w[4 * v], w[4 * v + 1], w[4 * v + 2], w[4 * v + 3]));
+    st.send(m, b, col, row0);
+  }
+  static __device__ __forceinline__ void run(const GemmParams& p, uint32_t tacc, int row,
+                                             bool /*row_ok*/, int n0, int N, int half, Stager& st,
+                                             const OutMaps& om, int row0) {
+    const int seg = (int)p.dd_seg;
+    const bool in = row < p.M;
+#pragma unroll 1
+    for (int c0 = half * (kBN / 2); c0 < (half + 1) * (kBN / 2); c0 += 32) {
+      uint32_t r[32];
+      tmem_ld32(tacc + c0, r);
+      tmem_wait_ld();
+      // du, da through shared memory and TMA stores, 32 columns a box
+      if (n0 + c0 >= N || row0 >= p.M) continue;
+      const long long gu = (long long)row * p.ldgu + n0 + c0;
+      uint32_t duw[16], daw[16];
+      {  // routed rows: u fp32, du and da also as bf16 residuals [du lo | da lo]
+        uint32_t dul[16], dal[16];
+#pragma unroll
+        for (int v = 0; v < 4; ++v) {
+          const uint4 g8 = in ? *reinterpret_cast<const uint4*>(p.g_in + gu + 8 * v)
+                              : make_uint4(0, 0, 0, 0);
+          const float4 u0 = in ? *reinterpret_cast<const float4*>(p.u_f32_in + gu + 8 * v)
+                               : make_float4(0.f, 0.f, 0.f, 0.f);
+          const float4 u1 = in ? *reinterpret_cast<const float4*>(p.u_f32_in + gu + 8 * v + 4)
+                               : make_float4(0.f, 0.f, 0.f, 0.f);
+          const uint32_t gw[4] = {g8.x, g8.y, g8.z, g8.w};
+          const float uf[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
-            const float2 t = unpack_bf16x2(uw[q]);
-            uf[2 * q] = t.x;
-            uf[2 * q + 1] = t.y;
+            const float2 g = unpack_bf16x2(gw[q]);
+            float du0, du1, da0, da1;
+            grads(p, __uint_as_float(r[8 * v + 2 * q]), g.x, uf[2 * q], du0, da0);
+            grads(p, __uint_as_float(r[8 * v + 2 * q + 1]), g.y, uf[2 * q + 1], du1, da1);
+            duw[4 * v + q] = pack_bf16x2(du0, du1);
+            daw[4 * v + q] = pack_bf16x2(da0, da1);
+            const float2 duh = unpack_bf16x2(duw[4 * v + q]);
+            const float2 dah = unpack_bf16x2(daw[4 * v + q]);
+            dul[4 * v + q] = pack_bf16x2(du0 - duh.x, du1 - duh.y);
+            dal[4 * v + q] = pack_bf16x2(da0 - dah.x, da1 - dah.y);
           }
         }
-        uint32_t duw[4], daw[4], dul[4], dal[4];
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const float2 g = unpack_bf16x2(gw[q]);
-          const float2 u = make_float2(uf[2 * q], uf[2 * q + 1]);
-          const float dh0 = __uint_as_float(r[8 * v + 2 * q]);
-          const float dh1 = __uint_as_float(r[8 * v + 2 * q + 1]);
-          const float du0 = dh0 * g.x, du1 = dh1 * g.y;
-          const float da0 = g.x > 0.f ? fmaf(dh0, u.x, p.lambda) : 0.f;
-          const float da1 = g.y > 0.f ? fmaf(dh1, u.y, p.lambda) : 0.f;
-          duw[q] = pack_bf16x2(du0, du1);
-          daw[q] = pack_bf16x2(da0, da1);
-          const float2 duh = unpack_bf16x2(duw[q]), dah = unpack_bf16x2(daw[q]);
-          dul[q] = pack_bf16x2(du0 - duh.x, du1 - duh.y);
-          dal[q] = pack_bf16x2(da0 - dah.x, da1 - dah.y);
-        }
-        uint16_t* base = p.dd + o + 8 * v;
-        *reinterpret_cast<uint4*>(base) = make_uint4(duw[0], duw[1], duw[2], duw[3]);
-        *reinterpret_cast<uint4*>(base + seg) = make_uint4(daw[0], daw[1], daw[2], daw[3]);
-        if (p.dd_split) {
-          *reinterpret_cast<uint4*>(base + 2 * seg) = make_uint4(dul[0], dul[1], dul[2], dul[3]);
-          *reinterpret_cast<uint4*>(base + 3 * seg) = make_uint4(dal[0], dal[1], dal[2], dal[3]);
-        }
+        send16(st, om.o0, duw, n0 + c0, row0);
+        send16(st, om.o0, daw, n0 + c0 + seg, row0);
+        send16(st, om.o0, dul, n0 + c0 + 2 * seg, row0);
+        send16(st, om.o0, dal, n0 + c0 + 3 * seg, row0);
       }
     }
   }
@@ -713,7 +739,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     const int quarter = warp & 3;
     const int half = (warp - 4) >> 2;
     const int r_local = quarter * 32 + lane;
-    Stager st{sOut + (warp - 4) * kStageBytes, lane, 0};
+    Stager st{sOut + (warp - 4) * kStageBytes, lane, 0, false};
     const OutMaps om{&tmO0, &tmO1, &tmO2};
     int it = 0;
     for (int unit = blockIdx.x; unit < total; unit += gridDim.x, ++it) {
@@ -808,7 +834,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           const int r_local = quarter * 32 + lane;
           const int row = mb * kBM + r_local;
           const uint32_t tacc = tmem_base + ((uint32_t)(quarter * 32) << 16);
-          Stager st{sOut + (warp - 4) * kStageBytes, lane, 0};
+          Stager st{sOut + (warp - 4) * kStageBytes, lane, 0, false};
           const OutMaps om{&tmO0, &tmO1, &tmO2};
           Epilogue<EPI>::run(p, tacc, row, row < M_eff, nb * kBN, p.N, half, st, om, 0, rsum,
                              r_local);

@@ -34,6 +34,7 @@ enum GemmKind {
   GK_PACK = 4,       // gate GEMM with the TwELL pack epilogue
   GK_GATED = 5,      // [Wg ; Wu] GEMM with the ReLU * up epilogue
   GK_BWD_GATE = 6,   // dh GEMM with the du / da epilogue
+  GK_BWD_GATE_RT = 7,  // the same for routed rows (fp32 u in, bf16 hi + lo out)
 };
 
 int num_sms();
