@@ -267,11 +267,15 @@ def run_own(args, dist):
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
 
-    def sparse_step():
-        twell.twell_pack(x, wg, shape, tiles)
-        twell.hybrid_route(tiles, shape, route)
-        twell.twell_ffn_fwd(x, wg, wu, wd, shape, y, route=route, ws=ws)
-        twell.twell_ffn_bwd(x, wg, wu, wd, dy, shape, route, L1, dx, *dws, ws)
+    def make_sparse_step(xb, dyb, yb, dxb):
+        def step():
+            twell.twell_pack(xb, wg, shape, tiles)
+            twell.hybrid_route(tiles, shape, route)
+            twell.twell_ffn_fwd(xb, wg, wu, wd, shape, yb, route=route, ws=ws)
+            twell.twell_ffn_bwd(xb, wg, wu, wd, dyb, shape, route, L1, dxb, *dws, ws)
+        return step
+
+    sparse_step = make_sparse_step(x, dy, y, dx)
 
     # inference workloads (uniform density, no routing) run the TwELL forward;
     # training workloads run the forward of their training step: pack, hybrid
@@ -544,14 +548,58 @@ def run_own(args, dist):
     yh = torch.empty((M, d), dtype=torch.bfloat16).pin_memory()
     dxh = torch.empty((M, d), dtype=torch.bfloat16).pin_memory()
 
-    def e2e_step():
-        x.copy_(xh, non_blocking=True)
-        dy.copy_(dyh, non_blocking=True)
-        sparse_step()
-        yh.copy_(y, non_blocking=True)
-        dxh.copy_(dx, non_blocking=True)
+    # double-buffered: while step i computes (graph replay on the compute
+    # stream, after its L2 flush), step i+1's inputs are copied in and step
+    # i-1's results copied out on two copy streams; events keep a buffer set
+    # from being overwritten while a copy or the compute still uses it
+    bufs = [(x, dy, y, dx), (torch.empty_like(x), torch.empty_like(dy), torch.empty_like(y),
+                             torch.empty_like(dx))]
+    step_graphs = [graphed(make_sparse_step(*b)) for b in bufs]
+    comp = stream
+    h2d, d2h = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    ev_in = [torch.cuda.Event() for _ in range(2)]    # inputs of set b copied in
+    ev_done = [torch.cuda.Event() for _ in range(2)]  # compute on set b finished
+    ev_out = [torch.cuda.Event() for _ in range(2)]   # results of set b copied out
 
-    ms_e2e, _, _, _ = timed(graphed(e2e_step), args.steps, args.warmup)
+    def copy_in(b):
+        with torch.cuda.stream(h2d):
+            h2d.wait_event(ev_done[b])
+            bufs[b][0].copy_(xh, non_blocking=True)
+            bufs[b][1].copy_(dyh, non_blocking=True)
+            ev_in[b].record(h2d)
+
+    def e2e_run(n_steps):
+        copy_in(0)
+        for i in range(n_steps):
+            b = i % 2
+            if i + 1 < n_steps:
+                copy_in(1 - b)
+            comp.wait_event(ev_out[b])
+            flush.zero_()
+            comp.wait_event(ev_in[b])
+            step_graphs[b]()
+            ev_done[b].record(comp)
+            with torch.cuda.stream(d2h):
+                d2h.wait_event(ev_done[b])
+                yh.copy_(bufs[b][2], non_blocking=True)
+                dxh.copy_(bufs[b][3], non_blocking=True)
+                ev_out[b].record(d2h)
+        comp.wait_stream(h2d)
+        comp.wait_stream(d2h)
+
+    e2e_run(args.warmup)
+    torch.cuda.synchronize()
+    dist.barrier()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(comp)
+    e2e_run(args.steps)
+    e1.record(comp)
+    torch.cuda.synchronize()
+    dist.barrier()
+    ms_e2e = dist.max(e0.elapsed_time(e1) / args.steps, dev)
+    if twell.twell_get_device_status() != 0:
+        raise RuntimeError("device status after the end-to-end run")
     bi = 2 * M * d * 2
     bo = 2 * M * d * 2
 
@@ -582,7 +630,11 @@ def run_own(args, dist):
         "torch_cublas_dense": torch_dense or None,
         "small_m": small_m or None,
         "e2e": {"value": n * M / (ms_e2e / 1e3), "unit": UNIT, "h2d_bytes_per_step": bi,
-                "d2h_bytes_per_step": bo},
+                "d2h_bytes_per_step": bo, "ms_per_step": ms_e2e,
+                "pipeline": "x, dY copied in from pinned host memory and y, dX copied out "
+                            "every step on two copy streams, double-buffered so the copies "
+                            "of steps i+1 and i-1 overlap step i's compute; the L2 flush "
+                            "before each step's compute is inside the timed region"},
         "gpu_launches": int(launches_per_step * args.steps),
         "gpu_launches_per_step": launches_per_step,
         "timing": "each step replayed from a CUDA graph of the library calls; "
