@@ -217,8 +217,10 @@ def cpu_sample_rate(wl, bits, W, seconds, step_budget=None):
 
 # ---------------------------------------------------------------- own arm
 def algorithmic_work(family, wl, nnz_ell, n_dense):
-    """(amount, unit, bound) per launch of a kernel family, from the formulas
-    of the hot path: flops for tensor-core GEMMs, bytes for gather kernels."""
+    """(amount, unit, bound) per step of a kernel family, from the formulas
+    of the hot path: flops for tensor-core GEMMs, bytes for gather kernels.
+    The bytes are those of one pass over the step's inputs; the partial sums
+    that L2-sized neuron passes carry between launches are not counted."""
     M, d, f = wl.M, wl.d_model, wl.d_ff
     if family == "gemm_gate_pack":
         return 2.0 * M * d * f, "flop", "tensor"
@@ -512,8 +514,13 @@ def run_own(args, dist):
         torch.cuda.synchronize()
         return 5 * n_rows * row_bytes / (e0.elapsed_time(e1) / 1e3) / 1e9
 
-    gather_probe = {"row_bytes": 2 * d, "l2_resident_table_bytes": 2 * f * d * 2,
-                    "l2_gbs": probe(2 * f * d * 2), "dram_table_bytes": 2 << 30,
+    # the L2-resident table is this workload's Wu + Wd, capped at half of L2
+    # (the neuron chunk one pass of the gather kernels holds when the weights
+    # exceed L2)
+    l2_bytes = torch.cuda.get_device_properties(dev).L2_cache_size
+    l2_table = min(2 * f * d * 2, l2_bytes // 2)
+    gather_probe = {"row_bytes": 2 * d, "l2_resident_table_bytes": l2_table,
+                    "l2_gbs": probe(l2_table), "dram_table_bytes": 2 << 30,
                     "dram_gbs": probe(2 << 30)}
 
     # roofline of the dominant kernel, from its events inside the timed region
@@ -523,6 +530,9 @@ def run_own(args, dist):
     work = algorithmic_work(dominant, wl, nnz_ell, n_dense)
     if work and cnt:
         amount, unit, bound = work
+        # the formulas give a whole step's work; a family launched in several
+        # L2-sized passes per step shares it among its launches
+        amount /= cnt / args.steps
         per_launch_s = dom_ms / cnt / 1e3
         if unit == "flop":
             achieved = amount / per_launch_s / 1e12
