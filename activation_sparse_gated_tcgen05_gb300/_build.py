@@ -14,7 +14,7 @@ OUT_DIR = os.path.join(PKG, "_build")
 LIB = os.path.join(OUT_DIR, "libtwell.so")
 
 SOURCES = ["api.cu", "gemm_tc.cu", "pack.cu", "sparse_fwd.cu", "sparse_bwd.cu", "probe.cu"]
-HEADERS = ["common.cuh", "gemm_tc.cuh", "internal.h"]
+HEADERS = ["common.cuh", "ell_gather.cuh", "gemm_tc.cuh", "internal.h"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ARCH + ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC",
                      "-I" + INCLUDE, "-I" + CSRC]

@@ -184,10 +184,12 @@ struct Carve {
 struct SparseWs {
   uint16_t *xr, *hr;                    // forward fallback
   float* part;
+  float* hbuf;                          // per-ELL-entry h of the split forward
   uint16_t *dyr, *gr, *ddr;             // backward fallback
   float* ur;
   int *mask_off, *csc_ptr, *csc_row, *slot_pos;
   float4* csc_vals;
+  float2* coef;                         // per-ELL-entry (du, da) of the split row phase
   size_t bytes;
 };
 
@@ -199,9 +201,10 @@ SparseWs carve_sparse(void* ws, const twell_shape& s, int W, int training) {
   w.xr = c.take<uint16_t>(Mp * d);
   w.hr = c.take<uint16_t>(Mp * 2 * f);
   w.part = c.take<float>(Mp * d);
+  const long long E = (long long)s.M * W;
+  w.hbuf = c.take<float>(E > 0 ? E : 1);
   if (training) {
     const long long NB = (s.M + 31) / 32;
-    const long long E = (long long)s.M * W;
     w.dyr = c.take<uint16_t>(Mp * d);
     w.gr = c.take<uint16_t>(Mp * f);
     w.ur = c.take<float>(Mp * f);
@@ -212,6 +215,7 @@ SparseWs carve_sparse(void* ws, const twell_shape& s, int W, int training) {
     w.csc_row = c.take<int>(E > 0 ? E : 1);
     w.slot_pos = c.take<int>(E > 0 ? E : 1);
     w.csc_vals = c.take<float4>(E > 0 ? E : 1);
+    w.coef = c.take<float2>(E > 0 ? E : 1);
   }
   w.bytes = c.off + 256;
   return w;
@@ -557,7 +561,7 @@ twell_status twell_ffn_fwd(const void* x, const void* wgT, const void* wuT, cons
     if ((st = check_tiles(tiles)) != TWELL_OK) return st;
     if (s.M == 0) return TWELL_OK;
     return cuda_status(launch_sparse_fwd(x, wuT, wd, s.M, s.d_model, s.d_ff, tiles, s.tile_n,
-                                         s.tile_cap, nullptr, y, nullptr, cs));
+                                         s.tile_cap, nullptr, y, nullptr, nullptr, cs));
   }
   if ((st = check_route(route)) != TWELL_OK) return st;
   if ((st = check_ptrs({wgT})) != TWELL_OK) return st;
@@ -570,7 +574,7 @@ twell_status twell_ffn_fwd(const void* x, const void* wgT, const void* wuT, cons
   // w.part carries y between L2-sized passes; the routed rows' split-K GEMM
   // reuses it afterwards on the same stream
   cudaError_t e = launch_sparse_fwd(x, wuT, wd, s.M, s.d_model, s.d_ff, nullptr, s.tile_n,
-                                    s.tile_cap, route, y, w.part, cs);
+                                    s.tile_cap, route, y, w.part, w.hbuf, cs);
   if (e == cudaSuccess)
     e = launch_gather_rows(x, s.M, s.d_model, route->dense_rows, route->n_dense, w.xr, (int)Mp, cs);
   if (e == cudaSuccess)
@@ -601,7 +605,7 @@ twell_status twell_ffn_bwd(const void* x, const void* wgT, const void* wuT, cons
                                    w.slot_pos, cs);
   if (e == cudaSuccess)
     e = launch_sparse_bwd_rows(x, dy, wgT, wuT, wd, s.M, s.d_model, s.d_ff, *route, w.slot_pos,
-                               l1_coeff, w.csc_vals, dx, w.part, cs);
+                               l1_coeff, w.csc_vals, dx, w.part, w.hbuf, w.coef, cs);
   if (e == cudaSuccess)
     e = launch_sparse_bwd_neurons(x, dy, s.M, s.d_model, s.d_ff, w.csc_ptr, w.csc_row, w.csc_vals,
                                   dwgT, dwuT, dwd, cs);

@@ -1,0 +1,272 @@
+// ell_gather.cuh -- the two gathers that ELL rows wider than 1024 are split
+// into, shared by the forward and the backward row phase.
+//
+// Page 2 "Sakana AI and NVIDIA introduce TwELL with CUDA kernels ...",
+// section "¿Qué hace distinto a TwELL frente a ELL clásico?", fuses the up
+// and down projections into one gather.  For wide rows that kernel needs a
+// team of warps per row whose partial dot products meet at a barrier for
+// every batch of entries, and it gathers two or three weight rows per entry,
+// so on large shapes its table outgrows L2 and it runs in several neuron
+// passes.  Split in two:
+//
+//   ell_dot_kernel   per ELL entry e = (m, j): the dot product of a row
+//                    vector v_m (x_m or dY_m) with a gathered weight row
+//                    R[j] (Wu^T[j] or Wd[j]).  The team forms each dot
+//                    exactly as the fused kernels do (same slabs, same warp
+//                    and cross-warp summation order) but meets at its named
+//                    barrier once per 32 entries: lane i keeps the warp's
+//                    partial of entry i and the team sums 32 partials at once.
+//                    The epilogue runs per entry on lane i:
+//                      kDotH     h = g u                  (forward, u = x.Wu)
+//                      kDotDh    dh                       (backward, dY.Wd)
+//                      kDotGrad  du = dh g, da = dh u + lambda, h = g u
+//                                (backward, u = x.Wu, dh from kDotDh)
+//   ell_axpy_kernel  out_m = sum_e c_e R[j_e] (+ c'_e R'[j_e]): independent
+//                    warps, each owning VPL slabs of one row, accumulate the
+//                    per-entry coefficients in entry order -- y = sum h Wd in
+//                    the forward, dX = sum du Wu^T + da Wg^T in the backward.
+//
+// Every entry's arithmetic and every output element's accumulation order are
+// those of the fused kernels, so results are bit-identical to them.  Each
+// kernel gathers one or two weight matrices (a smaller table than the fused
+// kernel's, so fewer L2-sized passes), and neither waits at a barrier per
+// batch.
+#pragma once
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace tw {
+namespace {
+
+constexpr int kDotH = 0, kDotDh = 1, kDotGrad = 2;
+constexpr int kEllPassFirst = 1, kEllPassLast = 2;
+
+// Element offset of slab v of warp wt in a team of TEAM warps: slabs of 256
+// elements (32 lanes x 8) dealt round-robin over the team.
+template <int TEAM>
+__device__ __forceinline__ int team_slab(int lane, int wt, int v) {
+  return 8 * (lane + 32 * (wt + TEAM * v));
+}
+
+// [a, b): the entries of row m whose columns lie in [j_lo, j_hi).  A row's
+// columns ascend, so the chunk is one contiguous slice.
+__device__ __forceinline__ void ell_slice(const uint16_t* __restrict__ ell_col, long long row_off,
+                                          int n, int j_lo, int j_hi, bool whole, int lane, int& a,
+                                          int& b) {
+  a = 0;
+  b = n;
+  if (whole) return;
+  a = b = 0;
+  for (int s0 = 0; s0 < n; s0 += 32) {
+    const int jc = s0 + lane < n ? (int)ell_col[row_off + s0 + lane] : 0x7fffffff;
+    a += __popc(__ballot_sync(0xffffffffu, jc < j_lo));
+    b += __popc(__ballot_sync(0xffffffffu, jc < j_hi));
+  }
+}
+
+struct EllDotArgs {
+  const uint16_t* vec;   // [M][d] row vectors (x or dY)
+  const uint16_t* rows;  // [f][d] gathered weight rows (Wu^T or Wd)
+  int M, d, W;
+  const uint16_t* ell_val;
+  const uint16_t* ell_col;
+  const int* ell_nnz;
+  int j_lo, j_hi, whole;
+  float* out;            // kDotH: h, kDotDh: dh  ([M][W] per slot)
+  const float* dh;       // kDotGrad: dh per slot
+  const int* slot_pos;   // kDotGrad: neuron-major position of each slot
+  float lambda;          // kDotGrad: L1 coefficient
+  float4* csc_vals;      // kDotGrad: (du, da, h, 0) at the neuron-major position
+  float2* coef;          // kDotGrad: (du, da) per slot, for the dX gather
+};
+
+template <int TEAM, int VPL, int B, int MINB, int MODE>
+__global__ void __launch_bounds__(256, MINB) ell_dot_kernel(const EllDotArgs p) {
+  static_assert(B % 2 == 0 && 32 % B == 0, "entries are summed over the warp in pairs");
+  constexpr int ROWS = 8 / TEAM;
+  __shared__ float red[2][ROWS][TEAM][32];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int team = warp / TEAM, wt = warp % TEAM;
+  const int m = blockIdx.x * ROWS + team;
+  if (m >= p.M) return;
+  const int d = p.d;
+
+  const uint64_t pol = l2_evict_first_policy();  // the row vectors stream through
+  uint4 vv[VPL];
+  int eoff[VPL];
+#pragma unroll
+  for (int v = 0; v < VPL; ++v) {
+    const int e = team_slab<TEAM>(lane, wt, v);
+    eoff[v] = e < d ? e : 0;
+    vv[v] = e < d ? ldg_v4_hint(p.vec + (long long)m * d + e, pol) : make_uint4(0, 0, 0, 0);
+  }
+  const long long row_off = (long long)m * p.W;
+  int a, bnd;
+  ell_slice(p.ell_col, row_off, p.ell_nnz[m], p.j_lo, p.j_hi, p.whole, lane, a, bnd);
+  int buf = 0;
+  for (int e0 = a; e0 < bnd; e0 += 32) {
+    const int count = min(32, bnd - e0);
+    const long long s = row_off + e0 + lane;
+    const int jl = lane < count ? (int)p.ell_col[s] : 0;  // slots past the slice: neuron 0
+    float mine = 0.f;  // the warp's partial dot product of entry e0 + lane
+    for (int i = 0; i < count; i += B) {
+      int j[B];
+#pragma unroll
+      for (int b = 0; b < B; ++b) j[b] = __shfl_sync(0xffffffffu, jl, (i + b) & 31);
+      uint4 r[B][VPL];
+#pragma unroll
+      for (int b = 0; b < B; ++b)
+#pragma unroll
+        for (int v = 0; v < VPL; ++v) r[b][v] = ldg_v4(p.rows + (long long)j[b] * d + eoff[v]);
+      float q[B];
+#pragma unroll
+      for (int b = 0; b < B; ++b) {
+        float a0 = 0.f, a1 = 0.f;
+#pragma unroll
+        for (int v = 0; v < VPL; ++v) dot8_bf16(vv[v], r[b][v], a0, a1);
+        q[b] = a0 + a1;
+      }
+#pragma unroll
+      for (int b = 0; b < B; b += 2) warp_sum2(q[b], q[b + 1]);
+#pragma unroll
+      for (int b = 0; b < B; ++b)
+        if (lane == i + b) mine = q[b];
+    }
+    float dot = mine;
+    if constexpr (TEAM > 1) {
+      red[buf][team][wt][lane] = mine;
+      named_barrier(1 + team, 32 * TEAM);
+      dot = 0.f;
+#pragma unroll
+      for (int w = 0; w < TEAM; ++w) dot += red[buf][team][w][lane];
+      buf ^= 1;
+    }
+    if (wt != 0 || lane >= count) continue;
+    if constexpr (MODE == kDotDh) {
+      p.out[s] = dot;
+    } else {
+      const float g = bf16_bits_to_float(p.ell_val[s]);
+      if constexpr (MODE == kDotH) {
+        p.out[s] = g * dot;
+      } else {  // ReLU'(a) = 1 on a live entry
+        const float dh = p.dh[s];
+        const float du = dh * g, da = fmaf(dh, dot, p.lambda);
+        p.csc_vals[p.slot_pos[s]] = make_float4(du, da, g * dot, 0.f);
+        p.coef[s] = make_float2(du, da);
+      }
+    }
+  }
+}
+
+struct EllAxpyArgs {
+  const uint16_t* rows0;  // [f][d] weight rows scaled by the first coefficient
+  const uint16_t* rows1;  // second matrix (NR = 2), scaled by the second
+  int M, d, W;
+  const uint16_t* ell_col;
+  const int* ell_nnz;
+  const void* coef;       // per slot: float (NR = 1) or float2 (NR = 2)
+  int j_lo, j_hi, pass;
+  float* part;            // [M][d] fp32 carry between neuron passes
+  uint16_t* out;          // [M][d] bf16 result
+};
+
+template <int VPL, int B, int MINB, int NR>
+__global__ void __launch_bounds__(256, MINB) ell_axpy_kernel(const EllAxpyArgs p) {
+  static_assert(32 % B == 0, "a batch never reaches past lane 31");
+  static_assert(NR == 1 || NR == 2, "one or two gathered matrices");
+  const int lane = threadIdx.x & 31;
+  const int d = p.d;
+  const int wpr = (d + 256 * VPL - 1) / (256 * VPL);  // warps per row
+  const long long gw = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);
+  const int m = (int)(gw / wpr), sg = (int)(gw % wpr);
+  if (m >= p.M) return;
+
+  const bool first = p.pass & kEllPassFirst, last = p.pass & kEllPassLast;
+  const uint64_t pol = l2_evict_first_policy();  // the result and its carry stream through
+  uint64_t acc[VPL][4];
+  int eoff[VPL];
+#pragma unroll
+  for (int v = 0; v < VPL; ++v) {
+    const int e = 8 * lane + 256 * (sg * VPL + v);
+    eoff[v] = e < d ? e : 0;
+    if (first || e >= d) {
+#pragma unroll
+      for (int k = 0; k < 4; ++k) acc[v][k] = 0;
+    } else {
+      const float* pp = p.part + (long long)m * d + e;
+      const uint4 q0 = ldg_v4_hint(pp, pol), q1 = ldg_v4_hint(pp + 4, pol);
+      acc[v][0] = f2_make(q0.x, q0.y);
+      acc[v][1] = f2_make(q0.z, q0.w);
+      acc[v][2] = f2_make(q1.x, q1.y);
+      acc[v][3] = f2_make(q1.z, q1.w);
+    }
+  }
+  const long long row_off = (long long)m * p.W;
+  int a, bnd;
+  ell_slice(p.ell_col, row_off, p.ell_nnz[m], p.j_lo, p.j_hi, first && last, lane, a, bnd);
+  for (int e0 = a; e0 < bnd; e0 += 32) {
+    const int count = min(32, bnd - e0);
+    const long long s = row_off + e0 + lane;
+    int jl = 0;  // slots past the slice: neuron 0 with zero coefficients
+    float c0 = 0.f, c1 = 0.f;
+    if (lane < count) {
+      jl = p.ell_col[s];
+      if constexpr (NR == 1) {
+        c0 = reinterpret_cast<const float*>(p.coef)[s];
+      } else {
+        const float2 c = reinterpret_cast<const float2*>(p.coef)[s];
+        c0 = c.x;
+        c1 = c.y;
+      }
+    }
+    for (int i = 0; i < count; i += B) {
+      int j[B];
+      float k0[B], k1[B];
+#pragma unroll
+      for (int b = 0; b < B; ++b) {
+        j[b] = __shfl_sync(0xffffffffu, jl, (i + b) & 31);
+        k0[b] = __shfl_sync(0xffffffffu, c0, (i + b) & 31);
+        if constexpr (NR == 2) k1[b] = __shfl_sync(0xffffffffu, c1, (i + b) & 31);
+      }
+      uint4 r0[B][VPL], r1[NR == 2 ? B : 1][VPL];
+#pragma unroll
+      for (int b = 0; b < B; ++b) {
+        const long long row = (long long)j[b] * d;
+#pragma unroll
+        for (int v = 0; v < VPL; ++v) {
+          r0[b][v] = ldg_v4(p.rows0 + row + eoff[v]);
+          if constexpr (NR == 2) r1[b][v] = ldg_v4(p.rows1 + row + eoff[v]);
+        }
+      }
+#pragma unroll
+      for (int b = 0; b < B; ++b) {
+        const uint64_t s0 = f2_splat(k0[b]);
+#pragma unroll
+        for (int v = 0; v < VPL; ++v) axpy8_f2(s0, r0[b][v], acc[v]);
+        if constexpr (NR == 2) {
+          const uint64_t s1 = f2_splat(k1[b]);
+#pragma unroll
+          for (int v = 0; v < VPL; ++v) axpy8_f2(s1, r1[b][v], acc[v]);
+        }
+      }
+    }
+  }
+#pragma unroll
+  for (int v = 0; v < VPL; ++v) {
+    const int e = 8 * lane + 256 * (sg * VPL + v);
+    if (e >= d) continue;
+    if (last) {
+      st_v4_hint(p.out + (long long)m * d + e, f2x4_to_bf8(acc[v]), pol);
+    } else {
+      float* pp = p.part + (long long)m * d + e;
+      st_v4_hint(pp, make_uint4((uint32_t)acc[v][0], (uint32_t)(acc[v][0] >> 32),
+                                (uint32_t)acc[v][1], (uint32_t)(acc[v][1] >> 32)), pol);
+      st_v4_hint(pp + 4, make_uint4((uint32_t)acc[v][2], (uint32_t)(acc[v][2] >> 32),
+                                    (uint32_t)acc[v][3], (uint32_t)(acc[v][3] >> 32)), pol);
+    }
+  }
+}
+
+}  // namespace
+}  // namespace tw

@@ -18,7 +18,9 @@
 //      ordering race: rank = prefix over groups of 32 blocks + prefix over the
 //      blocks of its group + popcount of lower bits.
 //   2. bwd_rows: one team of warps per row computes dh, u, du, da, h per entry
-//      (stored at the entry's neuron-major position) and dX_m.
+//      (stored at the entry's neuron-major position) and dX_m.  Rows wider
+//      than 1024 take three gathers instead (dh; u with du, da, h; dX), which
+//      meet no barrier per batch (ell_gather.cuh).
 // Gathered rows are loaded without predicates: a batch slot past the last
 // entry reads neuron (or row) 0 with zero coefficients, and lanes past
 // d_model read the first slab against zero x / dY, so no zero-fill selects
@@ -26,6 +28,7 @@
 //   3. bwd_neurons: one team per neuron sums its entries in ascending row
 //      order into dWd[j], dWu^T[j], dWg^T[j] (fp32, written once).
 #include "common.cuh"
+#include "ell_gather.cuh"
 #include "internal.h"
 
 namespace tw {
@@ -158,6 +161,7 @@ __global__ void __launch_bounds__(256, MINB)
                     const int* __restrict__ ell_nnz, int W, const int* __restrict__ slot_pos,
                     float lambda, float4* __restrict__ csc_vals, uint16_t* __restrict__ dx,
                     float* __restrict__ part, int j_lo, int j_hi, int pass) {
+  static_assert(32 % B == 0, "a batch never reaches past lane 31");
   constexpr int ROWS = 8 / TEAM;
   __shared__ float red[2][ROWS][TEAM][2 * B];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -352,11 +356,18 @@ __global__ void __launch_bounds__(256, MINB)
       float du[B], da[B], h[B];
 #pragma unroll
       for (int b = 0; b < B; ++b) {
+        // with B not dividing 32 the last batch reaches past lane 31: those
+        // slots take row 0 with zero coefficients, like slots past the end
+        const bool in = 32 % B == 0 || i + b < 32;
         const int src = (i + b) & 31;
         m[b] = __shfl_sync(kFull, ml, src);
         du[b] = __shfl_sync(kFull, vl.x, src);
         da[b] = __shfl_sync(kFull, vl.y, src);
         h[b] = __shfl_sync(kFull, vl.z, src);
+        if (!in) {
+          m[b] = 0;
+          du[b] = da[b] = h[b] = 0.f;
+        }
       }
       uint4 xv[B][VPL], dyv[B][VPL];
 #pragma unroll
@@ -496,26 +507,119 @@ cudaError_t launch_csc_build(const twell_hybrid& r, int M, int f, int* blk_count
   return e;
 }
 
+namespace {
+
+// Wide ELL rows: the fused row phase split into three gathers (ell_gather.cuh)
+//   dh = dY_m . Wd[j]                         over Wd
+//   u = x_m . Wu[:, j]; du, da, h per entry     over Wu^T (dh from the first)
+//   dX_m = sum du Wu[:, j]^T + da Wg[:, j]^T     over Wu^T and Wg^T
+// each in its own L2-sized neuron passes.  Per entry and per dX element the
+// arithmetic and accumulation order are the fused kernel's.
+template <int TEAM, int VPL>
+cudaError_t split_rows(const void* x, const void* dy, const void* wgT, const void* wuT,
+                       const void* wd, int M, int d, int f, const twell_hybrid& r,
+                       const int* slot_pos, float lambda, float4* csc_vals, void* dx, float* part,
+                       float* dhbuf, float2* coef, cudaStream_t s) {
+  constexpr int ROWS = 8 / TEAM;
+  const unsigned grid = (unsigned)((M + ROWS - 1) / ROWS);
+  EllDotArgs p{};
+  p.M = M;
+  p.d = d;
+  p.W = r.ell_width;
+  p.ell_val = reinterpret_cast<const uint16_t*>(r.ell_val);
+  p.ell_col = r.ell_col;
+  p.ell_nnz = r.ell_nnz;
+  p.slot_pos = slot_pos;
+  p.lambda = lambda;
+  p.csc_vals = csc_vals;
+  p.coef = coef;
+  p.dh = dhbuf;
+  p.out = dhbuf;
+  const int dot_chunks = part ? l2_chunks(2.0 * (double)f * d, 0.75, 0.5) : 1;
+  p.whole = dot_chunks == 1;
+  for (int phase = 0; phase < 2; ++phase) {
+    p.vec = reinterpret_cast<const uint16_t*>(phase == 0 ? dy : x);
+    p.rows = reinterpret_cast<const uint16_t*>(phase == 0 ? wd : wuT);
+    for (int c = 0; c < dot_chunks; ++c) {
+      p.j_lo = (int)((long long)f * c / dot_chunks);
+      p.j_hi = (int)((long long)f * (c + 1) / dot_chunks);
+      {
+        ProfScope prof(phase == 0 ? "bwd_dh" : "bwd_grad", s);
+        // two-slab warps take four entries per batch, four-slab warps two
+        if (phase == 0) {
+          if constexpr (VPL <= 2)
+            ell_dot_kernel<TEAM, VPL, 4, 2, kDotDh><<<grid, 256, 0, s>>>(p);
+          else
+            ell_dot_kernel<TEAM, VPL, 2, 3, kDotDh><<<grid, 256, 0, s>>>(p);
+        } else {
+          if constexpr (VPL <= 2)
+            ell_dot_kernel<TEAM, VPL, 4, 2, kDotGrad><<<grid, 256, 0, s>>>(p);
+          else
+            ell_dot_kernel<TEAM, VPL, 2, 3, kDotGrad><<<grid, 256, 0, s>>>(p);
+        }
+      }
+      count_launch();
+      const cudaError_t e = cudaGetLastError();
+      if (e != cudaSuccess) return e;
+    }
+  }
+  constexpr int DV = 2;  // dX: two slabs per warp, two entries per batch
+  EllAxpyArgs a{};
+  a.rows0 = reinterpret_cast<const uint16_t*>(wuT);
+  a.rows1 = reinterpret_cast<const uint16_t*>(wgT);
+  a.M = M;
+  a.d = d;
+  a.W = r.ell_width;
+  a.ell_col = r.ell_col;
+  a.ell_nnz = r.ell_nnz;
+  a.coef = coef;
+  a.part = part;
+  a.out = reinterpret_cast<uint16_t*>(dx);
+  const int dx_chunks = part ? l2_chunks(4.0 * (double)f * d, 0.75, 0.5) : 1;
+  const int wpr = (d + 256 * DV - 1) / (256 * DV);
+  const unsigned blocks = (unsigned)(((long long)M * wpr + 7) / 8);
+  for (int c = 0; c < dx_chunks; ++c) {
+    a.j_lo = (int)((long long)f * c / dx_chunks);
+    a.j_hi = (int)((long long)f * (c + 1) / dx_chunks);
+    a.pass = (c == 0 ? kEllPassFirst : 0) | (c == dx_chunks - 1 ? kEllPassLast : 0);
+    {
+      ProfScope prof("bwd_dx", s);
+      ell_axpy_kernel<DV, 2, 4, 2><<<blocks, 256, 0, s>>>(a);
+    }
+    count_launch();
+    const cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
+}
+
+}  // namespace
+
 cudaError_t launch_sparse_bwd_rows(const void* x, const void* dy, const void* wgT, const void* wuT,
                                    const void* wd, int M, int d, int f, const twell_hybrid& route,
                                    const int* slot_pos, float lambda, float4* csc_vals, void* dx,
-                                   float* part, cudaStream_t s) {
+                                   float* part, float* dhbuf, float2* coef, cudaStream_t s) {
   if (M == 0) return cudaSuccess;
+  if (d > 1024) {  // wide rows: the split gathers, with the forward's team shapes
+    if (!dhbuf || !coef) return cudaErrorInvalidValue;
+#define TW_SPLIT(T, V)                                                                          \
+  split_rows<T, V>(x, dy, wgT, wuT, wd, M, d, f, route, slot_pos, lambda, csc_vals, dx, part,  \
+                   dhbuf, coef, s)
+    if (d <= 2048) return TW_SPLIT(4, 2);
+    if (d <= 4096) return TW_SPLIT(4, 4);
+    return TW_SPLIT(8, 4);
+#undef TW_SPLIT
+  }
   // Wd, Wu^T and Wg^T rows: L2-sized neuron passes once they exceed half of
-  // L2 (x, dY and dX stream through L2 beside them; on the 2B-class shape,
-  // 101 MB of weights, two passes beat one by 7 %), chunks of at most 0.65 of
-  // L2 (on the 8B-class shape 4 passes beat 6 and 8), dX_m carried in `part`
+  // L2 (x, dY and dX stream through L2 beside them), chunks of at most 0.65
+  // of L2 (measured with this kernel on 101 MB and 352 MB of weights: two
+  // passes beat one by 7 %, four beat six and eight), dX_m carried in `part`
   // (fp32) with the accumulation order unchanged
   const int chunks = part ? l2_chunks(3.0 * 2.0 * (double)f * d, 0.5, 0.65) : 1;
-#define TW_ROWS(T, V, B, MINB)                                                                 \
-  rows_team<T, V, B, MINB>(x, dy, wgT, wuT, wd, M, d, f, route, slot_pos, lambda, csc_vals, dx, \
-                           part, chunks, s)
-  if (d <= 512) return TW_ROWS(1, 2, 2, 2);
-  if (d <= 1024) return TW_ROWS(1, 4, 1, 2);
-  if (d <= 2048) return TW_ROWS(4, 2, 2, 2);
-  if (d <= 4096) return TW_ROWS(8, 2, 2, 2);
-  return TW_ROWS(8, 4, 2, 1);
-#undef TW_ROWS
+  if (d <= 512) return rows_team<1, 2, 2, 2>(x, dy, wgT, wuT, wd, M, d, f, route, slot_pos, lambda,
+                                             csc_vals, dx, part, chunks, s);
+  return rows_team<1, 4, 1, 2>(x, dy, wgT, wuT, wd, M, d, f, route, slot_pos, lambda, csc_vals,
+                               dx, part, chunks, s);
 }
 
 cudaError_t launch_sparse_bwd_neurons(const void* x, const void* dy, int M, int d, int f,
@@ -527,12 +631,13 @@ cudaError_t launch_sparse_bwd_neurons(const void* x, const void* dy, int M, int 
 #define TW_NEU(T, V, B, MINB) \
   neurons_team<T, V, B, MINB>(x, dy, d, f, csc_ptr, csc_row, csc_vals, dwgT, dwuT, dwd, s)
   // one 256-element slab per warp (short accumulators, 3-4 blocks per SM)
-  // while a block's 8 warps cover d_model
+  // while a block's 8 warps cover d_model; at d = 4096 batches of three rows
+  // (6 % faster than two on the 8B-class shape)
   if (d <= 256) return TW_NEU(1, 1, 2, 4);
   if (d <= 512) return TW_NEU(2, 1, 2, 4);
   if (d <= 1024) return TW_NEU(4, 1, 2, 4);
   if (d <= 2048) return TW_NEU(8, 1, 4, 3);
-  if (d <= 4096) return TW_NEU(8, 2, 2, 2);
+  if (d <= 4096) return TW_NEU(8, 2, 3, 2);
   return TW_NEU(8, 4, 2, 1);
 #undef TW_NEU
 }

@@ -19,10 +19,14 @@
 // lanes past d_model read the row's first slab against a zero x, so the load
 // sequence has no zero-fill selects.  Up to d_model = 1024 a single warp owns
 // the row (no cross-warp reduction); wider rows split it over a team whose
-// partial dot products meet in shared memory behind a named barrier.
+// partial dot products meet in shared memory behind a named barrier.  Wide
+// ELL rows (the training path) instead take two gathers, up and down, that
+// meet no barrier per batch (ell_gather.cuh); TwELL rows of any width take
+// this kernel.
 #include <cooperative_groups.h>
 
 #include "common.cuh"
+#include "ell_gather.cuh"
 #include "internal.h"
 
 namespace tw {
@@ -54,6 +58,7 @@ __device__ __forceinline__ void process_entries(RowCtx<VPL>& c, int jl, float gl
                                                 const uint16_t* __restrict__ wd, int d, int lane,
                                                 int wt, int team, float (*red)[ROWS][TEAM][B],
                                                 int& buf) {
+  static_assert(32 % B == 0, "a batch never reaches past lane 31");
   for (int i = 0; i < count; i += B) {
     // lanes >= count hold (0, 0): a valid row with a zero gate
     int j[B];
@@ -386,23 +391,110 @@ cudaError_t launch_team(const void* x, const void* wuT, const void* wd, int M, i
   return cudaSuccess;
 }
 
-// One warp per row up to d_model = 1024 (four 256-element slabs), then teams
-// of d/512 warps with two slabs each.
+// Wide ELL rows: the fused gather split into an up gather (h = g x.Wu per
+// entry) and a down gather (y = sum h Wd), each over one weight matrix in its
+// own L2-sized neuron passes (ell_gather.cuh).  TEAM and VPL are the fused
+// kernel's, so y is bit-identical to it.
+template <int TEAM, int VPL>
+cudaError_t launch_split(const void* x, const void* wuT, const void* wd, int M, int d, int f,
+                         const twell_hybrid* route, void* y, float* part, float* hbuf,
+                         cudaStream_t s) {
+  constexpr int ROWS = 8 / TEAM;
+  const int chunks = part ? l2_chunks(2.0 * (double)f * d, 0.75, 0.5) : 1;
+  EllDotArgs up{};
+  up.vec = reinterpret_cast<const uint16_t*>(x);
+  up.rows = reinterpret_cast<const uint16_t*>(wuT);
+  up.M = M;
+  up.d = d;
+  up.W = route->ell_width;
+  up.ell_val = reinterpret_cast<const uint16_t*>(route->ell_val);
+  up.ell_col = route->ell_col;
+  up.ell_nnz = route->ell_nnz;
+  up.whole = chunks == 1;
+  up.out = hbuf;
+  for (int c = 0; c < chunks; ++c) {
+    up.j_lo = (int)((long long)f * c / chunks);
+    up.j_hi = (int)((long long)f * (c + 1) / chunks);
+    {
+      ProfScope prof("sparse_fwd_up", s);
+      // two-slab warps take four entries per batch, four-slab warps two
+      // (measured on the 2B- and 8B-class shapes)
+      if constexpr (VPL <= 2)
+        ell_dot_kernel<TEAM, VPL, 4, 2, kDotH><<<(M + ROWS - 1) / ROWS, 256, 0, s>>>(up);
+      else
+        ell_dot_kernel<TEAM, VPL, 2, 3, kDotH><<<(M + ROWS - 1) / ROWS, 256, 0, s>>>(up);
+    }
+    count_launch();
+    const cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  constexpr int DV = 2;  // down: two slabs per warp, two entries per batch
+  EllAxpyArgs down{};
+  down.rows0 = reinterpret_cast<const uint16_t*>(wd);
+  down.M = M;
+  down.d = d;
+  down.W = route->ell_width;
+  down.ell_col = route->ell_col;
+  down.ell_nnz = route->ell_nnz;
+  down.coef = hbuf;
+  down.part = part;
+  down.out = reinterpret_cast<uint16_t*>(y);
+  const int wpr = (d + 256 * DV - 1) / (256 * DV);
+  const long long blocks = ((long long)M * wpr + 7) / 8;
+  for (int c = 0; c < chunks; ++c) {
+    down.j_lo = (int)((long long)f * c / chunks);
+    down.j_hi = (int)((long long)f * (c + 1) / chunks);
+    down.pass = (c == 0 ? kEllPassFirst : 0) | (c == chunks - 1 ? kEllPassLast : 0);
+    {
+      ProfScope prof("sparse_fwd_down", s);
+      ell_axpy_kernel<DV, 2, 4, 1><<<(unsigned)blocks, 256, 0, s>>>(down);
+    }
+    count_launch();
+    const cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
+}
+
+// One warp per row up to d_model = 1024 (four 256-element slabs), four warps
+// of two slabs up to 2048, four warps of four slabs up to 4096 (on the
+// 8B-class shape 6 % faster than eight warps of two: half the warps meet at
+// each barrier), then eight warps of four slabs.
+// ELL rows up to d_model = 1024 take the fused kernel, wider ones the split
+// up and down gathers; TwELL rows take the fused kernel, split over clusters
+// for small batches.
+template <int TEAM, int VPL, bool ELL>
+cudaError_t launch_shape(const void* x, const void* wuT, const void* wd, int M, int d, int f,
+                         const twell_tiles* tiles, int T, int tile_n, int cap,
+                         const twell_hybrid* route, void* y, float* part, float* hbuf, int chunks,
+                         int cl, cudaStream_t s) {
+  if constexpr (ELL && TEAM > 1) {
+    if (!hbuf) return cudaErrorInvalidValue;
+    return launch_split<TEAM, VPL>(x, wuT, wd, M, d, f, route, y, part, hbuf, s);
+  } else if constexpr (ELL) {
+    return launch_team<TEAM, VPL, true>(x, wuT, wd, M, d, f, nullptr, T, tile_n, cap, route, y,
+                                        part, chunks, s);
+  } else {
+    if (cl > 1) return launch_cluster<TEAM, VPL>(x, wuT, wd, M, d, tiles, T, tile_n, cap, cl, y, s);
+    return launch_team<TEAM, VPL, false>(x, wuT, wd, M, d, f, tiles, T, tile_n, cap, nullptr, y,
+                                         nullptr, 1, s);
+  }
+}
+
 template <bool ELL>
 cudaError_t launch_fmt(const void* x, const void* wuT, const void* wd, int M, int d, int f,
                        const twell_tiles* tiles, int T, int tile_n, int cap,
-                       const twell_hybrid* route, void* y, float* part, int chunks,
+                       const twell_hybrid* route, void* y, float* part, float* hbuf, int chunks,
                        cudaStream_t s) {
-#define TW_FWD(TEAM, VPL)                                                                      \
-  (cl > 1 ? launch_cluster<TEAM, VPL>(x, wuT, wd, M, d, tiles, T, tile_n, cap, cl, y, s)        \
-          : launch_team<TEAM, VPL, ELL>(x, wuT, wd, M, d, f, tiles, T, tile_n, cap, route, y, part, \
-                                        chunks, s))
+#define TW_FWD(TEAM, VPL)                                                                       \
+  launch_shape<TEAM, VPL, ELL>(x, wuT, wd, M, d, f, tiles, T, tile_n, cap, route, y, part, hbuf, \
+                               chunks, cl, s)
   // TwELL rows too few to give every SM two blocks: split each row over a
   // cluster of up to 8 blocks, widening while the grid stays within four
   // blocks per SM (a row's slices then stay short even for the heaviest rows)
   int cl = 1;
   if (!ELL) {
-    const int team = d <= 1024 ? 1 : d <= 2048 ? 4 : 8;
+    const int team = d <= 1024 ? 1 : d <= 4096 ? 4 : 8;
     const int groups = (M + 8 / team - 1) / (8 / team);
     if (groups < 2 * num_sms())
       while (cl < 8 && groups * cl * 2 <= 4 * num_sms() && 2 * cl <= T &&
@@ -412,7 +504,7 @@ cudaError_t launch_fmt(const void* x, const void* wuT, const void* wd, int M, in
   if (d <= 512) return TW_FWD(1, 2);
   if (d <= 1024) return TW_FWD(1, 4);
   if (d <= 2048) return TW_FWD(4, 2);
-  if (d <= 4096) return TW_FWD(8, 2);
+  if (d <= 4096) return TW_FWD(4, 4);
   return TW_FWD(8, 4);
 #undef TW_FWD
 }
@@ -421,7 +513,8 @@ cudaError_t launch_fmt(const void* x, const void* wuT, const void* wd, int M, in
 
 cudaError_t launch_sparse_fwd(const void* x, const void* wuT, const void* wd, int M, int d, int f,
                               const twell_tiles* tiles, int tile_n, int cap,
-                              const twell_hybrid* route, void* y, float* part, cudaStream_t s) {
+                              const twell_hybrid* route, void* y, float* part, float* hbuf,
+                              cudaStream_t s) {
   if (M == 0) return cudaSuccess;
   const int T = f / tile_n;
   if (route) {
@@ -429,10 +522,11 @@ cudaError_t launch_sparse_fwd(const void* x, const void* wuT, const void* wd, in
     // exceed 3/4 of L2 (partial sums in `part`, same accumulation order; on
     // the 2B-class shape, 67 MB of weights, two passes were slower than one)
     const int chunks = part ? l2_chunks(2.0 * 2.0 * (double)f * d, 0.75, 0.5) : 1;
-    return launch_fmt<true>(x, wuT, wd, M, d, f, nullptr, T, tile_n, cap, route, y, part,
+    return launch_fmt<true>(x, wuT, wd, M, d, f, nullptr, T, tile_n, cap, route, y, part, hbuf,
                             chunks, s);
   }
-  return launch_fmt<false>(x, wuT, wd, M, d, f, tiles, T, tile_n, cap, nullptr, y, nullptr, 1, s);
+  return launch_fmt<false>(x, wuT, wd, M, d, f, tiles, T, tile_n, cap, nullptr, y, nullptr,
+                           nullptr, 1, s);
 }
 
 }  // namespace tw

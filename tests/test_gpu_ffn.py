@@ -227,13 +227,13 @@ def test_small_batch_forward(M):
                  out_bf16=True)
 
 
-@pytest.mark.parametrize("M,d", [(200, 320), (200, 704), (160, 1088), (64, 4160)])
+@pytest.mark.parametrize("M,d", [(200, 320), (200, 704), (160, 1088), (96, 3136), (64, 4160)])
 def test_d_model_leaving_partial_slabs(M, d):
     """The gathers load without predicates: lanes past d_model read the row's
     first slab against a zero x / dY and their sums are never stored.  These
     d_model values leave partial slabs in the one-warp (d <= 1024), four-warp
-    (d <= 2048) and eight-warp four-slab (d > 4096) team shapes of the
-    forward, row and neuron phases."""
+    two-slab (d <= 2048), four-warp four-slab (d <= 4096) and eight-warp
+    four-slab (d > 4096) team shapes of the forward, row and neuron phases."""
     r = Run(M, d, 1024, 64, 16, density=0.02, seed=8, exact=True)
     y = r.fwd(tiles=r.pack())
     torch.cuda.synchronize()
@@ -248,4 +248,23 @@ def test_d_model_leaving_partial_slabs(M, d):
     dx, (dwg, dwu, dwd) = r.bwd(h, W)
     torch.cuda.synchronize()
     assert twell.twell_get_device_status() == 0
+    _check_step(r, y, dx, dwg, dwu, dwd, allow=False)
+
+
+@pytest.mark.parametrize("d", [1024, 2048, 3136, 4160])
+def test_many_entries_per_row_and_neuron(d):
+    """Rows and neurons with several full 32-entry chunks: the gathers take
+    their entries from a 32-lane register in batches, and a batch size that
+    does not divide 32 must not wrap around to lane 0 of the same chunk.
+    Density 0.25 over d_ff = 256 gives ~64 live entries per row and ~75 live
+    rows per neuron, in every team shape of the row and neuron phases."""
+    r = Run(300, d, 256, 64, 64, density=0.25, seed=12, exact=True)
+    t = r.pack()
+    W = _quantile_width(t, r.shape, 1.0)  # no row routed
+    h = r.route(t, W)
+    y = r.fwd(route=h, W=W)
+    dx, (dwg, dwu, dwd) = r.bwd(h, W)
+    torch.cuda.synchronize()
+    assert twell.twell_get_device_status() == 0
+    assert int(twell.hybrid_view(h, r.shape)[4].item()) == 0
     _check_step(r, y, dx, dwg, dwu, dwd, allow=False)

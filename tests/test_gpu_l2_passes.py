@@ -1,13 +1,16 @@
 """The ELL forward gather split into L2-sized neuron passes.
 
-When the gathered weight rows (Wu^T and Wd, 4 * d_ff * d_model bytes) exceed
-about 3/4 of L2, the fused up+down kernel of page 2 "Sakana AI and NVIDIA
-introduce TwELL with CUDA kernels ...", section "¿Qué hace distinto a TwELL
-frente a ELL clásico?" runs once per neuron chunk and carries y_m between
-passes in fp32.  A row's ELL columns ascend, every chunk is a contiguous slice
-of it and the per-entry arithmetic and accumulation order are unchanged, so
-the result must equal the single-pass TwELL forward bit for bit; sampled
-rows are also checked against the oracle."""
+When the gathered weight rows exceed about 3/4 of L2, the gathers of page 2
+"Sakana AI and NVIDIA introduce TwELL with CUDA kernels ...", section "¿Qué
+hace distinto a TwELL frente a ELL clásico?" run once per neuron chunk and
+carry y_m between passes in fp32.  Up to d_model = 1024 the fused up+down
+kernel gathers Wu^T and Wd rows together (4 * d_ff * d_model bytes); wider
+rows split it into an up gather (Wu^T) and a down gather (Wd), each with its
+own passes over 2 * d_ff * d_model bytes.  A row's ELL columns ascend, every
+chunk is a contiguous slice of it and the per-entry arithmetic and
+accumulation order are unchanged, so the result must equal the single-pass
+fused TwELL forward bit for bit; sampled rows are also checked against the
+oracle."""
 import math
 import os
 
@@ -23,20 +26,23 @@ from helpers import assert_close, dev_bf16, fwd_allowance, to_np
 pytestmark = pytest.mark.gpu
 
 
-def _expected_passes(d, f):
+def _expected_passes(table_bytes):
     l2 = torch.cuda.get_device_properties(0).L2_cache_size
-    gathered = 4.0 * f * d
-    return 1 if gathered <= 0.75 * l2 else math.ceil(gathered / (0.5 * l2))
+    return 1 if table_bytes <= 0.75 * l2 else math.ceil(table_bytes / (0.5 * l2))
 
 
 # M large enough that the TwELL forward runs one team per row (batches of
 # fewer than two row groups per SM split rows over clusters, which sums in
-# another order): d = 4096 has one row per group, d = 2048 two
-@pytest.mark.parametrize("rows_per_group,d,f", [(1, 4096, 8192), (2, 2048, 16384)])
+# another order): eight rows per group at d = 1024, two at d = 2048 and 4096.
+# d_ff is chosen so that the gathered table exceeds L2: the fused kernel's
+# Wu^T + Wd at d = 1024, Wu^T or Wd alone for the split gathers.
+@pytest.mark.parametrize("rows_per_group,d,f", [(8, 1024, 32768), (2, 2048, 32768),
+                                                (2, 4096, 16384)])
 def test_multi_pass_forward_matches_single_pass(rows_per_group, d, f):
     sms = torch.cuda.get_device_properties(0).multi_processor_count
     M = 2 * sms * rows_per_group + 37
-    passes = _expected_passes(d, f)
+    split = d > 1024
+    passes = _expected_passes((2.0 if split else 4.0) * f * d)
     assert passes > 1, "shape no longer exceeds L2; pick a larger one"
     w = synthetic.make_inputs(M, d, f, seed=11, with_dy=False)
     x, wg, wu, wd = (dev_bf16(w[k]) for k in ("x", "wgT", "wuT", "wd"))
@@ -52,13 +58,17 @@ def test_multi_pass_forward_matches_single_pass(rows_per_group, d, f):
     y_single = torch.empty(M, d, dtype=torch.bfloat16, device="cuda")
     twell.twell_ffn_fwd(x, wg, wu, wd, shape, y_single, tiles=tiles)
     y_multi = torch.full((M, d), float("nan"), dtype=torch.bfloat16, device="cuda")
-    twell.twell_profile_begin("sparse_fwd")
+    twell.twell_profile_begin("*")
     twell.twell_ffn_fwd(x, wg, wu, wd, shape, y_multi, route=route, ws=ws)
     torch.cuda.synchronize()
     prof = twell.twell_profile_end()
     assert twell.twell_get_device_status() == 0
     assert int(twell.hybrid_view(route, shape)[4].item()) == 0
-    assert prof["sparse_fwd"][0] == passes
+    families = ("sparse_fwd_up", "sparse_fwd_down") if split else ("sparse_fwd",)
+    for fam in families:
+        assert prof[fam][0] == passes, (fam, prof)
+    if split:
+        assert "sparse_fwd" not in prof
     # same bytes: entries in the same order, fp32 carried exactly between passes
     assert torch.equal(y_multi.view(torch.int16), y_single.view(torch.int16))
     rows = np.array([0, 1, M // 2, M - 1], dtype=np.int64)
@@ -70,17 +80,27 @@ def test_multi_pass_forward_matches_single_pass(rows_per_group, d, f):
     assert_close(to_np(y_multi)[rows], ref, "y", out_bf16=True, allowance=fwd_allowance(w, rows))
 
 
-def test_multi_pass_backward_rows():
-    """dX over ELL rows in L2-sized passes (Wd, Wu^T, Wg^T rows exceed L2):
-    sampled rows of dX and sampled neurons of the weight gradients against
-    the oracle, and the pass count seen by the profiler."""
+def _chunks(table_bytes, fit, chunk):
+    l2 = torch.cuda.get_device_properties(0).L2_cache_size
+    return 1 if table_bytes <= fit * l2 else math.ceil(table_bytes / (chunk * l2))
+
+
+@pytest.mark.parametrize("d,f", [(1024, 16384), (4096, 16384)])
+def test_multi_pass_backward_rows(d, f):
+    """dX over ELL rows in L2-sized passes: sampled rows of dX and sampled
+    neurons of the weight gradients against the oracle, and the pass counts
+    seen by the profiler.  Up to d_model = 1024 the fused row kernel gathers
+    Wd, Wu^T and Wg^T together; wider rows split it into dh (Wd), u and the
+    gradients (Wu^T) and dX (Wu^T and Wg^T), each with its own passes."""
     from helpers import bwd_allowance_sampled
 
-    M, d, f, lam = 256, 4096, 8192, 2e-5
-    l2 = torch.cuda.get_device_properties(0).L2_cache_size
-    gathered = 6.0 * f * d
-    passes = 1 if gathered <= 0.5 * l2 else math.ceil(gathered / (0.65 * l2))
-    assert passes > 1, "shape no longer exceeds L2; pick a larger one"
+    M, lam = 256, 2e-5
+    if d <= 1024:
+        expect = {"bwd_rows": _chunks(6.0 * f * d, 0.5, 0.65)}
+    else:
+        dots = _chunks(2.0 * f * d, 0.75, 0.5)
+        expect = {"bwd_dh": dots, "bwd_grad": dots, "bwd_dx": _chunks(4.0 * f * d, 0.75, 0.5)}
+    assert min(expect.values()) > 1, "shape no longer exceeds L2; pick a larger one"
     w = synthetic.make_inputs(M, d, f, seed=12)
     x, wg, wu, wd, dy = (dev_bf16(w[k]) for k in ("x", "wgT", "wuT", "wd", "dy"))
     shape = twell.make_shape(M, d, f, 128, 32)
@@ -93,12 +113,13 @@ def test_multi_pass_backward_rows():
                      device="cuda")
     dx = torch.full((M, d), float("nan"), dtype=torch.bfloat16, device="cuda")
     dws = [torch.full((f, d), float("nan"), device="cuda") for _ in range(3)]
-    twell.twell_profile_begin("bwd_rows")
+    twell.twell_profile_begin("*")
     twell.twell_ffn_bwd(x, wg, wu, wd, dy, shape, route, lam, dx, *dws, ws)
     torch.cuda.synchronize()
     prof = twell.twell_profile_end()
     assert twell.twell_get_device_status() == 0
-    assert prof["bwd_rows"][0] == passes
+    for fam, n in expect.items():
+        assert prof[fam][0] == n, (fam, prof)
     rows = np.array([0, 7, M // 2, M - 1], dtype=np.int64)
     neurons = np.array([0, 5, f // 3, f - 1], dtype=np.int64)
     oracle.set_threads(os.cpu_count() or 1)
