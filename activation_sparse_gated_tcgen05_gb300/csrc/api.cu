@@ -84,17 +84,21 @@ int num_sms() {
   return cache[dev];
 }
 
-int l2_chunks(double gathered_bytes, double fit, double chunk) {
+double l2_bytes() {
   static int cache[kMaxDevices] = {0};
   const int dev = current_device();
-  if (dev < 0 || dev >= kMaxDevices) return 1;
+  if (dev < 0 || dev >= kMaxDevices) return 0.0;
   if (cache[dev] == 0) {
     int n = 0;
-    if (cudaDeviceGetAttribute(&n, cudaDevAttrL2CacheSize, dev) != cudaSuccess || n <= 0) return 1;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrL2CacheSize, dev) != cudaSuccess || n <= 0) return 0.0;
     cache[dev] = n;
   }
-  const double l2 = (double)cache[dev];
-  if (gathered_bytes <= fit * l2) return 1;
+  return (double)cache[dev];
+}
+
+int l2_chunks(double gathered_bytes, double fit, double chunk) {
+  const double l2 = l2_bytes();
+  if (l2 <= 0.0 || gathered_bytes <= fit * l2) return 1;
   return (int)std::ceil(gathered_bytes / (chunk * l2));
 }
 

@@ -38,6 +38,8 @@ enum GemmKind {
 };
 
 int num_sms();
+// L2 size of the current device in bytes (0 if unknown).
+double l2_bytes();
 // Passes over the neuron axis for a gather whose weight rows total
 // `gathered_bytes`: 1 while they fit in the fraction `fit` of L2, else
 // enough chunks of at most the fraction `chunk` of L2 each.

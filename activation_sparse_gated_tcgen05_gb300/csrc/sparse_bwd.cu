@@ -318,23 +318,32 @@ __global__ void __launch_bounds__(256, MINB)
 // ---------------------------------------------------------------- neuron phase
 // One team per neuron; each warp owns VPL slabs of d_model and needs no
 // cross-warp communication, so narrow slabs (VPL = 1) buy occupancy and
-// more gathered rows in flight per SM.
-template <int TEAM, int VPL, int B, int MINB>
+// more gathered rows in flight per SM.  PARTS selects the outputs: kNeuD
+// gathers dY rows for dWd, kNeuX gathers x rows for dWu^T and dWg^T, and
+// kNeuD | kNeuX does both in one pass.  Each output element sums its
+// entries in ascending row order either way.
+constexpr int kNeuD = 1, kNeuX = 2;
+
+template <int TEAM, int VPL, int B, int MINB, int PARTS>
 __global__ void __launch_bounds__(256, MINB)
     bwd_neurons_kernel(const uint16_t* __restrict__ x, const uint16_t* __restrict__ dy, int d,
                        int f, const int* __restrict__ csc_ptr, const int* __restrict__ csc_row,
                        const float4* __restrict__ csc_vals, float* __restrict__ dwgT,
                        float* __restrict__ dwuT, float* __restrict__ dwd) {
+  constexpr bool DO_D = PARTS & kNeuD, DO_X = PARTS & kNeuX;
   constexpr int ROWS = 8 / TEAM;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int team = warp / TEAM, wt = warp % TEAM;
   const int j = blockIdx.x * ROWS + team;
   if (j >= f) return;
-  uint64_t ad[VPL][4], au[VPL][4], ag[VPL][4];
+  uint64_t ad[DO_D ? VPL : 1][4], au[DO_X ? VPL : 1][4], ag[DO_X ? VPL : 1][4];
 #pragma unroll
   for (int v = 0; v < VPL; ++v)
 #pragma unroll
-    for (int k = 0; k < 4; ++k) ad[v][k] = au[v][k] = ag[v][k] = 0;
+    for (int k = 0; k < 4; ++k) {
+      if constexpr (DO_D) ad[v][k] = 0;
+      if constexpr (DO_X) au[v][k] = ag[v][k] = 0;
+    }
 
   int eoff[VPL];  // slab offsets, lanes past d_model read the first slab
 #pragma unroll
@@ -361,36 +370,40 @@ __global__ void __launch_bounds__(256, MINB)
         const bool in = 32 % B == 0 || i + b < 32;
         const int src = (i + b) & 31;
         m[b] = __shfl_sync(kFull, ml, src);
-        du[b] = __shfl_sync(kFull, vl.x, src);
-        da[b] = __shfl_sync(kFull, vl.y, src);
-        h[b] = __shfl_sync(kFull, vl.z, src);
+        if constexpr (DO_X) {
+          du[b] = __shfl_sync(kFull, vl.x, src);
+          da[b] = __shfl_sync(kFull, vl.y, src);
+        }
+        if constexpr (DO_D) h[b] = __shfl_sync(kFull, vl.z, src);
         if (!in) {
           m[b] = 0;
           du[b] = da[b] = h[b] = 0.f;
         }
       }
-      uint4 xv[B][VPL], dyv[B][VPL];
+      uint4 xv[DO_X ? B : 1][VPL], dyv[DO_D ? B : 1][VPL];
 #pragma unroll
       for (int b = 0; b < B; ++b) {
         const long long row = (long long)m[b] * d;
 #pragma unroll
         for (int v = 0; v < VPL; ++v) {
-          xv[b][v] = ldg_v4(x + row + eoff[v]);
-          dyv[b][v] = ldg_v4(dy + row + eoff[v]);
+          if constexpr (DO_X) xv[b][v] = ldg_v4(x + row + eoff[v]);
+          if constexpr (DO_D) dyv[b][v] = ldg_v4(dy + row + eoff[v]);
         }
       }
 #pragma unroll
       for (int b = 0; b < B; ++b) {
-        const uint64_t h2 = f2_splat(h[b]), du2 = f2_splat(du[b]), da2 = f2_splat(da[b]);
 #pragma unroll
         for (int v = 0; v < VPL; ++v) {
-          uint64_t xf[4];
-          bf8_to_f2(xv[b][v], xf);
-          axpy8_f2(h2, dyv[b][v], ad[v]);
+          if constexpr (DO_D) axpy8_f2(f2_splat(h[b]), dyv[b][v], ad[v]);
+          if constexpr (DO_X) {
+            const uint64_t du2 = f2_splat(du[b]), da2 = f2_splat(da[b]);
+            uint64_t xf[4];
+            bf8_to_f2(xv[b][v], xf);
 #pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            au[v][k] = f2_fma(du2, xf[k], au[v][k]);
-            ag[v][k] = f2_fma(da2, xf[k], ag[v][k]);
+            for (int k = 0; k < 4; ++k) {
+              au[v][k] = f2_fma(du2, xf[k], au[v][k]);
+              ag[v][k] = f2_fma(da2, xf[k], ag[v][k]);
+            }
           }
         }
       }
@@ -405,15 +418,19 @@ __global__ void __launch_bounds__(256, MINB)
     if (e < d) {
 #pragma unroll
       for (int q = 0; q < 2; ++q) {
-        const uint64_t d0 = ad[v][2 * q], d1 = ad[v][2 * q + 1];
-        const uint64_t u0 = au[v][2 * q], u1 = au[v][2 * q + 1];
-        const uint64_t g0 = ag[v][2 * q], g1 = ag[v][2 * q + 1];
-        st_v4_hint(dwd + row + e + 4 * q,
-                   make_uint4((uint32_t)d0, (uint32_t)(d0 >> 32), (uint32_t)d1, (uint32_t)(d1 >> 32)), pol);
-        st_v4_hint(dwuT + row + e + 4 * q,
-                   make_uint4((uint32_t)u0, (uint32_t)(u0 >> 32), (uint32_t)u1, (uint32_t)(u1 >> 32)), pol);
-        st_v4_hint(dwgT + row + e + 4 * q,
-                   make_uint4((uint32_t)g0, (uint32_t)(g0 >> 32), (uint32_t)g1, (uint32_t)(g1 >> 32)), pol);
+        if constexpr (DO_D) {
+          const uint64_t d0 = ad[v][2 * q], d1 = ad[v][2 * q + 1];
+          st_v4_hint(dwd + row + e + 4 * q,
+                     make_uint4((uint32_t)d0, (uint32_t)(d0 >> 32), (uint32_t)d1, (uint32_t)(d1 >> 32)), pol);
+        }
+        if constexpr (DO_X) {
+          const uint64_t u0 = au[v][2 * q], u1 = au[v][2 * q + 1];
+          const uint64_t g0 = ag[v][2 * q], g1 = ag[v][2 * q + 1];
+          st_v4_hint(dwuT + row + e + 4 * q,
+                     make_uint4((uint32_t)u0, (uint32_t)(u0 >> 32), (uint32_t)u1, (uint32_t)(u1 >> 32)), pol);
+          st_v4_hint(dwgT + row + e + 4 * q,
+                     make_uint4((uint32_t)g0, (uint32_t)(g0 >> 32), (uint32_t)g1, (uint32_t)(g1 >> 32)), pol);
+        }
       }
     }
   }
@@ -444,14 +461,14 @@ cudaError_t rows_team(const void* x, const void* dy, const void* wgT, const void
   return cudaSuccess;
 }
 
-template <int TEAM, int VPL, int B, int MINB>
+template <int TEAM, int VPL, int B, int MINB, int PARTS>
 cudaError_t neurons_team(const void* x, const void* dy, int d, int f, const int* csc_ptr,
                          const int* csc_row, const float4* csc_vals, float* dwgT, float* dwuT,
                          float* dwd, cudaStream_t s) {
   constexpr int ROWS = 8 / TEAM;
   {
-    ProfScope prof("bwd_neurons", s);
-    bwd_neurons_kernel<TEAM, VPL, B, MINB><<<(f + ROWS - 1) / ROWS, 256, 0, s>>>(
+    ProfScope prof(PARTS == kNeuD ? "bwd_neurons_dy" : PARTS == kNeuX ? "bwd_neurons_x" : "bwd_neurons", s);
+    bwd_neurons_kernel<TEAM, VPL, B, MINB, PARTS><<<(f + ROWS - 1) / ROWS, 256, 0, s>>>(
         reinterpret_cast<const uint16_t*>(x), reinterpret_cast<const uint16_t*>(dy), d, f,
         csc_ptr, csc_row, csc_vals, dwgT, dwuT, dwd);
   }
@@ -626,19 +643,39 @@ cudaError_t launch_sparse_bwd_neurons(const void* x, const void* dy, int M, int 
                                       const int* csc_ptr, const int* csc_row,
                                       const float4* csc_vals, float* dwgT, float* dwuT, float* dwd,
                                       cudaStream_t s) {
-  (void)M;
   if (f == 0) return cudaSuccess;
-#define TW_NEU(T, V, B, MINB) \
-  neurons_team<T, V, B, MINB>(x, dy, d, f, csc_ptr, csc_row, csc_vals, dwgT, dwuT, dwd, s)
+#define TW_NEU(T, V, B, MINB, P) \
+  neurons_team<T, V, B, MINB, P>(x, dy, d, f, csc_ptr, csc_row, csc_vals, dwgT, dwuT, dwd, s)
+  // Once x and dY together outgrow L2 the phase runs twice, over dY rows
+  // (dWd) and over x rows (dWu^T, dWg^T): each pass gathers from a table half
+  // the size, so more of its rows hit in L2.
+  if (4.0 * (double)M * d > 0.75 * l2_bytes()) {
+    cudaError_t e;
+    if (d <= 1024) {
+      if ((e = TW_NEU(4, 1, 4, 4, kNeuD)) != cudaSuccess) return e;
+      return TW_NEU(4, 1, 4, 4, kNeuX);
+    }
+    if (d <= 2048) {
+      if ((e = TW_NEU(8, 1, 4, 4, kNeuD)) != cudaSuccess) return e;
+      return TW_NEU(8, 1, 4, 3, kNeuX);
+    }
+    if (d <= 4096) {
+      if ((e = TW_NEU(8, 2, 4, 3, kNeuD)) != cudaSuccess) return e;
+      return TW_NEU(8, 2, 4, 3, kNeuX);
+    }
+    if ((e = TW_NEU(8, 4, 2, 2, kNeuD)) != cudaSuccess) return e;
+    return TW_NEU(8, 4, 2, 2, kNeuX);
+  }
   // one 256-element slab per warp (short accumulators, 3-4 blocks per SM)
   // while a block's 8 warps cover d_model; at d = 4096 batches of three rows
   // (6 % faster than two on the 8B-class shape)
-  if (d <= 256) return TW_NEU(1, 1, 2, 4);
-  if (d <= 512) return TW_NEU(2, 1, 2, 4);
-  if (d <= 1024) return TW_NEU(4, 1, 2, 4);
-  if (d <= 2048) return TW_NEU(8, 1, 4, 3);
-  if (d <= 4096) return TW_NEU(8, 2, 3, 2);
-  return TW_NEU(8, 4, 2, 1);
+  constexpr int kBoth = kNeuD | kNeuX;
+  if (d <= 256) return TW_NEU(1, 1, 2, 4, kBoth);
+  if (d <= 512) return TW_NEU(2, 1, 2, 4, kBoth);
+  if (d <= 1024) return TW_NEU(4, 1, 2, 4, kBoth);
+  if (d <= 2048) return TW_NEU(8, 1, 4, 3, kBoth);
+  if (d <= 4096) return TW_NEU(8, 2, 3, 2, kBoth);
+  return TW_NEU(8, 4, 2, 1, kBoth);
 #undef TW_NEU
 }
 

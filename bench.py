@@ -240,6 +240,10 @@ def algorithmic_work(family, wl, nnz_ell, n_dense):
         return 4.0 * d * nnz_ell + 2.0 * d * M + 10.0 * nnz_ell, "byte", "hbm"
     if family == "bwd_neurons":  # x and dy rows per entry + three fp32 dW rows per neuron
         return 4.0 * d * nnz_ell + 12.0 * f * d + 20.0 * nnz_ell, "byte", "hbm"
+    if family == "bwd_neurons_dy":  # dy rows per entry + the fp32 dWd row per neuron
+        return 2.0 * d * nnz_ell + 4.0 * f * d + 20.0 * nnz_ell, "byte", "hbm"
+    if family == "bwd_neurons_x":  # x rows per entry + the fp32 dWu^T, dWg^T rows per neuron
+        return 2.0 * d * nnz_ell + 8.0 * f * d + 20.0 * nnz_ell, "byte", "hbm"
     return None
 
 

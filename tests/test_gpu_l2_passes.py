@@ -134,3 +134,46 @@ def test_multi_pass_backward_rows(d, f):
     assert_close(dws[0].cpu().numpy()[neurons], og, "dwgT", allowance=al["dwgT"])
     assert_close(dws[1].cpu().numpy()[neurons], ou, "dwuT", allowance=al["dwuT"])
     assert_close(dws[2].cpu().numpy()[neurons], od, "dwd", allowance=al["dwd"])
+
+
+def test_neuron_phase_split_when_x_and_dy_exceed_l2():
+    """Once x and dY together outgrow 3/4 of L2 the neuron phase runs twice,
+    over dY rows for dWd and over x rows for dWu^T and dWg^T; sampled neurons
+    against the oracle and the two launches seen by the profiler."""
+    from helpers import bwd_allowance_sampled
+
+    l2 = torch.cuda.get_device_properties(0).L2_cache_size
+    d, f, lam = 4096, 2048, 2e-5
+    M = int(math.ceil(0.75 * l2 / (4 * d) / 128.0)) * 128 + 128
+    assert 4.0 * M * d > 0.75 * l2
+    w = synthetic.make_inputs(M, d, f, density=0.01, seed=13)
+    x, wg, wu, wd, dy = (dev_bf16(w[k]) for k in ("x", "wgT", "wuT", "wd", "dy"))
+    shape = twell.make_shape(M, d, f, 128, 32)
+    tiles = twell.alloc_tiles(shape)
+    twell.twell_pack(x, wg, shape, tiles)
+    W = int(twell.tiles_view(tiles, shape)[3].max().item())
+    route = twell.alloc_hybrid(shape, W)
+    twell.hybrid_route(tiles, shape, route)
+    ws = torch.empty(twell.twell_workspace_bytes(shape, W, True), dtype=torch.uint8,
+                     device="cuda")
+    dx = torch.empty((M, d), dtype=torch.bfloat16, device="cuda")
+    dws = [torch.full((f, d), float("nan"), device="cuda") for _ in range(3)]
+    twell.twell_profile_begin("*")
+    twell.twell_ffn_bwd(x, wg, wu, wd, dy, shape, route, lam, dx, *dws, ws)
+    torch.cuda.synchronize()
+    prof = twell.twell_profile_end()
+    assert twell.twell_get_device_status() == 0
+    assert prof["bwd_neurons_dy"][0] == 1 and prof["bwd_neurons_x"][0] == 1, prof
+    assert "bwd_neurons" not in prof
+    rows = np.array([0, M - 1], dtype=np.int64)
+    neurons = np.array([0, 7, f // 2, f - 1], dtype=np.int64)
+    oracle.set_threads(os.cpu_count() or 1)
+    try:
+        al = bwd_allowance_sampled(w, lam, rows, neurons)
+        og, ou, od = oracle.ffn_bwd_dw_neurons(w["x"], w["wgT"], w["wuT"], w["wd"], w["dy"], lam,
+                                               neurons)
+    finally:
+        oracle.set_threads(1)
+    assert_close(dws[0].cpu().numpy()[neurons], og, "dwgT", allowance=al["dwgT"])
+    assert_close(dws[1].cpu().numpy()[neurons], ou, "dwuT", allowance=al["dwuT"])
+    assert_close(dws[2].cpu().numpy()[neurons], od, "dwd", allowance=al["dwd"])
