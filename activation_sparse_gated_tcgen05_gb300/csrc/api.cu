@@ -225,6 +225,25 @@ SparseWs carve_sparse(void* ws, const twell_shape& s, int W, int training) {
   return w;
 }
 
+// Optional workspace of the TwELL (inference) forward for rows wider than
+// 1024, where it runs as two gathers:
+//   hbuf [M][T][C] fp32: h of every TwELL slot
+//   part [M][d] fp32: y carried between L2-sized neuron passes
+struct TilesWs {
+  float *hbuf, *part;
+  size_t bytes;
+};
+
+TilesWs carve_tiles(void* ws, const twell_shape& s) {
+  TilesWs w{};
+  if (s.d_model <= 1024) return w;
+  Carve c(ws);
+  w.hbuf = c.take<float>((long long)s.M * (s.d_ff / s.tile_n) * s.tile_cap);
+  w.part = c.take<float>((long long)s.M * s.d_model);
+  w.bytes = c.off + 256;
+  return w;
+}
+
 struct DenseWs {
   uint16_t *h, *g, *u, *dd;
   size_t bytes;
@@ -551,6 +570,11 @@ size_t twell_workspace_bytes(const twell_shape* shape, int32_t ell_width, int32_
   return carve_sparse(nullptr, *shape, ell_width, training ? 1 : 0).bytes;
 }
 
+size_t twell_tiles_workspace_bytes(const twell_shape* shape) {
+  if (check_shape(shape, true) != TWELL_OK) return 0;
+  return carve_tiles(nullptr, *shape).bytes;
+}
+
 twell_status twell_ffn_fwd(const void* x, const void* wgT, const void* wuT, const void* wd,
                            const twell_shape* shape, const twell_tiles* tiles,
                            const twell_hybrid* route, void* y, void* ws, size_t ws_bytes,
@@ -563,9 +587,15 @@ twell_status twell_ffn_fwd(const void* x, const void* wgT, const void* wuT, cons
   cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
   if (tiles) {
     if ((st = check_tiles(tiles)) != TWELL_OK) return st;
+    TilesWs w{};
+    if (ws && s.d_model > 1024) {  // wide rows: the split gathers, h in the workspace
+      if (ws_bytes < carve_tiles(nullptr, s).bytes) return TWELL_ERR_WORKSPACE;
+      if (!aligned16(ws)) return TWELL_ERR_ALIGNMENT;
+      w = carve_tiles(ws, s);
+    }
     if (s.M == 0) return TWELL_OK;
     return cuda_status(launch_sparse_fwd(x, wuT, wd, s.M, s.d_model, s.d_ff, tiles, s.tile_n,
-                                         s.tile_cap, nullptr, y, nullptr, nullptr, cs));
+                                         s.tile_cap, nullptr, y, w.part, w.hbuf, cs));
   }
   if ((st = check_route(route)) != TWELL_OK) return st;
   if ((st = check_ptrs({wgT})) != TWELL_OK) return st;

@@ -30,7 +30,9 @@
 // those of the fused kernels, so results are bit-identical to them.  Each
 // kernel gathers one or two weight matrices (a smaller table than the fused
 // kernel's, so fewer L2-sized passes), and neither waits at a barrier per
-// batch.
+// batch.  Entries come from an entry source: the ELL rows of the training
+// path (EllSrc) or the TwELL tiles of the inference path (TwellSrc); the
+// per-entry buffers are indexed like the source's value array.
 #pragma once
 
 #include "common.cuh"
@@ -65,15 +67,73 @@ __device__ __forceinline__ void ell_slice(const uint16_t* __restrict__ ell_col, 
   }
 }
 
+// Entry sources.  for_groups(m, lane, f) visits row m's live entries in
+// ascending column order, 32 at a time: f(count, j, slot) with lane i < count
+// holding entry i's column j and slot (the index of its value in the
+// source's bf16 value array); lanes >= count hold j = 0.
+struct EllSrc {
+  const uint16_t* val;  // [M][W] bf16 gate values
+  const uint16_t* col;  // [M][W] columns, ascending in a row
+  const int* nnz;       // [M]
+  int W;
+  int j_lo, j_hi, whole;  // neuron chunk [j_lo, j_hi); whole: every entry
+  template <class F>
+  __device__ __forceinline__ void for_groups(int m, int lane, F&& f) const {
+    const long long row_off = (long long)m * W;
+    int a, b;
+    ell_slice(col, row_off, nnz[m], j_lo, j_hi, whole, lane, a, b);
+    for (int e0 = a; e0 < b; e0 += 32) {
+      const int count = min(32, b - e0);
+      const long long s = row_off + e0 + lane;
+      f(count, lane < count ? (int)col[s] : 0, s);
+    }
+  }
+};
+
+struct TwellSrc {
+  const uint16_t* val;  // [M][T][C] bf16 gate values
+  const uint8_t* idx;   // [M][T][C] column inside the tile
+  const uint8_t* cnt;   // [M][T] live count (only the first C are stored)
+  int T, tile_n, cap;
+  int t_lo, t_hi;       // tile chunk: neurons [t_lo tile_n, t_hi tile_n)
+  int* status;          // non-null: a tile with cnt > C sets TWELL_ERR_CAPACITY
+  template <class F>
+  __device__ __forceinline__ void for_groups(int m, int lane, F&& f) const {
+    for (int t0 = t_lo; t0 < t_hi; t0 += 32) {
+      const int t = t0 + lane;
+      const int craw = t < t_hi ? cnt[(long long)m * T + t] : 0;
+      if (status && craw > cap) set_status(status, TWELL_ERR_CAPACITY);
+      const int ct = min(craw, cap);
+      const int incl = warp_incl_scan(ct);
+      const int excl = incl - ct;
+      const int total = __shfl_sync(0xffffffffu, incl, 31);
+      for (int e0 = 0; e0 < total; e0 += 32) {
+        const int e = e0 + lane;
+        int lo = 0;  // owner lane: number of lanes whose inclusive count is <= e
+#pragma unroll
+        for (int step = 16; step >= 1; step >>= 1) {
+          const int v = __shfl_sync(0xffffffffu, incl, lo + step - 1);
+          if (v <= e) lo += step;
+        }
+        const int ex = __shfl_sync(0xffffffffu, excl, lo);
+        int jl = 0;
+        long long sl = 0;
+        if (e < total) {
+          const int tt = t0 + lo;
+          sl = ((long long)m * T + tt) * cap + (e - ex);
+          jl = tt * tile_n + idx[sl];
+        }
+        f(min(32, total - e0), jl, sl);
+      }
+    }
+  }
+};
+
 struct EllDotArgs {
   const uint16_t* vec;   // [M][d] row vectors (x or dY)
   const uint16_t* rows;  // [f][d] gathered weight rows (Wu^T or Wd)
-  int M, d, W;
-  const uint16_t* ell_val;
-  const uint16_t* ell_col;
-  const int* ell_nnz;
-  int j_lo, j_hi, whole;
-  float* out;            // kDotH: h, kDotDh: dh  ([M][W] per slot)
+  int M, d;
+  float* out;            // kDotH: h, kDotDh: dh  (per slot of the source)
   const float* dh;       // kDotGrad: dh per slot
   const int* slot_pos;   // kDotGrad: neuron-major position of each slot
   float lambda;          // kDotGrad: L1 coefficient
@@ -81,8 +141,8 @@ struct EllDotArgs {
   float2* coef;          // kDotGrad: (du, da) per slot, for the dX gather
 };
 
-template <int TEAM, int VPL, int B, int MINB, int MODE>
-__global__ void __launch_bounds__(256, MINB) ell_dot_kernel(const EllDotArgs p) {
+template <int TEAM, int VPL, int B, int MINB, int MODE, class Src>
+__global__ void __launch_bounds__(256, MINB) ell_dot_kernel(const EllDotArgs p, const Src src) {
   static_assert(B % 2 == 0 && 32 % B == 0, "entries are summed over the warp in pairs");
   constexpr int ROWS = 8 / TEAM;
   __shared__ float red[2][ROWS][TEAM][32];
@@ -101,15 +161,9 @@ __global__ void __launch_bounds__(256, MINB) ell_dot_kernel(const EllDotArgs p) 
     eoff[v] = e < d ? e : 0;
     vv[v] = e < d ? ldg_v4_hint(p.vec + (long long)m * d + e, pol) : make_uint4(0, 0, 0, 0);
   }
-  const long long row_off = (long long)m * p.W;
-  int a, bnd;
-  ell_slice(p.ell_col, row_off, p.ell_nnz[m], p.j_lo, p.j_hi, p.whole, lane, a, bnd);
   int buf = 0;
-  for (int e0 = a; e0 < bnd; e0 += 32) {
-    const int count = min(32, bnd - e0);
-    const long long s = row_off + e0 + lane;
-    const int jl = lane < count ? (int)p.ell_col[s] : 0;  // slots past the slice: neuron 0
-    float mine = 0.f;  // the warp's partial dot product of entry e0 + lane
+  src.for_groups(m, lane, [&](int count, int jl, long long s) {
+    float mine = 0.f;  // the warp's partial dot product of entry lane
     for (int i = 0; i < count; i += B) {
       int j[B];
 #pragma unroll
@@ -142,11 +196,11 @@ __global__ void __launch_bounds__(256, MINB) ell_dot_kernel(const EllDotArgs p) 
       for (int w = 0; w < TEAM; ++w) dot += red[buf][team][w][lane];
       buf ^= 1;
     }
-    if (wt != 0 || lane >= count) continue;
+    if (wt != 0 || lane >= count) return;
     if constexpr (MODE == kDotDh) {
       p.out[s] = dot;
     } else {
-      const float g = bf16_bits_to_float(p.ell_val[s]);
+      const float g = bf16_bits_to_float(src.val[s]);
       if constexpr (MODE == kDotH) {
         p.out[s] = g * dot;
       } else {  // ReLU'(a) = 1 on a live entry
@@ -156,23 +210,21 @@ __global__ void __launch_bounds__(256, MINB) ell_dot_kernel(const EllDotArgs p) 
         p.coef[s] = make_float2(du, da);
       }
     }
-  }
+  });
 }
 
 struct EllAxpyArgs {
   const uint16_t* rows0;  // [f][d] weight rows scaled by the first coefficient
   const uint16_t* rows1;  // second matrix (NR = 2), scaled by the second
-  int M, d, W;
-  const uint16_t* ell_col;
-  const int* ell_nnz;
+  int M, d;
   const void* coef;       // per slot: float (NR = 1) or float2 (NR = 2)
-  int j_lo, j_hi, pass;
+  int pass;               // kEllPassFirst: start from 0, kEllPassLast: store out
   float* part;            // [M][d] fp32 carry between neuron passes
   uint16_t* out;          // [M][d] bf16 result
 };
 
-template <int VPL, int B, int MINB, int NR>
-__global__ void __launch_bounds__(256, MINB) ell_axpy_kernel(const EllAxpyArgs p) {
+template <int VPL, int B, int MINB, int NR, class Src>
+__global__ void __launch_bounds__(256, MINB) ell_axpy_kernel(const EllAxpyArgs p, const Src src) {
   static_assert(32 % B == 0, "a batch never reaches past lane 31");
   static_assert(NR == 1 || NR == 2, "one or two gathered matrices");
   const int lane = threadIdx.x & 31;
@@ -202,16 +254,9 @@ __global__ void __launch_bounds__(256, MINB) ell_axpy_kernel(const EllAxpyArgs p
       acc[v][3] = f2_make(q1.z, q1.w);
     }
   }
-  const long long row_off = (long long)m * p.W;
-  int a, bnd;
-  ell_slice(p.ell_col, row_off, p.ell_nnz[m], p.j_lo, p.j_hi, first && last, lane, a, bnd);
-  for (int e0 = a; e0 < bnd; e0 += 32) {
-    const int count = min(32, bnd - e0);
-    const long long s = row_off + e0 + lane;
-    int jl = 0;  // slots past the slice: neuron 0 with zero coefficients
-    float c0 = 0.f, c1 = 0.f;
+  src.for_groups(m, lane, [&](int count, int jl, long long s) {
+    float c0 = 0.f, c1 = 0.f;  // slots past the group: neuron 0 with zero coefficients
     if (lane < count) {
-      jl = p.ell_col[s];
       if constexpr (NR == 1) {
         c0 = reinterpret_cast<const float*>(p.coef)[s];
       } else {
@@ -251,7 +296,7 @@ __global__ void __launch_bounds__(256, MINB) ell_axpy_kernel(const EllAxpyArgs p
         }
       }
     }
-  }
+  });
 #pragma unroll
   for (int v = 0; v < VPL; ++v) {
     const int e = 8 * lane + 256 * (sg * VPL + v);

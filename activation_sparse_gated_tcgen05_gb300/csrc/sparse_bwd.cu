@@ -542,37 +542,35 @@ cudaError_t split_rows(const void* x, const void* dy, const void* wgT, const voi
   EllDotArgs p{};
   p.M = M;
   p.d = d;
-  p.W = r.ell_width;
-  p.ell_val = reinterpret_cast<const uint16_t*>(r.ell_val);
-  p.ell_col = r.ell_col;
-  p.ell_nnz = r.ell_nnz;
   p.slot_pos = slot_pos;
   p.lambda = lambda;
   p.csc_vals = csc_vals;
   p.coef = coef;
   p.dh = dhbuf;
   p.out = dhbuf;
+  EllSrc src{reinterpret_cast<const uint16_t*>(r.ell_val), r.ell_col, r.ell_nnz, r.ell_width, 0,
+             f, 1};
   const int dot_chunks = part ? l2_chunks(2.0 * (double)f * d, 0.75, 0.5) : 1;
-  p.whole = dot_chunks == 1;
   for (int phase = 0; phase < 2; ++phase) {
     p.vec = reinterpret_cast<const uint16_t*>(phase == 0 ? dy : x);
     p.rows = reinterpret_cast<const uint16_t*>(phase == 0 ? wd : wuT);
     for (int c = 0; c < dot_chunks; ++c) {
-      p.j_lo = (int)((long long)f * c / dot_chunks);
-      p.j_hi = (int)((long long)f * (c + 1) / dot_chunks);
+      src.j_lo = (int)((long long)f * c / dot_chunks);
+      src.j_hi = (int)((long long)f * (c + 1) / dot_chunks);
+      src.whole = dot_chunks == 1;
       {
         ProfScope prof(phase == 0 ? "bwd_dh" : "bwd_grad", s);
         // two-slab warps take four entries per batch, four-slab warps two
         if (phase == 0) {
           if constexpr (VPL <= 2)
-            ell_dot_kernel<TEAM, VPL, 4, 2, kDotDh><<<grid, 256, 0, s>>>(p);
+            ell_dot_kernel<TEAM, VPL, 4, 2, kDotDh><<<grid, 256, 0, s>>>(p, src);
           else
-            ell_dot_kernel<TEAM, VPL, 2, 3, kDotDh><<<grid, 256, 0, s>>>(p);
+            ell_dot_kernel<TEAM, VPL, 2, 3, kDotDh><<<grid, 256, 0, s>>>(p, src);
         } else {
           if constexpr (VPL <= 2)
-            ell_dot_kernel<TEAM, VPL, 4, 2, kDotGrad><<<grid, 256, 0, s>>>(p);
+            ell_dot_kernel<TEAM, VPL, 4, 2, kDotGrad><<<grid, 256, 0, s>>>(p, src);
           else
-            ell_dot_kernel<TEAM, VPL, 2, 3, kDotGrad><<<grid, 256, 0, s>>>(p);
+            ell_dot_kernel<TEAM, VPL, 2, 3, kDotGrad><<<grid, 256, 0, s>>>(p, src);
         }
       }
       count_launch();
@@ -586,9 +584,6 @@ cudaError_t split_rows(const void* x, const void* dy, const void* wgT, const voi
   a.rows1 = reinterpret_cast<const uint16_t*>(wgT);
   a.M = M;
   a.d = d;
-  a.W = r.ell_width;
-  a.ell_col = r.ell_col;
-  a.ell_nnz = r.ell_nnz;
   a.coef = coef;
   a.part = part;
   a.out = reinterpret_cast<uint16_t*>(dx);
@@ -596,12 +591,13 @@ cudaError_t split_rows(const void* x, const void* dy, const void* wgT, const voi
   const int wpr = (d + 256 * DV - 1) / (256 * DV);
   const unsigned blocks = (unsigned)(((long long)M * wpr + 7) / 8);
   for (int c = 0; c < dx_chunks; ++c) {
-    a.j_lo = (int)((long long)f * c / dx_chunks);
-    a.j_hi = (int)((long long)f * (c + 1) / dx_chunks);
+    src.j_lo = (int)((long long)f * c / dx_chunks);
+    src.j_hi = (int)((long long)f * (c + 1) / dx_chunks);
+    src.whole = dx_chunks == 1;
     a.pass = (c == 0 ? kEllPassFirst : 0) | (c == dx_chunks - 1 ? kEllPassLast : 0);
     {
       ProfScope prof("bwd_dx", s);
-      ell_axpy_kernel<DV, 2, 4, 2><<<blocks, 256, 0, s>>>(a);
+      ell_axpy_kernel<DV, 2, 4, 2><<<blocks, 256, 0, s>>>(a, src);
     }
     count_launch();
     const cudaError_t e = cudaGetLastError();
@@ -659,9 +655,9 @@ cudaError_t launch_sparse_bwd_neurons(const void* x, const void* dy, int M, int 
       if ((e = TW_NEU(8, 1, 4, 4, kNeuD)) != cudaSuccess) return e;
       return TW_NEU(8, 1, 4, 3, kNeuX);
     }
-    if (d <= 4096) {
-      if ((e = TW_NEU(8, 2, 4, 3, kNeuD)) != cudaSuccess) return e;
-      return TW_NEU(8, 2, 4, 3, kNeuX);
+    if (d <= 4096) {  // four blocks per SM: 14 % faster on the 8B-class shape than three
+      if ((e = TW_NEU(8, 2, 4, 4, kNeuD)) != cudaSuccess) return e;
+      return TW_NEU(8, 2, 4, 4, kNeuX);
     }
     if ((e = TW_NEU(8, 4, 2, 2, kNeuD)) != cudaSuccess) return e;
     return TW_NEU(8, 4, 2, 2, kNeuX);

@@ -391,38 +391,32 @@ cudaError_t launch_team(const void* x, const void* wuT, const void* wd, int M, i
   return cudaSuccess;
 }
 
-// Wide ELL rows: the fused gather split into an up gather (h = g x.Wu per
-// entry) and a down gather (y = sum h Wd), each over one weight matrix in its
-// own L2-sized neuron passes (ell_gather.cuh).  TEAM and VPL are the fused
-// kernel's, so y is bit-identical to it.
-template <int TEAM, int VPL>
-cudaError_t launch_split(const void* x, const void* wuT, const void* wd, int M, int d, int f,
-                         const twell_hybrid* route, void* y, float* part, float* hbuf,
+// Wide rows: the fused gather split into an up gather (h = g x.Wu per entry)
+// and a down gather (y = sum h Wd), each over one weight matrix in its own
+// L2-sized neuron passes (ell_gather.cuh), over ELL rows (training) or TwELL
+// tiles (inference, when the caller gives a workspace for h).  TEAM and VPL
+// are the fused kernel's, so y is bit-identical to it.
+template <int TEAM, int VPL, class Src, class Chunk>
+cudaError_t launch_split(const void* x, const void* wuT, const void* wd, int M, int d, Src src,
+                         int chunks, Chunk set_chunk, void* y, float* part, float* hbuf,
                          cudaStream_t s) {
   constexpr int ROWS = 8 / TEAM;
-  const int chunks = part ? l2_chunks(2.0 * (double)f * d, 0.75, 0.5) : 1;
   EllDotArgs up{};
   up.vec = reinterpret_cast<const uint16_t*>(x);
   up.rows = reinterpret_cast<const uint16_t*>(wuT);
   up.M = M;
   up.d = d;
-  up.W = route->ell_width;
-  up.ell_val = reinterpret_cast<const uint16_t*>(route->ell_val);
-  up.ell_col = route->ell_col;
-  up.ell_nnz = route->ell_nnz;
-  up.whole = chunks == 1;
   up.out = hbuf;
   for (int c = 0; c < chunks; ++c) {
-    up.j_lo = (int)((long long)f * c / chunks);
-    up.j_hi = (int)((long long)f * (c + 1) / chunks);
+    Src sc = set_chunk(src, c, true);
     {
       ProfScope prof("sparse_fwd_up", s);
       // two-slab warps take four entries per batch, four-slab warps two
       // (measured on the 2B- and 8B-class shapes)
       if constexpr (VPL <= 2)
-        ell_dot_kernel<TEAM, VPL, 4, 2, kDotH><<<(M + ROWS - 1) / ROWS, 256, 0, s>>>(up);
+        ell_dot_kernel<TEAM, VPL, 4, 2, kDotH><<<(M + ROWS - 1) / ROWS, 256, 0, s>>>(up, sc);
       else
-        ell_dot_kernel<TEAM, VPL, 2, 3, kDotH><<<(M + ROWS - 1) / ROWS, 256, 0, s>>>(up);
+        ell_dot_kernel<TEAM, VPL, 2, 3, kDotH><<<(M + ROWS - 1) / ROWS, 256, 0, s>>>(up, sc);
     }
     count_launch();
     const cudaError_t e = cudaGetLastError();
@@ -433,21 +427,17 @@ cudaError_t launch_split(const void* x, const void* wuT, const void* wd, int M, 
   down.rows0 = reinterpret_cast<const uint16_t*>(wd);
   down.M = M;
   down.d = d;
-  down.W = route->ell_width;
-  down.ell_col = route->ell_col;
-  down.ell_nnz = route->ell_nnz;
   down.coef = hbuf;
   down.part = part;
   down.out = reinterpret_cast<uint16_t*>(y);
   const int wpr = (d + 256 * DV - 1) / (256 * DV);
   const long long blocks = ((long long)M * wpr + 7) / 8;
   for (int c = 0; c < chunks; ++c) {
-    down.j_lo = (int)((long long)f * c / chunks);
-    down.j_hi = (int)((long long)f * (c + 1) / chunks);
+    Src sc = set_chunk(src, c, false);
     down.pass = (c == 0 ? kEllPassFirst : 0) | (c == chunks - 1 ? kEllPassLast : 0);
     {
       ProfScope prof("sparse_fwd_down", s);
-      ell_axpy_kernel<DV, 2, 4, 1><<<(unsigned)blocks, 256, 0, s>>>(down);
+      ell_axpy_kernel<DV, 2, 4, 1><<<(unsigned)blocks, 256, 0, s>>>(down, sc);
     }
     count_launch();
     const cudaError_t e = cudaGetLastError();
@@ -456,10 +446,6 @@ cudaError_t launch_split(const void* x, const void* wuT, const void* wd, int M, 
   return cudaSuccess;
 }
 
-// One warp per row up to d_model = 1024 (four 256-element slabs), four warps
-// of two slabs up to 2048, four warps of four slabs up to 4096 (on the
-// 8B-class shape 6 % faster than eight warps of two: half the warps meet at
-// each barrier), then eight warps of four slabs.
 // ELL rows up to d_model = 1024 take the fused kernel, wider ones the split
 // up and down gathers; TwELL rows take the fused kernel, split over clusters
 // for small batches.
@@ -470,12 +456,36 @@ cudaError_t launch_shape(const void* x, const void* wuT, const void* wd, int M, 
                          int cl, cudaStream_t s) {
   if constexpr (ELL && TEAM > 1) {
     if (!hbuf) return cudaErrorInvalidValue;
-    return launch_split<TEAM, VPL>(x, wuT, wd, M, d, f, route, y, part, hbuf, s);
+    EllSrc src{reinterpret_cast<const uint16_t*>(route->ell_val), route->ell_col, route->ell_nnz,
+               route->ell_width, 0, f, 1};
+    const int n = part ? l2_chunks(2.0 * (double)f * d, 0.75, 0.5) : 1;
+    auto chunk = [f, n](EllSrc c, int i, bool) {
+      c.j_lo = (int)((long long)f * i / n);
+      c.j_hi = (int)((long long)f * (i + 1) / n);
+      c.whole = n == 1;
+      return c;
+    };
+    return launch_split<TEAM, VPL>(x, wuT, wd, M, d, src, n, chunk, y, part, hbuf, s);
   } else if constexpr (ELL) {
     return launch_team<TEAM, VPL, true>(x, wuT, wd, M, d, f, nullptr, T, tile_n, cap, route, y,
                                         part, chunks, s);
   } else {
     if (cl > 1) return launch_cluster<TEAM, VPL>(x, wuT, wd, M, d, tiles, T, tile_n, cap, cl, y, s);
+    if constexpr (TEAM > 1) {
+      if (hbuf) {  // wide TwELL rows with a workspace for h: the split gathers
+        TwellSrc src{reinterpret_cast<const uint16_t*>(tiles->val), tiles->idx, tiles->cnt, T,
+                     tile_n, cap, 0, T, nullptr};
+        const int n = part ? l2_chunks(2.0 * (double)f * d, 0.75, 0.5) : 1;
+        int* status = device_status_ptr();
+        auto chunk = [T, n, status](TwellSrc c, int i, bool up) {
+          c.t_lo = (int)((long long)T * i / n);
+          c.t_hi = (int)((long long)T * (i + 1) / n);
+          c.status = up ? status : nullptr;  // the up gather flags overfull tiles once
+          return c;
+        };
+        return launch_split<TEAM, VPL>(x, wuT, wd, M, d, src, n, chunk, y, part, hbuf, s);
+      }
+    }
     return launch_team<TEAM, VPL, false>(x, wuT, wd, M, d, f, tiles, T, tile_n, cap, nullptr, y,
                                          nullptr, 1, s);
   }
@@ -525,8 +535,8 @@ cudaError_t launch_sparse_fwd(const void* x, const void* wuT, const void* wd, in
     return launch_fmt<true>(x, wuT, wd, M, d, f, nullptr, T, tile_n, cap, route, y, part, hbuf,
                             chunks, s);
   }
-  return launch_fmt<false>(x, wuT, wd, M, d, f, tiles, T, tile_n, cap, nullptr, y, nullptr,
-                           nullptr, 1, s);
+  return launch_fmt<false>(x, wuT, wd, M, d, f, tiles, T, tile_n, cap, nullptr, y, part, hbuf, 1,
+                           s);
 }
 
 }  // namespace tw

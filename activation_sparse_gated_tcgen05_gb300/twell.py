@@ -28,7 +28,8 @@ STATUS = {
     6: "TWELL_ERR_DEVICE_TIMEOUT", 7: "TWELL_ERR_WORKSPACE",
 }
 EXPORTS = (
-    "twell_pack", "twell_pack_dense", "hybrid_route", "twell_workspace_bytes", "twell_ffn_fwd",
+    "twell_pack", "twell_pack_dense", "hybrid_route", "twell_workspace_bytes",
+    "twell_tiles_workspace_bytes", "twell_ffn_fwd",
     "twell_ffn_bwd", "twell_dense_workspace_bytes", "twell_dense_ffn_fwd", "twell_dense_ffn_bwd",
     "twell_dense_ffn_fwd_act", "twell_dense_ffn_bwd_act",
     "twell_gemm_bf16", "twell_get_device_status", "twell_status_string", "twell_num_sms",
@@ -80,6 +81,7 @@ def load():
         "twell_pack_dense": (I32, [P, I32, SP, TP, P]),
         "hybrid_route": (I32, [TP, SP, HP, P]),
         "twell_workspace_bytes": (SZ, [SP, I32, I32]),
+        "twell_tiles_workspace_bytes": (SZ, [SP]),
         "twell_ffn_fwd": (I32, [P, P, P, P, SP, TP, HP, P, P, SZ, P]),
         "twell_ffn_bwd": (I32, [P, P, P, P, P, SP, HP, F, P, P, P, P, P, SZ, P]),
         "twell_ffn_fwd_noalloc": (I32, [P, P, P, P, SP, HP, P, P]),
@@ -222,6 +224,10 @@ def hybrid_route(tiles: TwellTiles, shape: Shape, out: TwellHybrid, stream=None)
 
 def twell_workspace_bytes(shape: Shape, ell_width: int, training: bool) -> int:
     return int(load().twell_workspace_bytes(ctypes.byref(shape), int(ell_width), int(training)))
+
+
+def twell_tiles_workspace_bytes(shape: Shape) -> int:
+    return int(load().twell_tiles_workspace_bytes(ctypes.byref(shape)))
 
 
 def twell_ffn_fwd(x, wgT, wuT, wd, shape: Shape, y, tiles: Optional[TwellTiles] = None,

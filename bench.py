@@ -298,13 +298,18 @@ def run_own(args, dist):
     # route, ELL gather plus the dense fallback for the routed rows
     fwd_path = "hybrid" if rf > 0 else "twell"
 
+    # the TwELL forward's optional workspace (d_model > 1024: the split gathers)
+    tiles_ws_bytes = twell.twell_tiles_workspace_bytes(shape)
+    ws_t = (torch.empty(tiles_ws_bytes, dtype=torch.uint8, device=dev) if tiles_ws_bytes
+            else None)
+
     def sparse_fwd():
         twell.twell_pack(x, wg, shape, tiles)
         if fwd_path == "hybrid":
             twell.hybrid_route(tiles, shape, route)
             twell.twell_ffn_fwd(x, wg, wu, wd, shape, y, route=route, ws=ws)
         else:
-            twell.twell_ffn_fwd(x, wg, wu, wd, shape, y, tiles=tiles)
+            twell.twell_ffn_fwd(x, wg, wu, wd, shape, y, tiles=tiles, ws=ws_t)
 
     def dense_fwd():
         twell.twell_dense_ffn_fwd(x, wg, wu, wd, shape, y_d, False, ws_d)
@@ -435,7 +440,7 @@ def run_own(args, dist):
         def classic_fwd():
             twell.twell_gemm_bf16(x, wg, a_dense, M, f, d, False, False)
             twell.twell_pack_dense(a_dense, shape, tiles)
-            twell.twell_ffn_fwd(x, wg, wu, wd, shape, y, tiles=tiles)
+            twell.twell_ffn_fwd(x, wg, wu, wd, shape, y, tiles=tiles, ws=ws_t)
 
         ms_classic, _, _, _ = timed(graphed(classic_fwd), args.steps, args.warmup)
         del a_dense

@@ -131,6 +131,15 @@ twell_status hybrid_route(const twell_tiles* in, const twell_shape* shape,
  * invalid shape. */
 size_t twell_workspace_bytes(const twell_shape* shape, int32_t ell_width, int32_t training);
 
+/* Bytes of the optional workspace of twell_ffn_fwd with `tiles` (inference).
+ * For d_model > 1024 a workspace this large (h of every TwELL slot, fp32
+ * [M][d_ff / tile_n][tile_cap], and the fp32 running y between L2-sized
+ * neuron passes, [M][d_model]) lets the forward run as two gathers, up then
+ * down, that meet no barrier per batch; the result is the same bit for bit.
+ * Returns 0 for d_model <= 1024, where no workspace is used, and for an
+ * invalid shape. */
+size_t twell_tiles_workspace_bytes(const twell_shape* shape);
+
 /* Fused sparse up + down projection.  Source: page 2, "¿Qué hace distinto a
  * TwELL frente a ELL clásico?" (one kernel reads the packed activations and
  * does both projections; the intermediate never reaches global memory) and,
@@ -147,8 +156,11 @@ size_t twell_workspace_bytes(const twell_shape* shape, int32_t ell_width, int32_
  * routed rows' buffers it carries the fp32 running y between passes when
  * the gathered Wu / Wd rows exceed L2 and the ELL gather is split into
  * L2-sized neuron passes (same result, bit for bit).  With `tiles` the
- * workspace is not used (may be NULL); batches too small to fill the GPU
- * split each row over a thread-block cluster, which sums in another order. */
+ * workspace is optional: NULL keeps the fused gather; for d_model > 1024 a
+ * workspace of at least twell_tiles_workspace_bytes(shape) bytes (16-byte
+ * aligned; smaller returns TWELL_ERR_WORKSPACE) runs it as two gathers with
+ * the same result, bit for bit; batches too small to fill the GPU split each
+ * row over a thread-block cluster instead, which sums in another order. */
 twell_status twell_ffn_fwd(const void* x, const void* wgT, const void* wuT, const void* wd,
                            const twell_shape* shape, const twell_tiles* tiles,
                            const twell_hybrid* route, void* y, void* ws, size_t ws_bytes,

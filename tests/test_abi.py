@@ -65,6 +65,10 @@ def test_host_validation_before_launch(lib):
     h = twell.Hybrid(16, 16, 16, 8, 16, 16)
     assert lib.twell_ffn_fwd(16, 16, 16, 16, ctypes.byref(s), None, ctypes.byref(h), 16, 16, 8,
                              None) == 7
+    # TwELL forward of wide rows: a workspace that is given must hold h
+    wide = twell.make_shape(256, 2048, 1024, 64, 16)
+    assert lib.twell_ffn_fwd(16, 16, 16, 16, ctypes.byref(wide), ctypes.byref(t), None, 16, 16,
+                             8, None) == 7
     assert lib.twell_pack_dense(16, 3, ctypes.byref(s), ctypes.byref(t), None) == 1
     assert lib.twell_gemm_bf16(16, 16, 16, 10, 12, 16, 0, 0, 0, 0, None) == 2
     # dense comparator: unknown activation; SiLU has no L1 term
@@ -83,3 +87,8 @@ def test_workspace_sizes(lib):
     assert 0 < inf < tr
     assert twell.twell_workspace_bytes(twell.make_shape(16, 100, 1024, 64, 16), 4, True) == 0
     assert twell.twell_dense_workspace_bytes(s, True) >= 5 * 16384 * 4096 * 2
+    # TwELL forward: no workspace up to d_model = 1024, then h per slot + the y carry
+    assert twell.twell_tiles_workspace_bytes(s) == 0
+    wide = twell.make_shape(32768, 2048, 8192, 128, 32)
+    assert twell.twell_tiles_workspace_bytes(wide) >= 4 * 32768 * (64 * 32 + 2048)
+    assert twell.twell_tiles_workspace_bytes(twell.make_shape(16, 100, 1024, 64, 16)) == 0

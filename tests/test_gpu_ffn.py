@@ -268,3 +268,46 @@ def test_many_entries_per_row_and_neuron(d):
     assert twell.twell_get_device_status() == 0
     assert int(twell.hybrid_view(h, r.shape)[4].item()) == 0
     _check_step(r, y, dx, dwg, dwu, dwd, allow=False)
+
+
+@pytest.mark.parametrize("d,f", [(2048, 1024), (3136, 1024), (4096, 2048), (4160, 1024)])
+def test_twell_split_forward_matches_fused(d, f):
+    """TwELL rows wider than 1024 given a workspace run as two gathers (up:
+    h per tile slot, down: y).  The dot products and the accumulation order
+    are the fused kernel's, so y must equal the fused forward bit for bit,
+    and the oracle within tolerance.  M keeps both on one team per row."""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    M = 4 * sms + 37
+    r = Run(M, d, f, 128, 32, density=0.02, seed=14, exact=True)
+    t = r.pack()
+    y_fused = r.fwd(tiles=t)
+    ws = torch.empty(twell.twell_tiles_workspace_bytes(r.shape), dtype=torch.uint8, device="cuda")
+    y_split = torch.full_like(y_fused, float("nan"))
+    twell.twell_profile_begin("*")
+    twell.twell_ffn_fwd(r.x, r.wg, r.wu, r.wd, r.shape, y_split, tiles=t, ws=ws)
+    torch.cuda.synchronize()
+    prof = twell.twell_profile_end()
+    assert twell.twell_get_device_status() == 0
+    assert prof["sparse_fwd_up"][0] == 1 and prof["sparse_fwd_down"][0] == 1, prof
+    assert torch.equal(y_split.view(torch.int16), y_fused.view(torch.int16))
+    y_ref = oracle.ffn_fwd_dense(r.w["x"], r.w["wgT"], r.w["wuT"], r.w["wd"])
+    assert_close(to_np(y_split), y_ref, "y", out_bf16=True)
+
+
+def test_twell_split_forward_flags_overfull_tiles():
+    """The split TwELL forward reads only the C stored entries of a tile and
+    flags a tile whose count exceeds C, like the fused forward."""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    M = 4 * sms + 5
+    r = Run(M, 2048, 1024, 64, 2, density=0.2, seed=15, exact=True)
+    t = r.pack()
+    assert twell.twell_get_device_status() == 0
+    y_fused = r.fwd(tiles=t)
+    torch.cuda.synchronize()
+    assert twell.twell_get_device_status() == 4  # TWELL_ERR_CAPACITY
+    ws = torch.empty(twell.twell_tiles_workspace_bytes(r.shape), dtype=torch.uint8, device="cuda")
+    y_split = torch.empty_like(y_fused)
+    twell.twell_ffn_fwd(r.x, r.wg, r.wu, r.wd, r.shape, y_split, tiles=t, ws=ws)
+    torch.cuda.synchronize()
+    assert twell.twell_get_device_status() == 4  # TWELL_ERR_CAPACITY
+    assert torch.equal(y_split.view(torch.int16), y_fused.view(torch.int16))
