@@ -56,15 +56,26 @@ def _check_route(tiles, route, shape, W):
 
 
 def _fwd_inference(w, wl, M=None):
+    """The TwELL forward as bench.py runs it: with the optional workspace,
+    which for d_model > 1024 selects the split up / down gathers.  Where it
+    does, the forward without a workspace (the fused gather) must give the
+    same bytes."""
     M = wl.M if M is None else M
     x, wg, wu, wd = _upload(w, ("x", "wgT", "wuT", "wd"))
     shape = twell.make_shape(M, wl.d_model, wl.d_ff, wl.tile_n, wl.tile_cap)
     tiles = twell.alloc_tiles(shape)
     twell.twell_pack(x, wg, shape, tiles)
     y = torch.empty(M, wl.d_model, dtype=torch.bfloat16, device="cuda")
-    twell.twell_ffn_fwd(x, wg, wu, wd, shape, y, tiles=tiles)
+    nbytes = twell.twell_tiles_workspace_bytes(shape)
+    ws = torch.empty(nbytes, dtype=torch.uint8, device="cuda") if nbytes else None
+    twell.twell_ffn_fwd(x, wg, wu, wd, shape, y, tiles=tiles, ws=ws)
     torch.cuda.synchronize()
     assert twell.twell_get_device_status() == 0
+    if ws is not None:
+        y_fused = torch.empty_like(y)
+        twell.twell_ffn_fwd(x, wg, wu, wd, shape, y_fused, tiles=tiles)
+        torch.cuda.synchronize()
+        assert torch.equal(y.view(torch.int16), y_fused.view(torch.int16))
     return y, tiles, shape
 
 
