@@ -84,6 +84,10 @@ int num_sms() {
   return cache[dev];
 }
 
+// Process-wide choice of the wide-row gathers (see twell_set_split_gathers).
+std::atomic<int> g_split_gathers{1};
+bool split_gathers() { return g_split_gathers.load(std::memory_order_relaxed) != 0; }
+
 double l2_bytes() {
   static int cache[kMaxDevices] = {0};
   const int dev = current_device();
@@ -568,6 +572,10 @@ twell_status hybrid_route(const twell_tiles* in, const twell_shape* shape, const
 size_t twell_workspace_bytes(const twell_shape* shape, int32_t ell_width, int32_t training) {
   if (check_shape(shape, true) != TWELL_OK || ell_width < 0) return 0;
   return carve_sparse(nullptr, *shape, ell_width, training ? 1 : 0).bytes;
+}
+
+int32_t twell_set_split_gathers(int32_t enable) {
+  return g_split_gathers.exchange(enable ? 1 : 0) ? 1 : 0;
 }
 
 size_t twell_tiles_workspace_bytes(const twell_shape* shape) {

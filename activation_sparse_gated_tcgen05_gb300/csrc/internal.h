@@ -40,6 +40,9 @@ enum GemmKind {
 int num_sms();
 // L2 size of the current device in bytes (0 if unknown).
 double l2_bytes();
+// Rows wider than 1024 take the split gathers (true, the default) or the
+// fused kernels (twell_set_split_gathers).
+bool split_gathers();
 // Passes over the neuron axis for a gather whose weight rows total
 // `gathered_bytes`: 1 while they fit in the fraction `fit` of L2, else
 // enough chunks of at most the fraction `chunk` of L2 each.

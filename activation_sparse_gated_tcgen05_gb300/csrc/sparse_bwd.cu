@@ -613,7 +613,7 @@ cudaError_t launch_sparse_bwd_rows(const void* x, const void* dy, const void* wg
                                    const int* slot_pos, float lambda, float4* csc_vals, void* dx,
                                    float* part, float* dhbuf, float2* coef, cudaStream_t s) {
   if (M == 0) return cudaSuccess;
-  if (d > 1024) {  // wide rows: the split gathers, with the forward's team shapes
+  if (d > 1024 && split_gathers()) {  // wide rows: the split gathers, the forward's team shapes
     if (!dhbuf || !coef) return cudaErrorInvalidValue;
 #define TW_SPLIT(T, V)                                                                          \
   split_rows<T, V>(x, dy, wgT, wuT, wd, M, d, f, route, slot_pos, lambda, csc_vals, dx, part,  \
@@ -629,10 +629,17 @@ cudaError_t launch_sparse_bwd_rows(const void* x, const void* dy, const void* wg
   // passes beat one by 7 %, four beat six and eight), dX_m carried in `part`
   // (fp32) with the accumulation order unchanged
   const int chunks = part ? l2_chunks(3.0 * 2.0 * (double)f * d, 0.5, 0.65) : 1;
-  if (d <= 512) return rows_team<1, 2, 2, 2>(x, dy, wgT, wuT, wd, M, d, f, route, slot_pos, lambda,
-                                             csc_vals, dx, part, chunks, s);
-  return rows_team<1, 4, 1, 2>(x, dy, wgT, wuT, wd, M, d, f, route, slot_pos, lambda, csc_vals,
-                               dx, part, chunks, s);
+#define TW_ROWS(T, V, B, MINB)                                                                 \
+  rows_team<T, V, B, MINB>(x, dy, wgT, wuT, wd, M, d, f, route, slot_pos, lambda, csc_vals, dx, \
+                           part, chunks, s)
+  // wider rows here only with the split gathers switched off; team shapes as
+  // measured on the 2B- and 8B-class shapes (one entry per batch from d = 2048)
+  if (d <= 512) return TW_ROWS(1, 2, 2, 2);
+  if (d <= 1024) return TW_ROWS(1, 4, 1, 2);
+  if (d <= 2048) return TW_ROWS(4, 2, 1, 3);
+  if (d <= 4096) return TW_ROWS(4, 4, 1, 2);
+  return TW_ROWS(8, 4, 2, 1);
+#undef TW_ROWS
 }
 
 cudaError_t launch_sparse_bwd_neurons(const void* x, const void* dy, int M, int d, int f,

@@ -447,14 +447,18 @@ cudaError_t launch_split(const void* x, const void* wuT, const void* wd, int M, 
 }
 
 // ELL rows up to d_model = 1024 take the fused kernel, wider ones the split
-// up and down gathers; TwELL rows take the fused kernel, split over clusters
-// for small batches.
+// up and down gathers (the fused kernel when twell_set_split_gathers(0));
+// TwELL rows take the fused kernel, split over clusters for small batches,
+// or the split gathers when wide and given a workspace for h.
 template <int TEAM, int VPL, bool ELL>
 cudaError_t launch_shape(const void* x, const void* wuT, const void* wd, int M, int d, int f,
                          const twell_tiles* tiles, int T, int tile_n, int cap,
                          const twell_hybrid* route, void* y, float* part, float* hbuf, int chunks,
                          int cl, cudaStream_t s) {
   if constexpr (ELL && TEAM > 1) {
+    if (!split_gathers())
+      return launch_team<TEAM, VPL, true>(x, wuT, wd, M, d, f, nullptr, T, tile_n, cap, route, y,
+                                          part, chunks, s);
     if (!hbuf) return cudaErrorInvalidValue;
     EllSrc src{reinterpret_cast<const uint16_t*>(route->ell_val), route->ell_col, route->ell_nnz,
                route->ell_width, 0, f, 1};
@@ -472,7 +476,7 @@ cudaError_t launch_shape(const void* x, const void* wuT, const void* wd, int M, 
   } else {
     if (cl > 1) return launch_cluster<TEAM, VPL>(x, wuT, wd, M, d, tiles, T, tile_n, cap, cl, y, s);
     if constexpr (TEAM > 1) {
-      if (hbuf) {  // wide TwELL rows with a workspace for h: the split gathers
+      if (hbuf && split_gathers()) {  // wide TwELL rows with a workspace for h: the split gathers
         TwellSrc src{reinterpret_cast<const uint16_t*>(tiles->val), tiles->idx, tiles->cnt, T,
                      tile_n, cap, 0, T, nullptr};
         const int n = part ? l2_chunks(2.0 * (double)f * d, 0.75, 0.5) : 1;

@@ -29,7 +29,7 @@ STATUS = {
 }
 EXPORTS = (
     "twell_pack", "twell_pack_dense", "hybrid_route", "twell_workspace_bytes",
-    "twell_tiles_workspace_bytes", "twell_ffn_fwd",
+    "twell_tiles_workspace_bytes", "twell_set_split_gathers", "twell_ffn_fwd",
     "twell_ffn_bwd", "twell_dense_workspace_bytes", "twell_dense_ffn_fwd", "twell_dense_ffn_bwd",
     "twell_dense_ffn_fwd_act", "twell_dense_ffn_bwd_act",
     "twell_gemm_bf16", "twell_get_device_status", "twell_status_string", "twell_num_sms",
@@ -82,6 +82,7 @@ def load():
         "hybrid_route": (I32, [TP, SP, HP, P]),
         "twell_workspace_bytes": (SZ, [SP, I32, I32]),
         "twell_tiles_workspace_bytes": (SZ, [SP]),
+        "twell_set_split_gathers": (I32, [I32]),
         "twell_ffn_fwd": (I32, [P, P, P, P, SP, TP, HP, P, P, SZ, P]),
         "twell_ffn_bwd": (I32, [P, P, P, P, P, SP, HP, F, P, P, P, P, P, SZ, P]),
         "twell_ffn_fwd_noalloc": (I32, [P, P, P, P, SP, HP, P, P]),
@@ -228,6 +229,12 @@ def twell_workspace_bytes(shape: Shape, ell_width: int, training: bool) -> int:
 
 def twell_tiles_workspace_bytes(shape: Shape) -> int:
     return int(load().twell_tiles_workspace_bytes(ctypes.byref(shape)))
+
+
+def twell_set_split_gathers(enable: bool) -> bool:
+    """Split (True, the default) or fused (False) gathers for rows wider than
+    1024; returns the previous setting."""
+    return bool(load().twell_set_split_gathers(int(bool(enable))))
 
 
 def twell_ffn_fwd(x, wgT, wuT, wd, shape: Shape, y, tiles: Optional[TwellTiles] = None,

@@ -431,6 +431,16 @@ def run_own(args, dist):
     # the same steps without the L2 flush (weights warm, as in back-to-back layers of one shape)
     ms_step_warm, _, _, _ = timed(step_g, args.steps, args.warmup, l2_flush=False)
     ms_fwd_warm, _, _, _ = timed(fwd_g, args.steps, args.warmup, l2_flush=False)
+    # rows wider than 1024: the same step and forward with the pages' fused
+    # gathers (h never leaves registers) in place of the default split ones
+    ms_step_fused = ms_fwd_fused = None
+    if d > 1024:
+        twell.twell_set_split_gathers(False)
+        try:
+            ms_step_fused = timed(graphed(sparse_step), args.steps, args.warmup)[0]
+            ms_fwd_fused = timed(graphed(sparse_fwd), args.steps, args.warmup)[0]
+        finally:
+            twell.twell_set_split_gathers(True)
     # classic-ELL ablation (inference path): the dense gate written to HBM in
     # bf16, converted by a separate pack kernel, then the same fused forward
     ms_classic = None
@@ -648,7 +658,8 @@ def run_own(args, dist):
         "ms": {"sparse_fwd_bwd": ms_step, "sparse_fwd": ms_fwd, "dense_fwd": ms_dfwd,
                "dense_fwd_bwd": ms_dstep, "sparse_fwd_bwd_eager": ms_eager,
                "sparse_fwd_bwd_warm_l2": ms_step_warm, "sparse_fwd_warm_l2": ms_fwd_warm,
-               "classic_ell_fwd": ms_classic, "dense_silu_fwd": ms_sfwd,
+               "classic_ell_fwd": ms_classic, "sparse_fwd_bwd_fused_gathers": ms_step_fused,
+               "sparse_fwd_fused_gathers": ms_fwd_fused, "dense_silu_fwd": ms_sfwd,
                "dense_silu_fwd_bwd": ms_sstep},
         "ms_median": medians,
         "ms_per_step_median": medians.get("sparse_fwd_bwd"),

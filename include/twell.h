@@ -140,6 +140,18 @@ size_t twell_workspace_bytes(const twell_shape* shape, int32_t ell_width, int32_
  * invalid shape. */
 size_t twell_tiles_workspace_bytes(const twell_shape* shape);
 
+/* Choice of the gathers for rows wider than 1024, process-wide; returns the
+ * previous setting.  enable = 1 (the default): the forward runs as an up
+ * gather (h = g (x . Wu[:, j]) per live entry, 4 bytes each in the
+ * workspace) and a down gather (y = sum h Wd[j, :]), and the backward row
+ * phase as dh, gradient and dX gathers; each meets no barrier per batch and
+ * takes one or two weight matrices per L2-sized pass.  enable = 0: the fused
+ * kernels of page 2, section "¿Qué hace distinto a TwELL frente a ELL
+ * clásico?" (one gather per row, h kept in registers and never written to
+ * global memory).  Both give the same bytes in every output.  Not
+ * synchronised with work in flight: change it between calls. */
+int32_t twell_set_split_gathers(int32_t enable);
+
 /* Fused sparse up + down projection.  Source: page 2, "¿Qué hace distinto a
  * TwELL frente a ELL clásico?" (one kernel reads the packed activations and
  * does both projections; the intermediate never reaches global memory) and,

@@ -80,6 +80,12 @@ def test_host_validation_before_launch(lib):
                                        16, 16, 8, None) == 7
 
 
+def test_split_gathers_switch(lib):
+    assert twell.twell_set_split_gathers(False) is True   # the default is on
+    assert twell.twell_set_split_gathers(True) is False
+    assert twell.twell_set_split_gathers(True) is True
+
+
 def test_workspace_sizes(lib):
     s = twell.make_shape(16384, 1024, 4096, 128, 32)
     inf = twell.twell_workspace_bytes(s, 30, False)

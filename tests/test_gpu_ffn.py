@@ -311,3 +311,34 @@ def test_twell_split_forward_flags_overfull_tiles():
     torch.cuda.synchronize()
     assert twell.twell_get_device_status() == 4  # TWELL_ERR_CAPACITY
     assert torch.equal(y_split.view(torch.int16), y_fused.view(torch.int16))
+
+
+@pytest.mark.parametrize("M,d,f", [(300, 2048, 1024), (200, 3136, 1024), (256, 4096, 8192),
+                                   (160, 4160, 1024)])
+def test_split_and_fused_wide_gathers_agree(M, d, f):
+    """Rows wider than 1024 run as split gathers by default; with
+    twell_set_split_gathers(0) the fused kernels of the pages run instead (h
+    never leaves registers).  Same per-entry arithmetic and accumulation
+    order, so y, dX and every dW must agree bit for bit (d = 4096, f = 8192
+    also runs both in several L2-sized passes, with different pass counts)."""
+    r = Run(M, d, f, 128, 32, density=0.02, seed=16, exact=True, mixed=True)
+    t = r.pack()
+    W = _quantile_width(t, r.shape, 0.9)
+    h = r.route(t, W)
+    out = {}
+    try:
+        for split in (True, False):
+            twell.twell_set_split_gathers(split)
+            twell.twell_profile_begin("*")
+            y = r.fwd(route=h, W=W)
+            dx, dws = r.bwd(h, W)
+            torch.cuda.synchronize()
+            prof = twell.twell_profile_end()
+            assert twell.twell_get_device_status() == 0
+            assert ("sparse_fwd_up" in prof) == split and ("bwd_rows" in prof) != split, prof
+            out[split] = [y.view(torch.int16), dx.view(torch.int16)] + [w.view(torch.int32) for w in dws]
+    finally:
+        twell.twell_set_split_gathers(True)
+    for a, b in zip(out[True], out[False]):
+        assert torch.equal(a, b)
+    _check_step(r, *[o for o in (y, dx)], *dws, allow=False)
