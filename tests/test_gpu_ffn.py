@@ -313,9 +313,10 @@ def test_twell_split_forward_flags_overfull_tiles():
     assert torch.equal(y_split.view(torch.int16), y_fused.view(torch.int16))
 
 
-@pytest.mark.parametrize("M,d,f", [(300, 2048, 1024), (200, 3136, 1024), (256, 4096, 8192),
-                                   (160, 4160, 1024)])
-def test_split_and_fused_wide_gathers_agree(M, d, f):
+@pytest.mark.parametrize("M,d,f,q", [(300, 2048, 1024, 0.9), (300, 2048, 1024, 0.0),
+                                     (200, 3136, 1024, 1.0), (256, 4096, 8192, 0.9),
+                                     (160, 4160, 1024, 0.9)])
+def test_split_and_fused_wide_gathers_agree(M, d, f, q):
     """Rows wider than 1024 run as split gathers by default; with
     twell_set_split_gathers(0) the fused kernels of the pages run instead (h
     never leaves registers).  Same per-entry arithmetic and accumulation
@@ -323,7 +324,7 @@ def test_split_and_fused_wide_gathers_agree(M, d, f):
     also runs both in several L2-sized passes, with different pass counts)."""
     r = Run(M, d, f, 128, 32, density=0.02, seed=16, exact=True, mixed=True)
     t = r.pack()
-    W = _quantile_width(t, r.shape, 0.9)
+    W = _quantile_width(t, r.shape, q) if q > 0 else 0  # W = 0: every live row routed
     h = r.route(t, W)
     out = {}
     try:
@@ -336,6 +337,8 @@ def test_split_and_fused_wide_gathers_agree(M, d, f):
             prof = twell.twell_profile_end()
             assert twell.twell_get_device_status() == 0
             assert ("sparse_fwd_up" in prof) == split and ("bwd_rows" in prof) != split, prof
+            if W == 0:
+                assert int(twell.hybrid_view(h, r.shape)[4].item()) > 0
             out[split] = [y.view(torch.int16), dx.view(torch.int16)] + [w.view(torch.int32) for w in dws]
     finally:
         twell.twell_set_split_gathers(True)
