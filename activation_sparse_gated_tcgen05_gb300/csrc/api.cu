@@ -231,7 +231,7 @@ SparseWs carve_sparse(void* ws, const twell_shape& s, int W, int training) {
 
 // Optional workspace of the TwELL (inference) forward for rows wider than
 // 1024, where it runs as two gathers:
-//   hbuf [M][T][C] fp32: h of every TwELL slot
+//   hbuf [M][T * C] fp32: h of each row's live entries, in order
 //   part [M][d] fp32: y carried between L2-sized neuron passes
 struct TilesWs {
   float *hbuf, *part;

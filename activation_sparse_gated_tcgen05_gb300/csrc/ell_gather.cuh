@@ -32,7 +32,7 @@
 // kernel's, so fewer L2-sized passes), and neither waits at a barrier per
 // batch.  Entries come from an entry source: the ELL rows of the training
 // path (EllSrc) or the TwELL tiles of the inference path (TwellSrc); the
-// per-entry buffers are indexed like the source's value array.
+// per-entry buffers hold a row's entries contiguously, in order.
 #pragma once
 
 #include "common.cuh"
@@ -68,9 +68,10 @@ __device__ __forceinline__ void ell_slice(const uint16_t* __restrict__ ell_col, 
 }
 
 // Entry sources.  for_groups(m, lane, f) visits row m's live entries in
-// ascending column order, 32 at a time: f(count, j, slot) with lane i < count
-// holding entry i's column j and slot (the index of its value in the
-// source's bf16 value array); lanes >= count hold j = 0.
+// ascending column order, 32 at a time: f(count, j, slot, e) with lane
+// i < count holding entry i's column j, its slot (the index of its value in
+// the source's bf16 value array) and e, its index in the per-entry buffers
+// (row m's entries at consecutive e); lanes >= count hold j = 0.
 struct EllSrc {
   const uint16_t* val;  // [M][W] bf16 gate values
   const uint16_t* col;  // [M][W] columns, ascending in a row
@@ -85,7 +86,7 @@ struct EllSrc {
     for (int e0 = a; e0 < b; e0 += 32) {
       const int count = min(32, b - e0);
       const long long s = row_off + e0 + lane;
-      f(count, lane < count ? (int)col[s] : 0, s);
+      f(count, lane < count ? (int)col[s] : 0, s, s);
     }
   }
 };
@@ -99,6 +100,15 @@ struct TwellSrc {
   int* status;          // non-null: a tile with cnt > C sets TWELL_ERR_CAPACITY
   template <class F>
   __device__ __forceinline__ void for_groups(int m, int lane, F&& f) const {
+    // a row's entries at [m T C, m T C + row_nnz): its tiles' stored entries
+    // in order, whatever tile chunk a pass covers (entries of earlier tiles
+    // counted first)
+    long long e_row = (long long)m * T * cap;
+    for (int t0 = 0; t0 < t_lo; t0 += 32) {
+      const int t = t0 + lane;
+      const int c = t < t_lo ? min((int)cnt[(long long)m * T + t], cap) : 0;
+      e_row += __reduce_add_sync(0xffffffffu, c);
+    }
     for (int t0 = t_lo; t0 < t_hi; t0 += 32) {
       const int t = t0 + lane;
       const int craw = t < t_hi ? cnt[(long long)m * T + t] : 0;
@@ -123,8 +133,9 @@ struct TwellSrc {
           sl = ((long long)m * T + tt) * cap + (e - ex);
           jl = tt * tile_n + idx[sl];
         }
-        f(min(32, total - e0), jl, sl);
+        f(min(32, total - e0), jl, sl, e_row + e);
       }
+      e_row += total;
     }
   }
 };
@@ -133,12 +144,12 @@ struct EllDotArgs {
   const uint16_t* vec;   // [M][d] row vectors (x or dY)
   const uint16_t* rows;  // [f][d] gathered weight rows (Wu^T or Wd)
   int M, d;
-  float* out;            // kDotH: h, kDotDh: dh  (per slot of the source)
-  const float* dh;       // kDotGrad: dh per slot
+  float* out;            // kDotH: h, kDotDh: dh  (per entry, the source's buffer index)
+  const float* dh;       // kDotGrad: dh per entry
   const int* slot_pos;   // kDotGrad: neuron-major position of each slot
   float lambda;          // kDotGrad: L1 coefficient
   float4* csc_vals;      // kDotGrad: (du, da, h, 0) at the neuron-major position
-  float2* coef;          // kDotGrad: (du, da) per slot, for the dX gather
+  float2* coef;          // kDotGrad: (du, da) per entry, for the dX gather
 };
 
 template <int TEAM, int VPL, int B, int MINB, int MODE, class Src>
@@ -162,7 +173,7 @@ __global__ void __launch_bounds__(256, MINB) ell_dot_kernel(const EllDotArgs p, 
     vv[v] = e < d ? ldg_v4_hint(p.vec + (long long)m * d + e, pol) : make_uint4(0, 0, 0, 0);
   }
   int buf = 0;
-  src.for_groups(m, lane, [&](int count, int jl, long long s) {
+  src.for_groups(m, lane, [&](int count, int jl, long long s, long long he) {
     float mine = 0.f;  // the warp's partial dot product of entry lane
     for (int i = 0; i < count; i += B) {
       int j[B];
@@ -198,16 +209,16 @@ __global__ void __launch_bounds__(256, MINB) ell_dot_kernel(const EllDotArgs p, 
     }
     if (wt != 0 || lane >= count) return;
     if constexpr (MODE == kDotDh) {
-      p.out[s] = dot;
+      p.out[he] = dot;
     } else {
       const float g = bf16_bits_to_float(src.val[s]);
       if constexpr (MODE == kDotH) {
-        p.out[s] = g * dot;
+        p.out[he] = g * dot;
       } else {  // ReLU'(a) = 1 on a live entry
-        const float dh = p.dh[s];
+        const float dh = p.dh[he];
         const float du = dh * g, da = fmaf(dh, dot, p.lambda);
         p.csc_vals[p.slot_pos[s]] = make_float4(du, da, g * dot, 0.f);
-        p.coef[s] = make_float2(du, da);
+        p.coef[he] = make_float2(du, da);
       }
     }
   });
@@ -217,7 +228,7 @@ struct EllAxpyArgs {
   const uint16_t* rows0;  // [f][d] weight rows scaled by the first coefficient
   const uint16_t* rows1;  // second matrix (NR = 2), scaled by the second
   int M, d;
-  const void* coef;       // per slot: float (NR = 1) or float2 (NR = 2)
+  const void* coef;       // per entry: float (NR = 1) or float2 (NR = 2)
   int pass;               // kEllPassFirst: start from 0, kEllPassLast: store out
   float* part;            // [M][d] fp32 carry between neuron passes
   uint16_t* out;          // [M][d] bf16 result
@@ -254,13 +265,13 @@ __global__ void __launch_bounds__(256, MINB) ell_axpy_kernel(const EllAxpyArgs p
       acc[v][3] = f2_make(q1.z, q1.w);
     }
   }
-  src.for_groups(m, lane, [&](int count, int jl, long long s) {
+  src.for_groups(m, lane, [&](int count, int jl, long long, long long he) {
     float c0 = 0.f, c1 = 0.f;  // slots past the group: neuron 0 with zero coefficients
     if (lane < count) {
       if constexpr (NR == 1) {
-        c0 = reinterpret_cast<const float*>(p.coef)[s];
+        c0 = reinterpret_cast<const float*>(p.coef)[he];
       } else {
-        const float2 c = reinterpret_cast<const float2*>(p.coef)[s];
+        const float2 c = reinterpret_cast<const float2*>(p.coef)[he];
         c0 = c.x;
         c1 = c.y;
       }

@@ -132,10 +132,11 @@ twell_status hybrid_route(const twell_tiles* in, const twell_shape* shape,
 size_t twell_workspace_bytes(const twell_shape* shape, int32_t ell_width, int32_t training);
 
 /* Bytes of the optional workspace of twell_ffn_fwd with `tiles` (inference).
- * For d_model > 1024 a workspace this large (h of every TwELL slot, fp32
- * [M][d_ff / tile_n][tile_cap], and the fp32 running y between L2-sized
- * neuron passes, [M][d_model]) lets the forward run as two gathers, up then
- * down, that meet no barrier per batch; the result is the same bit for bit.
+ * For d_model > 1024 a workspace this large (h of each row's live entries,
+ * fp32, room for d_ff / tile_n * tile_cap per row, and the fp32 running y
+ * between L2-sized neuron passes, [M][d_model]) lets the forward run as two
+ * gathers, up then down, that meet no barrier per batch; the result is the
+ * same bit for bit.
  * Returns 0 for d_model <= 1024, where no workspace is used, and for an
  * invalid shape. */
 size_t twell_tiles_workspace_bytes(const twell_shape* shape);

@@ -270,15 +270,16 @@ def test_many_entries_per_row_and_neuron(d):
     _check_step(r, y, dx, dwg, dwu, dwd, allow=False)
 
 
-@pytest.mark.parametrize("d,f", [(2048, 1024), (3136, 1024), (4096, 2048), (4160, 1024)])
-def test_twell_split_forward_matches_fused(d, f):
+@pytest.mark.parametrize("d,f,tile_n", [(2048, 1024, 128), (3136, 1024, 128), (4096, 2048, 128),
+                                        (4160, 1024, 128), (2048, 2560, 64)])
+def test_twell_split_forward_matches_fused(d, f, tile_n):
     """TwELL rows wider than 1024 given a workspace run as two gathers (up:
     h per tile slot, down: y).  The dot products and the accumulation order
     are the fused kernel's, so y must equal the fused forward bit for bit,
     and the oracle within tolerance.  M keeps both on one team per row."""
     sms = torch.cuda.get_device_properties(0).multi_processor_count
     M = 4 * sms + 37
-    r = Run(M, d, f, 128, 32, density=0.02, seed=14, exact=True)
+    r = Run(M, d, f, tile_n, tile_n // 4, density=0.02, seed=14, exact=True)
     t = r.pack()
     y_fused = r.fwd(tiles=t)
     ws = torch.empty(twell.twell_tiles_workspace_bytes(r.shape), dtype=torch.uint8, device="cuda")

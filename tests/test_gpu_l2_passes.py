@@ -177,3 +177,31 @@ def test_neuron_phase_split_when_x_and_dy_exceed_l2():
     assert_close(dws[0].cpu().numpy()[neurons], og, "dwgT", allowance=al["dwgT"])
     assert_close(dws[1].cpu().numpy()[neurons], ou, "dwuT", allowance=al["dwuT"])
     assert_close(dws[2].cpu().numpy()[neurons], od, "dwd", allowance=al["dwd"])
+
+
+def test_multi_pass_twell_split_forward_matches_fused():
+    """The TwELL (inference) forward of wide rows with a workspace: the up
+    and down gathers each run in L2-sized tile ranges once Wu^T (or Wd) alone
+    outgrows 3/4 of L2; a row's h stay in order across the ranges, so y must
+    equal the fused single-pass forward bit for bit."""
+    d, f = 4096, 16384
+    passes = _expected_passes(2.0 * f * d)
+    assert passes > 1, "shape no longer exceeds L2; pick a larger one"
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    M = 4 * sms + 37  # two rows per team group: no cluster split for the fused forward
+    w = synthetic.make_inputs(M, d, f, seed=17, with_dy=False)
+    x, wg, wu, wd = (dev_bf16(w[k]) for k in ("x", "wgT", "wuT", "wd"))
+    shape = twell.make_shape(M, d, f, 128, 32)
+    tiles = twell.alloc_tiles(shape)
+    twell.twell_pack(x, wg, shape, tiles)
+    y_fused = torch.empty(M, d, dtype=torch.bfloat16, device="cuda")
+    twell.twell_ffn_fwd(x, wg, wu, wd, shape, y_fused, tiles=tiles)
+    ws = torch.empty(twell.twell_tiles_workspace_bytes(shape), dtype=torch.uint8, device="cuda")
+    y_split = torch.full((M, d), float("nan"), dtype=torch.bfloat16, device="cuda")
+    twell.twell_profile_begin("*")
+    twell.twell_ffn_fwd(x, wg, wu, wd, shape, y_split, tiles=tiles, ws=ws)
+    torch.cuda.synchronize()
+    prof = twell.twell_profile_end()
+    assert twell.twell_get_device_status() == 0
+    assert prof["sparse_fwd_up"][0] == passes and prof["sparse_fwd_down"][0] == passes, prof
+    assert torch.equal(y_split.view(torch.int16), y_fused.view(torch.int16))
