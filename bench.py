@@ -578,6 +578,10 @@ def run_own(args, dist):
             # its ceiling is the measured L2 row-gather bandwidth
             roof["l2_gather_peak"] = gather_probe["l2_gbs"]
             roof["frac_of_l2_gather"] = achieved / gather_probe["l2_gbs"]
+            roof["note"] = ("algorithmic bytes of a gather whose rows L2 serves; frac is "
+                            "against the HBM copy rate (above 1 when L2 serves them), "
+                            "frac_of_l2_gather against the measured L2 row-gather probe; "
+                            "traffic is the DRAM bytes per launch from ncu")
 
     # end to end through the C ABI with host buffers (H2D inputs, D2H results)
     xh = torch.empty((M, d), dtype=torch.bfloat16).pin_memory()
