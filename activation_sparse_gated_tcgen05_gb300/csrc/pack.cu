@@ -244,7 +244,7 @@ cudaError_t launch_splitk_scatter(const float* part, int buf_rows, int num_kb, i
                                   cudaStream_t s) {
   {
     ProfScope prof("splitk_scatter", s);
-    splitk_scatter_kernel<<<num_sms() * 4, 256, 0, s>>>(part, buf_rows, num_kb, s_max, n_rows,
+    splitk_scatter_kernel<<<num_sms() * 2, 256, 0, s>>>(part, buf_rows, num_kb, s_max, n_rows,
                                                         rows, M, N, reinterpret_cast<uint16_t*>(out));
   }
   count_launch();
@@ -317,7 +317,10 @@ cudaError_t launch_gather_rows(const void* src, int M, int d, const int* rows, c
   if (dst_rows == 0) return cudaSuccess;
   {
     ProfScope prof("gather_rows", s);
-    gather_rows_kernel<<<blocks_for(dst_rows), kWarpsPerBlock * 32, 0, s>>>(
+    // two blocks per SM: the rows are strided over the grid, and with no row
+    // routed (the count is on the device) every block only reads the count
+    const int grid = min(blocks_for(dst_rows), 2 * num_sms());
+    gather_rows_kernel<<<grid, kWarpsPerBlock * 32, 0, s>>>(
         reinterpret_cast<const uint16_t*>(src), M, d, rows, n_rows, reinterpret_cast<uint16_t*>(dst),
         dst_rows);
   }
