@@ -67,15 +67,12 @@ __global__ void __launch_bounds__(1024)
   const bool ok = j < f && b < NB;
   c[w][lane] = ok ? __popc(mask[(long long)b * f + j]) : 0;  // coalesced over neurons
   __syncthreads();
-  if (w == 0) {  // warp 0: lane = neuron, serial prefix over the group's 32 blocks
-    int run = 0;
-#pragma unroll 8
-    for (int i = 0; i < kScanG; ++i) {
-      const int v = c[i][lane];
-      c[i][lane] = run;
-      run += v;
-    }
-    if (j < f) gtot[(long long)blockIdx.y * f + j] = run;
+  {  // warp w scans neuron w of the block over the group's 32 row blocks (lane)
+    const int v = c[lane][w];
+    const int incl = warp_incl_scan(v);
+    c[lane][w] = incl - v;
+    const int jw = blockIdx.x * 32 + w;
+    if (lane == 31 && jw < f) gtot[(long long)blockIdx.y * f + jw] = incl;
   }
   __syncthreads();
   if (ok) off[(long long)b * f + j] = c[w][lane];
