@@ -346,3 +346,20 @@ def test_split_and_fused_wide_gathers_agree(M, d, f, q):
     for a, b in zip(out[True], out[False]):
         assert torch.equal(a, b)
     _check_step(r, *[o for o in (y, dx)], *dws, allow=False)
+
+
+@pytest.mark.parametrize("M,d", [(1, 2048), (3, 4096), (17, 3136)])
+def test_wide_rows_tiny_batches_training_step(M, d):
+    """The split gathers with fewer rows than a block holds (teams and warps
+    past the last row leave at once, each team's named barrier its own): a
+    full step against the oracle, with and without a routed row."""
+    r = Run(M, d, 1024, 128, 32, density=0.05, seed=18, exact=True)
+    t = r.pack()
+    for q in (1.0, 0.0):
+        W = _quantile_width(t, r.shape, q) if q > 0 else 0
+        h = r.route(t, W)
+        y = r.fwd(route=h, W=W)
+        dx, (dwg, dwu, dwd) = r.bwd(h, W)
+        torch.cuda.synchronize()
+        assert twell.twell_get_device_status() == 0
+        _check_step(r, y, dx, dwg, dwu, dwd, allow=False)
