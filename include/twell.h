@@ -214,8 +214,12 @@ twell_status twell_ffn_fwd_noalloc(const void* x, const void* wgT, const void* w
  * routed rows.  The route must come from hybrid_route on the same x and Wg.
  * The reduction order is fixed, so results are bit-reproducible.
  * ws/ws_bytes: at least twell_workspace_bytes(shape, W, 1) bytes (16-byte
- * aligned); it also carries the fp32 running dX when the row phase is split
- * into L2-sized neuron passes (Wd, Wu and Wg rows beyond half of L2). */
+ * aligned); it also carries the fp32 running dX when the row phase runs in
+ * L2-sized neuron passes and, for rows wider than 1024 (split gathers, see
+ * twell_set_split_gathers), dh and (du, da) of every live ELL entry.  When x
+ * and dY together exceed 3/4 of L2 the weight gradients are formed in two
+ * passes, over dY rows (dwd) and over x rows (dwuT, dwgT), with the same
+ * per-element order. */
 twell_status twell_ffn_bwd(const void* x, const void* wgT, const void* wuT, const void* wd,
                            const void* dy, const twell_shape* shape, const twell_hybrid* route,
                            float l1_coeff, void* dx, float* dwgT, float* dwuT, float* dwd,
