@@ -168,7 +168,8 @@ int32_t twell_set_split_gathers(int32_t enable);
  * twell_workspace_bytes(shape, W, 0) bytes (16-byte aligned); besides the
  * routed rows' buffers it carries the fp32 running y between passes when
  * the gathered Wu / Wd rows exceed L2 and the ELL gather is split into
- * L2-sized neuron passes (same result, bit for bit).  With `tiles` the
+ * L2-sized neuron passes (same result, bit for bit), and for rows wider than
+ * 1024 the fp32 h of every live ELL entry between the up and down gathers.  With `tiles` the
  * workspace is optional: NULL keeps the fused gather; for d_model > 1024 a
  * workspace of at least twell_tiles_workspace_bytes(shape) bytes (16-byte
  * aligned; smaller returns TWELL_ERR_WORKSPACE) runs it as two gathers with
