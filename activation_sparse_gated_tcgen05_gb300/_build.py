@@ -1,5 +1,6 @@
 """Build libtwell.so in-tree for sm_103a (nvcc, one translation unit per kernel
-family, compiled in parallel, then linked into one shared library)."""
+family, compiled in parallel, then linked into one shared library), and the
+benchmark's row-gather probe as a library of its own (libtwell_probe.so)."""
 from __future__ import annotations
 
 import concurrent.futures
@@ -12,8 +13,10 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 OUT_DIR = os.path.join(PKG, "_build")
 LIB = os.path.join(OUT_DIR, "libtwell.so")
+PROBE_LIB = os.path.join(OUT_DIR, "libtwell_probe.so")
 
-SOURCES = ["api.cu", "gemm_tc.cu", "pack.cu", "sparse_fwd.cu", "sparse_bwd.cu", "probe.cu"]
+SOURCES = ["api.cu", "gemm_tc.cu", "pack.cu", "sparse_fwd.cu", "sparse_bwd.cu", "selftest.cu"]
+PROBE_SOURCES = ["gather_probe.cu"]
 HEADERS = ["common.cuh", "ell_gather.cuh", "gemm_tc.cuh", "internal.h"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ARCH + ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC",
@@ -28,16 +31,19 @@ def _nvcc() -> str:
 
 
 def _newest_input() -> float:
-    files = [os.path.join(CSRC, s) for s in SOURCES + HEADERS]
+    files = [os.path.join(CSRC, s) for s in SOURCES + PROBE_SOURCES + HEADERS]
     files.append(os.path.join(INCLUDE, "twell.h"))
     files.append(os.path.abspath(__file__))
     return max(os.path.getmtime(f) for f in files)
 
 
 def build(force: bool = False, verbose: bool = False) -> str:
-    """Compile and link libtwell.so if any input is newer than it."""
+    """Compile and link libtwell.so and libtwell_probe.so if any input is
+    newer than them."""
     os.makedirs(OUT_DIR, exist_ok=True)
-    if not force and os.path.exists(LIB) and os.path.getmtime(LIB) >= _newest_input():
+    newest = _newest_input()
+    if (not force and all(os.path.exists(p) and os.path.getmtime(p) >= newest
+                          for p in (LIB, PROBE_LIB))):
         return LIB
     nvcc = _nvcc()
 
@@ -53,14 +59,16 @@ def build(force: bool = False, verbose: bool = False) -> str:
             print(res.stderr)
         return obj
 
-    with concurrent.futures.ThreadPoolExecutor(max_workers=len(SOURCES)) as ex:
-        objs = list(ex.map(compile_one, SOURCES))
-    tmp = LIB + ".tmp%d" % os.getpid()
-    cmd = [nvcc] + ARCH + ["-shared", "-cudart", "shared", "-o", tmp] + objs
-    res = subprocess.run(cmd, capture_output=True, text=True)
-    if res.returncode != 0:
-        raise RuntimeError("link failed:\n%s%s" % (res.stdout, res.stderr))
-    os.replace(tmp, LIB)
+    srcs = SOURCES + PROBE_SOURCES
+    with concurrent.futures.ThreadPoolExecutor(max_workers=len(srcs)) as ex:
+        objs = dict(zip(srcs, ex.map(compile_one, srcs)))
+    for lib, group in ((LIB, SOURCES), (PROBE_LIB, PROBE_SOURCES)):
+        tmp = lib + ".tmp%d" % os.getpid()
+        cmd = [nvcc] + ARCH + ["-shared", "-cudart", "shared", "-o", tmp] + [objs[g] for g in group]
+        res = subprocess.run(cmd, capture_output=True, text=True)
+        if res.returncode != 0:
+            raise RuntimeError("link failed:\n%s%s" % (res.stdout, res.stderr))
+        os.replace(tmp, lib)
     return LIB
 
 

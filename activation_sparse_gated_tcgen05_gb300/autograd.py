@@ -53,14 +53,19 @@ class SparseGatedFFNFunction(torch.autograd.Function):
         W = ell_width_for(row_nnz, route_fraction)
         route = twell.alloc_hybrid(shape, W, x.device)
         twell.hybrid_route(tiles, shape, route)
-        ws = torch.empty(twell.twell_workspace_bytes(shape, W, True), dtype=torch.uint8,
-                         device=x.device)
+        # the routed-row count is on the device: read it and size the
+        # workspace's dense-backup buffers for exactly those rows
+        n_dense = int(route.n_dense[0].item())
+        route.dense_cap = n_dense
+        ws = torch.empty(twell.twell_workspace_bytes(shape, W, True, dense_cap=n_dense),
+                         dtype=torch.uint8, device=x.device)
         y = torch.empty(M, d, dtype=torch.bfloat16, device=x.device)
         twell.twell_ffn_fwd(xb, wg, wu, wdb, shape, y, route=route, ws=ws)
         if stats is not None:
             stats["density"] = float(row_nnz.to(torch.float64).sum().item()) / max(1, M * f)
             stats["ell_width"] = W
-            stats["routed_rows"] = int(route.n_dense[0].item())
+            stats["routed_rows"] = n_dense
+            stats["workspace_bytes"] = ws.numel()
         ctx.save_for_backward(xb, wg, wu, wdb)
         ctx.shape, ctx.route, ctx.ws, ctx.l1 = shape, route, ws, float(l1_coeff)
         ctx.in_dtypes = (x.dtype, wgT.dtype, wuT.dtype, wd.dtype)

@@ -8,6 +8,8 @@
 #include <string>
 #include <vector>
 
+#include <nvtx3/nvToolsExt.h>
+
 #include "gemm_tc.cuh"
 #include "internal.h"
 
@@ -51,7 +53,11 @@ std::vector<ProfRecord> g_prof_records;
 std::vector<ProfEntry> g_prof_report;
 }  // namespace
 
+NvtxRange::NvtxRange(const char* name) { nvtxRangePushA(name); }
+NvtxRange::~NvtxRange() { nvtxRangePop(); }
+
 ProfScope::ProfScope(const char* name, cudaStream_t s) : slot(-1), stream(s) {
+  nvtxRangePushA(name);
   if (!g_prof_on.load(std::memory_order_relaxed)) return;
   std::lock_guard<std::mutex> lock(g_prof_mu);
   if (g_prof_filter != "*" && g_prof_filter != name) return;
@@ -67,6 +73,7 @@ ProfScope::ProfScope(const char* name, cudaStream_t s) : slot(-1), stream(s) {
 }
 
 ProfScope::~ProfScope() {
+  nvtxRangePop();
   if (slot < 0) return;
   std::lock_guard<std::mutex> lock(g_prof_mu);
   cudaEventRecord(g_prof_records[slot].stop, stream);
@@ -156,7 +163,7 @@ twell_status check_tiles(const twell_tiles* t) {
 
 twell_status check_route(const twell_hybrid* r) {
   if (!r) return TWELL_ERR_INVALID_ARG;
-  if (r->ell_width < 0) return TWELL_ERR_INVALID_ARG;
+  if (r->ell_width < 0 || r->dense_cap < 0) return TWELL_ERR_INVALID_ARG;
   twell_status st = check_ptrs({r->ell_nnz, r->dense_rows, r->n_dense});
   if (st != TWELL_OK) return st;
   if (r->ell_width > 0) return check_ptrs({r->ell_val, r->ell_col});
@@ -181,14 +188,16 @@ struct Carve {
   }
 };
 
-// Workspace of the sparse path.  Routed-row buffers are sized for every row
-// being routed; they hold whole 128-row tiles (Mp rows).  The dense backup
-// keeps its intermediates h, du, da as bf16 hi + lo pairs, so routed rows
-// are as accurate as the fp32 gather path:
-//   hr  [Mp][2f] = [h hi | h lo]
-//   part [Mp][d] fp32: split-K partials of the routed rows' y and dX GEMMs
-//   ur  [Mp][f]  fp32 u
-//   ddr [Mp][4f] = [du hi | da hi | du lo | da lo]
+// Workspace of the sparse path.  Routed-row buffers hold the route's
+// capacity (dense_cap, at most M) in whole 128-row tiles (Mr rows).  The
+// dense backup keeps its intermediates h, du, da as bf16 hi + lo pairs, so
+// routed rows are as accurate as the fp32 gather path:
+//   hr  [Mr][2f] = [h hi | h lo]
+//   part [Mp][d] fp32 (Mp = M in whole tiles): the running y / dX of
+//        L2-sized passes, then the split-K partials of the routed rows' y
+//        and dX GEMMs
+//   ur  [Mr][f]  fp32 u
+//   ddr [Mr][4f] = [du hi | da hi | du lo | da lo]
 struct SparseWs {
   uint16_t *xr, *hr;                    // forward fallback
   float* part;
@@ -198,25 +207,30 @@ struct SparseWs {
   int *mask_off, *csc_ptr, *csc_row, *slot_pos;
   float4* csc_vals;
   float2* coef;                         // per-ELL-entry (du, da) of the split row phase
+  long long Mr;                         // routed-row buffer rows (capacity in whole tiles)
+  long long Mp;                         // rows of part
   size_t bytes;
 };
 
-SparseWs carve_sparse(void* ws, const twell_shape& s, int W, int training) {
+SparseWs carve_sparse(void* ws, const twell_shape& s, int W, int dense_cap, int training) {
   const long long Mp = round_up(s.M, 128);
+  const long long Mr = round_up(dense_cap < s.M ? dense_cap : s.M, 128);
   const long long d = s.d_model, f = s.d_ff;
   Carve c(ws);
   SparseWs w{};
-  w.xr = c.take<uint16_t>(Mp * d);
-  w.hr = c.take<uint16_t>(Mp * 2 * f);
+  w.Mr = Mr;
+  w.Mp = Mp;
+  w.xr = c.take<uint16_t>(Mr * d);
+  w.hr = c.take<uint16_t>(Mr * 2 * f);
   w.part = c.take<float>(Mp * d);
   const long long E = (long long)s.M * W;
   w.hbuf = c.take<float>(E > 0 ? E : 1);
   if (training) {
     const long long NB = (s.M + 31) / 32;
-    w.dyr = c.take<uint16_t>(Mp * d);
-    w.gr = c.take<uint16_t>(Mp * f);
-    w.ur = c.take<float>(Mp * f);
-    w.ddr = c.take<uint16_t>(Mp * 4 * f);
+    w.dyr = c.take<uint16_t>(Mr * d);
+    w.gr = c.take<uint16_t>(Mr * f);
+    w.ur = c.take<float>(Mr * f);
+    w.ddr = c.take<uint16_t>(Mr * 4 * f);
     const long long NG = (NB + 31) / 32;
     w.mask_off = c.take<int>((2 * NB + (NG > 0 ? NG : 1)) * f);
     w.csc_ptr = c.take<int>(f + 1);
@@ -315,30 +329,31 @@ cudaError_t gated_gemm(const void* x_rows, long long rows, const twell_shape& s,
 
 // Routed rows: out[row_map[r]] = A[r] B with the K range split across CTAs
 // (the few routed rows give too few output tiles to fill the GPU); each split
-// stores an fp32 partial in `part` and a reduction kernel sums them in fixed
-// order and scatters the bf16 rows.
+// stores an fp32 partial in `part` (part_rows rows) and a reduction kernel
+// sums them in fixed order and scatters the bf16 rows.
 constexpr int kSplitKMax = 8;
 cudaError_t routed_gemm(const Mat& A, const Mat& B, const Mat* B2, long long rows, int K,
                         const twell_shape& s, int k_split, const int* m_dev, const int* row_map,
-                        float* part, void* out, cudaStream_t st) {
+                        float* part, long long part_rows, void* out, cudaStream_t st) {
   GemmParams p = base_params((int)rows, s.d_model, K, kBN);
   p.m_dev = m_dev;
   p.k_split = k_split;
   p.c_f32 = 1;
   p.tma_out = 1;
   p.split_k_max = kSplitKMax;
-  const OutMat o{part, rows, s.d_model, s.d_model, 1, 32};
+  p.split_rows = (int)part_rows;
+  const OutMat o{part, part_rows, s.d_model, s.d_model, 1, 32};
   cudaError_t e = gemm_launch(GK_STORE_KM, A, B, B2, p, st, &o, 1);
   if (e != cudaSuccess) return e;
-  return launch_splitk_scatter(part, (int)rows, (K + kBK - 1) / kBK, kSplitKMax, m_dev, row_map,
-                               s.M, s.d_model, out, st);
+  return launch_splitk_scatter(part, (int)part_rows, (int)rows, (K + kBK - 1) / kBK, kSplitKMax,
+                               m_dev, row_map, s.M, s.d_model, out, st);
 }
 
 // out[row_map ? row_map[r] : r] = h[r] Wd (bf16); with split, h = hi + lo and
 // the GEMM runs over K = 2f against [Wd ; Wd].
 cudaError_t down_gemm(const uint16_t* h, long long rows, const twell_shape& s, const void* wd,
                       bool split, const int* m_dev, const int* row_map, void* out,
-                      cudaStream_t st, float* part = nullptr) {
+                      cudaStream_t st, float* part = nullptr, long long part_rows = 0) {
   const long long K = split ? 2LL * s.d_ff : s.d_ff;
   GemmParams p = base_params((int)rows, s.d_model, (int)K, kBN);
   p.m_dev = m_dev;
@@ -349,7 +364,8 @@ cudaError_t down_gemm(const uint16_t* h, long long rows, const twell_shape& s, c
   const Mat A = mat(h, rows, K, K);
   const Mat B = mat(wd, s.d_ff, s.d_model, s.d_model);  // [K = f][N = d], MN-major
   if (row_map && part)
-    return routed_gemm(A, B, &B, rows, (int)K, s, s.d_ff / kBK, m_dev, row_map, part, out, st);
+    return routed_gemm(A, B, &B, rows, (int)K, s, s.d_ff / kBK, m_dev, row_map, part, part_rows,
+                       out, st);
   if (!row_map && !m_dev) {
     p.tma_out = 1;
     const OutMat o{out, rows, s.d_model, s.d_model, 0, 32};
@@ -388,7 +404,7 @@ cudaError_t dgate_gemm(const void* dy_rows, long long rows, const twell_shape& s
 // K = 2f (or 4f with the lo halves) against [WuT ; WgT (; WuT ; WgT)].
 cudaError_t dx_gemm(const uint16_t* dd, long long rows, const twell_shape& s, const void* wgT,
                     const void* wuT, bool split, const int* m_dev, const int* row_map, void* out,
-                    cudaStream_t st, float* part = nullptr) {
+                    cudaStream_t st, float* part = nullptr, long long part_rows = 0) {
   const long long K = (split ? 4LL : 2LL) * s.d_ff;
   GemmParams p = base_params((int)rows, s.d_model, (int)K, kBN);
   p.m_dev = m_dev;
@@ -400,7 +416,8 @@ cudaError_t dx_gemm(const uint16_t* dd, long long rows, const twell_shape& s, co
   const Mat B = mat(wuT, s.d_ff, s.d_model, s.d_model);   // [K][N], MN-major
   const Mat B2 = mat(wgT, s.d_ff, s.d_model, s.d_model);
   if (row_map && part)
-    return routed_gemm(A, B, &B2, rows, (int)K, s, s.d_ff / kBK, m_dev, row_map, part, out, st);
+    return routed_gemm(A, B, &B2, rows, (int)K, s, s.d_ff / kBK, m_dev, row_map, part, part_rows,
+                       out, st);
   if (!row_map && !m_dev) {
     p.tma_out = 1;
     const OutMat o{out, rows, s.d_model, s.d_model, 0, 32};
@@ -513,6 +530,7 @@ twell_status twell_get_device_status(void* stream, int32_t* out) {
 
 twell_status twell_pack(const void* x, const void* wgT, const twell_shape* shape,
                         const twell_tiles* out, void* stream) {
+  NvtxRange nvtx("twell_pack");
   twell_status st = check_shape(shape, true);
   if (st != TWELL_OK) return st;
   if ((st = check_ptrs({x, wgT})) != TWELL_OK) return st;
@@ -547,6 +565,7 @@ twell_status twell_pack(const void* x, const void* wgT, const twell_shape* shape
 
 twell_status twell_pack_dense(const void* a, int32_t a_dtype, const twell_shape* shape,
                               const twell_tiles* out, void* stream) {
+  NvtxRange nvtx("twell_pack_dense");
   twell_status st = check_shape(shape, true);
   if (st != TWELL_OK) return st;
   if (a_dtype != 0 && a_dtype != 1) return TWELL_ERR_INVALID_ARG;
@@ -559,6 +578,7 @@ twell_status twell_pack_dense(const void* a, int32_t a_dtype, const twell_shape*
 
 twell_status hybrid_route(const twell_tiles* in, const twell_shape* shape, const twell_hybrid* out,
                           void* stream) {
+  NvtxRange nvtx("hybrid_route");
   twell_status st = check_shape(shape, true);
   if (st != TWELL_OK) return st;
   if ((st = check_tiles(in)) != TWELL_OK) return st;
@@ -566,12 +586,19 @@ twell_status hybrid_route(const twell_tiles* in, const twell_shape* shape, const
   const twell_shape& s = *shape;
   // the routing flags live in dense_rows until the stable list overwrites them
   return cuda_status(launch_route(*in, s.M, s.d_ff, s.tile_n, s.tile_cap, *out, out->dense_rows,
+                                  out->dense_cap < s.M ? out->dense_cap : s.M,
                                   reinterpret_cast<cudaStream_t>(stream)));
 }
 
+size_t twell_workspace_bytes_capped(const twell_shape* shape, int32_t ell_width,
+                                    int32_t dense_cap, int32_t training) {
+  if (check_shape(shape, true) != TWELL_OK || ell_width < 0 || dense_cap < 0) return 0;
+  return carve_sparse(nullptr, *shape, ell_width, dense_cap, training ? 1 : 0).bytes;
+}
+
 size_t twell_workspace_bytes(const twell_shape* shape, int32_t ell_width, int32_t training) {
-  if (check_shape(shape, true) != TWELL_OK || ell_width < 0) return 0;
-  return carve_sparse(nullptr, *shape, ell_width, training ? 1 : 0).bytes;
+  if (check_shape(shape, true) != TWELL_OK) return 0;
+  return twell_workspace_bytes_capped(shape, ell_width, shape->M, training);
 }
 
 int32_t twell_set_split_gathers(int32_t enable) {
@@ -587,6 +614,7 @@ twell_status twell_ffn_fwd(const void* x, const void* wgT, const void* wuT, cons
                            const twell_shape* shape, const twell_tiles* tiles,
                            const twell_hybrid* route, void* y, void* ws, size_t ws_bytes,
                            void* stream) {
+  NvtxRange nvtx("twell_ffn_fwd");
   twell_status st = check_shape(shape, true);
   if (st != TWELL_OK) return st;
   if ((tiles == nullptr) == (route == nullptr)) return TWELL_ERR_INVALID_ARG;
@@ -607,23 +635,24 @@ twell_status twell_ffn_fwd(const void* x, const void* wgT, const void* wuT, cons
   }
   if ((st = check_route(route)) != TWELL_OK) return st;
   if ((st = check_ptrs({wgT})) != TWELL_OK) return st;
-  const SparseWs need = carve_sparse(nullptr, s, route->ell_width, 0);
+  const SparseWs need = carve_sparse(nullptr, s, route->ell_width, route->dense_cap, 0);
   if (!ws || ws_bytes < need.bytes) return TWELL_ERR_WORKSPACE;
   if (!aligned16(ws)) return TWELL_ERR_ALIGNMENT;
   if (s.M == 0) return TWELL_OK;
-  const SparseWs w = carve_sparse(ws, s, route->ell_width, 0);
-  const long long Mp = round_up(s.M, 128);
+  const SparseWs w = carve_sparse(ws, s, route->ell_width, route->dense_cap, 0);
+  const long long Mr = w.Mr;
   // w.part carries y between L2-sized passes; the routed rows' split-K GEMM
   // reuses it afterwards on the same stream
   cudaError_t e = launch_sparse_fwd(x, wuT, wd, s.M, s.d_model, s.d_ff, nullptr, s.tile_n,
                                     s.tile_cap, route, y, w.part, w.hbuf, cs);
+  if (Mr == 0) return cuda_status(e);  // no routed-row capacity: nothing else to run
   if (e == cudaSuccess)
-    e = launch_gather_rows(x, s.M, s.d_model, route->dense_rows, route->n_dense, w.xr, (int)Mp, cs);
+    e = launch_gather_rows(x, s.M, s.d_model, route->dense_rows, route->n_dense, w.xr, (int)Mr, cs);
   if (e == cudaSuccess)
-    e = gated_gemm(w.xr, Mp, s, wgT, wuT, route->n_dense, w.hr, true, nullptr, nullptr,
+    e = gated_gemm(w.xr, Mr, s, wgT, wuT, route->n_dense, w.hr, true, nullptr, nullptr,
                    nullptr, 0, cs);
   if (e == cudaSuccess)
-    e = down_gemm(w.hr, Mp, s, wd, true, route->n_dense, route->dense_rows, y, cs, w.part);
+    e = down_gemm(w.hr, Mr, s, wd, true, route->n_dense, route->dense_rows, y, cs, w.part, w.Mp);
   return cuda_status(e);
 }
 
@@ -631,17 +660,18 @@ twell_status twell_ffn_bwd(const void* x, const void* wgT, const void* wuT, cons
                            const void* dy, const twell_shape* shape, const twell_hybrid* route,
                            float l1_coeff, void* dx, float* dwgT, float* dwuT, float* dwd,
                            void* ws, size_t ws_bytes, void* stream) {
+  NvtxRange nvtx("twell_ffn_bwd");
   twell_status st = check_shape(shape, true);
   if (st != TWELL_OK) return st;
   if ((st = check_ptrs({x, wgT, wuT, wd, dy, dx, dwgT, dwuT, dwd})) != TWELL_OK) return st;
   if ((st = check_route(route)) != TWELL_OK) return st;
   const twell_shape& s = *shape;
-  const SparseWs need = carve_sparse(nullptr, s, route->ell_width, 1);
+  const SparseWs need = carve_sparse(nullptr, s, route->ell_width, route->dense_cap, 1);
   if (!ws || ws_bytes < need.bytes) return TWELL_ERR_WORKSPACE;
   if (!aligned16(ws)) return TWELL_ERR_ALIGNMENT;
   cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
-  const SparseWs w = carve_sparse(ws, s, route->ell_width, 1);
-  const long long Mp = round_up(s.M, 128);
+  const SparseWs w = carve_sparse(ws, s, route->ell_width, route->dense_cap, 1);
+  const long long Mr = w.Mr;
   const long long f = s.d_ff;
   cudaError_t e = launch_csc_build(*route, s.M, s.d_ff, w.mask_off, w.csc_ptr, w.csc_row,
                                    w.slot_pos, cs);
@@ -651,23 +681,23 @@ twell_status twell_ffn_bwd(const void* x, const void* wgT, const void* wuT, cons
   if (e == cudaSuccess)
     e = launch_sparse_bwd_neurons(x, dy, s.M, s.d_model, s.d_ff, w.csc_ptr, w.csc_row, w.csc_vals,
                                   dwgT, dwuT, dwd, cs);
-  if (s.M == 0) return cuda_status(e);
+  if (s.M == 0 || Mr == 0) return cuda_status(e);
   // routed rows: dense tensor-core backward, accumulated into the same dW
   const int* nd = route->n_dense;
   if (e == cudaSuccess)
-    e = launch_gather_rows(x, s.M, s.d_model, route->dense_rows, nd, w.xr, (int)Mp, cs);
+    e = launch_gather_rows(x, s.M, s.d_model, route->dense_rows, nd, w.xr, (int)Mr, cs);
   if (e == cudaSuccess)
-    e = launch_gather_rows(dy, s.M, s.d_model, route->dense_rows, nd, w.dyr, (int)Mp, cs);
+    e = launch_gather_rows(dy, s.M, s.d_model, route->dense_rows, nd, w.dyr, (int)Mr, cs);
   if (e == cudaSuccess)
-    e = gated_gemm(w.xr, Mp, s, wgT, wuT, nd, w.hr, true, w.gr, nullptr, w.ur, 1, cs);
+    e = gated_gemm(w.xr, Mr, s, wgT, wuT, nd, w.hr, true, w.gr, nullptr, w.ur, 1, cs);
   if (e == cudaSuccess)
-    e = dgate_gemm(w.dyr, Mp, s, wd, nd, w.gr, nullptr, w.ur, w.ddr, true, l1_coeff, 1, cs);
+    e = dgate_gemm(w.dyr, Mr, s, wd, nd, w.gr, nullptr, w.ur, w.ddr, true, l1_coeff, 1, cs);
   if (e == cudaSuccess)
-    e = dx_gemm(w.ddr, Mp, s, wgT, wuT, true, nd, route->dense_rows, dx, cs, w.part);
+    e = dx_gemm(w.ddr, Mr, s, wgT, wuT, true, nd, route->dense_rows, dx, cs, w.part, w.Mp);
   // dW += (hi + lo)^T B, both halves in one launch per weight
-  if (e == cudaSuccess) e = dw_gemm(w.hr, 2 * f, w.dyr, Mp, s, nd, dwd, 1, cs, f);
-  if (e == cudaSuccess) e = dw_gemm(w.ddr, 4 * f, w.xr, Mp, s, nd, dwuT, 1, cs, 2 * f);
-  if (e == cudaSuccess) e = dw_gemm(w.ddr + f, 4 * f, w.xr, Mp, s, nd, dwgT, 1, cs, 2 * f);
+  if (e == cudaSuccess) e = dw_gemm(w.hr, 2 * f, w.dyr, Mr, s, nd, dwd, 1, cs, f);
+  if (e == cudaSuccess) e = dw_gemm(w.ddr, 4 * f, w.xr, Mr, s, nd, dwuT, 1, cs, 2 * f);
+  if (e == cudaSuccess) e = dw_gemm(w.ddr + f, 4 * f, w.xr, Mr, s, nd, dwgT, 1, cs, 2 * f);
   return cuda_status(e);
 }
 
@@ -680,6 +710,7 @@ twell_status twell_dense_ffn_fwd_act(const void* x, const void* wgT, const void*
                                      const void* wd, const twell_shape* shape,
                                      int32_t activation, void* y, int32_t training, void* ws,
                                      size_t ws_bytes, void* stream) {
+  NvtxRange nvtx("twell_dense_ffn_fwd_act");
   twell_status st = check_shape(shape, false);
   if (st != TWELL_OK) return st;
   if (activation != TWELL_ACT_RELU && activation != TWELL_ACT_SILU) return TWELL_ERR_INVALID_ARG;
@@ -709,6 +740,7 @@ twell_status twell_dense_ffn_bwd_act(const void* x, const void* wgT, const void*
                                      int32_t activation, float l1_coeff, void* dx, float* dwgT,
                                      float* dwuT, float* dwd, void* ws, size_t ws_bytes,
                                      void* stream) {
+  NvtxRange nvtx("twell_dense_ffn_bwd_act");
   twell_status st = check_shape(shape, false);
   if (st != TWELL_OK) return st;
   if (activation != TWELL_ACT_RELU && activation != TWELL_ACT_SILU) return TWELL_ERR_INVALID_ARG;
@@ -746,6 +778,7 @@ twell_status twell_dense_ffn_bwd(const void* x, const void* wgT, const void* wuT
 twell_status twell_gemm_bf16(const void* A, const void* B, void* C, int32_t M, int32_t N,
                              int32_t K, int32_t a_mn_major, int32_t b_mn_major, int32_t c_dtype,
                              int32_t accumulate, void* stream) {
+  NvtxRange nvtx("twell_gemm_bf16");
   if (M < 0 || N <= 0 || K <= 0) return TWELL_ERR_INVALID_ARG;
   if (c_dtype != 0 && c_dtype != 1) return TWELL_ERR_INVALID_ARG;
   if (accumulate && c_dtype != 1) return TWELL_ERR_INVALID_ARG;
@@ -811,7 +844,7 @@ extern "C" twell_status twell_ffn_fwd_noalloc(const void* x, const void* wgT, co
   if (st != TWELL_OK) return st;
   if ((st = check_ptrs({x, wgT, wuT, wd, y})) != TWELL_OK) return st;
   if ((st = check_route(route)) != TWELL_OK) return st;
-  const size_t need = carve_sparse(nullptr, *shape, route->ell_width, 0).bytes;
+  const size_t need = carve_sparse(nullptr, *shape, route->ell_width, route->dense_cap, 0).bytes;
   if (need > kNoAllocScratchBytes) return TWELL_ERR_WORKSPACE;
   void* ws = noalloc_scratch();
   if (!ws) return TWELL_ERR_CUDA;

@@ -62,6 +62,7 @@ struct GemmParams {
   int cluster_k;        // EPI_PACK only: > 1 = split K over the blocks of a cluster (see kernel)
   int split_k_max;      // > 1: split K (plan from splitk_plan); split s stores its fp32 partial
                         // at rows [s * rows_eff, (s + 1) * rows_eff) of the output map
+  int split_rows;       // rows of that output map (0: M)
   int* status;
   // EPI_STORE
   void* c;
@@ -195,7 +196,8 @@ struct Epilogue<EPI_STORE> {
         uint32_t r[32];
         tmem_ld32(tacc + c0, r);
         tmem_wait_ld();
-        if (n0 + c0 >= N || row0 >= p.M) continue;  // box wholly outside C (warp-uniform)
+        // box wholly outside C (warp-uniform); split-K partials fill split_rows rows
+        if (n0 + c0 >= N || row0 >= (p.split_rows > 0 ? p.split_rows : p.M)) continue;
         if (p.c_f32) {
           uint8_t* b = st.full();
 #pragma unroll
@@ -598,7 +600,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     splits = cluster_k;
     kps = (num_kb + cluster_k - 1) / cluster_k;
   } else if (p.split_k_max > 1 && num_kb > 0 && M_eff > 0) {
-    splitk_plan(m_tiles * kBM, p.M, num_kb, p.split_k_max, splits, kps);
+    splitk_plan(m_tiles * kBM, p.split_rows > 0 ? p.split_rows : p.M, num_kb, p.split_k_max,
+                splits, kps);
   }
   const int total = (num_kb > 0 && M_eff > 0) ? tiles * splits : 0;
   // nothing to do (e.g. no routed rows): leave before touching TMEM or barriers

@@ -49,8 +49,9 @@ bool split_gathers();
 int l2_chunks(double gathered_bytes, double fit, double chunk);
 void count_launch(int n = 1);  // kernels launched by the library (process-wide)
 
-// While profiling is on for `name` (or "*"), brackets one kernel launch with
-// CUDA events recorded on its stream; otherwise does nothing.
+// Brackets one kernel launch: an NVTX range named after the kernel family
+// (seen by Nsight tools; a no-op without one) and, while profiling is on for
+// `name` (or "*"), CUDA events recorded on the launch's stream.
 struct ProfScope {
   ProfScope(const char* name, cudaStream_t s);
   ~ProfScope();
@@ -58,6 +59,12 @@ struct ProfScope {
   cudaStream_t stream;
 };
 int* device_status_ptr();  // per-device status word (device address)
+
+// NVTX range over one entry point (named after it) for Nsight timelines.
+struct NvtxRange {
+  explicit NvtxRange(const char* name);
+  ~NvtxRange();
+};
 
 // Launch the persistent GEMM.  A is the M-side operand, B (and B2 for a
 // second K range or the up half of EPI_GATED) the N-side one, each given in
@@ -70,11 +77,14 @@ cudaError_t gemm_launch(GemmKind kind, const Mat& A, const Mat& B, const Mat* B2
 // Non-tensor-core kernels (pack.cu, sparse_fwd.cu, sparse_bwd.cu).
 cudaError_t launch_pack_dense(const void* a, int a_f32, int M, int f, int tile_n, int cap,
                               const twell_tiles& out, cudaStream_t s);
+// dense_cap: routed rows the workspace holds; more routed rows than that
+// record TWELL_ERR_CAPACITY in the device status word.
 cudaError_t launch_route(const twell_tiles& in, int M, int f, int tile_n, int cap,
-                         const twell_hybrid& out, int* scan_flags, cudaStream_t s);
-cudaError_t launch_splitk_scatter(const float* part, int buf_rows, int num_kb, int s_max,
-                                  const int* n_rows, const int* rows, int M, int N, void* out,
-                                  cudaStream_t s);
+                         const twell_hybrid& out, int* scan_flags, int dense_cap, cudaStream_t s);
+// part holds buf_rows rows of split-K partials of at most row_cap routed rows
+cudaError_t launch_splitk_scatter(const float* part, int buf_rows, int row_cap, int num_kb,
+                                  int s_max, const int* n_rows, const int* rows, int M, int N,
+                                  void* out, cudaStream_t s);
 cudaError_t launch_gather_rows(const void* src, int M, int d, const int* rows, const int* n_rows,
                                void* dst, int dst_rows, cudaStream_t s);
 // `part` ([M][d] fp32) carries y between the passes of an ELL gather split

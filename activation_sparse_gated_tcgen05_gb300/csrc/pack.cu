@@ -134,12 +134,14 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32)
   if (lane == 0) ell_nnz[m] = base;
 }
 
-// Stable list of routed rows: one block scans the flags in order.
+// Stable list of routed rows: one block scans the flags in order.  More
+// routed rows than the caller's capacity dense_cap records TWELL_ERR_CAPACITY.
 constexpr int kListThreads = 1024;
 constexpr int kListItems = 16;
 
 __global__ void __launch_bounds__(kListThreads)
-    route_list_kernel(const int* flags, int M, int* dense_rows, int* n_dense) {
+    route_list_kernel(const int* flags, int M, int* dense_rows, int* n_dense, int dense_cap,
+                      int* status) {
   __shared__ int warp_tot[kListThreads / 32];
   __shared__ int carry;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -172,7 +174,10 @@ __global__ void __launch_bounds__(kListThreads)
     if (tid == kListThreads - 1) carry = pos;
     __syncthreads();
   }
-  if (tid == 0) *n_dense = carry;
+  if (tid == 0) {
+    *n_dense = carry;
+    if (carry > dense_cap) set_status(status, TWELL_ERR_CAPACITY);
+  }
 }
 
 // dst[i] = src[rows[i]] for i < n (n on the device); rows [n, roundup(n, 128))
@@ -201,10 +206,10 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32)
 // Sum the split-K partials of the routed rows in fixed order (split 0, 1, ...)
 // and scatter the bf16 result to out[rows[r]] -- deterministic, no atomics.
 __global__ void __launch_bounds__(256)
-    splitk_scatter_kernel(const float* __restrict__ part, int buf_rows, int num_kb, int s_max,
-                          const int* __restrict__ n_rows, const int* __restrict__ rows, int M, int N,
-                          uint16_t* __restrict__ out) {
-  const int n = min(*n_rows, buf_rows);
+    splitk_scatter_kernel(const float* __restrict__ part, int buf_rows, int row_cap, int num_kb,
+                          int s_max, const int* __restrict__ n_rows, const int* __restrict__ rows,
+                          int M, int N, uint16_t* __restrict__ out) {
+  const int n = min(*n_rows, row_cap);
   if (n <= 0) return;
   const int rows_eff = ((n + 127) / 128) * 128;
   int splits, kps;
@@ -239,13 +244,14 @@ int blocks_for(long long warps_needed) {
 
 }  // namespace
 
-cudaError_t launch_splitk_scatter(const float* part, int buf_rows, int num_kb, int s_max,
-                                  const int* n_rows, const int* rows, int M, int N, void* out,
-                                  cudaStream_t s) {
+cudaError_t launch_splitk_scatter(const float* part, int buf_rows, int row_cap, int num_kb,
+                                  int s_max, const int* n_rows, const int* rows, int M, int N,
+                                  void* out, cudaStream_t s) {
   {
     ProfScope prof("splitk_scatter", s);
-    splitk_scatter_kernel<<<num_sms() * 2, 256, 0, s>>>(part, buf_rows, num_kb, s_max, n_rows,
-                                                        rows, M, N, reinterpret_cast<uint16_t*>(out));
+    splitk_scatter_kernel<<<num_sms() * 2, 256, 0, s>>>(part, buf_rows, row_cap, num_kb, s_max,
+                                                        n_rows, rows, M, N,
+                                                        reinterpret_cast<uint16_t*>(out));
   }
   count_launch();
   return cudaGetLastError();
@@ -291,7 +297,7 @@ cudaError_t launch_pack_dense(const void* a, int a_f32, int M, int f, int tile_n
 }
 
 cudaError_t launch_route(const twell_tiles& in, int M, int f, int tile_n, int cap,
-                         const twell_hybrid& out, int* flags, cudaStream_t s) {
+                         const twell_hybrid& out, int* flags, int dense_cap, cudaStream_t s) {
   if (M == 0) return cudaMemsetAsync(out.n_dense, 0, sizeof(int), s);
   const int T = f / tile_n;
   const int grid = (M + kWarpsPerBlock - 1) / kWarpsPerBlock;
@@ -306,7 +312,8 @@ cudaError_t launch_route(const twell_tiles& in, int M, int f, int tile_n, int ca
   if (e != cudaSuccess) return e;
   {
     ProfScope prof("route_list", s);
-    route_list_kernel<<<1, kListThreads, 0, s>>>(flags, M, out.dense_rows, out.n_dense);
+    route_list_kernel<<<1, kListThreads, 0, s>>>(flags, M, out.dense_rows, out.n_dense, dense_cap,
+                                                 device_status_ptr());
   }
   count_launch();
   return cudaGetLastError();

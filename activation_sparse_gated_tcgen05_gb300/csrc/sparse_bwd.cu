@@ -313,18 +313,20 @@ __global__ void __launch_bounds__(256, MINB)
 }
 
 // ---------------------------------------------------------------- neuron phase
-// One team per neuron; each warp owns VPL slabs of d_model and needs no
-// cross-warp communication, so narrow slabs (VPL = 1) buy occupancy and
-// more gathered rows in flight per SM.  PARTS selects the outputs: kNeuD
-// gathers dY rows for dWd, kNeuX gathers x rows for dWu^T and dWg^T, and
-// kNeuD | kNeuX does both in one pass.  Each output element sums its
-// entries in ascending row order either way.
+// One team per neuron; each warp owns VPL slabs of the column window
+// [c0, c1) of d_model and needs no cross-warp communication, so narrow slabs
+// (VPL = 1) buy occupancy and more gathered rows in flight per SM.  PARTS
+// selects the outputs: kNeuD gathers dY rows for dWd, kNeuX gathers x rows
+// for dWu^T and dWg^T, and kNeuD | kNeuX does both in one pass.  Each output
+// element sums its entries in ascending row order either way, and a column
+// window owns its output columns outright, so windows need no carry.
 constexpr int kNeuD = 1, kNeuX = 2;
 
 template <int TEAM, int VPL, int B, int MINB, int PARTS>
 __global__ void __launch_bounds__(256, MINB)
     bwd_neurons_kernel(const uint16_t* __restrict__ x, const uint16_t* __restrict__ dy, int d,
-                       int f, const int* __restrict__ csc_ptr, const int* __restrict__ csc_row,
+                       int f, int c0, int c1, const int* __restrict__ csc_ptr,
+                       const int* __restrict__ csc_row,
                        const float4* __restrict__ csc_vals, float* __restrict__ dwgT,
                        float* __restrict__ dwuT, float* __restrict__ dwd) {
   constexpr bool DO_D = PARTS & kNeuD, DO_X = PARTS & kNeuX;
@@ -342,11 +344,11 @@ __global__ void __launch_bounds__(256, MINB)
       if constexpr (DO_X) au[v][k] = ag[v][k] = 0;
     }
 
-  int eoff[VPL];  // slab offsets, lanes past d_model read the first slab
+  int eoff[VPL];  // slab offsets, lanes past the window read its first slab
 #pragma unroll
   for (int v = 0; v < VPL; ++v) {
-    const int e = slab<TEAM>(lane, wt, v);
-    eoff[v] = e < d ? e : 0;
+    const int e = c0 + slab<TEAM>(lane, wt, v);
+    eoff[v] = e < c1 ? e : c0;
   }
   const int p0 = csc_ptr[j], p1 = csc_ptr[j + 1];
   for (int e0 = p0; e0 < p1; e0 += 32) {
@@ -411,8 +413,8 @@ __global__ void __launch_bounds__(256, MINB)
   const long long row = (long long)j * d;
 #pragma unroll
   for (int v = 0; v < VPL; ++v) {
-    const int e = slab<TEAM>(lane, wt, v);
-    if (e < d) {
+    const int e = c0 + slab<TEAM>(lane, wt, v);
+    if (e < c1) {
 #pragma unroll
       for (int q = 0; q < 2; ++q) {
         if constexpr (DO_D) {
@@ -458,19 +460,27 @@ cudaError_t rows_team(const void* x, const void* dy, const void* wgT, const void
   return cudaSuccess;
 }
 
+// One launch per column window: windows of d / windows columns (a multiple
+// of 8, so every slab stays 16-byte aligned), the team covering one window.
 template <int TEAM, int VPL, int B, int MINB, int PARTS>
 cudaError_t neurons_team(const void* x, const void* dy, int d, int f, const int* csc_ptr,
                          const int* csc_row, const float4* csc_vals, float* dwgT, float* dwuT,
-                         float* dwd, cudaStream_t s) {
+                         float* dwd, cudaStream_t s, int windows = 1) {
   constexpr int ROWS = 8 / TEAM;
-  {
-    ProfScope prof(PARTS == kNeuD ? "bwd_neurons_dy" : PARTS == kNeuX ? "bwd_neurons_x" : "bwd_neurons", s);
-    bwd_neurons_kernel<TEAM, VPL, B, MINB, PARTS><<<(f + ROWS - 1) / ROWS, 256, 0, s>>>(
-        reinterpret_cast<const uint16_t*>(x), reinterpret_cast<const uint16_t*>(dy), d, f,
-        csc_ptr, csc_row, csc_vals, dwgT, dwuT, dwd);
+  const int width = d / windows;
+  if (width % 8 != 0 || width > TEAM * 32 * 8 * VPL) return cudaErrorInvalidValue;
+  for (int w = 0; w < windows; ++w) {
+    {
+      ProfScope prof(PARTS == kNeuD ? "bwd_neurons_dy" : PARTS == kNeuX ? "bwd_neurons_x" : "bwd_neurons", s);
+      bwd_neurons_kernel<TEAM, VPL, B, MINB, PARTS><<<(f + ROWS - 1) / ROWS, 256, 0, s>>>(
+          reinterpret_cast<const uint16_t*>(x), reinterpret_cast<const uint16_t*>(dy), d, f,
+          w * width, (w + 1) * width, csc_ptr, csc_row, csc_vals, dwgT, dwuT, dwd);
+    }
+    count_launch();
+    const cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
   }
-  count_launch();
-  return cudaGetLastError();
+  return cudaSuccess;
 }
 
 }  // namespace
@@ -646,11 +656,18 @@ cudaError_t launch_sparse_bwd_neurons(const void* x, const void* dy, int M, int 
   if (f == 0) return cudaSuccess;
 #define TW_NEU(T, V, B, MINB, P) \
   neurons_team<T, V, B, MINB, P>(x, dy, d, f, csc_ptr, csc_row, csc_vals, dwgT, dwuT, dwd, s)
+#define TW_NEU_W(T, V, B, MINB, P, NW) \
+  neurons_team<T, V, B, MINB, P>(x, dy, d, f, csc_ptr, csc_row, csc_vals, dwgT, dwuT, dwd, s, NW)
   // Once x and dY together outgrow L2 the phase runs twice, over dY rows
   // (dWd) and over x rows (dWu^T, dWg^T): each pass gathers from a table half
-  // the size, so more of its rows hit in L2.
+  // the size, so more of its rows hit in L2.  A pass whose table (x or dY,
+  // 2 M d bytes) still outgrows half of L2 runs in column windows, each
+  // gathering a column slice of the rows (d / 2 columns: a table half the
+  // size again) and writing its own columns of dW, so no partial sums are
+  // carried between launches.
   if (4.0 * (double)M * d > 0.75 * l2_bytes()) {
     cudaError_t e;
+    const int windows = (2.0 * (double)M * d > 0.5 * l2_bytes() && d % 16 == 0) ? 2 : 1;
     if (d <= 1024) {
       if ((e = TW_NEU(4, 1, 4, 4, kNeuD)) != cudaSuccess) return e;
       return TW_NEU(4, 1, 4, 4, kNeuX);
@@ -658,6 +675,10 @@ cudaError_t launch_sparse_bwd_neurons(const void* x, const void* dy, int M, int 
     if (d <= 2048) {
       if ((e = TW_NEU(8, 1, 4, 4, kNeuD)) != cudaSuccess) return e;
       return TW_NEU(8, 1, 4, 3, kNeuX);
+    }
+    if (d <= 4096 && windows == 2) {  // 2048-column windows: the 2048-wide shapes
+      if ((e = TW_NEU_W(8, 1, 4, 4, kNeuD, 2)) != cudaSuccess) return e;
+      return TW_NEU_W(8, 1, 4, 3, kNeuX, 2);
     }
     if (d <= 4096) {  // four blocks per SM: 14 % faster on the 8B-class shape than three
       if ((e = TW_NEU(8, 2, 4, 4, kNeuD)) != cudaSuccess) return e;
@@ -677,6 +698,7 @@ cudaError_t launch_sparse_bwd_neurons(const void* x, const void* dy, int M, int 
   if (d <= 4096) return TW_NEU(8, 2, 3, 2, kBoth);
   return TW_NEU(8, 4, 2, 1, kBoth);
 #undef TW_NEU
+#undef TW_NEU_W
 }
 
 }  // namespace tw

@@ -29,12 +29,13 @@ STATUS = {
 }
 EXPORTS = (
     "twell_pack", "twell_pack_dense", "hybrid_route", "twell_workspace_bytes",
+    "twell_workspace_bytes_capped",
     "twell_tiles_workspace_bytes", "twell_set_split_gathers", "twell_ffn_fwd",
     "twell_ffn_bwd", "twell_dense_workspace_bytes", "twell_dense_ffn_fwd", "twell_dense_ffn_bwd",
     "twell_dense_ffn_fwd_act", "twell_dense_ffn_bwd_act",
     "twell_gemm_bf16", "twell_get_device_status", "twell_status_string", "twell_num_sms",
     "twell_launch_count", "twell_profile_begin", "twell_profile_end", "twell_profile_entry",
-    "twell_ffn_fwd_noalloc", "twell_selftest_wait_timeout", "twell_probe_gather",
+    "twell_ffn_fwd_noalloc", "twell_selftest_wait_timeout",
 )
 
 
@@ -57,7 +58,8 @@ class Tiles(ctypes.Structure):
 class Hybrid(ctypes.Structure):
     _fields_ = [("ell_val", ctypes.c_void_p), ("ell_col", ctypes.c_void_p),
                 ("ell_nnz", ctypes.c_void_p), ("ell_width", ctypes.c_int32),
-                ("dense_rows", ctypes.c_void_p), ("n_dense", ctypes.c_void_p)]
+                ("dense_rows", ctypes.c_void_p), ("n_dense", ctypes.c_void_p),
+                ("dense_cap", ctypes.c_int32)]
 
 
 def library_path() -> str:
@@ -81,13 +83,13 @@ def load():
         "twell_pack_dense": (I32, [P, I32, SP, TP, P]),
         "hybrid_route": (I32, [TP, SP, HP, P]),
         "twell_workspace_bytes": (SZ, [SP, I32, I32]),
+        "twell_workspace_bytes_capped": (SZ, [SP, I32, I32, I32]),
         "twell_tiles_workspace_bytes": (SZ, [SP]),
         "twell_set_split_gathers": (I32, [I32]),
         "twell_ffn_fwd": (I32, [P, P, P, P, SP, TP, HP, P, P, SZ, P]),
         "twell_ffn_bwd": (I32, [P, P, P, P, P, SP, HP, F, P, P, P, P, P, SZ, P]),
         "twell_ffn_fwd_noalloc": (I32, [P, P, P, P, SP, HP, P, P]),
         "twell_selftest_wait_timeout": (I32, [I32, P]),
-        "twell_probe_gather": (I32, [P, ctypes.c_int64, I32, P, ctypes.c_int64, P, I32, P]),
         "twell_dense_workspace_bytes": (SZ, [SP, I32]),
         "twell_dense_ffn_fwd": (I32, [P, P, P, P, SP, P, I32, P, SZ, P]),
         "twell_dense_ffn_bwd": (I32, [P, P, P, P, P, SP, F, P, P, P, P, P, SZ, P]),
@@ -151,10 +153,11 @@ class TwellHybrid:
     ell_width: int
     dense_rows: torch.Tensor  # int32 [M]
     n_dense: torch.Tensor     # int32 [1]
+    dense_cap: int            # routed rows the workspace holds (host value)
 
     def c(self) -> Hybrid:
         return Hybrid(_ptr(self.ell_val), _ptr(self.ell_col), _ptr(self.ell_nnz), int(self.ell_width),
-                      _ptr(self.dense_rows), _ptr(self.n_dense))
+                      _ptr(self.dense_rows), _ptr(self.n_dense), int(self.dense_cap))
 
 
 def make_shape(M: int, d_model: int, d_ff: int, tile_n: int = 128, tile_cap: int = 32) -> Shape:
@@ -182,14 +185,17 @@ def tiles_view(t: TwellTiles, shape: Shape):
             t.cnt[: M * T].view(M, T), t.row_nnz[:M])
 
 
-def alloc_hybrid(shape: Shape, ell_width: int, device="cuda") -> TwellHybrid:
+def alloc_hybrid(shape: Shape, ell_width: int, device="cuda",
+                 dense_cap: Optional[int] = None) -> TwellHybrid:
+    """Routing buffers; dense_cap (default M, every row) is the routed-row
+    capacity the workspace will be sized for."""
     M, W = shape.M, int(ell_width)
     ev = torch.empty(_pad16(M * W * 2) // 2, dtype=torch.bfloat16, device=device)
     ec = torch.empty(_pad16(M * W * 2) // 2, dtype=torch.int16, device=device)
     en = torch.empty(_pad16(M * 4) // 4, dtype=torch.int32, device=device)
     dr = torch.empty(_pad16(M * 4) // 4, dtype=torch.int32, device=device)
     nd = torch.zeros(4, dtype=torch.int32, device=device)
-    return TwellHybrid(ev, ec, en, W, dr, nd)
+    return TwellHybrid(ev, ec, en, W, dr, nd, M if dense_cap is None else int(dense_cap))
 
 
 def hybrid_view(h: TwellHybrid, shape: Shape):
@@ -223,8 +229,15 @@ def hybrid_route(tiles: TwellTiles, shape: Shape, out: TwellHybrid, stream=None)
                                                ctypes.byref(h), _stream(stream)))
 
 
-def twell_workspace_bytes(shape: Shape, ell_width: int, training: bool) -> int:
-    return int(load().twell_workspace_bytes(ctypes.byref(shape), int(ell_width), int(training)))
+def twell_workspace_bytes(shape: Shape, ell_width: int, training: bool,
+                          dense_cap: Optional[int] = None) -> int:
+    """Workspace bytes of the sparse forward (and backward, training); room for
+    dense_cap routed rows (default: every row)."""
+    if dense_cap is None:
+        return int(load().twell_workspace_bytes(ctypes.byref(shape), int(ell_width),
+                                                int(training)))
+    return int(load().twell_workspace_bytes_capped(ctypes.byref(shape), int(ell_width),
+                                                   int(dense_cap), int(training)))
 
 
 def twell_tiles_workspace_bytes(shape: Shape) -> int:
@@ -323,12 +336,6 @@ def twell_num_sms() -> int:
 def twell_selftest_wait_timeout(limit_us: int, stream=None):
     _check("twell_selftest_wait_timeout",
            load().twell_selftest_wait_timeout(int(limit_us), _stream(stream)))
-
-
-def twell_probe_gather(table, row_bytes: int, idx, out, blocks: int, stream=None):
-    _check("twell_probe_gather", load().twell_probe_gather(
-        _ptr(table), table.numel() * table.element_size() // int(row_bytes), int(row_bytes),
-        _ptr(idx), idx.numel(), _ptr(out), int(blocks), _stream(stream)))
 
 
 def twell_launch_count() -> int:

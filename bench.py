@@ -250,7 +250,7 @@ def algorithmic_work(family, wl, nnz_ell, n_dense):
 def run_own(args, dist):
     import torch
 
-    from activation_sparse_gated_tcgen05_gb300 import twell
+    from activation_sparse_gated_tcgen05_gb300 import probe, twell
 
     dev = torch.device("cuda", dist.local)
     torch.cuda.set_device(dev)
@@ -271,8 +271,15 @@ def run_own(args, dist):
     nnz = twell.tiles_view(tiles, shape)[3].cpu().numpy()
     rf = wl.route_fraction if args.route_fraction is None else args.route_fraction
     W = synthetic.ell_width(nnz, rf)
+    # route once with room for every row, read the routed-row count from the
+    # device and size the workspace's dense-backup buffers for exactly those
+    # rows (every timed step routes the same inputs the same way; a step that
+    # routed more would record TWELL_ERR_CAPACITY, which voids the run)
     route = twell.alloc_hybrid(shape, W, dev)
-    ws = torch.empty(twell.twell_workspace_bytes(shape, W, True), dtype=torch.uint8, device=dev)
+    twell.hybrid_route(tiles, shape, route)
+    route.dense_cap = int(route.n_dense[0].item())
+    ws = torch.empty(twell.twell_workspace_bytes(shape, W, True, dense_cap=route.dense_cap),
+                     dtype=torch.uint8, device=dev)
     y = torch.empty(M, d, dtype=torch.bfloat16, device=dev)
     dx = torch.empty_like(y)
     dws = [torch.empty(f, d, dtype=torch.float32, device=dev) for _ in range(3)]
@@ -526,19 +533,19 @@ def run_own(args, dist):
     # achievable row-gather bandwidth (the sparse kernels' access pattern):
     # rows of 2*d_model bytes at random ids from a table that fits in L2
     # (the weights of this workload) and from one ten times larger than L2
-    def probe(table_bytes, n_rows=1 << 20):
+    def gather_rate(table_bytes, n_rows=1 << 20):
         row_bytes = 2 * d
         rows = table_bytes // row_bytes
         table = torch.empty(rows * row_bytes // 4, dtype=torch.int32, device=dev)
         idx = torch.randint(0, rows, (n_rows,), dtype=torch.int32, device=dev)
-        out = torch.empty(152 * 32 * 8, dtype=torch.int32, device=dev)
         blocks = 32 * twell.twell_num_sms()
+        out = torch.empty(blocks * 8, dtype=torch.int32, device=dev)
         for _ in range(2):
-            twell.twell_probe_gather(table, row_bytes, idx, out, blocks)
+            probe.gather(table, row_bytes, idx, out, blocks)
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(stream)
         for _ in range(5):
-            twell.twell_probe_gather(table, row_bytes, idx, out, blocks)
+            probe.gather(table, row_bytes, idx, out, blocks)
         e1.record(stream)
         torch.cuda.synchronize()
         return 5 * n_rows * row_bytes / (e0.elapsed_time(e1) / 1e3) / 1e9
@@ -549,8 +556,8 @@ def run_own(args, dist):
     l2_bytes = torch.cuda.get_device_properties(dev).L2_cache_size
     l2_table = min(2 * f * d * 2, l2_bytes // 2)
     gather_probe = {"row_bytes": 2 * d, "l2_resident_table_bytes": l2_table,
-                    "l2_gbs": probe(l2_table), "dram_table_bytes": 2 << 30,
-                    "dram_gbs": probe(2 << 30)}
+                    "l2_gbs": gather_rate(l2_table), "dram_table_bytes": 2 << 30,
+                    "dram_gbs": gather_rate(2 << 30)}
 
     # roofline of the dominant kernel, from its events inside the timed region
     peaks, peak_src = load_peaks()
@@ -563,25 +570,30 @@ def run_own(args, dist):
         # L2-sized passes per step shares it among its launches
         amount /= cnt / args.steps
         per_launch_s = dom_ms / cnt / 1e3
+        traffic, traffic_src = traffic_for(dominant, wl.name)
         if unit == "flop":
             achieved = amount / per_launch_s / 1e12
-            peak, punit = peaks["bf16_tflops"], "TFLOP/s"
+            roof = {"kernel": dominant, "bound": "tensor", "achieved": achieved,
+                    "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                    "frac": achieved / peaks["bf16_tflops"],
+                    "peak_source": "%s bf16 burst (MEASURED_PEAKS.json)" % peak_src}
         else:
+            # a gather whose weight rows L2 serves (DRAM traffic far below the
+            # algorithmic bytes): its ceiling is the row-gather rate measured
+            # in this run; the HBM copy rate is reported beside it
             achieved = amount / per_launch_s / 1e9
-            peak, punit = peaks["hbm_gbs"], "GB/s"
-        roof = {"kernel": dominant, "bound": bound, "achieved": achieved, "peak": peak,
-                "unit": punit, "frac": achieved / peak, "peak_source": peak_src,
-                "work_per_launch": amount, "work_unit": unit, "ms_per_launch": dom_ms / cnt,
-                "traffic": traffic_for(dominant, wl.name)}
-        if unit == "byte":
-            # the weight rows this kernel gathers are L2-resident at this size:
-            # its ceiling is the measured L2 row-gather bandwidth
-            roof["l2_gather_peak"] = gather_probe["l2_gbs"]
-            roof["frac_of_l2_gather"] = achieved / gather_probe["l2_gbs"]
-            roof["note"] = ("algorithmic bytes of a gather whose rows L2 serves; frac is "
-                            "against the HBM copy rate (above 1 when L2 serves them), "
-                            "frac_of_l2_gather against the measured L2 row-gather probe; "
-                            "traffic is the DRAM bytes per launch from ncu")
+            roof = {"kernel": dominant, "bound": "l2", "achieved": achieved,
+                    "peak": gather_probe["l2_gbs"], "unit": "GB/s",
+                    "frac": achieved / gather_probe["l2_gbs"],
+                    "peak_source": "row-gather probe of this run (%d-byte rows at random ids "
+                                   "from an L2-resident table)" % gather_probe["row_bytes"],
+                    "hbm_peak": peaks["hbm_gbs"], "frac_of_hbm": achieved / peaks["hbm_gbs"],
+                    "hbm_peak_source": "%s HBM copy (MEASURED_PEAKS.json)" % peak_src}
+        roof.update({"work_per_launch": amount, "work_unit": unit,
+                     "ms_per_launch": dom_ms / cnt, "launches_per_step": cnt / args.steps,
+                     "traffic": traffic, "traffic_source": traffic_src})
+
+    memory = measure_memory(twell, shape, W, x, wg, wu, wd, dy, dev)
 
     # end to end through the C ABI with host buffers (H2D inputs, D2H results)
     xh = torch.empty((M, d), dtype=torch.bfloat16).pin_memory()
@@ -668,6 +680,7 @@ def run_own(args, dist):
         "ms_median": medians,
         "ms_per_step_median": medians.get("sparse_fwd_bwd"),
         "saved_for_backward_bytes": saved_bytes(shape, W, M, f, d),
+        "memory": memory,
         "measured_density": density, "routed_rows": n_dense, "ell_entries": nnz_ell,
         "roofline": roof, "gather_probe": gather_probe, "kernels": kernels,
         "kernels_fwd": kernels_fwd, "kernels_dense_step": kernels_dense,
@@ -696,6 +709,75 @@ def run_own(args, dist):
     dist.close()
 
 
+def measure_memory(twell, shape, W, x, wg, wu, wd, dy, dev):
+    """Device memory of one training step, measured with the caching
+    allocator's peak counter: every buffer a step allocates (packed format,
+    routing arrays, workspace, y, dX, dW) from a state holding only the
+    inputs and weights, the step run, and the peak read after it.  Also the
+    bytes alive between forward and backward beyond y (what a training
+    framework keeps for the backward)."""
+    import torch
+
+    M, d, f = shape.M, shape.d_model, shape.d_ff
+
+    def window(run):
+        torch.cuda.synchronize(dev)
+        base = torch.cuda.memory_allocated(dev)
+        torch.cuda.reset_peak_memory_stats(dev)
+        kept = run()
+        torch.cuda.synchronize(dev)
+        peak = torch.cuda.max_memory_allocated(dev) - base
+        return peak, kept
+
+    def sparse():
+        tiles = twell.alloc_tiles(shape, dev)
+        twell.twell_pack(x, wg, shape, tiles)
+        route = twell.alloc_hybrid(shape, W, dev)
+        twell.hybrid_route(tiles, shape, route)
+        del tiles  # transient: the route holds what the backward reads
+        route.dense_cap = int(route.n_dense[0].item())
+        ws = torch.empty(twell.twell_workspace_bytes(shape, W, True, dense_cap=route.dense_cap),
+                         dtype=torch.uint8, device=dev)
+        y = torch.empty(M, d, dtype=torch.bfloat16, device=dev)
+        twell.twell_ffn_fwd(x, wg, wu, wd, shape, y, route=route, ws=ws)
+        torch.cuda.synchronize(dev)
+        saved = torch.cuda.memory_allocated(dev) - base0[0] - y.numel() * 2
+        dx = torch.empty_like(y)
+        dws = [torch.empty(f, d, dtype=torch.float32, device=dev) for _ in range(3)]
+        twell.twell_ffn_bwd(x, wg, wu, wd, dy, shape, route, L1, dx, *dws, ws)
+        return saved, ws.numel()
+
+    def dense():
+        ws = torch.empty(twell.twell_dense_workspace_bytes(shape, True), dtype=torch.uint8,
+                         device=dev)
+        y = torch.empty(M, d, dtype=torch.bfloat16, device=dev)
+        twell.twell_dense_ffn_fwd(x, wg, wu, wd, shape, y, True, ws)
+        torch.cuda.synchronize(dev)
+        saved = torch.cuda.memory_allocated(dev) - base0[0] - y.numel() * 2
+        dx = torch.empty_like(y)
+        dws = [torch.empty(f, d, dtype=torch.float32, device=dev) for _ in range(3)]
+        twell.twell_dense_ffn_bwd(x, wg, wu, wd, dy, shape, L1, dx, *dws, ws)
+        return saved, ws.numel()
+
+    base0 = [torch.cuda.memory_allocated(dev)]
+    sp_peak, (sp_saved, sp_ws) = window(sparse)
+    torch.cuda.synchronize(dev)
+    base0[0] = torch.cuda.memory_allocated(dev)
+    de_peak, (de_saved, de_ws) = window(dense)
+    if twell.twell_get_device_status() != 0:
+        raise RuntimeError("device status after the memory measurement")
+    outputs = 2 * M * d * 2 + 3 * f * d * 4
+    return {"sparse_step_peak_bytes": sp_peak, "dense_step_peak_bytes": de_peak,
+            "sparse_over_dense_peak": sp_peak / de_peak,
+            "sparse_saved_for_bwd_bytes": sp_saved, "dense_saved_for_bwd_bytes": de_saved,
+            "sparse_workspace_bytes": sp_ws, "dense_workspace_bytes": de_ws,
+            "outputs_bytes": outputs,
+            "how": "torch.cuda.max_memory_allocated over one fwd+bwd step that allocates its "
+                   "own buffers (packed tiles, routing arrays, workspace sized for the routed "
+                   "rows, y, dX, dW; inputs and weights resident before); saved_for_bwd = bytes "
+                   "alive after the forward beyond y"}
+
+
 def saved_bytes(shape, W, M, f, d):
     """Activation memory kept from the forward for the backward: the sparse
     path keeps the hybrid ELL arrays (the TwELL tiles are transient: routing
@@ -708,16 +790,45 @@ def saved_bytes(shape, W, M, f, d):
             "dense_over_sparse": dense / ell}
 
 
+# device sources each kernel family is built from: a committed DRAM capture
+# counts only while these files are unchanged
+FAMILY_SOURCES = {
+    "gemm": ("gemm_tc.cuh", "gemm_tc.cu", "common.cuh"),
+    "sparse_fwd": ("sparse_fwd.cu", "ell_gather.cuh", "common.cuh"),
+    "bwd": ("sparse_bwd.cu", "ell_gather.cuh", "common.cuh"),
+}
+
+
+def source_sha(kernel):
+    """Fingerprint (sha256, 16 hex digits) of the sources of a kernel family."""
+    import hashlib
+
+    key = ("gemm" if kernel.startswith("gemm") else
+           "sparse_fwd" if kernel.startswith("sparse_fwd") else "bwd")
+    h = hashlib.sha256()
+    for name in FAMILY_SOURCES[key]:
+        with open(os.path.join(ROOT, "activation_sparse_gated_tcgen05_gb300", "csrc", name),
+                  "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
 def traffic_for(kernel, workload):
-    """DRAM bytes per launch from a committed ncu capture, if one exists for
-    this kernel and workload (profiles/dram_traffic.json)."""
+    """DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum)
+    from a committed ncu capture of this kernel and workload
+    (profiles/dram_traffic.json), and where it came from.  None when there
+    is no capture or the kernel's sources changed since it was taken."""
     path = os.path.join(ROOT, "profiles", "dram_traffic.json")
     try:
         with open(path) as fh:
-            t = json.load(fh)
-        return t.get(workload, {}).get(kernel)
+            e = json.load(fh).get(workload, {}).get(kernel)
     except (OSError, ValueError):
-        return None
+        e = None
+    if not isinstance(e, dict) or "bytes" not in e:
+        return None, "no ncu capture of this kernel and workload"
+    if e.get("source_sha16") != source_sha(kernel):
+        return None, "ncu capture predates the current kernel sources"
+    return float(e["bytes"]), "ncu capture %s (profiles/dram_traffic.json)" % e.get("capture", "")
 
 
 # ---------------------------------------------------------------- reference arm
@@ -730,9 +841,15 @@ def run_reference(args, dist):
     bits = synthetic.make_workload(wl)
     import oracle
 
-    x64 = oracle.f64(bits["x"])
-    a = oracle.gate_preact(x64[: min(wl.M, 2048)], oracle.f64(bits["wgT"]))
-    _, _, _, nnz = oracle.twell_pack(a, wl.tile_n, wl.tile_cap)
+    # the ELL width from every row of the workload, as the GPU arm takes it
+    oracle.set_threads(os.cpu_count() or 1)
+    wg64 = oracle.f64(bits["wgT"])
+    nnz = []
+    for r0 in range(0, wl.M, 4096):  # row blocks bound the fp64 pre-activation's memory
+        a = oracle.gate_preact(oracle.f64(bits["x"][r0:r0 + 4096]), wg64)
+        nnz.append(oracle.twell_pack(a, wl.tile_n, wl.tile_cap)[3])
+        del a
+    nnz = np.concatenate(nnz)
     rf = wl.route_fraction if args.route_fraction is None else args.route_fraction
     W = synthetic.ell_width(nnz, rf)
     budget = 150.0 / max(1, args.steps + args.warmup)  # whole run within a few minutes

@@ -81,12 +81,22 @@ typedef struct twell_tiles {
   int32_t* row_nnz;
 } twell_tiles;
 
-/* Hybrid ELL / dense-backup routing (device).
+/* Hybrid ELL / dense-backup routing (device arrays, one host field).
  *   ell_val    bf16 [M][ell_width]  live gate values, ascending global column
  *   ell_col    u16  [M][ell_width]  global column (neuron) of each value
  *   ell_nnz    i32  [M]             entries used in the row; 0 for routed rows
  *   dense_rows i32  [M]             routed rows, ascending, first *n_dense valid
- *   n_dense    i32  [1]             number of routed rows (stays on the device) */
+ *   n_dense    i32  [1]             number of routed rows (stays on the device)
+ *   dense_cap  host int: how many routed rows the caller's workspace holds
+ *              (0 <= dense_cap; values above M count as M).  The routed rows'
+ *              buffers of the workspace, and so its size, scale with it.
+ *              hybrid_route records TWELL_ERR_CAPACITY in the device status
+ *              word when it routes more rows than dense_cap; the forward and
+ *              backward then compute only the first dense_cap routed rows and
+ *              leave the others' y / dx rows and dW terms out.  The count is
+ *              on the device, so a caller that can read it may route with
+ *              dense_cap = M, read *n_dense and size the workspace for exactly
+ *              that many rows (setting dense_cap to it). */
 typedef struct twell_hybrid {
   void* ell_val;
   uint16_t* ell_col;
@@ -94,6 +104,7 @@ typedef struct twell_hybrid {
   int32_t ell_width;
   int32_t* dense_rows;
   int32_t* n_dense;
+  int32_t dense_cap;
 } twell_hybrid;
 
 /* Gate projection with the TwELL pack fused into its epilogue.
@@ -126,9 +137,16 @@ twell_status hybrid_route(const twell_tiles* in, const twell_shape* shape,
                           const twell_hybrid* out, void* stream);
 
 /* Bytes of workspace twell_ffn_fwd (training = 0) or twell_ffn_fwd +
- * twell_ffn_bwd (training = 1) need for this shape and ELL width.  The
- * workspace is sized for the worst case (every row routed).  Returns 0 for an
- * invalid shape. */
+ * twell_ffn_bwd (training = 1) need for this shape, ELL width and routed-row
+ * capacity (the route's dense_cap; values above M count as M).  The routed
+ * rows' buffers hold dense_cap rows in whole 128-row tiles; the rest grows
+ * with M * ell_width (per-entry values of the backward) and M * d_model (the
+ * fp32 running y / dX of L2-sized passes, and the routed rows' split-K
+ * partials).  Returns 0 for an invalid shape or a negative width or capacity. */
+size_t twell_workspace_bytes_capped(const twell_shape* shape, int32_t ell_width,
+                                    int32_t dense_cap, int32_t training);
+
+/* twell_workspace_bytes_capped with dense_cap = M (room for every row routed). */
 size_t twell_workspace_bytes(const twell_shape* shape, int32_t ell_width, int32_t training);
 
 /* Bytes of the optional workspace of twell_ffn_fwd with `tiles` (inference).
@@ -165,8 +183,8 @@ int32_t twell_set_split_gathers(int32_t enable);
  * routed rows by a dense tensor-core gated FFN that recomputes their gate)
  * is non-NULL.  wgT is read only for routed rows (may be NULL with tiles).
  * ws/ws_bytes: with `route`, a workspace of at least
- * twell_workspace_bytes(shape, W, 0) bytes (16-byte aligned); besides the
- * routed rows' buffers it carries the fp32 running y between passes when
+ * twell_workspace_bytes_capped(shape, W, route->dense_cap, 0) bytes (16-byte
+ * aligned); besides the routed rows' buffers it carries the fp32 running y between passes when
  * the gathered Wu / Wd rows exceed L2 and the ELL gather is split into
  * L2-sized neuron passes (same result, bit for bit), and for rows wider than
  * 1024 the fp32 h of every live ELL entry between the up and down gathers.  With `tiles` the
@@ -182,23 +200,27 @@ twell_status twell_ffn_fwd(const void* x, const void* wgT, const void* wuT, cons
 
 /* Allocation-free variant of twell_ffn_fwd for the training (route) path.
  * The pages have no counterpart: this entry point exists for callers that
- * cannot allocate device memory when they run the FFN (inside a stream
- * capture, under a host runtime that owns all allocations, or with a fixed
- * memory budget).  It computes exactly what twell_ffn_fwd(..., tiles = NULL,
- * route, ...) computes, with the routed-row scratch taken from a 32 MiB
- * array compiled into the library (held by every device that loads the
- * library until the process exits) instead of a caller workspace.  It
- * allocates nothing and calls no allocating routine.
- *   - Limit: twell_workspace_bytes(shape, route->ell_width, 0) must not exceed
- *     32 MiB (e.g. M <= 1408 at d_model = 1024, d_ff = 4096); larger shapes
- *     return TWELL_ERR_WORKSPACE before any launch.
- *   - The first call on each device looks up the array's device address
- *     (with that device current); make that first call before any stream
- *     capture.
+ * cannot allocate device memory when they run the FFN -- a plugin whose host
+ * runtime owns every allocation, a scheduler that must not call cudaMalloc
+ * (which can synchronise the device) in the middle of a step, or a
+ * deployment whose memory footprint is fixed up front.  It computes exactly
+ * what twell_ffn_fwd(..., tiles = NULL, route, ...) computes, with the
+ * routed-row scratch taken from a 32 MiB array compiled into the library
+ * (held by every device that loads the library until the process exits)
+ * instead of a caller workspace.  It allocates nothing and calls no
+ * allocating routine.
+ *   - Limit: twell_workspace_bytes_capped(shape, route->ell_width,
+ *     route->dense_cap, 0) must not exceed 32 MiB (e.g. M <= 1408 at
+ *     d_model = 1024, d_ff = 4096 with room for every row routed); larger
+ *     needs return TWELL_ERR_WORKSPACE before any launch.
+ *   - The array's device address is looked up on the first call on each
+ *     device (with that device current) and cached; make that first call
+ *     before any stream capture.  `stream` must belong to the current
+ *     device, and the cached address does not survive cudaDeviceReset.
  *   - Every call on a device shares the one array and it keeps the previous
  *     call's contents; nothing in it needs to start at zero.  Calls that
- *     overlap on the GPU (different streams, or graphs replayed concurrently)
- *     race on it and must be serialised by the caller. */
+ *     overlap on the GPU (on different streams, for example) race on it and
+ *     must be serialised by the caller. */
 twell_status twell_ffn_fwd_noalloc(const void* x, const void* wgT, const void* wuT,
                                    const void* wd, const twell_shape* shape,
                                    const twell_hybrid* route, void* y, void* stream);
@@ -214,8 +236,8 @@ twell_status twell_ffn_fwd_noalloc(const void* x, const void* wgT, const void* w
  * using only the live entries of ELL rows and a dense tensor-core path for the
  * routed rows.  The route must come from hybrid_route on the same x and Wg.
  * The reduction order is fixed, so results are bit-reproducible.
- * ws/ws_bytes: at least twell_workspace_bytes(shape, W, 1) bytes (16-byte
- * aligned); it also carries the fp32 running dX when the row phase runs in
+ * ws/ws_bytes: at least twell_workspace_bytes_capped(shape, W, route->dense_cap, 1)
+ * bytes (16-byte aligned); it also carries the fp32 running dX when the row phase runs in
  * L2-sized neuron passes and, for rows wider than 1024 (split gathers, see
  * twell_set_split_gathers), dh and (du, da) of every live ELL entry.  When x
  * and dY together exceed 3/4 of L2 the weight gradients are formed in two
@@ -279,15 +301,6 @@ twell_status twell_gemm_bf16(const void* A, const void* B, void* C, int32_t M, i
  * Read the result with twell_get_device_status.  Not part of the method. */
 twell_status twell_selftest_wait_timeout(int32_t limit_us, void* stream);
 
-/* Row-gather bandwidth probe (measurement helper, not part of the method):
- * blocks x 8 warps read n_idx whole rows table[idx[i]] (row_bytes each, a
- * multiple of 16, 16-byte loads) -- the access pattern of the sparse gather
- * kernels -- and write one folded word per warp to out (blocks * 8 words).
- * Time it with the profiler family "gather_probe" or events. */
-twell_status twell_probe_gather(const void* table, int64_t table_rows, int32_t row_bytes,
-                                const int32_t* idx, int64_t n_idx, uint32_t* out, int32_t blocks,
-                                void* stream);
-
 /* Reads and clears the device status word of the current device after
  * synchronising `stream`.  *out receives TWELL_OK or the first error seen. */
 twell_status twell_get_device_status(void* stream, int32_t* out);
@@ -310,7 +323,7 @@ uint64_t twell_launch_count(void);
  * available from twell_profile_entry (name valid until the next begin/end).
  * Families: gemm_gate_pack, gemm_gated, gemm_dgate, gemm_store_kk/mk/km/mm,
  * pack_dense, route_rows, route_list, gather_rows, sparse_fwd, csc_mark,
- * csc_colscan, csc_ptr, csc_place, bwd_rows, bwd_neurons, gather_probe.  Host-side state,
+ * csc_colscan, csc_ptr, csc_place, bwd_rows, bwd_neurons.  Host-side state,
  * process-wide; not for use while another thread launches. */
 twell_status twell_profile_begin(const char* kernel);
 int32_t twell_profile_end(void);

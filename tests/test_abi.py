@@ -62,9 +62,14 @@ def test_host_validation_before_launch(lib):
     # exactly one of tiles / route
     assert lib.twell_ffn_fwd(16, 16, 16, 16, ctypes.byref(s), None, None, 16, None, 0, None) == 1
     # workspace too small
-    h = twell.Hybrid(16, 16, 16, 8, 16, 16)
+    h = twell.Hybrid(16, 16, 16, 8, 16, 16, 256)
     assert lib.twell_ffn_fwd(16, 16, 16, 16, ctypes.byref(s), None, ctypes.byref(h), 16, 16, 8,
                              None) == 7
+    # a negative routed-row capacity
+    hneg = twell.Hybrid(16, 16, 16, 8, 16, 16, -1)
+    assert lib.hybrid_route(ctypes.byref(t), ctypes.byref(s), ctypes.byref(hneg), None) == 1
+    assert lib.twell_ffn_fwd(16, 16, 16, 16, ctypes.byref(s), None, ctypes.byref(hneg), 16, 16,
+                             1 << 30, None) == 1
     # TwELL forward of wide rows: a workspace that is given must hold h
     wide = twell.make_shape(256, 2048, 1024, 64, 16)
     assert lib.twell_ffn_fwd(16, 16, 16, 16, ctypes.byref(wide), ctypes.byref(t), None, 16, 16,
@@ -92,9 +97,34 @@ def test_workspace_sizes(lib):
     tr = twell.twell_workspace_bytes(s, 30, True)
     assert 0 < inf < tr
     assert twell.twell_workspace_bytes(twell.make_shape(16, 100, 1024, 64, 16), 4, True) == 0
+    # the dense-backup buffers scale with the routed-row capacity
+    assert twell.twell_workspace_bytes(s, 30, True, dense_cap=16384) == tr
+    assert twell.twell_workspace_bytes(s, 30, True, dense_cap=1 << 20) == tr
+    c512 = twell.twell_workspace_bytes(s, 30, True, dense_cap=512)
+    c0 = twell.twell_workspace_bytes(s, 30, True, dense_cap=0)
+    assert 0 < c0 < c512 < tr / 2
+    assert twell.twell_workspace_bytes(s, 30, True, dense_cap=-1) == 0
+    # 512 routed rows (4 tiles) of x, dY, h hi+lo, g, u fp32, du/da hi+lo
+    f, d = 4096, 1024
+    assert c512 - c0 >= 512 * (2 * d * 2 + 2 * f * 2 + f * 2 + f * 4 + 4 * f * 2)
     assert twell.twell_dense_workspace_bytes(s, True) >= 5 * 16384 * 4096 * 2
     # TwELL forward: no workspace up to d_model = 1024, then h per slot + the y carry
     assert twell.twell_tiles_workspace_bytes(s) == 0
     wide = twell.make_shape(32768, 2048, 8192, 128, 32)
     assert twell.twell_tiles_workspace_bytes(wide) >= 4 * 32768 * (64 * 32 + 2048)
     assert twell.twell_tiles_workspace_bytes(twell.make_shape(16, 100, 1024, 64, 16)) == 0
+
+
+def test_gather_probe_lives_in_its_own_library(lib):
+    """The benchmark's row-gather probe is a separate library, not part of
+    the FFN library's ABI."""
+    assert not hasattr(lib, "twell_probe_gather")
+    from activation_sparse_gated_tcgen05_gb300 import probe
+
+    plib = probe.load()
+    assert hasattr(plib, "twell_probe_gather")
+    # host-side checks: null table, output shorter than one word per warp
+    assert plib.twell_probe_gather(None, 4, 16, 16, 1, 16, 8, 1, None) == 1
+    assert plib.twell_probe_gather(16, 4, 16, 16, 1, 16, 7, 1, None) == 1
+    assert plib.twell_probe_gather(16, 4, 24, 16, 1, 16, 8, 1, None) == 2
+    assert plib.twell_probe_gather(8, 4, 16, 16, 1, 16, 8, 1, None) == 3

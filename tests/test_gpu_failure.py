@@ -28,16 +28,3 @@ def test_bounded_wait_reports_timeout_and_context_survives():
     ref = A.double().cpu() @ B.double().cpu().t()
     np.testing.assert_array_equal(C.cpu().double().numpy(), ref.numpy())
 
-
-def test_gather_probe_reads_rows():
-    rows, row_bytes = 1024, 2048
-    table = torch.randint(0, 2 ** 31 - 1, (rows * row_bytes // 4,), dtype=torch.int32).cuda()
-    idx = torch.randint(0, rows, (4096,), dtype=torch.int32).cuda()
-    out = torch.zeros(8 * 4, dtype=torch.int32).cuda()
-    twell.twell_probe_gather(table, row_bytes, idx, out, 4)
-    torch.cuda.synchronize()
-    # fold on the host: warp w reads rows idx[w], idx[w + 32], ...
-    t = table.cpu().numpy().view(np.uint32).reshape(rows, -1)
-    i = idx.cpu().numpy()
-    want = [np.bitwise_xor.reduce(t[i[w::32]].reshape(-1)) for w in range(32)]
-    np.testing.assert_array_equal(out.cpu().numpy().view(np.uint32), np.array(want, np.uint32))

@@ -205,3 +205,48 @@ def test_multi_pass_twell_split_forward_matches_fused():
     assert twell.twell_get_device_status() == 0
     assert prof["sparse_fwd_up"][0] == passes and prof["sparse_fwd_down"][0] == passes, prof
     assert torch.equal(y_split.view(torch.int16), y_fused.view(torch.int16))
+
+
+def test_neuron_phase_column_windows_when_x_alone_exceeds_half_of_l2():
+    """When x (or dY) alone outgrows half of L2, each neuron pass runs in two
+    column windows that gather a column slice of the rows and own their dW
+    columns: four launches in all.  Sampled neurons (every column, both
+    windows) against the oracle."""
+    from helpers import bwd_allowance_sampled
+
+    l2 = torch.cuda.get_device_properties(0).L2_cache_size
+    d, f, lam = 4096, 1024, 2e-5
+    M = int(math.ceil(0.5 * l2 / (2 * d) / 128.0)) * 128 + 256
+    assert 2.0 * M * d > 0.5 * l2
+    w = synthetic.make_inputs(M, d, f, density=0.01, seed=14)
+    x, wg, wu, wd, dy = (dev_bf16(w[k]) for k in ("x", "wgT", "wuT", "wd", "dy"))
+    shape = twell.make_shape(M, d, f, 128, 32)
+    tiles = twell.alloc_tiles(shape)
+    twell.twell_pack(x, wg, shape, tiles)
+    W = int(twell.tiles_view(tiles, shape)[3].max().item())
+    route = twell.alloc_hybrid(shape, W, dense_cap=0)
+    twell.hybrid_route(tiles, shape, route)
+    ws = torch.empty(twell.twell_workspace_bytes(shape, W, True, dense_cap=0), dtype=torch.uint8,
+                     device="cuda")
+    dx = torch.empty((M, d), dtype=torch.bfloat16, device="cuda")
+    dws = [torch.full((f, d), float("nan"), device="cuda") for _ in range(3)]
+    twell.twell_profile_begin("*")
+    twell.twell_ffn_bwd(x, wg, wu, wd, dy, shape, route, lam, dx, *dws, ws)
+    torch.cuda.synchronize()
+    prof = twell.twell_profile_end()
+    assert twell.twell_get_device_status() == 0
+    assert prof["bwd_neurons_dy"][0] == 2 and prof["bwd_neurons_x"][0] == 2, prof
+    for t in dws:
+        assert torch.isfinite(t).all()  # both windows wrote every column
+    rows = np.array([0, M - 1], dtype=np.int64)
+    neurons = np.array([0, 3, f // 2, f - 1], dtype=np.int64)
+    oracle.set_threads(os.cpu_count() or 1)
+    try:
+        al = bwd_allowance_sampled(w, lam, rows, neurons)
+        og, ou, od = oracle.ffn_bwd_dw_neurons(w["x"], w["wgT"], w["wuT"], w["wd"], w["dy"], lam,
+                                               neurons)
+    finally:
+        oracle.set_threads(1)
+    assert_close(dws[0].cpu().numpy()[neurons], og, "dwgT", allowance=al["dwgT"])
+    assert_close(dws[1].cpu().numpy()[neurons], ou, "dwuT", allowance=al["dwuT"])
+    assert_close(dws[2].cpu().numpy()[neurons], od, "dwd", allowance=al["dwd"])
