@@ -14,6 +14,9 @@ INCLUDE = os.path.join(ROOT, "include")
 OUT_DIR = os.path.join(PKG, "_build")
 LIB = os.path.join(OUT_DIR, "libtwell.so")
 PROBE_LIB = os.path.join(OUT_DIR, "libtwell_probe.so")
+# the checked (debug) build: every index a gather reads is bounds-checked on
+# the device and reported as TWELL_ERR_INDEX (see common.cuh)
+CHECKED_LIB = os.path.join(OUT_DIR, "libtwell_checked.so")
 
 SOURCES = ["api.cu", "gemm_tc.cu", "pack.cu", "sparse_fwd.cu", "sparse_bwd.cu", "selftest.cu"]
 PROBE_SOURCES = ["gather_probe.cu"]
@@ -35,6 +38,33 @@ def _newest_input() -> float:
     files.append(os.path.join(INCLUDE, "twell.h"))
     files.append(os.path.abspath(__file__))
     return max(os.path.getmtime(f) for f in files)
+
+
+def build_checked(force: bool = False) -> str:
+    """Compile and link libtwell_checked.so (-DTWELL_CHECKED) if any input is
+    newer than it."""
+    os.makedirs(OUT_DIR, exist_ok=True)
+    if not force and os.path.exists(CHECKED_LIB) and os.path.getmtime(CHECKED_LIB) >= _newest_input():
+        return CHECKED_LIB
+    nvcc = _nvcc()
+
+    def compile_one(src: str) -> str:
+        obj = os.path.join(OUT_DIR, os.path.splitext(src)[0] + "_checked.o")
+        cmd = [nvcc] + NVCC_FLAGS + ["-DTWELL_CHECKED", "-c", os.path.join(CSRC, src), "-o", obj]
+        res = subprocess.run(cmd, capture_output=True, text=True)
+        if res.returncode != 0:
+            raise RuntimeError("nvcc failed for %s:\n%s%s" % (src, res.stdout, res.stderr))
+        return obj
+
+    with concurrent.futures.ThreadPoolExecutor(max_workers=len(SOURCES)) as ex:
+        objs = list(ex.map(compile_one, SOURCES))
+    tmp = CHECKED_LIB + ".tmp%d" % os.getpid()
+    cmd = [nvcc] + ARCH + ["-shared", "-cudart", "shared", "-o", tmp] + objs
+    res = subprocess.run(cmd, capture_output=True, text=True)
+    if res.returncode != 0:
+        raise RuntimeError("link failed:\n%s%s" % (res.stdout, res.stderr))
+    os.replace(tmp, CHECKED_LIB)
+    return CHECKED_LIB
 
 
 def build(force: bool = False, verbose: bool = False) -> str:
@@ -74,4 +104,7 @@ def build(force: bool = False, verbose: bool = False) -> str:
 
 if __name__ == "__main__":
     import sys
-    print(build(force=True, verbose="-v" in sys.argv))
+    if "--checked" in sys.argv:
+        print(build_checked(force=True))
+    else:
+        print(build(force=True, verbose="-v" in sys.argv))

@@ -461,6 +461,7 @@ const char* twell_status_string(int32_t status) {
     case TWELL_ERR_CUDA: return "CUDA error";
     case TWELL_ERR_DEVICE_TIMEOUT: return "device pipeline wait timed out";
     case TWELL_ERR_WORKSPACE: return "workspace missing or too small";
+    case TWELL_ERR_INDEX: return "index out of range (checked build)";
   }
   return "unknown status";
 }

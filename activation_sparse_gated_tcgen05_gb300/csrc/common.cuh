@@ -35,6 +35,47 @@ TW_DEV void set_status(int* status, int code) {
   if (status) atomicCAS(status, 0, code);
 }
 
+// ------------------------------------------------------------ checked build
+// Built with -DTWELL_CHECKED (a debug library), every index a gather or
+// index kernel reads from memory -- a column below d_ff, an in-tile column
+// below T_n, a row below M, an entry position below M * W, an ELL length of
+// at most W -- is tested before it is used: a bad one is replaced by 0 (an
+// index that is always in bounds) and TWELL_ERR_INDEX is recorded in the
+// device status word, with no trap.  In the normal build the checks vanish.
+// Each translation unit keeps its own copy of the status word's address,
+// set by checked_setup() (host) before its first launch on a device; that
+// setup is a synchronous copy, so the first call on a device must not be
+// inside a stream capture.
+int* device_status_ptr();
+#ifdef TWELL_CHECKED
+static __device__ int* g_checked_status;
+#define TW_CHECK_INDEX(v, ok)                                    \
+  do {                                                           \
+    if (!(ok)) {                                                 \
+      ::tw::set_status(::tw::g_checked_status, TWELL_ERR_INDEX); \
+      (v) = 0;                                                   \
+    }                                                            \
+  } while (0)
+static inline cudaError_t checked_setup() {
+  static int* done[64] = {nullptr};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  int* st = device_status_ptr();
+  if (!st) return cudaErrorInvalidSymbol;
+  if (done[dev] == st) return cudaSuccess;
+  e = cudaMemcpyToSymbol(g_checked_status, &st, sizeof(st));
+  if (e == cudaSuccess) done[dev] = st;
+  return e;
+}
+#else
+#define TW_CHECK_INDEX(v, ok) \
+  do {                        \
+  } while (0)
+static inline cudaError_t checked_setup() { return cudaSuccess; }
+#endif
+
 // ------------------------------------------------------------------ mbarrier
 TW_DEV void mbar_init(uint64_t* bar, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count)

@@ -78,15 +78,20 @@ struct EllSrc {
   const int* nnz;       // [M]
   int W;
   int j_lo, j_hi, whole;  // neuron chunk [j_lo, j_hi); whole: every entry
+  int f;                  // d_ff (columns are below it)
   template <class F>
-  __device__ __forceinline__ void for_groups(int m, int lane, F&& f) const {
+  __device__ __forceinline__ void for_groups(int m, int lane, F&& fn) const {
     const long long row_off = (long long)m * W;
+    int n = nnz[m];
+    TW_CHECK_INDEX(n, n >= 0 && n <= W);
     int a, b;
-    ell_slice(col, row_off, nnz[m], j_lo, j_hi, whole, lane, a, b);
+    ell_slice(col, row_off, n, j_lo, j_hi, whole, lane, a, b);
     for (int e0 = a; e0 < b; e0 += 32) {
       const int count = min(32, b - e0);
       const long long s = row_off + e0 + lane;
-      f(count, lane < count ? (int)col[s] : 0, s, s);
+      int j = lane < count ? (int)col[s] : 0;
+      TW_CHECK_INDEX(j, j < f);
+      fn(count, j, s, s);
     }
   }
 };
@@ -131,7 +136,9 @@ struct TwellSrc {
         if (e < total) {
           const int tt = t0 + lo;
           sl = ((long long)m * T + tt) * cap + (e - ex);
-          jl = tt * tile_n + idx[sl];
+          int il = idx[sl];
+          TW_CHECK_INDEX(il, il < tile_n);
+          jl = tt * tile_n + il;
         }
         f(min(32, total - e0), jl, sl, e_row + e);
       }
@@ -217,7 +224,9 @@ __global__ void __launch_bounds__(256, MINB) ell_dot_kernel(const EllDotArgs p, 
       } else {  // ReLU'(a) = 1 on a live entry
         const float dh = p.dh[he];
         const float du = dh * g, da = fmaf(dh, dot, p.lambda);
-        p.csc_vals[p.slot_pos[s]] = make_float4(du, da, g * dot, 0.f);
+        long long pos = p.slot_pos[s];
+        TW_CHECK_INDEX(pos, pos >= 0 && pos < (long long)p.M * src.W);
+        p.csc_vals[pos] = make_float4(du, da, g * dot, 0.f);
         p.coef[he] = make_float2(du, da);
       }
     }

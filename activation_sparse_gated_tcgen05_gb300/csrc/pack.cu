@@ -125,8 +125,10 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32)
         const int tt = t0 + lo;
         const long long src = ((long long)m * T + tt) * cap + (e - ex);
         const long long dst = (long long)m * W + base + e;
+        int il = idx[src];
+        TW_CHECK_INDEX(il, il < tile_n);
         ell_val[dst] = val[src];
-        ell_col[dst] = (uint16_t)(tt * tile_n + idx[src]);
+        ell_col[dst] = (uint16_t)(tt * tile_n + il);
       }
     }
     base += total;
@@ -299,6 +301,10 @@ cudaError_t launch_pack_dense(const void* a, int a_f32, int M, int f, int tile_n
 cudaError_t launch_route(const twell_tiles& in, int M, int f, int tile_n, int cap,
                          const twell_hybrid& out, int* flags, int dense_cap, cudaStream_t s) {
   if (M == 0) return cudaMemsetAsync(out.n_dense, 0, sizeof(int), s);
+  {
+    const cudaError_t ce = checked_setup();
+    if (ce != cudaSuccess) return ce;
+  }
   const int T = f / tile_n;
   const int grid = (M + kWarpsPerBlock - 1) / kWarpsPerBlock;
   {

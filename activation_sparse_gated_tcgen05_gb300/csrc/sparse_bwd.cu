@@ -46,10 +46,15 @@ __global__ void __launch_bounds__(kWarps * 32)
   const int lane = threadIdx.x & 31;
   const int m = blockIdx.x * kWarps + (threadIdx.x >> 5);
   if (m >= M) return;
-  const int n = ell_nnz[m];
+  int n = ell_nnz[m];
+  TW_CHECK_INDEX(n, n >= 0 && n <= W);
   unsigned* mrow = mask + (long long)(m >> 5) * f;
   const unsigned bit = 1u << (m & 31);
-  for (int s = lane; s < n; s += 32) atomicOr(mrow + ell_col[(long long)m * W + s], bit);
+  for (int s = lane; s < n; s += 32) {
+    int j = ell_col[(long long)m * W + s];
+    TW_CHECK_INDEX(j, j < f);
+    atomicOr(mrow + j, bit);
+  }
 }
 
 // Column scan of the row masks, in groups of 32 row blocks.  CTA (jb, g)
@@ -130,12 +135,14 @@ __global__ void __launch_bounds__(kWarps * 32)
   const int lane = threadIdx.x & 31;
   const int m = blockIdx.x * kWarps + (threadIdx.x >> 5);
   if (m >= M) return;
-  const int n = ell_nnz[m];
+  int n = ell_nnz[m];
+  TW_CHECK_INDEX(n, n >= 0 && n <= W);
   const long long blk = (long long)(m >> 5) * f;
   const long long grp = (long long)((m >> 5) / kScanG) * f;
   const unsigned below = (1u << (m & 31)) - 1u;
   for (int s = lane; s < n; s += 32) {
-    const int j = ell_col[(long long)m * W + s];
+    int j = ell_col[(long long)m * W + s];
+    TW_CHECK_INDEX(j, j < f);
     const int pos = csc_ptr[j] + gpre[grp + j] + off[blk + j] + __popc(mask[blk + j] & below);
     csc_row[pos] = m;
     slot_pos[(long long)m * W + s] = pos;
@@ -193,7 +200,8 @@ __global__ void __launch_bounds__(256, MINB)
     }
   }
   int buf = 0;
-  const int n = ell_nnz[m];
+  int n = ell_nnz[m];
+  TW_CHECK_INDEX(n, n >= 0 && n <= W);
   // a row's columns ascend: the neuron chunk [j_lo, j_hi) is the slice [a, b)
   int a = 0, bnd = n;
   if (!(first && last)) {
@@ -211,8 +219,10 @@ __global__ void __launch_bounds__(256, MINB)
     if (lane < count) {
       const long long s = (long long)m * W + e0 + lane;
       jl = ell_col[s];
+      TW_CHECK_INDEX(jl, jl >= j_lo && jl < j_hi);  // the pass's neuron chunk
       gl = bf16_bits_to_float(ell_val[s]);
       pl = slot_pos[s];
+      TW_CHECK_INDEX(pl, pl >= 0 && (long long)pl < (long long)M * W);
     }
     for (int i = 0; i < count; i += B) {
       int j[B], pos[B];
@@ -324,8 +334,8 @@ constexpr int kNeuD = 1, kNeuX = 2;
 
 template <int TEAM, int VPL, int B, int MINB, int PARTS>
 __global__ void __launch_bounds__(256, MINB)
-    bwd_neurons_kernel(const uint16_t* __restrict__ x, const uint16_t* __restrict__ dy, int d,
-                       int f, int c0, int c1, const int* __restrict__ csc_ptr,
+    bwd_neurons_kernel(const uint16_t* __restrict__ x, const uint16_t* __restrict__ dy, int M,
+                       int d, int f, int c0, int c1, const int* __restrict__ csc_ptr,
                        const int* __restrict__ csc_row,
                        const float4* __restrict__ csc_vals, float* __restrict__ dwgT,
                        float* __restrict__ dwuT, float* __restrict__ dwd) {
@@ -357,6 +367,7 @@ __global__ void __launch_bounds__(256, MINB)
     float4 vl = make_float4(0.f, 0.f, 0.f, 0.f);
     if (lane < count) {
       ml = csc_row[e0 + lane];
+      TW_CHECK_INDEX(ml, ml >= 0 && ml < M);
       vl = csc_vals[e0 + lane];
     }
     for (int i = 0; i < count; i += B) {
@@ -463,7 +474,7 @@ cudaError_t rows_team(const void* x, const void* dy, const void* wgT, const void
 // One launch per column window: windows of d / windows columns (a multiple
 // of 8, so every slab stays 16-byte aligned), the team covering one window.
 template <int TEAM, int VPL, int B, int MINB, int PARTS>
-cudaError_t neurons_team(const void* x, const void* dy, int d, int f, const int* csc_ptr,
+cudaError_t neurons_team(const void* x, const void* dy, int M, int d, int f, const int* csc_ptr,
                          const int* csc_row, const float4* csc_vals, float* dwgT, float* dwuT,
                          float* dwd, cudaStream_t s, int windows = 1) {
   constexpr int ROWS = 8 / TEAM;
@@ -473,7 +484,7 @@ cudaError_t neurons_team(const void* x, const void* dy, int d, int f, const int*
     {
       ProfScope prof(PARTS == kNeuD ? "bwd_neurons_dy" : PARTS == kNeuX ? "bwd_neurons_x" : "bwd_neurons", s);
       bwd_neurons_kernel<TEAM, VPL, B, MINB, PARTS><<<(f + ROWS - 1) / ROWS, 256, 0, s>>>(
-          reinterpret_cast<const uint16_t*>(x), reinterpret_cast<const uint16_t*>(dy), d, f,
+          reinterpret_cast<const uint16_t*>(x), reinterpret_cast<const uint16_t*>(dy), M, d, f,
           w * width, (w + 1) * width, csc_ptr, csc_row, csc_vals, dwgT, dwuT, dwd);
     }
     count_launch();
@@ -492,6 +503,10 @@ cudaError_t launch_csc_build(const twell_hybrid& r, int M, int f, int* blk_count
   const int NB = (M + 31) / 32;
   const int NG = (NB + kScanG - 1) / kScanG;
   unsigned* mask = reinterpret_cast<unsigned*>(blk_counts);
+  {
+    const cudaError_t ce = checked_setup();
+    if (ce != cudaSuccess) return ce;
+  }
   int* off = blk_counts + (long long)NB * f;
   int* gtot = off + (long long)NB * f;
   cudaError_t e = cudaMemsetAsync(mask, 0, sizeof(unsigned) * (size_t)NB * f, s);
@@ -556,7 +571,7 @@ cudaError_t split_rows(const void* x, const void* dy, const void* wgT, const voi
   p.dh = dhbuf;
   p.out = dhbuf;
   EllSrc src{reinterpret_cast<const uint16_t*>(r.ell_val), r.ell_col, r.ell_nnz, r.ell_width, 0,
-             f, 1};
+             f, 1, f};
   const int dot_chunks = part ? l2_chunks(2.0 * (double)f * d, 0.75, 0.5) : 1;
   for (int phase = 0; phase < 2; ++phase) {
     p.vec = reinterpret_cast<const uint16_t*>(phase == 0 ? dy : x);
@@ -620,6 +635,10 @@ cudaError_t launch_sparse_bwd_rows(const void* x, const void* dy, const void* wg
                                    const int* slot_pos, float lambda, float4* csc_vals, void* dx,
                                    float* part, float* dhbuf, float2* coef, cudaStream_t s) {
   if (M == 0) return cudaSuccess;
+  {
+    const cudaError_t ce = checked_setup();
+    if (ce != cudaSuccess) return ce;
+  }
   if (d > 1024 && split_gathers()) {  // wide rows: the split gathers, the forward's team shapes
     if (!dhbuf || !coef) return cudaErrorInvalidValue;
 #define TW_SPLIT(T, V)                                                                          \
@@ -654,10 +673,15 @@ cudaError_t launch_sparse_bwd_neurons(const void* x, const void* dy, int M, int 
                                       const float4* csc_vals, float* dwgT, float* dwuT, float* dwd,
                                       cudaStream_t s) {
   if (f == 0) return cudaSuccess;
+  {
+    const cudaError_t ce = checked_setup();
+    if (ce != cudaSuccess) return ce;
+  }
 #define TW_NEU(T, V, B, MINB, P) \
-  neurons_team<T, V, B, MINB, P>(x, dy, d, f, csc_ptr, csc_row, csc_vals, dwgT, dwuT, dwd, s)
+  neurons_team<T, V, B, MINB, P>(x, dy, M, d, f, csc_ptr, csc_row, csc_vals, dwgT, dwuT, dwd, s)
 #define TW_NEU_W(T, V, B, MINB, P, NW) \
-  neurons_team<T, V, B, MINB, P>(x, dy, d, f, csc_ptr, csc_row, csc_vals, dwgT, dwuT, dwd, s, NW)
+  neurons_team<T, V, B, MINB, P>(x, dy, M, d, f, csc_ptr, csc_row, csc_vals, dwgT, dwuT, dwd, s, \
+                                 NW)
   // Once x and dY together outgrow L2 the phase runs twice, over dY rows
   // (dWd) and over x rows (dWu^T, dWg^T): each pass gathers from a table half
   // the size, so more of its rows hit in L2.  A pass whose table (x or dY,

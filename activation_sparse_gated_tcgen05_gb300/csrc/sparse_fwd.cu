@@ -157,7 +157,8 @@ __global__ void __launch_bounds__(256, VPL > 2 ? 2 : 3)
   int buf = 0;
 
   if (ELL) {
-    const int n = ell_nnz[m];
+    int n = ell_nnz[m];
+    TW_CHECK_INDEX(n, n >= 0 && n <= W);
     // a row's columns ascend: the chunk [j_lo, j_hi) is the slice [a, b)
     int a = 0, b = n;
     if (!(first && last)) {
@@ -175,6 +176,7 @@ __global__ void __launch_bounds__(256, VPL > 2 ? 2 : 3)
       if (lane < count) {
         const long long s = (long long)m * W + e0 + lane;
         jl = ell_col[s];
+        TW_CHECK_INDEX(jl, jl < T * tile_n);
         gl = bf16_bits_to_float(ell_val[s]);
       }
       process_entries<TEAM, VPL, B, ROWS>(c, jl, gl, count, wuT, wd, d, lane, wt, team, red,
@@ -203,7 +205,9 @@ __global__ void __launch_bounds__(256, VPL > 2 ? 2 : 3)
         if (e < total) {
           const int tt = t0 + lo;
           const long long sl = ((long long)m * T + tt) * cap + (e - ex);
-          jl = tt * tile_n + idx[sl];
+          int il = idx[sl];
+          TW_CHECK_INDEX(il, il < tile_n);
+          jl = tt * tile_n + il;
           gl = bf16_bits_to_float(val[sl]);
         }
         process_entries<TEAM, VPL, B, ROWS>(c, jl, gl, min(32, total - e0), wuT, wd, d, lane,
@@ -289,7 +293,9 @@ __global__ void __launch_bounds__(256, VPL > 2 ? 2 : 3)
         if (e < total) {
           const int tt = t0 + lo;
           const long long sl = ((long long)m * T + tt) * cap + (e - ex);
-          jl = tt * tile_n + idx[sl];
+          int il = idx[sl];
+          TW_CHECK_INDEX(il, il < tile_n);
+          jl = tt * tile_n + il;
           gl = bf16_bits_to_float(val[sl]);
         }
         process_entries<TEAM, VPL, B, ROWS>(c, jl, gl, min(32, total - e0), wuT, wd, d, lane,
@@ -461,7 +467,7 @@ cudaError_t launch_shape(const void* x, const void* wuT, const void* wd, int M, 
                                           part, chunks, s);
     if (!hbuf) return cudaErrorInvalidValue;
     EllSrc src{reinterpret_cast<const uint16_t*>(route->ell_val), route->ell_col, route->ell_nnz,
-               route->ell_width, 0, f, 1};
+               route->ell_width, 0, f, 1, f};
     const int n = part ? l2_chunks(2.0 * (double)f * d, 0.75, 0.5) : 1;
     auto chunk = [f, n](EllSrc c, int i, bool) {
       c.j_lo = (int)((long long)f * i / n);
@@ -530,6 +536,8 @@ cudaError_t launch_sparse_fwd(const void* x, const void* wuT, const void* wd, in
                               const twell_hybrid* route, void* y, float* part, float* hbuf,
                               cudaStream_t s) {
   if (M == 0) return cudaSuccess;
+  cudaError_t ce = checked_setup();
+  if (ce != cudaSuccess) return ce;
   const int T = f / tile_n;
   if (route) {
     // Wu^T and Wd rows: split the neuron axis into L2-sized passes once they

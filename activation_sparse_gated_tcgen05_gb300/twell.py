@@ -25,7 +25,7 @@ _lib = None
 STATUS = {
     0: "TWELL_OK", 1: "TWELL_ERR_INVALID_ARG", 2: "TWELL_ERR_UNSUPPORTED",
     3: "TWELL_ERR_ALIGNMENT", 4: "TWELL_ERR_CAPACITY", 5: "TWELL_ERR_CUDA",
-    6: "TWELL_ERR_DEVICE_TIMEOUT", 7: "TWELL_ERR_WORKSPACE",
+    6: "TWELL_ERR_DEVICE_TIMEOUT", 7: "TWELL_ERR_WORKSPACE", 8: "TWELL_ERR_INDEX",
 }
 EXPORTS = (
     "twell_pack", "twell_pack_dense", "hybrid_route", "twell_workspace_bytes",
@@ -63,15 +63,17 @@ class Hybrid(ctypes.Structure):
 
 
 def library_path() -> str:
-    return _build.LIB
+    """libtwell.so, or the checked (bounds-checking debug) build
+    libtwell_checked.so when the environment sets TWELL_CHECKED=1."""
+    return _build.CHECKED_LIB if os.environ.get("TWELL_CHECKED") == "1" else _build.LIB
 
 
 def load():
-    """Load libtwell.so (raises if it has not been built)."""
+    """Load the library (raises if it has not been built)."""
     global _lib
     if _lib is not None:
         return _lib
-    path = _build.LIB
+    path = library_path()
     if not os.path.exists(path):
         raise RuntimeError("libtwell.so not found at %s: run __graft_entry__.build() "
                            "(or python -m activation_sparse_gated_tcgen05_gb300._build)" % path)

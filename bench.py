@@ -607,8 +607,10 @@ def run_own(args, dist):
     # stream, after its L2 flush), step i+1's inputs are copied in and step
     # i-1's results copied out on two copy streams; events keep a buffer set
     # from being overwritten while a copy or the compute still uses it
-    bufs = [(x, dy, y, dx), (torch.empty_like(x), torch.empty_like(dy), torch.empty_like(y),
-                             torch.empty_like(dx))]
+    # (the second set starts as a copy of the first: the eager call made
+    # before each graph capture then routes the same rows, within the
+    # route's capacity)
+    bufs = [(x, dy, y, dx), (x.clone(), dy.clone(), torch.empty_like(y), torch.empty_like(dx))]
     step_graphs = [graphed(make_sparse_step(*b)) for b in bufs]
     comp = stream
     h2d, d2h = torch.cuda.Stream(dev), torch.cuda.Stream(dev)

@@ -58,7 +58,9 @@ typedef enum twell_status {
   TWELL_ERR_CAPACITY = 4,       /* a packed tile overflowed with no route */
   TWELL_ERR_CUDA = 5,           /* a CUDA call or launch failed */
   TWELL_ERR_DEVICE_TIMEOUT = 6, /* a device-side pipeline wait gave up */
-  TWELL_ERR_WORKSPACE = 7       /* workspace missing or smaller than required */
+  TWELL_ERR_WORKSPACE = 7,      /* workspace missing or smaller than required */
+  TWELL_ERR_INDEX = 8           /* checked build only: an index read from memory
+                                   (column, row, entry position) was out of range */
 } twell_status;
 
 /* Problem shape.  tile_n = T_n, the TwELL tile width (columns of the gate

@@ -19,9 +19,9 @@ pytestmark = pytest.mark.gpu
 LAM = 2e-5
 
 
-def _inputs(M, d, f, tile_n, cap, exact=True, seed=3):
+def _inputs(M, d, f, tile_n, cap, exact=True, seed=3, mixed=True):
     if exact:
-        w = synthetic.make_exact_gate_inputs(M, d, f, density=0.02, seed=seed, mixed_rows=True)
+        w = synthetic.make_exact_gate_inputs(M, d, f, density=0.02, seed=seed, mixed_rows=mixed)
     else:
         w = synthetic.make_inputs(M, d, f, density=0.005, seed=seed, lognormal_sigma=1.0)
     x, wg, wu, wd, dy = (dev_bf16(w[k]) for k in ("x", "wgT", "wuT", "wd", "dy"))
@@ -75,7 +75,7 @@ def test_capped_workspace_gives_the_same_bytes(M, d, f, tile_n, cap, q):
 def test_zero_capacity_without_routed_rows():
     # the widest row as ELL width and capacity zero: no dense-backup launch
     M, d, f = 512, 512, 1024
-    x, wg, wu, wd, dy, shape = _inputs(M, d, f, 128, 32)
+    x, wg, wu, wd, dy, shape = _inputs(M, d, f, 128, 32, mixed=False)
     t = twell.alloc_tiles(shape)
     twell.twell_pack(x, wg, shape, t)
     _, _, cnt, nnz = twell.tiles_view(t, shape)
