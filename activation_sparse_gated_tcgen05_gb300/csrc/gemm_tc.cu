@@ -110,7 +110,10 @@ cudaError_t launch_t(const char* name, const Mat& A, const Mat& B, const Mat* B2
     if (le != cudaSuccess) return le;
     return cudaGetLastError();
   }
-  const int grid = (int)(tiles < num_sms() ? tiles : num_sms());
+  // split-K GEMMs run up to split_k_max units per output tile (the plan
+  // depends on the device-side row count); blocks past the work exit at once
+  const long long units = tiles * (p.split_k_max > 1 ? p.split_k_max : 1);
+  const int grid = (int)(units < num_sms() ? units : num_sms());
   {
     ProfScope prof(name, s);
     kern<<<grid, kGemmThreads, kGemmSmem, s>>>(ta, tb, tb2, to[0], to[1], to[2], p);

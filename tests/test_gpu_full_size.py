@@ -3,6 +3,7 @@ times, on outputs the oracle can compute one by one: sampled rows of y and
 dX, sampled neurons of dWg / dWu / dWd, plus properties that hold at any size
 (routing consistency, counts).  Tolerance as in test_gpu_ffn.py, with the
 gate-decision allowance computed from the oracle for the sampled outputs."""
+import math
 import os
 
 import numpy as np
@@ -101,6 +102,19 @@ def test_fwd_2b_density_sweep_forward(density):
     assert_close(to_np(y)[rows], ref, "y", out_bf16=True, allowance=fwd_allowance(w, rows))
 
 
+def _pass_boundaries(f, d):
+    """First neurons of the L2-sized neuron passes of the wide-row gathers
+    (one weight matrix per pass for the up / down / dh / gradient gathers,
+    two for dX), by the library's rule: one pass while the table fits in
+    3/4 of L2, else passes of at most half of L2 each."""
+    l2 = torch.cuda.get_device_properties(0).L2_cache_size
+    out = set()
+    for table in (2.0 * f * d, 4.0 * f * d):
+        n = 1 if table <= 0.75 * l2 else math.ceil(table / (0.5 * l2))
+        out.update(f * c // n for c in range(1, n))
+    return sorted(out)
+
+
 @pytest.mark.parametrize("name", ["train_2b", "train_8b"])
 def test_training_step(name):
     wl = synthetic.WORKLOADS[name]
@@ -114,7 +128,10 @@ def test_training_step(name):
     W = synthetic.ell_width(nnz, wl.route_fraction)
     route = twell.alloc_hybrid(shape, W)
     twell.hybrid_route(tiles, shape, route)
-    ws = torch.empty(twell.twell_workspace_bytes(shape, W, True), dtype=torch.uint8, device="cuda")
+    # as bench.py runs it: a workspace for exactly the rows routed
+    route.dense_cap = int(route.n_dense[0].item())
+    ws = torch.empty(twell.twell_workspace_bytes(shape, W, True, dense_cap=route.dense_cap),
+                     dtype=torch.uint8, device="cuda")
     y = torch.empty(M, d, dtype=torch.bfloat16, device="cuda")
     twell.twell_ffn_fwd(x, wg, wu, wd, shape, y, route=route, ws=ws)
     dx = torch.empty_like(y)
@@ -126,8 +143,15 @@ def test_training_step(name):
     assert 0.01 * M < n_dense < 0.06 * M  # about 3 % of rows routed
     dr = twell.hybrid_view(route, shape)[3][:n_dense].cpu().numpy()
     rng = np.random.default_rng(5)
-    rows = np.unique(np.concatenate([_sample(M, 8, 4), rng.choice(dr, 4, replace=False)]))
-    neurons = _sample(f, 6, 6)
+    # rows: random ones, the last rows (the final row block of every gather
+    # pass), and among the routed rows the first and the last row of every
+    # 128-row tile of the dense backup's buffer
+    tile_rows = [dr[i] for k in range(0, n_dense, 128) for i in (k, min(k + 127, n_dense - 1))]
+    rows = np.unique(np.concatenate([_sample(M, 8, 4), [M - 2, M - 3],
+                                     rng.choice(dr, 2, replace=False), tile_rows]))
+    # neurons: random ones and both sides of every L2-pass boundary
+    edges = [j + o for j in _pass_boundaries(f, d) for o in (-1, 0)]
+    neurons = np.unique(np.concatenate([_sample(f, 6, 6), edges])).astype(np.int64)
     y_ref = oracle.ffn_fwd_dense(w["x"], w["wgT"], w["wuT"], w["wd"], rows=rows)
     assert_close(to_np(y)[rows], y_ref, "y", out_bf16=True, allowance=fwd_allowance(w, rows))
     al = bwd_allowance_sampled(w, LAM, rows, neurons)
