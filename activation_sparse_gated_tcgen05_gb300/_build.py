@@ -18,7 +18,8 @@ PROBE_LIB = os.path.join(OUT_DIR, "libtwell_probe.so")
 # the device and reported as TWELL_ERR_INDEX (see common.cuh)
 CHECKED_LIB = os.path.join(OUT_DIR, "libtwell_checked.so")
 
-SOURCES = ["api.cu", "gemm_tc.cu", "pack.cu", "sparse_fwd.cu", "sparse_bwd.cu", "selftest.cu"]
+SOURCES = ["api.cu", "gemm_tc.cu", "gate_smallm.cu", "pack.cu", "sparse_fwd.cu", "sparse_bwd.cu",
+           "selftest.cu"]
 PROBE_SOURCES = ["gather_probe.cu"]
 HEADERS = ["common.cuh", "ell_gather.cuh", "gemm_tc.cuh", "internal.h"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

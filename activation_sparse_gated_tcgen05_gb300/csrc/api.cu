@@ -541,6 +541,10 @@ twell_status twell_pack(const void* x, const void* wgT, const twell_shape* shape
   cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
   cudaError_t e = cudaMemsetAsync(out->row_nnz, 0, sizeof(int32_t) * (size_t)s.M, cs);
   if (e != cudaSuccess) return TWELL_ERR_CUDA;
+  // a handful of tokens: neurons on the MMA's M dimension (gate_smallm.cu)
+  if (gate_pack_smallm_fits(s.M, s.d_model, s.d_ff, s.tile_n))
+    return cuda_status(launch_gate_pack_smallm(x, wgT, s.M, s.d_model, s.d_ff, s.tile_n,
+                                               s.tile_cap, *out, cs));
   GemmParams p = base_params(s.M, s.d_ff, s.d_model, kBN);
   p.val = reinterpret_cast<uint16_t*>(out->val);
   p.idx = out->idx;

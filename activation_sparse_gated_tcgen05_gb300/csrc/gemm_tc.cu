@@ -59,6 +59,14 @@ bool make_out_map(CUtensorMap* m, const OutMat& o) {
   return r == CUDA_SUCCESS;
 }
 
+}  // namespace
+
+bool make_tma_map_bf16(CUtensorMap* m, const Mat& a, uint32_t box_inner, uint32_t box_outer) {
+  return make_map(m, a, box_inner, box_outer);
+}
+
+namespace {
+
 template <bool A_MN, bool B_MN, int EPI>
 cudaError_t launch_t(const char* name, const Mat& A, const Mat& B, const Mat* B2,
                      const GemmParams& p, cudaStream_t s, const OutMat* outs, int n_outs) {

@@ -1,6 +1,7 @@
 // internal.h -- host-side interfaces between the library's translation units.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -73,6 +74,16 @@ struct NvtxRange {
 cudaError_t gemm_launch(GemmKind kind, const Mat& A, const Mat& B, const Mat* B2,
                         const GemmParams& p, cudaStream_t stream, const OutMat* outs = nullptr,
                         int n_outs = 0);
+// 2-D tensor map over a bf16 matrix, 128-byte swizzled boxes of
+// box_inner (contiguous) x box_outer elements.
+bool make_tma_map_bf16(CUtensorMap* m, const Mat& a, uint32_t box_inner, uint32_t box_outer);
+
+// Gate GEMM + TwELL pack for small batches (gate_smallm.cu): neurons on the
+// MMA's M dimension, up to kSmallGateMaxM tokens on its N dimension.
+constexpr int kSmallGateMaxM = 64;
+bool gate_pack_smallm_fits(int M, int d, int f, int tile_n);
+cudaError_t launch_gate_pack_smallm(const void* x, const void* wgT, int M, int d, int f,
+                                    int tile_n, int cap, const twell_tiles& out, cudaStream_t s);
 
 // Non-tensor-core kernels (pack.cu, sparse_fwd.cu, sparse_bwd.cu).
 cudaError_t launch_pack_dense(const void* a, int a_f32, int M, int f, int tile_n, int cap,

@@ -506,6 +506,9 @@ def run_own(args, dist):
             wsd = torch.empty(twell.twell_dense_workspace_bytes(shp, False), dtype=torch.uint8,
                               device=dev)
 
+            def small_gate():
+                twell.twell_pack(xs, wg, shp, tl)
+
             def small_sparse():
                 twell.twell_pack(xs, wg, shp, tl)
                 twell.twell_ffn_fwd(xs, wg, wu, wd, shp, ys, tiles=tl)
@@ -513,6 +516,7 @@ def run_own(args, dist):
             def small_dense():
                 twell.twell_dense_ffn_fwd(xs, wg, wu, wd, shp, ys, False, wsd)
 
+            t_gate = timed(graphed(small_gate), args.steps, args.warmup)[0]
             t_sp = timed(graphed(small_sparse), args.steps, args.warmup)[0]
             t_de = timed(graphed(small_dense), args.steps, args.warmup)[0]
             vt, it_, ct, _ = twell.tiles_view(tl, shp)
@@ -522,9 +526,13 @@ def run_own(args, dist):
                                   < ct.long().clamp(max=C_).unsqueeze(2)]
             n_unique = int(torch.unique(cols).numel())
             byts = 2 * f * d + 2 * 2 * n_unique * d + 2 * 2 * Ms * d
+            gate_bytes = 2 * f * d + 2 * Ms * d
             small_m[str(Ms)] = {"sparse_fwd_us": t_sp * 1e3, "dense_fwd_us": t_de * 1e3,
                                 "distinct_live_neurons": n_unique, "hbm_bytes": byts,
-                                "frac_of_hbm": byts / (t_sp / 1e3) / 1e9 / peaks_["hbm_gbs"]}
+                                "frac_of_hbm": byts / (t_sp / 1e3) / 1e9 / peaks_["hbm_gbs"],
+                                "gate_pack_us": t_gate * 1e3,
+                                "gate_pack_frac_of_hbm": gate_bytes / (t_gate / 1e3) / 1e9
+                                / peaks_["hbm_gbs"]}
 
     # eager steps with the dominant kernel's launches bracketed by CUDA events
     ms_eager, eager_launches, prof, _ = timed(sparse_step, args.steps, args.warmup,
