@@ -206,7 +206,6 @@ struct SparseWs {
   float* ur;
   int *mask_off, *csc_ptr, *csc_row, *slot_pos;
   float4* csc_vals;
-  float2* coef;                         // per-ELL-entry (du, da) of the split row phase
   long long Mr;                         // routed-row buffer rows (capacity in whole tiles)
   long long Mp;                         // rows of part
   size_t bytes;
@@ -237,7 +236,6 @@ SparseWs carve_sparse(void* ws, const twell_shape& s, int W, int dense_cap, int 
     w.csc_row = c.take<int>(E > 0 ? E : 1);
     w.slot_pos = c.take<int>(E > 0 ? E : 1);
     w.csc_vals = c.take<float4>(E > 0 ? E : 1);
-    w.coef = c.take<float2>(E > 0 ? E : 1);
   }
   w.bytes = c.off + 256;
   return w;
@@ -682,7 +680,7 @@ twell_status twell_ffn_bwd(const void* x, const void* wgT, const void* wuT, cons
                                    w.slot_pos, cs);
   if (e == cudaSuccess)
     e = launch_sparse_bwd_rows(x, dy, wgT, wuT, wd, s.M, s.d_model, s.d_ff, *route, w.slot_pos,
-                               l1_coeff, w.csc_vals, dx, w.part, w.hbuf, w.coef, cs);
+                               l1_coeff, w.csc_vals, dx, w.part, w.hbuf, cs);
   if (e == cudaSuccess)
     e = launch_sparse_bwd_neurons(x, dy, s.M, s.d_model, s.d_ff, w.csc_ptr, w.csc_row, w.csc_vals,
                                   dwgT, dwuT, dwd, cs);

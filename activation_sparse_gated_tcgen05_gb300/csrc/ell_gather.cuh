@@ -19,18 +19,18 @@
 //                    The epilogue runs per entry on lane i:
 //                      kDotH     h = g u                  (forward, u = x.Wu)
 //                      kDotDh    dh                       (backward, dY.Wd)
-//                      kDotGrad  du = dh g, da = dh u + lambda, h = g u
-//                                (backward, u = x.Wu, dh from kDotDh)
-//   ell_axpy_kernel  out_m = sum_e c_e R[j_e] (+ c'_e R'[j_e]): independent
-//                    warps, each owning VPL slabs of one row, accumulate the
-//                    per-entry coefficients in entry order -- y = sum h Wd in
-//                    the forward, dX = sum du Wu^T + da Wg^T in the backward.
+//   ell_axpy_kernel  out_m = sum_e c_e R[j_e]: independent warps, each
+//                    owning VPL slabs of one row, accumulate the per-entry
+//                    coefficients in entry order -- y = sum h Wd in the
+//                    forward.
+//   ell_grad_dx_kernel  the backward's u, du, da, h per entry and dX in one
+//                    gather over Wu^T and Wg^T (see below).
 //
-// Every entry's arithmetic and every output element's accumulation order are
-// those of the fused kernels, so results are bit-identical to them.  Each
-// kernel gathers one or two weight matrices (a smaller table than the fused
-// kernel's, so fewer L2-sized passes), and neither waits at a barrier per
-// batch.  Entries come from an entry source: the ELL rows of the training
+// Every entry's arithmetic, and y's and dW's accumulation order, are those
+// of the fused kernels, so y and dW are bit-identical to them; dX sums the
+// same terms grouped by 32 entries.  Each kernel gathers one or two weight
+// matrices (a smaller table than the fused kernel's, so fewer L2-sized
+// passes), and none waits at a barrier per batch.  Entries come from an entry source: the ELL rows of the training
 // path (EllSrc) or the TwELL tiles of the inference path (TwellSrc); the
 // per-entry buffers hold a row's entries contiguously, in order.
 #pragma once
@@ -41,7 +41,7 @@
 namespace tw {
 namespace {
 
-constexpr int kDotH = 0, kDotDh = 1, kDotGrad = 2;
+constexpr int kDotH = 0, kDotDh = 1;
 constexpr int kEllPassFirst = 1, kEllPassLast = 2;
 
 // Element offset of slab v of warp wt in a team of TEAM warps: slabs of 256
@@ -152,11 +152,6 @@ struct EllDotArgs {
   const uint16_t* rows;  // [f][d] gathered weight rows (Wu^T or Wd)
   int M, d;
   float* out;            // kDotH: h, kDotDh: dh  (per entry, the source's buffer index)
-  const float* dh;       // kDotGrad: dh per entry
-  const int* slot_pos;   // kDotGrad: neuron-major position of each slot
-  float lambda;          // kDotGrad: L1 coefficient
-  float4* csc_vals;      // kDotGrad: (du, da, h, 0) at the neuron-major position
-  float2* coef;          // kDotGrad: (du, da) per entry, for the dX gather
 };
 
 template <int TEAM, int VPL, int B, int MINB, int MODE, class Src>
@@ -217,36 +212,24 @@ __global__ void __launch_bounds__(256, MINB) ell_dot_kernel(const EllDotArgs p, 
     if (wt != 0 || lane >= count) return;
     if constexpr (MODE == kDotDh) {
       p.out[he] = dot;
-    } else {
-      const float g = bf16_bits_to_float(src.val[s]);
-      if constexpr (MODE == kDotH) {
-        p.out[he] = g * dot;
-      } else {  // ReLU'(a) = 1 on a live entry
-        const float dh = p.dh[he];
-        const float du = dh * g, da = fmaf(dh, dot, p.lambda);
-        long long pos = p.slot_pos[s];
-        TW_CHECK_INDEX(pos, pos >= 0 && pos < (long long)p.M * src.W);
-        p.csc_vals[pos] = make_float4(du, da, g * dot, 0.f);
-        p.coef[he] = make_float2(du, da);
-      }
+    } else {  // kDotH
+      p.out[he] = bf16_bits_to_float(src.val[s]) * dot;
     }
   });
 }
 
 struct EllAxpyArgs {
-  const uint16_t* rows0;  // [f][d] weight rows scaled by the first coefficient
-  const uint16_t* rows1;  // second matrix (NR = 2), scaled by the second
+  const uint16_t* rows0;  // [f][d] weight rows scaled by the per-entry coefficient
   int M, d;
-  const void* coef;       // per entry: float (NR = 1) or float2 (NR = 2)
+  const float* coef;      // per entry (the source's buffer index)
   int pass;               // kEllPassFirst: start from 0, kEllPassLast: store out
   float* part;            // [M][d] fp32 carry between neuron passes
   uint16_t* out;          // [M][d] bf16 result
 };
 
-template <int VPL, int B, int MINB, int NR, class Src>
+template <int VPL, int B, int MINB, class Src>
 __global__ void __launch_bounds__(256, MINB) ell_axpy_kernel(const EllAxpyArgs p, const Src src) {
   static_assert(32 % B == 0, "a batch never reaches past lane 31");
-  static_assert(NR == 1 || NR == 2, "one or two gathered matrices");
   const int lane = threadIdx.x & 31;
   const int d = p.d;
   const int wpr = (d + 256 * VPL - 1) / (256 * VPL);  // warps per row
@@ -275,45 +258,28 @@ __global__ void __launch_bounds__(256, MINB) ell_axpy_kernel(const EllAxpyArgs p
     }
   }
   src.for_groups(m, lane, [&](int count, int jl, long long, long long he) {
-    float c0 = 0.f, c1 = 0.f;  // slots past the group: neuron 0 with zero coefficients
-    if (lane < count) {
-      if constexpr (NR == 1) {
-        c0 = reinterpret_cast<const float*>(p.coef)[he];
-      } else {
-        const float2 c = reinterpret_cast<const float2*>(p.coef)[he];
-        c0 = c.x;
-        c1 = c.y;
-      }
-    }
+    // slots past the group: neuron 0 with a zero coefficient
+    const float c0 = lane < count ? p.coef[he] : 0.f;
     for (int i = 0; i < count; i += B) {
       int j[B];
-      float k0[B], k1[B];
+      float k0[B];
 #pragma unroll
       for (int b = 0; b < B; ++b) {
         j[b] = __shfl_sync(0xffffffffu, jl, (i + b) & 31);
         k0[b] = __shfl_sync(0xffffffffu, c0, (i + b) & 31);
-        if constexpr (NR == 2) k1[b] = __shfl_sync(0xffffffffu, c1, (i + b) & 31);
       }
-      uint4 r0[B][VPL], r1[NR == 2 ? B : 1][VPL];
+      uint4 r0[B][VPL];
 #pragma unroll
       for (int b = 0; b < B; ++b) {
         const long long row = (long long)j[b] * d;
 #pragma unroll
-        for (int v = 0; v < VPL; ++v) {
-          r0[b][v] = ldg_v4(p.rows0 + row + eoff[v]);
-          if constexpr (NR == 2) r1[b][v] = ldg_v4(p.rows1 + row + eoff[v]);
-        }
+        for (int v = 0; v < VPL; ++v) r0[b][v] = ldg_v4(p.rows0 + row + eoff[v]);
       }
 #pragma unroll
       for (int b = 0; b < B; ++b) {
         const uint64_t s0 = f2_splat(k0[b]);
 #pragma unroll
         for (int v = 0; v < VPL; ++v) axpy8_f2(s0, r0[b][v], acc[v]);
-        if constexpr (NR == 2) {
-          const uint64_t s1 = f2_splat(k1[b]);
-#pragma unroll
-          for (int v = 0; v < VPL; ++v) axpy8_f2(s1, r1[b][v], acc[v]);
-        }
       }
     }
   });
@@ -323,6 +289,158 @@ __global__ void __launch_bounds__(256, MINB) ell_axpy_kernel(const EllAxpyArgs p
     if (e >= d) continue;
     if (last) {
       st_v4_hint(p.out + (long long)m * d + e, f2x4_to_bf8(acc[v]), pol);
+    } else {
+      float* pp = p.part + (long long)m * d + e;
+      st_v4_hint(pp, make_uint4((uint32_t)acc[v][0], (uint32_t)(acc[v][0] >> 32),
+                                (uint32_t)acc[v][1], (uint32_t)(acc[v][1] >> 32)), pol);
+      st_v4_hint(pp + 4, make_uint4((uint32_t)acc[v][2], (uint32_t)(acc[v][2] >> 32),
+                                    (uint32_t)acc[v][3], (uint32_t)(acc[v][3] >> 32)), pol);
+    }
+  }
+}
+
+// The gradient gather and the dX gather of the backward rows in one pass
+// over Wu^T and Wg^T.  Per ELL entry e = (m, j), with dh from the dh gather:
+//   u = x_m . Wu[:, j],  du = dh g,  da = dh u + lambda,  h = g u
+//   dX_m += du Wu[:, j]^T + da Wg[:, j]^T
+// du is known before u, so the Wu^T row the dot product reads also feeds
+// dX straight away; da needs the whole dot product, which the team forms
+// once per group of 32 entries, after which the group's Wg^T rows are read.
+// Each entry reads Wu^T[j] and Wg^T[j] once (4 d bytes instead of the 6 d
+// of a gradient gather plus a dX gather).  Per dX element the sum runs
+// group by group: the group's du Wu^T terms in entry order, then its
+// da Wg^T terms.  u, du, da and h are those of the gradient gather, bit for
+// bit.  The team and slab layout are ell_dot_kernel's.
+struct EllGradDxArgs {
+  const uint16_t* x;     // [M][d] bf16
+  const uint16_t* wuT;   // [f][d] bf16
+  const uint16_t* wgT;   // [f][d] bf16
+  int M, d;
+  const float* dh;       // dh per entry (the source's buffer index)
+  const int* slot_pos;   // neuron-major position of each slot
+  float lambda;          // L1 coefficient
+  float4* csc_vals;      // (du, da, h, 0) at the neuron-major position
+  int pass;              // kEllPassFirst: start from 0, kEllPassLast: store dx
+  float* part;           // [M][d] fp32 dX carry between neuron passes
+  uint16_t* dx;          // [M][d] bf16 result
+};
+
+template <int TEAM, int VPL, int B, int MINB>
+__global__ void __launch_bounds__(256, MINB)
+    ell_grad_dx_kernel(const EllGradDxArgs p, const EllSrc src) {
+  static_assert(B % 2 == 0 && 32 % B == 0, "entries are summed over the warp in pairs");
+  constexpr int ROWS = 8 / TEAM;
+  __shared__ float red[2][ROWS][TEAM][32];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int team = warp / TEAM, wt = warp % TEAM;
+  const int m = blockIdx.x * ROWS + team;
+  if (m >= p.M) return;
+  const int d = p.d;
+  const bool first = p.pass & kEllPassFirst, last = p.pass & kEllPassLast;
+
+  const uint64_t pol = l2_evict_first_policy();  // x and the dX carry stream through
+  uint4 xv[VPL];
+  int eoff[VPL];
+  uint64_t acc[VPL][4];
+#pragma unroll
+  for (int v = 0; v < VPL; ++v) {
+    const int e = team_slab<TEAM>(lane, wt, v);
+    eoff[v] = e < d ? e : 0;
+    xv[v] = e < d ? ldg_v4_hint(p.x + (long long)m * d + e, pol) : make_uint4(0, 0, 0, 0);
+    if (first || e >= d) {
+#pragma unroll
+      for (int k = 0; k < 4; ++k) acc[v][k] = 0;
+    } else {  // dX_m of the earlier neuron chunks
+      const float* pp = p.part + (long long)m * d + e;
+      const uint4 q0 = ldg_v4_hint(pp, pol), q1 = ldg_v4_hint(pp + 4, pol);
+      acc[v][0] = f2_make(q0.x, q0.y);
+      acc[v][1] = f2_make(q0.z, q0.w);
+      acc[v][2] = f2_make(q1.x, q1.y);
+      acc[v][3] = f2_make(q1.z, q1.w);
+    }
+  }
+  int buf = 0;
+  src.for_groups(m, lane, [&](int count, int jl, long long s, long long he) {
+    // entry `lane` of the group; slots past it: neuron 0 with zero coefficients
+    const bool live = lane < count;
+    const float dhl = live ? p.dh[he] : 0.f;
+    const float gl = live ? bf16_bits_to_float(src.val[s]) : 0.f;
+    const float dul = dhl * gl;
+    float mine = 0.f;  // the warp's partial dot product of entry lane
+    // Wu^T rows: dot products with x_m, and du Wu[:, j]^T into dX_m
+    for (int i = 0; i < count; i += B) {
+      int j[B];
+      float du[B];
+#pragma unroll
+      for (int b = 0; b < B; ++b) {
+        j[b] = __shfl_sync(0xffffffffu, jl, (i + b) & 31);
+        du[b] = __shfl_sync(0xffffffffu, dul, (i + b) & 31);
+      }
+      uint4 r[B][VPL];
+#pragma unroll
+      for (int b = 0; b < B; ++b)
+#pragma unroll
+        for (int v = 0; v < VPL; ++v) r[b][v] = ldg_v4(p.wuT + (long long)j[b] * d + eoff[v]);
+      float q[B];
+#pragma unroll
+      for (int b = 0; b < B; ++b) {
+        float a0 = 0.f, a1 = 0.f;
+#pragma unroll
+        for (int v = 0; v < VPL; ++v) dot8_bf16(xv[v], r[b][v], a0, a1);
+        q[b] = a0 + a1;
+        const uint64_t s2 = f2_splat(du[b]);
+#pragma unroll
+        for (int v = 0; v < VPL; ++v) axpy8_f2(s2, r[b][v], acc[v]);
+      }
+#pragma unroll
+      for (int b = 0; b < B; b += 2) warp_sum2(q[b], q[b + 1]);
+#pragma unroll
+      for (int b = 0; b < B; ++b)
+        if (lane == i + b) mine = q[b];
+    }
+    float u = mine;
+    if constexpr (TEAM > 1) {
+      red[buf][team][wt][lane] = mine;
+      named_barrier(1 + team, 32 * TEAM);
+      u = 0.f;
+#pragma unroll
+      for (int w = 0; w < TEAM; ++w) u += red[buf][team][w][lane];
+      buf ^= 1;
+    }
+    const float dal = live ? fmaf(dhl, u, p.lambda) : 0.f;  // ReLU'(a) = 1 on a live entry
+    if (wt == 0 && live) {
+      long long pos = p.slot_pos[s];
+      TW_CHECK_INDEX(pos, pos >= 0 && pos < (long long)p.M * src.W);
+      p.csc_vals[pos] = make_float4(dul, dal, gl * u, 0.f);
+    }
+    // Wg^T rows: da Wg[:, j]^T into dX_m
+    for (int i = 0; i < count; i += B) {
+      int j[B];
+      float da[B];
+#pragma unroll
+      for (int b = 0; b < B; ++b) {
+        j[b] = __shfl_sync(0xffffffffu, jl, (i + b) & 31);
+        da[b] = __shfl_sync(0xffffffffu, dal, (i + b) & 31);
+      }
+      uint4 r[B][VPL];
+#pragma unroll
+      for (int b = 0; b < B; ++b)
+#pragma unroll
+        for (int v = 0; v < VPL; ++v) r[b][v] = ldg_v4(p.wgT + (long long)j[b] * d + eoff[v]);
+#pragma unroll
+      for (int b = 0; b < B; ++b) {
+        const uint64_t s2 = f2_splat(da[b]);
+#pragma unroll
+        for (int v = 0; v < VPL; ++v) axpy8_f2(s2, r[b][v], acc[v]);
+      }
+    }
+  });
+#pragma unroll
+  for (int v = 0; v < VPL; ++v) {
+    const int e = team_slab<TEAM>(lane, wt, v);
+    if (e >= d) continue;
+    if (last) {
+      st_v4_hint(p.dx + (long long)m * d + e, f2x4_to_bf8(acc[v]), pol);
     } else {
       float* pp = p.part + (long long)m * d + e;
       st_v4_hint(pp, make_uint4((uint32_t)acc[v][0], (uint32_t)(acc[v][0] >> 32),

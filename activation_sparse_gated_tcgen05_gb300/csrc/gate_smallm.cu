@@ -11,15 +11,19 @@
 // With a handful of tokens the usual orientation (tokens on the MMA's
 // 128-row M dimension) pads M to 128 and spreads Wg over few, wide tiles.
 // Here the operands are swapped: a tile is 128 neurons (rows of Wg^T, the
-// MMA's M) by NP tokens (x padded to 16, 32 or 64 rows, the MMA's N), so
-// Wg streams through many small tiles, and K is split over the blocks of a
-// thread-block cluster so that about three blocks run per SM.  The
-// accumulator then holds one neuron per TMEM lane and one token per column,
+// MMA's M) by NP tokens (x padded to 16, 32 or 64 rows, the MMA's N), one
+// block per tile and SM, streaming its slice of Wg through a TMA ring of
+// about 200 KB (measured on the 8B-class shape: ~45 GB/s per SM with eight
+// 16 KB stages; an L2 prefetch of the whole slice ahead of the ring made the
+// first data arrive later and the kernel slower).  Where the tiles are
+// fewer than the SMs, K is split over the blocks of a thread-block cluster.
+// The accumulator holds one neuron per TMEM lane and one token per column,
 // and the pack works across lanes: per token, each warp ballots which of its
-// 32 neurons are live, the four warps' counts give every live neuron its slot
-// in ascending neuron order, and the counts are the TwELL counts.  The
-// blocks of a cluster sum their partial accumulators through distributed
-// shared memory in rank order (deterministic; no global scratch).
+// 32 neurons are live; a lane per token then combines the four warps' counts
+// into the TwELL count and walks its warp's live neurons in ascending order
+// to their slots.  The blocks of a cluster sum their partial accumulators
+// through distributed shared memory in rank order (deterministic; no global
+// scratch).
 //
 // Warp roles (192 threads): warps 0-3 epilogue (warp w owns TMEM lanes
 // 32w..32w+31, the only lanes it may read), warp 4 TMA producer, warp 5
@@ -40,15 +44,17 @@ constexpr int kSmABytes = kSmBM * kSmBK * 2;
 
 template <int NP>
 struct SmCfg {
-  static constexpr int kBBytes = NP * kSmBK * 2;
-  static constexpr int kStages = NP <= 16 ? 4 : 3;
-  static constexpr int kStageBytes = kSmABytes + kBBytes;
+  static constexpr int kBPS = 1;  // k-blocks (TMA boxes of A and of B) per ring stage
+  static constexpr int kBBytes = kBPS * NP * kSmBK * 2;
+  static constexpr int kABytes = kBPS * kSmABytes;
+  static constexpr int kStages = (200 * 1024) / (kABytes + kBBytes);
+  static constexpr int kStageBytes = kABytes + kBBytes;
   static constexpr uint32_t kTmemCols = NP <= 32 ? 32 : 64;
   // stage buffers (1024-byte aligned: up to 1008 bytes of slack), barriers,
-  // and the per-token warp counts of the pack: 74.2 KB at NP = 64, so three
-  // blocks fit on an SM
+  // and the per-token warp counts of the pack (one block per SM)
   static constexpr int kSmem = kStages * kStageBytes + 1008 + 256 + NP * 4 * 4;
   static_assert(NP * kSmBM * 4 <= kStages * kStageBytes, "partials fit in the stage buffers");
+  static_assert(kSmem <= 227 * 1024, "one block's shared memory");
 };
 
 struct SmallGateParams {
@@ -62,7 +68,7 @@ struct SmallGateParams {
 };
 
 template <int NP>
-__global__ void __launch_bounds__(kSmThreads, 3)
+__global__ void __launch_bounds__(kSmThreads, 1)
     gate_pack_smallm_kernel(const __grid_constant__ CUtensorMap tmW,
                             const __grid_constant__ CUtensorMap tmX, const SmallGateParams p) {
   using C = SmCfg<NP>;
@@ -71,8 +77,8 @@ __global__ void __launch_bounds__(kSmThreads, 3)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
-  uint8_t* sA = smem;                          // stages x 128 neuron rows of Wg^T
-  uint8_t* sB = smem + C::kStages * kSmABytes;  // stages x NP token rows of x
+  uint8_t* sA = smem;                            // stages x 128 neuron rows of Wg^T
+  uint8_t* sB = smem + C::kStages * C::kABytes;  // stages x NP token rows of x
   uint64_t* full = reinterpret_cast<uint64_t*>(sB + C::kStages * C::kBBytes);
   uint64_t* empty = full + C::kStages;
   uint64_t* tfull = empty + C::kStages;
@@ -113,14 +119,19 @@ __global__ void __launch_bounds__(kSmThreads, 3)
       int stage = 0;
       uint32_t phase = 0;
       bool ok = true;
-      for (int kb = kb0; kb < kb1; ++kb) {
+      for (int kb = kb0; kb < kb1; kb += C::kBPS) {
         if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag)) {
           ok = false;
           break;
         }
-        mbar_arrive_expect_tx(&full[stage], kSmABytes + C::kBBytes);
-        tma_load_2d(sA + stage * kSmABytes, &tmW, &full[stage], kb * kSmBK, nt * kSmBM);
-        tma_load_2d(sB + stage * C::kBBytes, &tmX, &full[stage], kb * kSmBK, 0);
+        const int nb = min(C::kBPS, kb1 - kb);
+        mbar_arrive_expect_tx(&full[stage], (uint32_t)nb * (kSmABytes + NP * kSmBK * 2));
+        for (int b = 0; b < nb; ++b) {
+          tma_load_2d(sA + stage * C::kABytes + b * kSmABytes, &tmW, &full[stage],
+                      (kb + b) * kSmBK, nt * kSmBM);
+          tma_load_2d(sB + stage * C::kBBytes + b * NP * kSmBK * 2, &tmX, &full[stage],
+                      (kb + b) * kSmBK, 0);
+        }
         if (++stage == C::kStages) {
           stage = 0;
           phase ^= 1u;
@@ -139,18 +150,22 @@ __global__ void __launch_bounds__(kSmThreads, 3)
       int stage = 0;
       uint32_t phase = 0;
       bool ok = true;
-      for (int kb = kb0; kb < kb1; ++kb) {
+      for (int kb = kb0; kb < kb1; kb += C::kBPS) {
         if (!mbar_wait(&full[stage], phase, abort_flag)) {
           ok = false;
           break;
         }
         tc_fence_after();
-        const uint32_t a0 = smem_u32(sA + stage * kSmABytes);
-        const uint32_t b0 = smem_u32(sB + stage * C::kBBytes);
+        const int nb = min(C::kBPS, kb1 - kb);
+        for (int b = 0; b < nb; ++b) {
+          const uint32_t a0 = smem_u32(sA + stage * C::kABytes + b * kSmABytes);
+          const uint32_t b0 = smem_u32(sB + stage * C::kBBytes + b * NP * kSmBK * 2);
 #pragma unroll
-        for (int k = 0; k < kSmBK / 16; ++k)
-          tc_mma_bf16(tmem, sdesc_sw128(a0 + k * 32, 16, 1024), sdesc_sw128(b0 + k * 32, 16, 1024),
-                      idesc, (kb != kb0 || k != 0) ? 1u : 0u);
+          for (int k = 0; k < kSmBK / 16; ++k)
+            tc_mma_bf16(tmem, sdesc_sw128(a0 + k * 32, 16, 1024),
+                        sdesc_sw128(b0 + k * 32, 16, 1024), idesc,
+                        (kb + b != kb0 || k != 0) ? 1u : 0u);
+        }
         tc_commit(&empty[stage]);
         if (++stage == C::kStages) {
           stage = 0;
@@ -205,7 +220,10 @@ __global__ void __launch_bounds__(kSmThreads, 3)
     const int per_tile = p.tile_n / 32;     // warps per TwELL tile: 4 or 2
     const int t = nt * (kSmBM / p.tile_n) + warp / per_tile;
     const int w0 = warp - warp % per_tile;  // first warp of this TwELL tile
-    const uint32_t below = (1u << lane) - 1u;
+    // this block's operand buffers are free (its MMAs completed): the
+    // chunk's values [token][neuron]
+    float* sv = reinterpret_cast<float*>(smem);
+    uint32_t mk = 0;
 #pragma unroll 1
     for (int h = 0; h < kChunks; ++h) {
       if (32 * h >= p.M) break;  // block-uniform
@@ -222,11 +240,13 @@ __global__ void __launch_bounds__(kSmThreads, 3)
         for (int i = 0; i < 32; ++i)
           if (32 * h + i < NP) v[i] += rp[(32 * h + i) * kSmBM + nrow];
       }
-      // lane i keeps this warp's live mask of token 32 h + i
-      uint32_t mk = 0;
+      mk = 0;
+      // pass 1 (unrolled over the chunk's tokens): lane i keeps this warp's
+      // live mask of token 32 h + i; the values go to shared memory
 #pragma unroll
       for (int i = 0; i < 32; ++i) {
         const int m = 32 * h + i;
+        sv[i * kSmBM + nrow] = v[i];
         if (m < NP && m < p.M) {  // warp-uniform
           const uint32_t b = __ballot_sync(0xffffffffu, v[i] > kLiveMin);
           if (lane == i) {
@@ -236,11 +256,12 @@ __global__ void __launch_bounds__(kSmThreads, 3)
         }
       }
       named_barrier(1, 128);
-#pragma unroll
-      for (int i = 0; i < 32; ++i) {
-        const int m = 32 * h + i;
+      // pass 2, a lane per token: the TwELL count of the token's tile from
+      // the warps' counts, then this warp's live neurons, ascending, to
+      // their slots after those of the warps before it
+      {
+        const int m = 32 * h + lane;
         if (m < NP && m < p.M) {
-          const uint32_t b = __shfl_sync(0xffffffffu, mk, i);
           int pre = 0, total = 0;
           for (int w = w0; w < w0 + per_tile; ++w) {
             const int c = s_cnt[m][w];
@@ -248,19 +269,19 @@ __global__ void __launch_bounds__(kSmThreads, 3)
             total += c;
           }
           const long long slot0 = ((long long)m * p.T + t) * p.cap;
-          if ((b >> lane) & 1u) {
-            const int slot = pre + __popc(b & below);
-            if (slot < p.cap) {
-              p.val[slot0 + slot] = (uint16_t)relu_bf16_bits(v[i]);
-              p.idx[slot0 + slot] = (uint8_t)(nrow % p.tile_n);
-            }
+          int slot = pre;
+          for (uint32_t bits = mk; bits && slot < p.cap; bits &= bits - 1u, ++slot) {
+            const int n = __ffs(bits) - 1;  // neuron 32 warp + n of the 128-neuron tile
+            p.val[slot0 + slot] = (uint16_t)relu_bf16_bits(sv[lane * kSmBM + warp * 32 + n]);
+            p.idx[slot0 + slot] = (uint8_t)((warp * 32 + n) % p.tile_n);
           }
-          if (warp == w0 && lane == 0) {
+          if (warp == w0) {
             p.cnt[(long long)m * p.T + t] = (uint8_t)total;
             if (total) atomicAdd(p.row_nnz + m, total);
           }
         }
       }
+      named_barrier(1, 128);  // sv is rewritten by the next chunk
     }
   }
   if (warp < 4) tc_fence_before();
@@ -314,10 +335,10 @@ cudaError_t launch_gate_pack_smallm(const void* x, const void* wgT, int M, int d
   const int num_kb = d / kSmBK;
   // K split over a cluster: the largest power of two (at most 8) dividing
   // the k-blocks that keeps every rank at four k-blocks or more and the grid
-  // within three blocks per SM (all resident at once)
+  // within one block per SM (all resident at once)
   int ks = 1;
   for (int next = 2; next <= 8; next *= 2) {
-    if (num_kb % next != 0 || num_kb / next < 4 || (long long)n_tiles * next > 3LL * num_sms())
+    if (num_kb % next != 0 || num_kb / next < 4 || (long long)n_tiles * next > num_sms())
       break;
     ks = next;
   }

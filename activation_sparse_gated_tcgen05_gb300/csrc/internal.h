@@ -109,13 +109,12 @@ cudaError_t launch_sparse_fwd(const void* x, const void* wuT, const void* wd, in
 cudaError_t launch_csc_build(const twell_hybrid& route, int M, int f, int* blk_counts,
                              int* csc_ptr, int* csc_row, int* slot_pos, cudaStream_t s);
 // `part` ([M][d] fp32) carries dX between L2-sized neuron passes (may be null).
-// `dhbuf` ([M][ell_width] fp32) and `coef` ([M][ell_width] (du, da)) hold the
-// per-entry values of the split row phase used for rows wider than 1024;
-// null keeps the fused kernel.
+// `dhbuf` ([M][ell_width] fp32) holds the per-entry dh of the split row phase
+// used for rows wider than 1024; null keeps the fused kernel.
 cudaError_t launch_sparse_bwd_rows(const void* x, const void* dy, const void* wgT, const void* wuT,
                                    const void* wd, int M, int d, int f, const twell_hybrid& route,
                                    const int* slot_pos, float lambda, float4* csc_vals, void* dx,
-                                   float* part, float* dhbuf, float2* coef, cudaStream_t s);
+                                   float* part, float* dhbuf, cudaStream_t s);
 cudaError_t launch_sparse_bwd_neurons(const void* x, const void* dy, int M, int d, int f,
                                       const int* csc_ptr, const int* csc_row,
                                       const float4* csc_vals, float* dwgT, float* dwuT, float* dwd,

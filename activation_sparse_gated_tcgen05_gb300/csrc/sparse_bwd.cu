@@ -19,8 +19,8 @@
 //      blocks of its group + popcount of lower bits.
 //   2. bwd_rows: one team of warps per row computes dh, u, du, da, h per entry
 //      (stored at the entry's neuron-major position) and dX_m.  Rows wider
-//      than 1024 take three gathers instead (dh; u with du, da, h; dX), which
-//      meet no barrier per batch (ell_gather.cuh).
+//      than 1024 take two gathers instead (dh; then u with du, da, h and dX),
+//      which meet one barrier per 32 entries (ell_gather.cuh).
 // Gathered rows are loaded without predicates: a batch slot past the last
 // entry reads neuron (or row) 0 with zero coefficients, and lanes past
 // d_model read the first slab against zero x / dY, so no zero-fill selects
@@ -548,78 +548,69 @@ cudaError_t launch_csc_build(const twell_hybrid& r, int M, int f, int* blk_count
 
 namespace {
 
-// Wide ELL rows: the fused row phase split into three gathers (ell_gather.cuh)
-//   dh = dY_m . Wd[j]                         over Wd
-//   u = x_m . Wu[:, j]; du, da, h per entry     over Wu^T (dh from the first)
-//   dX_m = sum du Wu[:, j]^T + da Wg[:, j]^T     over Wu^T and Wg^T
-// each in its own L2-sized neuron passes.  Per entry and per dX element the
-// arithmetic and accumulation order are the fused kernel's.
+// Wide ELL rows: the fused row phase split into two gathers (ell_gather.cuh)
+//   dh = dY_m . Wd[j]                                   over Wd
+//   u = x_m . Wu[:, j]; du, da, h per entry;
+//   dX_m = sum du Wu[:, j]^T + da Wg[:, j]^T             over Wu^T and Wg^T
+// each in its own L2-sized neuron passes.  Per entry the arithmetic is the
+// fused kernel's; dX sums each group of 32 entries' du Wu^T terms before its
+// da Wg^T terms (see ell_grad_dx_kernel).
 template <int TEAM, int VPL>
 cudaError_t split_rows(const void* x, const void* dy, const void* wgT, const void* wuT,
                        const void* wd, int M, int d, int f, const twell_hybrid& r,
                        const int* slot_pos, float lambda, float4* csc_vals, void* dx, float* part,
-                       float* dhbuf, float2* coef, cudaStream_t s) {
+                       float* dhbuf, cudaStream_t s) {
   constexpr int ROWS = 8 / TEAM;
   const unsigned grid = (unsigned)((M + ROWS - 1) / ROWS);
   EllDotArgs p{};
   p.M = M;
   p.d = d;
-  p.slot_pos = slot_pos;
-  p.lambda = lambda;
-  p.csc_vals = csc_vals;
-  p.coef = coef;
-  p.dh = dhbuf;
   p.out = dhbuf;
+  p.vec = reinterpret_cast<const uint16_t*>(dy);
+  p.rows = reinterpret_cast<const uint16_t*>(wd);
   EllSrc src{reinterpret_cast<const uint16_t*>(r.ell_val), r.ell_col, r.ell_nnz, r.ell_width, 0,
              f, 1, f};
   const int dot_chunks = part ? l2_chunks(2.0 * (double)f * d, 0.75, 0.5) : 1;
-  for (int phase = 0; phase < 2; ++phase) {
-    p.vec = reinterpret_cast<const uint16_t*>(phase == 0 ? dy : x);
-    p.rows = reinterpret_cast<const uint16_t*>(phase == 0 ? wd : wuT);
-    for (int c = 0; c < dot_chunks; ++c) {
-      src.j_lo = (int)((long long)f * c / dot_chunks);
-      src.j_hi = (int)((long long)f * (c + 1) / dot_chunks);
-      src.whole = dot_chunks == 1;
-      {
-        ProfScope prof(phase == 0 ? "bwd_dh" : "bwd_grad", s);
-        // two-slab warps take four entries per batch, four-slab warps two
-        if (phase == 0) {
-          if constexpr (VPL <= 2)
-            ell_dot_kernel<TEAM, VPL, 4, 2, kDotDh><<<grid, 256, 0, s>>>(p, src);
-          else
-            ell_dot_kernel<TEAM, VPL, 2, 3, kDotDh><<<grid, 256, 0, s>>>(p, src);
-        } else {
-          if constexpr (VPL <= 2)
-            ell_dot_kernel<TEAM, VPL, 4, 2, kDotGrad><<<grid, 256, 0, s>>>(p, src);
-          else
-            ell_dot_kernel<TEAM, VPL, 2, 3, kDotGrad><<<grid, 256, 0, s>>>(p, src);
-        }
-      }
-      count_launch();
-      const cudaError_t e = cudaGetLastError();
-      if (e != cudaSuccess) return e;
-    }
-  }
-  constexpr int DV = 2;  // dX: two slabs per warp, two entries per batch
-  EllAxpyArgs a{};
-  a.rows0 = reinterpret_cast<const uint16_t*>(wuT);
-  a.rows1 = reinterpret_cast<const uint16_t*>(wgT);
-  a.M = M;
-  a.d = d;
-  a.coef = coef;
-  a.part = part;
-  a.out = reinterpret_cast<uint16_t*>(dx);
-  const int dx_chunks = part ? l2_chunks(4.0 * (double)f * d, 0.75, 0.5) : 1;
-  const int wpr = (d + 256 * DV - 1) / (256 * DV);
-  const unsigned blocks = (unsigned)(((long long)M * wpr + 7) / 8);
-  for (int c = 0; c < dx_chunks; ++c) {
-    src.j_lo = (int)((long long)f * c / dx_chunks);
-    src.j_hi = (int)((long long)f * (c + 1) / dx_chunks);
-    src.whole = dx_chunks == 1;
-    a.pass = (c == 0 ? kEllPassFirst : 0) | (c == dx_chunks - 1 ? kEllPassLast : 0);
+  for (int c = 0; c < dot_chunks; ++c) {
+    src.j_lo = (int)((long long)f * c / dot_chunks);
+    src.j_hi = (int)((long long)f * (c + 1) / dot_chunks);
+    src.whole = dot_chunks == 1;
     {
-      ProfScope prof("bwd_dx", s);
-      ell_axpy_kernel<DV, 2, 4, 2><<<blocks, 256, 0, s>>>(a, src);
+      ProfScope prof("bwd_dh", s);
+      // two-slab warps take four entries per batch, four-slab warps two
+      if constexpr (VPL <= 2)
+        ell_dot_kernel<TEAM, VPL, 4, 2, kDotDh><<<grid, 256, 0, s>>>(p, src);
+      else
+        ell_dot_kernel<TEAM, VPL, 2, 3, kDotDh><<<grid, 256, 0, s>>>(p, src);
+    }
+    count_launch();
+    const cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  EllGradDxArgs g{};
+  g.x = reinterpret_cast<const uint16_t*>(x);
+  g.wuT = reinterpret_cast<const uint16_t*>(wuT);
+  g.wgT = reinterpret_cast<const uint16_t*>(wgT);
+  g.M = M;
+  g.d = d;
+  g.dh = dhbuf;
+  g.slot_pos = slot_pos;
+  g.lambda = lambda;
+  g.csc_vals = csc_vals;
+  g.part = part;
+  g.dx = reinterpret_cast<uint16_t*>(dx);
+  const int gd_chunks = part ? l2_chunks(4.0 * (double)f * d, 0.75, 0.5) : 1;
+  for (int c = 0; c < gd_chunks; ++c) {
+    src.j_lo = (int)((long long)f * c / gd_chunks);
+    src.j_hi = (int)((long long)f * (c + 1) / gd_chunks);
+    src.whole = gd_chunks == 1;
+    g.pass = (c == 0 ? kEllPassFirst : 0) | (c == gd_chunks - 1 ? kEllPassLast : 0);
+    {
+      ProfScope prof("bwd_grad_dx", s);
+      if constexpr (VPL <= 2)
+        ell_grad_dx_kernel<TEAM, VPL, 4, 2><<<grid, 256, 0, s>>>(g, src);
+      else
+        ell_grad_dx_kernel<TEAM, VPL, 2, 2><<<grid, 256, 0, s>>>(g, src);
     }
     count_launch();
     const cudaError_t e = cudaGetLastError();
@@ -633,17 +624,17 @@ cudaError_t split_rows(const void* x, const void* dy, const void* wgT, const voi
 cudaError_t launch_sparse_bwd_rows(const void* x, const void* dy, const void* wgT, const void* wuT,
                                    const void* wd, int M, int d, int f, const twell_hybrid& route,
                                    const int* slot_pos, float lambda, float4* csc_vals, void* dx,
-                                   float* part, float* dhbuf, float2* coef, cudaStream_t s) {
+                                   float* part, float* dhbuf, cudaStream_t s) {
   if (M == 0) return cudaSuccess;
   {
     const cudaError_t ce = checked_setup();
     if (ce != cudaSuccess) return ce;
   }
   if (d > 1024 && split_gathers()) {  // wide rows: the split gathers, the forward's team shapes
-    if (!dhbuf || !coef) return cudaErrorInvalidValue;
+    if (!dhbuf) return cudaErrorInvalidValue;
 #define TW_SPLIT(T, V)                                                                          \
   split_rows<T, V>(x, dy, wgT, wuT, wd, M, d, f, route, slot_pos, lambda, csc_vals, dx, part,  \
-                   dhbuf, coef, s)
+                   dhbuf, s)
     if (d <= 2048) return TW_SPLIT(4, 2);
     if (d <= 4096) return TW_SPLIT(4, 4);
     return TW_SPLIT(8, 4);

@@ -443,7 +443,7 @@ cudaError_t launch_split(const void* x, const void* wuT, const void* wd, int M, 
     down.pass = (c == 0 ? kEllPassFirst : 0) | (c == chunks - 1 ? kEllPassLast : 0);
     {
       ProfScope prof("sparse_fwd_down", s);
-      ell_axpy_kernel<DV, 2, 4, 1><<<(unsigned)blocks, 256, 0, s>>>(down, sc);
+      ell_axpy_kernel<DV, 2, 4><<<(unsigned)blocks, 256, 0, s>>>(down, sc);
     }
     count_launch();
     const cudaError_t e = cudaGetLastError();

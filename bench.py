@@ -234,10 +234,9 @@ def algorithmic_work(family, wl, nnz_ell, n_dense):
         return 6.0 * d * nnz_ell + 6.0 * d * M + 24.0 * nnz_ell, "byte", "hbm"
     if family == "bwd_dh":  # Wd rows + dy read + ELL columns + per-entry dh written
         return 2.0 * d * nnz_ell + 2.0 * d * M + 6.0 * nnz_ell, "byte", "hbm"
-    if family == "bwd_grad":  # Wu^T rows + x read + ELL entry, dh, slot in; (du, da, h), (du, da) out
-        return 2.0 * d * nnz_ell + 2.0 * d * M + 36.0 * nnz_ell, "byte", "hbm"
-    if family == "bwd_dx":  # Wu^T and Wg^T rows + dx written + ELL columns + (du, da)
-        return 4.0 * d * nnz_ell + 2.0 * d * M + 10.0 * nnz_ell, "byte", "hbm"
+    if family == "bwd_grad_dx":  # Wu^T and Wg^T rows + x read, dX written + per entry:
+        # column, value, dh and slot in, (du, da, h) out
+        return 4.0 * d * nnz_ell + 4.0 * d * M + 28.0 * nnz_ell, "byte", "hbm"
     if family == "bwd_neurons":  # x and dy rows per entry + three fp32 dW rows per neuron
         return 4.0 * d * nnz_ell + 12.0 * f * d + 20.0 * nnz_ell, "byte", "hbm"
     if family == "bwd_neurons_dy":  # dy rows per entry + the fp32 dWd row per neuron

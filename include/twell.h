@@ -165,12 +165,15 @@ size_t twell_tiles_workspace_bytes(const twell_shape* shape);
  * previous setting.  enable = 1 (the default): the forward runs as an up
  * gather (h = g (x . Wu[:, j]) per live entry, 4 bytes each in the
  * workspace) and a down gather (y = sum h Wd[j, :]), and the backward row
- * phase as dh, gradient and dX gathers; each meets no barrier per batch and
+ * phase as a dh gather (over Wd) and a gradient + dX gather (over Wu^T and
+ * Wg^T, each read once per entry); none meets a barrier per batch and each
  * takes one or two weight matrices per L2-sized pass.  enable = 0: the fused
  * kernels of page 2, section "¿Qué hace distinto a TwELL frente a ELL
  * clásico?" (one gather per row, h kept in registers and never written to
- * global memory).  Both give the same bytes in every output.  Not
- * synchronised with work in flight: change it between calls. */
+ * global memory).  Both give the same bytes in y and in every dW; dX sums
+ * the same fp32 terms in another grouping and may differ by one bf16
+ * rounding step.  Not synchronised with work in flight: change it between
+ * calls. */
 int32_t twell_set_split_gathers(int32_t enable);
 
 /* Fused sparse up + down projection.  Source: page 2, "¿Qué hace distinto a
@@ -241,7 +244,7 @@ twell_status twell_ffn_fwd_noalloc(const void* x, const void* wgT, const void* w
  * ws/ws_bytes: at least twell_workspace_bytes_capped(shape, W, route->dense_cap, 1)
  * bytes (16-byte aligned); it also carries the fp32 running dX when the row phase runs in
  * L2-sized neuron passes and, for rows wider than 1024 (split gathers, see
- * twell_set_split_gathers), dh and (du, da) of every live ELL entry.  When x
+ * twell_set_split_gathers), dh of every live ELL entry.  When x
  * and dY together exceed 3/4 of L2 the weight gradients are formed in two
  * passes, over dY rows (dwd) and over x rows (dwuT, dwgT), with the same
  * per-element order. */
@@ -323,9 +326,11 @@ uint64_t twell_launch_count(void);
  * synchronises those events and aggregates them per family, returning the
  * number of families (or -1 if an event could not be read); entry i is then
  * available from twell_profile_entry (name valid until the next begin/end).
- * Families: gemm_gate_pack, gemm_gated, gemm_dgate, gemm_store_kk/mk/km/mm,
- * pack_dense, route_rows, route_list, gather_rows, sparse_fwd, csc_mark,
- * csc_colscan, csc_ptr, csc_place, bwd_rows, bwd_neurons.  Host-side state,
+ * Families: gemm_gate_pack (also the small-batch gate), gemm_gated,
+ * gemm_dgate, gemm_store_kk/mk/km/mm, pack_dense, route_rows, route_list,
+ * gather_rows, splitk_scatter, sparse_fwd, sparse_fwd_up, sparse_fwd_down,
+ * csc_mark, csc_colscan, csc_ptr, csc_place, bwd_rows, bwd_dh, bwd_grad_dx,
+ * bwd_neurons, bwd_neurons_dy, bwd_neurons_x.  Host-side state,
  * process-wide; not for use while another thread launches. */
 twell_status twell_profile_begin(const char* kernel);
 int32_t twell_profile_end(void);

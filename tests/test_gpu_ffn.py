@@ -320,9 +320,13 @@ def test_twell_split_forward_flags_overfull_tiles():
 def test_split_and_fused_wide_gathers_agree(M, d, f, q):
     """Rows wider than 1024 run as split gathers by default; with
     twell_set_split_gathers(0) the fused kernels of the pages run instead (h
-    never leaves registers).  Same per-entry arithmetic and accumulation
-    order, so y, dX and every dW must agree bit for bit (d = 4096, f = 8192
-    also runs both in several L2-sized passes, with different pass counts)."""
+    never leaves registers).  Same per-entry arithmetic and, for y and dW,
+    the same accumulation order, so y and every dW must agree bit for bit
+    (d = 4096, f = 8192 also runs both in several L2-sized passes, with
+    different pass counts).  dX sums the same fp32 terms, grouped per 32
+    entries in the split gather (each group's du Wu^T terms before its
+    da Wg^T terms) and entry by entry in the fused kernel, so the two may
+    round differently: they must agree to one bf16 step."""
     r = Run(M, d, f, 128, 32, density=0.02, seed=16, exact=True, mixed=True)
     t = r.pack()
     W = _quantile_width(t, r.shape, q) if q > 0 else 0  # W = 0: every live row routed
@@ -343,8 +347,14 @@ def test_split_and_fused_wide_gathers_agree(M, d, f, q):
             out[split] = [y.view(torch.int16), dx.view(torch.int16)] + [w.view(torch.int32) for w in dws]
     finally:
         twell.twell_set_split_gathers(True)
-    for a, b in zip(out[True], out[False]):
-        assert torch.equal(a, b)
+    for k, (a, b) in enumerate(zip(out[True], out[False])):
+        if k == 1:  # dX: at most one bf16 step apart, almost always equal
+            da, db = a.view(torch.bfloat16).float(), b.view(torch.bfloat16).float()
+            step = torch.maximum(da.abs(), db.abs()) * 2.0 ** -7 + 1e-30
+            assert ((da - db).abs() <= step).all()
+            assert (a == b).float().mean().item() > 0.9
+        else:
+            assert torch.equal(a, b)
     _check_step(r, *[o for o in (y, dx)], *dws, allow=False)
 
 
