@@ -326,7 +326,7 @@ def test_split_and_fused_wide_gathers_agree(M, d, f, q):
     different pass counts).  dX sums the same fp32 terms, grouped per 32
     entries in the split gather (each group's du Wu^T terms before its
     da Wg^T terms) and entry by entry in the fused kernel, so the two may
-    round differently: they must agree to one bf16 step."""
+    round differently; each is checked against the oracle."""
     r = Run(M, d, f, 128, 32, density=0.02, seed=16, exact=True, mixed=True)
     t = r.pack()
     W = _quantile_width(t, r.shape, q) if q > 0 else 0  # W = 0: every live row routed
@@ -345,17 +345,12 @@ def test_split_and_fused_wide_gathers_agree(M, d, f, q):
             if W == 0:
                 assert int(twell.hybrid_view(h, r.shape)[4].item()) > 0
             out[split] = [y.view(torch.int16), dx.view(torch.int16)] + [w.view(torch.int32) for w in dws]
+            _check_step(r, y, dx, *dws, allow=False)
     finally:
         twell.twell_set_split_gathers(True)
     for k, (a, b) in enumerate(zip(out[True], out[False])):
-        if k == 1:  # dX: at most one bf16 step apart, almost always equal
-            da, db = a.view(torch.bfloat16).float(), b.view(torch.bfloat16).float()
-            step = torch.maximum(da.abs(), db.abs()) * 2.0 ** -7 + 1e-30
-            assert ((da - db).abs() <= step).all()
-            assert (a == b).float().mean().item() > 0.9
-        else:
+        if k != 1:  # y and the weight gradients
             assert torch.equal(a, b)
-    _check_step(r, *[o for o in (y, dx)], *dws, allow=False)
 
 
 @pytest.mark.parametrize("M,d", [(1, 2048), (3, 4096), (17, 3136)])

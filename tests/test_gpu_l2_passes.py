@@ -90,16 +90,16 @@ def test_multi_pass_backward_rows(d, f):
     """dX over ELL rows in L2-sized passes: sampled rows of dX and sampled
     neurons of the weight gradients against the oracle, and the pass counts
     seen by the profiler.  Up to d_model = 1024 the fused row kernel gathers
-    Wd, Wu^T and Wg^T together; wider rows split it into dh (Wd), u and the
-    gradients (Wu^T) and dX (Wu^T and Wg^T), each with its own passes."""
+    Wd, Wu^T and Wg^T together; wider rows split it into dh (Wd) and u, the
+    gradients and dX (Wu^T and Wg^T), each with its own passes."""
     from helpers import bwd_allowance_sampled
 
     M, lam = 256, 2e-5
     if d <= 1024:
         expect = {"bwd_rows": _chunks(6.0 * f * d, 0.5, 0.65)}
     else:
-        dots = _chunks(2.0 * f * d, 0.75, 0.5)
-        expect = {"bwd_dh": dots, "bwd_grad": dots, "bwd_dx": _chunks(4.0 * f * d, 0.75, 0.5)}
+        expect = {"bwd_dh": _chunks(2.0 * f * d, 0.75, 0.5),
+                  "bwd_grad_dx": _chunks(4.0 * f * d, 0.75, 0.5)}
     assert min(expect.values()) > 1, "shape no longer exceeds L2; pick a larger one"
     w = synthetic.make_inputs(M, d, f, seed=12)
     x, wg, wu, wd, dy = (dev_bf16(w[k]) for k in ("x", "wgT", "wuT", "wd", "dy"))
