@@ -26,9 +26,9 @@
 //   ell_grad_dx_kernel  the backward's u, du, da, h per entry and dX in one
 //                    gather over Wu^T and Wg^T (see below).
 //
-// Every entry's arithmetic, and y's and dW's accumulation order, are those
-// of the fused kernels, so y and dW are bit-identical to them; dX sums the
-// same terms grouped by 32 entries.  Each kernel gathers one or two weight
+// The forward's per-entry arithmetic and y's accumulation order are those of
+// the fused kernels, so y is bit-identical to them; the backward's gradient
+// + dX gather sums the same terms in another grouping.  Each kernel gathers one or two weight
 // matrices (a smaller table than the fused kernel's, so fewer L2-sized
 // passes), and none waits at a barrier per batch.  Entries come from an entry source: the ELL rows of the training
 // path (EllSrc) or the TwELL tiles of the inference path (TwellSrc); the
@@ -309,8 +309,8 @@ __global__ void __launch_bounds__(256, MINB) ell_axpy_kernel(const EllAxpyArgs p
 // Each entry reads Wu^T[j] and Wg^T[j] once (4 d bytes instead of the 6 d
 // of a gradient gather plus a dX gather).  Per dX element the sum runs
 // group by group: the group's du Wu^T terms in entry order, then its
-// da Wg^T terms.  u, du, da and h are those of the gradient gather, bit for
-// bit.  The team and slab layout are ell_dot_kernel's.
+// da Wg^T terms.  The team and slab layout are ell_dot_kernel's (the team
+// size is the caller's choice, so u is summed over that many warps).
 struct EllGradDxArgs {
   const uint16_t* x;     // [M][d] bf16
   const uint16_t* wuT;   // [f][d] bf16

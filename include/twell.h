@@ -170,10 +170,10 @@ size_t twell_tiles_workspace_bytes(const twell_shape* shape);
  * takes one or two weight matrices per L2-sized pass.  enable = 0: the fused
  * kernels of page 2, section "¿Qué hace distinto a TwELL frente a ELL
  * clásico?" (one gather per row, h kept in registers and never written to
- * global memory).  Both give the same bytes in y and in every dW; dX sums
- * the same fp32 terms in another grouping and may differ by one bf16
- * rounding step.  Not synchronised with work in flight: change it between
- * calls. */
+ * global memory).  Both give the same bytes in y; the backward sums the
+ * same fp32 terms in another grouping (u over another set of warps, dX per
+ * group of 32 entries), so dX and dW may differ in their last bits.  Not
+ * synchronised with work in flight: change it between calls. */
 int32_t twell_set_split_gathers(int32_t enable);
 
 /* Fused sparse up + down projection.  Source: page 2, "¿Qué hace distinto a

@@ -320,13 +320,13 @@ def test_twell_split_forward_flags_overfull_tiles():
 def test_split_and_fused_wide_gathers_agree(M, d, f, q):
     """Rows wider than 1024 run as split gathers by default; with
     twell_set_split_gathers(0) the fused kernels of the pages run instead (h
-    never leaves registers).  Same per-entry arithmetic and, for y and dW,
-    the same accumulation order, so y and every dW must agree bit for bit
-    (d = 4096, f = 8192 also runs both in several L2-sized passes, with
-    different pass counts).  dX sums the same fp32 terms, grouped per 32
-    entries in the split gather (each group's du Wu^T terms before its
-    da Wg^T terms) and entry by entry in the fused kernel, so the two may
-    round differently; each is checked against the oracle."""
+    never leaves registers).  The forward has the same per-entry arithmetic
+    and accumulation order, so y must agree bit for bit (d = 4096, f = 8192
+    also runs both in several L2-sized passes, with different pass counts).
+    The backward's gradient + dX gather forms u over eight warps per row
+    (the fused kernel over its own team) and sums dX per group of 32
+    entries, so dX and dW may round differently; each is checked against
+    the oracle."""
     r = Run(M, d, f, 128, 32, density=0.02, seed=16, exact=True, mixed=True)
     t = r.pack()
     W = _quantile_width(t, r.shape, q) if q > 0 else 0  # W = 0: every live row routed
@@ -348,9 +348,7 @@ def test_split_and_fused_wide_gathers_agree(M, d, f, q):
             _check_step(r, y, dx, *dws, allow=False)
     finally:
         twell.twell_set_split_gathers(True)
-    for k, (a, b) in enumerate(zip(out[True], out[False])):
-        if k != 1:  # y and the weight gradients
-            assert torch.equal(a, b)
+    assert torch.equal(out[True][0], out[False][0])  # y
 
 
 @pytest.mark.parametrize("M,d", [(1, 2048), (3, 4096), (17, 3136)])
