@@ -501,6 +501,10 @@ def run_own(args, dist):
             xs = x[:Ms].contiguous()
             shp = twell.make_shape(Ms, d, f, wl.tile_n, wl.tile_cap)
             tl = twell.alloc_tiles(shp, dev)
+            # the forward's optional workspace (rows wider than 1024): with
+            # it, a handful of rows run as entry-parallel gathers
+            tws = twell.twell_tiles_workspace_bytes(shp)
+            wst = torch.empty(tws, dtype=torch.uint8, device=dev) if tws else None
             ys = torch.empty(Ms, d, dtype=torch.bfloat16, device=dev)
             wsd = torch.empty(twell.twell_dense_workspace_bytes(shp, False), dtype=torch.uint8,
                               device=dev)
@@ -510,7 +514,7 @@ def run_own(args, dist):
 
             def small_sparse():
                 twell.twell_pack(xs, wg, shp, tl)
-                twell.twell_ffn_fwd(xs, wg, wu, wd, shp, ys, tiles=tl)
+                twell.twell_ffn_fwd(xs, wg, wu, wd, shp, ys, tiles=tl, ws=wst)
 
             def small_dense():
                 twell.twell_dense_ffn_fwd(xs, wg, wu, wd, shp, ys, False, wsd)

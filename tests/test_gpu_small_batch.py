@@ -67,18 +67,61 @@ def test_small_batch_pack_twice_is_stable():
 
 
 @pytest.mark.parametrize("M", [1, 3, 16, 64])
-def test_small_batch_forward_matches_oracle(M):
+@pytest.mark.parametrize("with_ws", [False, True])
+def test_small_batch_forward_matches_oracle(M, with_ws):
     # real-valued inputs at a mid-size shape: the TwELL forward of the packed
-    # small batch against the oracle (gate decisions within the fp32 band)
+    # small batch against the oracle (gate decisions within the fp32 band),
+    # with and without the forward's optional workspace (a small batch runs
+    # a cluster of blocks per row either way)
     d, f = 2048, 8192
     w = synthetic.make_inputs(M, d, f, density=0.005, seed=21, with_dy=False)
     x, wg, wu, wd = (dev_bf16(w[k]) for k in ("x", "wgT", "wuT", "wd"))
     shape = twell.make_shape(M, d, f, 128, 32)
     t = twell.alloc_tiles(shape)
     twell.twell_pack(x, wg, shape, t)
-    y = torch.empty(M, d, dtype=torch.bfloat16, device="cuda")
-    twell.twell_ffn_fwd(x, wg, wu, wd, shape, y, tiles=t)
+    y = torch.full((M, d), float("nan"), dtype=torch.bfloat16, device="cuda")
+    ws = (torch.empty(twell.twell_tiles_workspace_bytes(shape), dtype=torch.uint8, device="cuda")
+          if with_ws else None)
+    twell.twell_ffn_fwd(x, wg, wu, wd, shape, y, tiles=t, ws=ws)
     torch.cuda.synchronize()
     assert twell.twell_get_device_status() == 0
     ref = oracle.ffn_fwd_dense(w["x"], w["wgT"], w["wuT"], w["wd"])
     assert_close(to_np(y), ref, "y", out_bf16=True, allowance=fwd_allowance(w))
+
+
+@pytest.mark.parametrize("M,d,f,tile_n,cap", [(5, 3136, 1024, 128, 32), (40, 2048, 2560, 64, 16)])
+def test_small_batch_forward_exact_gate(M, d, f, tile_n, cap):
+    # integer gate inputs (both sides take the same gate decisions): the
+    # small-batch forward against the oracle with the plain tolerance, on a
+    # d_model that leaves a partial 256-column slab and on T_n = 64
+    w = synthetic.make_exact_gate_inputs(M, d, f, density=0.03, seed=M)
+    x, wg, wu, wd = (dev_bf16(w[k]) for k in ("x", "wgT", "wuT", "wd"))
+    shape = twell.make_shape(M, d, f, tile_n, cap)
+    t = twell.alloc_tiles(shape)
+    twell.twell_pack(x, wg, shape, t)
+    assert int(twell.tiles_view(t, shape)[2].max().item()) <= cap
+    y = torch.full((M, d), float("nan"), dtype=torch.bfloat16, device="cuda")
+    ws = torch.empty(twell.twell_tiles_workspace_bytes(shape), dtype=torch.uint8, device="cuda")
+    twell.twell_ffn_fwd(x, wg, wu, wd, shape, y, tiles=t, ws=ws)
+    torch.cuda.synchronize()
+    assert twell.twell_get_device_status() == 0
+    ref = oracle.ffn_fwd_dense(w["x"], w["wgT"], w["wuT"], w["wd"])
+    assert_close(to_np(y), ref, "y", out_bf16=True)
+
+
+def test_small_batch_forward_flags_overfull_tiles():
+    # a tile with more live columns than its capacity: the stored entries
+    # are used and TWELL_ERR_CAPACITY is recorded, as in every TwELL forward
+    M, d, f = 8, 2048, 1024
+    w = synthetic.make_exact_gate_inputs(M, d, f, density=0.3, seed=2)
+    x, wg, wu, wd = (dev_bf16(w[k]) for k in ("x", "wgT", "wuT", "wd"))
+    shape = twell.make_shape(M, d, f, 128, 4)
+    t = twell.alloc_tiles(shape)
+    twell.twell_pack(x, wg, shape, t)
+    assert int(twell.tiles_view(t, shape)[2].max().item()) > 4
+    y = torch.empty(M, d, dtype=torch.bfloat16, device="cuda")
+    ws = torch.empty(twell.twell_tiles_workspace_bytes(shape), dtype=torch.uint8, device="cuda")
+    twell.twell_ffn_fwd(x, wg, wu, wd, shape, y, tiles=t, ws=ws)
+    torch.cuda.synchronize()
+    assert twell.twell_get_device_status() == 4
+    assert torch.isfinite(y.float()).all()
