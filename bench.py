@@ -60,7 +60,8 @@ def parse_args():
                     help="skip the M = 1, 16, 64 forward timings at the workload's shape")
     ap.add_argument("--no-torch-dense", action="store_true",
                     help="skip the PyTorch (cuBLAS) dense FFN reference timing")
-    ap.add_argument("--only", choices=("sparse_step", "sparse_fwd", "dense_fwd", "dense_step"),
+    ap.add_argument("--only", choices=("sparse_step", "sparse_fwd", "dense_fwd", "dense_step",
+                                       "small_fwd"),
                     help="time just this part (a short command for kernel profiling); prints "
                          "a reduced JSON line")
     return ap.parse_args()
@@ -282,9 +283,12 @@ def run_own(args, dist):
     y = torch.empty(M, d, dtype=torch.bfloat16, device=dev)
     dx = torch.empty_like(y)
     dws = [torch.empty(f, d, dtype=torch.float32, device=dev) for _ in range(3)]
-    dws_d = [torch.empty(f, d, dtype=torch.float32, device=dev) for _ in range(3)]
-    ws_d = torch.empty(twell.twell_dense_workspace_bytes(shape, True), dtype=torch.uint8,
-                       device=dev)
+    # the dense comparator's buffers (not allocated for a sparse-only profiling run)
+    need_dense = args.only is None or args.only.startswith("dense")
+    dws_d = [torch.empty(f if need_dense else 1, d, dtype=torch.float32, device=dev)
+             for _ in range(3)]
+    ws_d = torch.empty(twell.twell_dense_workspace_bytes(shape, True) if need_dense else 16,
+                       dtype=torch.uint8, device=dev)
     y_d, dx_d = torch.empty_like(y), torch.empty_like(y)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
@@ -381,9 +385,20 @@ def run_own(args, dist):
             raise RuntimeError("device status %d after timing" % st)
         return dist.max(ms, dev), launches, prof, ck
 
+    def small_fwd():  # the first 64 tokens through the small-batch gate and TwELL forward
+        twell.twell_pack(x_small, wg, shape_small, tiles_small)
+        twell.twell_ffn_fwd(x_small, wg, wu, wd, shape_small, y_small, tiles=tiles_small)
+
+    if args.only == "small_fwd":
+        ms_ = min(64, M)
+        x_small = x[:ms_].contiguous()
+        shape_small = twell.make_shape(ms_, d, f, wl.tile_n, wl.tile_cap)
+        tiles_small = twell.alloc_tiles(shape_small, dev)
+        y_small = torch.empty(ms_, d, dtype=torch.bfloat16, device=dev)
+
     if args.only:
         fn = {"sparse_step": sparse_step, "sparse_fwd": sparse_fwd, "dense_fwd": dense_fwd,
-              "dense_step": dense_step}[args.only]
+              "dense_step": dense_step, "small_fwd": small_fwd}[args.only]
         ms, launches, _, _ = timed(fn, args.steps, args.warmup)
         st = twell.twell_get_device_status()
         if dist.rank == 0:
