@@ -600,10 +600,10 @@ cudaError_t split_rows(const void* x, const void* dy, const void* wgT, const voi
   g.part = part;
   g.dx = reinterpret_cast<uint16_t*>(dx);
   // the gradient + dX gather runs eight warps per row (half the dot
-  // gathers' slabs per warp, four entries per batch, three blocks per SM):
-  // on the 2B- and 8B-class shapes 10 % / 14 % faster than the dot
-  // gathers' team shape, and 5 % / 8 % faster than separate gradient and
-  // dX gathers
+  // gathers' slabs per warp, four entries per batch, four blocks per SM):
+  // on the 2B- and 8B-class shapes 19 % / 20 % faster than the dot
+  // gathers' team shape (two entries, two blocks), and 14 % / 14 % faster
+  // than separate gradient and dX gathers
   constexpr int GT = 8, GV = (TEAM * VPL + 7) / 8;
   const int gd_chunks = part ? l2_chunks(4.0 * (double)f * d, 0.75, 0.5) : 1;
   for (int c = 0; c < gd_chunks; ++c) {
@@ -614,7 +614,7 @@ cudaError_t split_rows(const void* x, const void* dy, const void* wgT, const voi
     {
       ProfScope prof("bwd_grad_dx", s);
       if constexpr (GV <= 2)
-        ell_grad_dx_kernel<GT, GV, 4, 3><<<(unsigned)M, 256, 0, s>>>(g, src);
+        ell_grad_dx_kernel<GT, GV, 4, 4><<<(unsigned)M, 256, 0, s>>>(g, src);
       else
         ell_grad_dx_kernel<GT, GV, 2, 2><<<(unsigned)M, 256, 0, s>>>(g, src);
     }
