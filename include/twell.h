@@ -116,7 +116,10 @@ typedef struct twell_hybrid {
  * Computes a = x Wg (bf16 in, fp32 accumulate on tcgen05 tensor cores), then
  * for every (row, tile) g = bf16(ReLU(a)), keeps the live (g > 0) columns in
  * ascending order and writes `out` (all four arrays).  No dense activation is
- * written to global memory.
+ * written to global memory.  Batches of at most 64 rows run with the
+ * operands swapped (128 neurons on the MMA's M dimension, the rows padded
+ * to 16, 32 or 64 on its N dimension) and pack across TMEM lanes; the
+ * format is the same, the fp32 sums run in another order.
  *   x    bf16 [M][d_model], wgT bf16 [d_ff][d_model]. */
 twell_status twell_pack(const void* x, const void* wgT, const twell_shape* shape,
                         const twell_tiles* out, void* stream);
