@@ -204,7 +204,7 @@ struct SparseWs {
   float* hbuf;                          // per-ELL-entry h of the split forward
   uint16_t *dyr, *gr, *ddr;             // backward fallback
   float* ur;
-  int *mask_off, *csc_ptr, *csc_row;
+  int *mask_off, *csc_ptr, *csc_row, *slot_pos;
   float4* csc_vals;
   long long Mr;                         // routed-row buffer rows (capacity in whole tiles)
   long long Mp;                         // rows of part
@@ -234,6 +234,7 @@ SparseWs carve_sparse(void* ws, const twell_shape& s, int W, int dense_cap, int 
     w.mask_off = c.take<int>((2 * NB + (NG > 0 ? NG : 1)) * f);
     w.csc_ptr = c.take<int>(f + 1);
     w.csc_row = c.take<int>(E > 0 ? E : 1);
+    w.slot_pos = c.take<int>(E > 0 ? E : 1);
     w.csc_vals = c.take<float4>(E > 0 ? E : 1);
   }
   w.bytes = c.off + 256;
@@ -675,11 +676,10 @@ twell_status twell_ffn_bwd(const void* x, const void* wgT, const void* wuT, cons
   const SparseWs w = carve_sparse(ws, s, route->ell_width, route->dense_cap, 1);
   const long long Mr = w.Mr;
   const long long f = s.d_ff;
-  CscPlace place{};
-  cudaError_t e = launch_csc_build(*route, s.M, s.d_ff, w.mask_off, w.csc_ptr, w.csc_row, &place,
-                                   cs);
+  cudaError_t e = launch_csc_build(*route, s.M, s.d_ff, w.mask_off, w.csc_ptr, w.csc_row,
+                                   w.slot_pos, cs);
   if (e == cudaSuccess)
-    e = launch_sparse_bwd_rows(x, dy, wgT, wuT, wd, s.M, s.d_model, s.d_ff, *route, place,
+    e = launch_sparse_bwd_rows(x, dy, wgT, wuT, wd, s.M, s.d_model, s.d_ff, *route, w.slot_pos,
                                l1_coeff, w.csc_vals, dx, w.part, w.hbuf, cs);
   if (e == cudaSuccess)
     e = launch_sparse_bwd_neurons(x, dy, s.M, s.d_model, s.d_ff, w.csc_ptr, w.csc_row, w.csc_vals,

@@ -42,7 +42,6 @@ namespace tw {
 namespace {
 
 constexpr int kDotH = 0, kDotDh = 1;
-
 constexpr int kEllPassFirst = 1, kEllPassLast = 2;
 
 // Element offset of slab v of warp wt in a team of TEAM warps: slabs of 256
@@ -318,7 +317,7 @@ struct EllGradDxArgs {
   const uint16_t* wgT;   // [f][d] bf16
   int M, d;
   const float* dh;       // dh per entry (the source's buffer index)
-  CscPlace place;        // neuron-major position of each entry; its row is written there
+  const int* slot_pos;   // neuron-major position of each slot
   float lambda;          // L1 coefficient
   float4* csc_vals;      // (du, da, h, 0) at the neuron-major position
   int pass;              // kEllPassFirst: start from 0, kEllPassLast: store dx
@@ -410,10 +409,9 @@ __global__ void __launch_bounds__(256, MINB)
     }
     const float dal = live ? fmaf(dhl, u, p.lambda) : 0.f;  // ReLU'(a) = 1 on a live entry
     if (wt == 0 && live) {
-      long long pos = p.place.pos(m, jl);
+      long long pos = p.slot_pos[s];
       TW_CHECK_INDEX(pos, pos >= 0 && pos < (long long)p.M * src.W);
       p.csc_vals[pos] = make_float4(dul, dal, gl * u, 0.f);
-      p.place.row[pos] = m;
     }
     // Wg^T rows: da Wg[:, j]^T into dX_m
     for (int i = 0; i < count; i += B) {

@@ -106,33 +106,14 @@ cudaError_t launch_sparse_fwd(const void* x, const void* wuT, const void* wd, in
                               const twell_tiles* tiles, int tile_n, int cap,
                               const twell_hybrid* route, void* y, float* part, float* hbuf,
                               cudaStream_t s);
-// The neuron-major (CSC) position of a live entry (m, j), from the index the
-// backward builds per 32-row block and neuron (sparse_bwd.cu): the neuron's
-// start, the live rows of earlier groups of 32 blocks, of earlier blocks of
-// the group, and of lower rows of the block (a popcount of the block's row
-// mask).  The row phase computes it for each entry it visits and writes the
-// entry's row there, so no separate placing pass is needed.
-struct CscPlace {
-  const unsigned* mask;  // [ceil(M/32)][f] rows of each 32-row block that use the neuron
-  const int* off;        // [ceil(M/32)][f] live rows in earlier blocks of the group
-  const int* gpre;       // [ceil(M/1024)][f] live rows in earlier groups
-  const int* ptr;        // [f + 1] first position of each neuron
-  int* row;              // [nnz] row of each position (written by the row phase)
-  int f;
-  __device__ __forceinline__ int pos(int m, int j) const {
-    const long long blk = (long long)(m >> 5) * f + j;
-    const long long grp = (long long)((m >> 5) >> 5) * f + j;
-    return ptr[j] + gpre[grp] + off[blk] + __popc(mask[blk] & ((1u << (m & 31)) - 1u));
-  }
-};
 cudaError_t launch_csc_build(const twell_hybrid& route, int M, int f, int* blk_counts,
-                             int* csc_ptr, int* csc_row, CscPlace* place, cudaStream_t s);
+                             int* csc_ptr, int* csc_row, int* slot_pos, cudaStream_t s);
 // `part` ([M][d] fp32) carries dX between L2-sized neuron passes (may be null).
 // `dhbuf` ([M][ell_width] fp32) holds the per-entry dh of the split row phase
 // used for rows wider than 1024; null keeps the fused kernel.
 cudaError_t launch_sparse_bwd_rows(const void* x, const void* dy, const void* wgT, const void* wuT,
                                    const void* wd, int M, int d, int f, const twell_hybrid& route,
-                                   const CscPlace& place, float lambda, float4* csc_vals, void* dx,
+                                   const int* slot_pos, float lambda, float4* csc_vals, void* dx,
                                    float* part, float* dhbuf, cudaStream_t s);
 cudaError_t launch_sparse_bwd_neurons(const void* x, const void* dy, int M, int d, int f,
                                       const int* csc_ptr, const int* csc_row,

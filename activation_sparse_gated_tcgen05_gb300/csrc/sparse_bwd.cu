@@ -127,6 +127,28 @@ __global__ void __launch_bounds__(1024)
   if (tid == 0) csc_ptr[f] = carry;
 }
 
+__global__ void __launch_bounds__(kWarps * 32)
+    csc_place_kernel(const uint16_t* __restrict__ ell_col, const int* __restrict__ ell_nnz, int M,
+                     int W, int f, const unsigned* __restrict__ mask, const int* __restrict__ off,
+                     const int* __restrict__ gpre, const int* __restrict__ csc_ptr,
+                     int* __restrict__ csc_row, int* __restrict__ slot_pos) {
+  const int lane = threadIdx.x & 31;
+  const int m = blockIdx.x * kWarps + (threadIdx.x >> 5);
+  if (m >= M) return;
+  int n = ell_nnz[m];
+  TW_CHECK_INDEX(n, n >= 0 && n <= W);
+  const long long blk = (long long)(m >> 5) * f;
+  const long long grp = (long long)((m >> 5) / kScanG) * f;
+  const unsigned below = (1u << (m & 31)) - 1u;
+  for (int s = lane; s < n; s += 32) {
+    int j = ell_col[(long long)m * W + s];
+    TW_CHECK_INDEX(j, j < f);
+    const int pos = csc_ptr[j] + gpre[grp + j] + off[blk + j] + __popc(mask[blk + j] & below);
+    csc_row[pos] = m;
+    slot_pos[(long long)m * W + s] = pos;
+  }
+}
+
 // ---------------------------------------------------------------- row phase
 template <int TEAM>
 __device__ __forceinline__ int slab(int lane, int wt, int v) {
@@ -140,7 +162,7 @@ __global__ void __launch_bounds__(256, MINB)
                     const uint16_t* __restrict__ wgT, const uint16_t* __restrict__ wuT,
                     const uint16_t* __restrict__ wd, int M, int d,
                     const uint16_t* __restrict__ ell_val, const uint16_t* __restrict__ ell_col,
-                    const int* __restrict__ ell_nnz, int W, const CscPlace place,
+                    const int* __restrict__ ell_nnz, int W, const int* __restrict__ slot_pos,
                     float lambda, float4* __restrict__ csc_vals, uint16_t* __restrict__ dx,
                     float* __restrict__ part, int j_lo, int j_hi, int pass) {
   static_assert(32 % B == 0, "a batch never reaches past lane 31");
@@ -199,7 +221,7 @@ __global__ void __launch_bounds__(256, MINB)
       jl = ell_col[s];
       TW_CHECK_INDEX(jl, jl >= j_lo && jl < j_hi);  // the pass's neuron chunk
       gl = bf16_bits_to_float(ell_val[s]);
-      pl = place.pos(m, jl);
+      pl = slot_pos[s];
       TW_CHECK_INDEX(pl, pl >= 0 && (long long)pl < (long long)M * W);
     }
     for (int i = 0; i < count; i += B) {
@@ -274,10 +296,7 @@ __global__ void __launch_bounds__(256, MINB)
         const bool live = i + b < count;
         const float du = dh[b] * g[b];
         const float da = live ? fmaf(dh[b], u[b], lambda) : 0.f;
-        if (live && wt == 0 && lane == 0) {
-          csc_vals[pos[b]] = make_float4(du, da, g[b] * u[b], 0.f);
-          place.row[pos[b]] = m;
-        }
+        if (live && wt == 0 && lane == 0) csc_vals[pos[b]] = make_float4(du, da, g[b] * u[b], 0.f);
         const uint64_t du2 = f2_splat(du), da2 = f2_splat(da);
 #pragma unroll
         for (int v = 0; v < VPL; ++v) {
@@ -430,7 +449,7 @@ __global__ void __launch_bounds__(256, MINB)
 template <int TEAM, int VPL, int B, int MINB>
 cudaError_t rows_team(const void* x, const void* dy, const void* wgT, const void* wuT,
                       const void* wd, int M, int d, int f, const twell_hybrid& r,
-                      const CscPlace& place, float lambda, float4* csc_vals, void* dx, float* part,
+                      const int* slot_pos, float lambda, float4* csc_vals, void* dx, float* part,
                       int chunks, cudaStream_t s) {
   constexpr int ROWS = 8 / TEAM;
   for (int c = 0; c < chunks; ++c) {
@@ -443,7 +462,7 @@ cudaError_t rows_team(const void* x, const void* dy, const void* wgT, const void
           reinterpret_cast<const uint16_t*>(wgT), reinterpret_cast<const uint16_t*>(wuT),
           reinterpret_cast<const uint16_t*>(wd), M, d,
           reinterpret_cast<const uint16_t*>(r.ell_val), r.ell_col, r.ell_nnz, r.ell_width,
-          place, lambda, csc_vals, reinterpret_cast<uint16_t*>(dx), part, j_lo, j_hi, pass);
+          slot_pos, lambda, csc_vals, reinterpret_cast<uint16_t*>(dx), part, j_lo, j_hi, pass);
     }
     count_launch();
     const cudaError_t e = cudaGetLastError();
@@ -478,10 +497,9 @@ cudaError_t neurons_team(const void* x, const void* dy, int M, int d, int f, con
 }  // namespace
 
 // blk_counts holds the row masks and block offsets ([ceil(M/32)][f] ints each)
-// followed by the group totals / prefixes ([ceil(M/1024)][f] ints).  The row
-// phase places the entries (CscPlace): `place` receives the index it reads.
+// followed by the group totals / prefixes ([ceil(M/1024)][f] ints).
 cudaError_t launch_csc_build(const twell_hybrid& r, int M, int f, int* blk_counts, int* csc_ptr,
-                             int* csc_row, CscPlace* place, cudaStream_t s) {
+                             int* csc_row, int* slot_pos, cudaStream_t s) {
   const int NB = (M + 31) / 32;
   const int NG = (NB + kScanG - 1) / kScanG;
   unsigned* mask = reinterpret_cast<unsigned*>(blk_counts);
@@ -491,7 +509,6 @@ cudaError_t launch_csc_build(const twell_hybrid& r, int M, int f, int* blk_count
   }
   int* off = blk_counts + (long long)NB * f;
   int* gtot = off + (long long)NB * f;
-  *place = CscPlace{mask, off, gtot, csc_ptr, csc_row, f};
   cudaError_t e = cudaMemsetAsync(mask, 0, sizeof(unsigned) * (size_t)NB * f, s);
   if (e != cudaSuccess) return e;
   if (M > 0) {
@@ -516,7 +533,17 @@ cudaError_t launch_csc_build(const twell_hybrid& r, int M, int f, int* blk_count
     csc_ptr_kernel<<<1, 1024, 0, s>>>(gtot, M > 0 ? NG : 1, f, csc_ptr);
   }
   count_launch();
-  return cudaGetLastError();
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  if (M > 0) {
+    {
+      ProfScope prof("csc_place", s);
+      csc_place_kernel<<<(M + kWarps - 1) / kWarps, kWarps * 32, 0, s>>>(
+          r.ell_col, r.ell_nnz, M, r.ell_width, f, mask, off, gtot, csc_ptr, csc_row, slot_pos);
+    }
+    count_launch();
+    e = cudaGetLastError();
+  }
+  return e;
 }
 
 namespace {
@@ -531,7 +558,7 @@ namespace {
 template <int TEAM, int VPL>
 cudaError_t split_rows(const void* x, const void* dy, const void* wgT, const void* wuT,
                        const void* wd, int M, int d, int f, const twell_hybrid& r,
-                       const CscPlace& place, float lambda, float4* csc_vals, void* dx, float* part,
+                       const int* slot_pos, float lambda, float4* csc_vals, void* dx, float* part,
                        float* dhbuf, cudaStream_t s) {
   constexpr int ROWS = 8 / TEAM;
   const unsigned grid = (unsigned)((M + ROWS - 1) / ROWS);
@@ -567,7 +594,7 @@ cudaError_t split_rows(const void* x, const void* dy, const void* wgT, const voi
   g.M = M;
   g.d = d;
   g.dh = dhbuf;
-  g.place = place;
+  g.slot_pos = slot_pos;
   g.lambda = lambda;
   g.csc_vals = csc_vals;
   g.part = part;
@@ -602,7 +629,7 @@ cudaError_t split_rows(const void* x, const void* dy, const void* wgT, const voi
 
 cudaError_t launch_sparse_bwd_rows(const void* x, const void* dy, const void* wgT, const void* wuT,
                                    const void* wd, int M, int d, int f, const twell_hybrid& route,
-                                   const CscPlace& place, float lambda, float4* csc_vals, void* dx,
+                                   const int* slot_pos, float lambda, float4* csc_vals, void* dx,
                                    float* part, float* dhbuf, cudaStream_t s) {
   if (M == 0) return cudaSuccess;
   {
@@ -612,7 +639,7 @@ cudaError_t launch_sparse_bwd_rows(const void* x, const void* dy, const void* wg
   if (d > 1024 && split_gathers()) {  // wide rows: the split gathers, the forward's team shapes
     if (!dhbuf) return cudaErrorInvalidValue;
 #define TW_SPLIT(T, V)                                                                          \
-  split_rows<T, V>(x, dy, wgT, wuT, wd, M, d, f, route, place, lambda, csc_vals, dx, part,  \
+  split_rows<T, V>(x, dy, wgT, wuT, wd, M, d, f, route, slot_pos, lambda, csc_vals, dx, part,  \
                    dhbuf, s)
     if (d <= 2048) return TW_SPLIT(4, 2);
     if (d <= 4096) return TW_SPLIT(4, 4);
@@ -626,7 +653,7 @@ cudaError_t launch_sparse_bwd_rows(const void* x, const void* dy, const void* wg
   // (fp32) with the accumulation order unchanged
   const int chunks = part ? l2_chunks(3.0 * 2.0 * (double)f * d, 0.5, 0.65) : 1;
 #define TW_ROWS(T, V, B, MINB)                                                                 \
-  rows_team<T, V, B, MINB>(x, dy, wgT, wuT, wd, M, d, f, route, place, lambda, csc_vals, dx, \
+  rows_team<T, V, B, MINB>(x, dy, wgT, wuT, wd, M, d, f, route, slot_pos, lambda, csc_vals, dx, \
                            part, chunks, s)
   // wider rows here only with the split gathers switched off; team shapes as
   // measured on the 2B- and 8B-class shapes (one entry per batch from d = 2048)
