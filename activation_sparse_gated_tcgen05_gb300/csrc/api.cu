@@ -18,16 +18,14 @@ namespace tw {
 __device__ int g_device_status;
 
 namespace {
-
 constexpr int kMaxDevices = 64;
+}  // namespace
 
 int current_device() {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return -1;
   return dev;
 }
-
-}  // namespace
 
 namespace {
 std::atomic<unsigned long long> g_launches{0};
@@ -94,6 +92,10 @@ int num_sms() {
 // Process-wide choice of the wide-row gathers (see twell_set_split_gathers).
 std::atomic<int> g_split_gathers{1};
 bool split_gathers() { return g_split_gathers.load(std::memory_order_relaxed) != 0; }
+
+// Process-wide choice of the GEMM tile form (see twell_set_pair_gemm).
+std::atomic<int> g_pair_gemm{1};
+bool pair_gemm() { return g_pair_gemm.load(std::memory_order_relaxed) != 0; }
 
 double l2_bytes() {
   static int cache[kMaxDevices] = {0};
@@ -606,6 +608,10 @@ size_t twell_workspace_bytes(const twell_shape* shape, int32_t ell_width, int32_
 
 int32_t twell_set_split_gathers(int32_t enable) {
   return g_split_gathers.exchange(enable ? 1 : 0) ? 1 : 0;
+}
+
+int32_t twell_set_pair_gemm(int32_t enable) {
+  return g_pair_gemm.exchange(enable ? 1 : 0) ? 1 : 0;
 }
 
 size_t twell_tiles_workspace_bytes(const twell_shape* shape) {

@@ -67,13 +67,68 @@ bool make_tma_map_bf16(CUtensorMap* m, const Mat& a, uint32_t box_inner, uint32_
 
 namespace {
 
+// Clusters of the CTA-pair kernel that fit on the device at once (0: none,
+// or the query failed), cached per device.
+template <bool A_MN, bool B_MN, int EPI>
+int pair_clusters() {
+  constexpr int kDevices = 64;
+  static int cache[kDevices] = {0};  // 0 = not asked yet, -1 = unavailable
+  const int dev = current_device();
+  if (dev < 0 || dev >= kDevices) return 0;
+  if (cache[dev] == 0) {
+    auto kern = gemm_kernel<A_MN, B_MN, EPI, true>;
+    int n = 0;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         kGemmSmem);
+    if (e == cudaSuccess) {
+      cudaLaunchConfig_t cfg = {};
+      cfg.gridDim = dim3(2 * (unsigned)(num_sms() / 2));
+      cfg.blockDim = dim3(kGemmThreads);
+      cfg.dynamicSmemBytes = kGemmSmem;
+      cudaLaunchAttribute attr[1];
+      attr[0].id = cudaLaunchAttributeClusterDimension;
+      attr[0].val.clusterDim.x = 2;
+      attr[0].val.clusterDim.y = 1;
+      attr[0].val.clusterDim.z = 1;
+      cfg.attrs = attr;
+      cfg.numAttrs = 1;
+      e = cudaOccupancyMaxActiveClusters(&n, kern, &cfg);
+    }
+    if (e != cudaSuccess) {
+      n = 0;
+      cudaGetLastError();  // the failed query's error is not left for the caller
+    }
+    cache[dev] = n > 0 ? n : -1;
+  }
+  return cache[dev] > 0 ? cache[dev] : 0;
+}
+
 template <bool A_MN, bool B_MN, int EPI>
 cudaError_t launch_t(const char* name, const Mat& A, const Mat& B, const Mat* B2,
                      const GemmParams& p, cudaStream_t s, const OutMat* outs, int n_outs) {
+  // CTA pairs (256 x 256 tiles) unless the GEMM splits K (split-K partials
+  // and cluster split-K keep single CTAs) or the pairs would need more waves
+  // of tiles than single CTAs (a pair tile takes about as long as a single
+  // CTA's 128 x 256 tile)
+  int clusters = 0;
+  long long pair_tiles = 0;
+  if (pair_gemm() && p.split_k_max <= 1 && !(EPI == EPI_PACK && p.cluster_k > 1) && p.M > 0 &&
+      p.n_tiles > 0) {
+    pair_tiles = (long long)((p.M + 2 * kBM - 1) / (2 * kBM)) * p.n_tiles;
+    const long long single_tiles = (long long)((p.M + kBM - 1) / kBM) * p.n_tiles;
+    const int sms = num_sms();
+    clusters = pair_clusters<A_MN, B_MN, EPI>();
+    if (clusters > 0 && sms > 0 &&
+        (pair_tiles + clusters - 1) / clusters > (single_tiles + sms - 1) / sms)
+      clusters = 0;
+  }
+  const bool pair = clusters > 0;
   CUtensorMap ta, tb, tb2;
   // A: K-major [M][K] -> box {64 (K), 128 rows}; MN-major [K][M] -> box {64 (M), 64 (K)}
   if (!make_map(&ta, A, 64, A_MN ? 64 : kBM)) return cudaErrorInvalidValue;
-  const uint32_t b_rows = (EPI == EPI_GATED) ? 128 : kBN;
+  // B: K-major -> box {64 (K), rows of B a CTA stages}: 128 for the gated
+  // GEMM (one of [Wg ; Wu]) and for a pair (half of the tile's 256), else 256
+  const uint32_t b_rows = (EPI == EPI_GATED || pair) ? 128 : kBN;
   if (!make_map(&tb, B, 64, B_MN ? 64 : b_rows)) return cudaErrorInvalidValue;
   if (B2) {
     if (!make_map(&tb2, *B2, 64, B_MN ? 64 : b_rows)) return cudaErrorInvalidValue;
@@ -88,7 +143,35 @@ cudaError_t launch_t(const char* name, const Mat& A, const Mat& B, const Mat* B2
       to[i] = ta;  // unused
     }
   }
-  auto kern = gemm_kernel<A_MN, B_MN, EPI>;
+  if (pair) {
+    // one 2-CTA cluster per pair, at most one pair per resident cluster slot
+    auto kern = gemm_kernel<A_MN, B_MN, EPI, true>;
+    cudaError_t e =
+        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kGemmSmem);
+    if (e != cudaSuccess) return e;
+    const long long n_pairs = pair_tiles < clusters ? pair_tiles : clusters;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(2 * n_pairs));
+    cfg.blockDim = dim3(kGemmThreads);
+    cfg.dynamicSmemBytes = kGemmSmem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaError_t le;
+    {
+      ProfScope prof(name, s);
+      le = cudaLaunchKernelEx(&cfg, kern, ta, tb, tb2, to[0], to[1], to[2], p);
+    }
+    count_launch();
+    if (le != cudaSuccess) return le;
+    return cudaGetLastError();
+  }
+  auto kern = gemm_kernel<A_MN, B_MN, EPI, false>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kGemmSmem);
   if (e != cudaSuccess) return e;
   const long long m_tiles = (p.M + kBM - 1) / kBM;

@@ -27,6 +27,83 @@
 
 namespace tw {
 
+// ---- CTA-pair forms (cta_group::2).  A kernel uses either these or the
+// single-CTA forms above for alloc / dealloc / relinquish / mma / commit,
+// never both.  The pair is the two CTAs of a 2-CTA cluster: rank 0 issues the
+// MMAs, which read A and B from both CTAs' shared memory (same offsets) and
+// write each CTA's own accumulator rows into that CTA's TMEM.
+
+// Collective over the pair: one warp of each CTA executes it.
+TW_DEV void tmem_alloc_pair(uint32_t* holder, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                   smem_u32(holder)),
+               "r"(ncols)
+               : "memory");
+}
+TW_DEV void tmem_relinquish_pair() {
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+TW_DEV void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+               : "memory");
+}
+
+// Arrive once on the barrier at this shared-memory offset in every CTA of
+// `cta_mask` when the pair MMAs issued so far are done.
+TW_DEV void tc_commit_pair(uint64_t* bar, uint16_t cta_mask) {
+  asm volatile(
+      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+      " [%0], %1;" ::"r"(smem_u32(bar)),
+      "h"(cta_mask)
+      : "memory");
+}
+
+// D[tmem] (+)= A * B^T over the pair: M = 256 (128 rows from each CTA), N
+// columns of B (the first N/2 rows of B from rank 0, the rest from rank 1).
+TW_DEV void tc_mma_bf16_pair(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                             uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// Address of the same shared-memory offset in CTA `rank` of the cluster.
+TW_DEV uint32_t cluster_addr(const void* p, uint32_t rank) {
+  uint32_t out;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(out) : "r"(smem_u32(p)), "r"(rank));
+  return out;
+}
+
+// TMA load into this CTA's shared memory whose completion is counted on a
+// barrier of either CTA of the pair (a shared::cluster address).
+TW_DEV void tma_load_2d_pair(void* dst, const CUtensorMap* map, uint32_t bar_cluster, int c0,
+                             int c1) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.cta_group::2"
+      " [%0], [%1, {%3, %4}], [%2];" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar_cluster), "r"(c0), "r"(c1)
+      : "memory");
+}
+
+// Arrive on a barrier given by its shared::cluster address.
+TW_DEV void mbar_arrive_cluster(uint32_t bar_cluster) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar_cluster)
+               : "memory");
+}
+
+TW_DEV uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+TW_DEV void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::
+                   : "memory");
+}
+
 enum EpiKind { EPI_STORE = 0, EPI_PACK = 1, EPI_GATED = 2, EPI_BWD_GATE = 3, EPI_BWD_GATE_RT = 4 };
 
 constexpr int kBM = 128;
@@ -564,67 +641,97 @@ struct Epilogue<EPI_BWD_GATE_RT> {
 };
 
 // ------------------------------------------------------------------ kernel
-template <bool A_MN, bool B_MN, int EPI>
+// PAIR = true: the CTA-pair form.  The kernel runs as 2-CTA clusters; a pair
+// owns 256 x 256 output tiles, rank r of the pair loads A rows [128 r, 128 r
+// + 128) of the tile and B rows (output columns) [128 r, 128 r + 128) into
+// its own ring, and rank 0's MMA warp issues 256 x 256 x 16 MMAs that read
+// both rings and leave each rank's 128 accumulator rows in that rank's TMEM.
+// Per SM this halves the B bytes staged and read per MMA, which is what
+// bounds the single-CTA 128 x 256 tile.  A stage holds 32 KB per CTA (16 KB
+// A + 16 KB B), so the same shared memory gives a 6-deep ring.  Not used
+// with split-K or cluster split-K.
+constexpr int kPairStages = 6;
+static_assert(kPairStages * (kABytes + kBBytes / 2) <= kStages * (kABytes + kBBytes),
+              "the pair ring fits the single-CTA ring's shared memory");
+
+template <bool A_MN, bool B_MN, int EPI, bool PAIR = false>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                 const __grid_constant__ CUtensorMap tmB2, const __grid_constant__ CUtensorMap tmO0,
                 const __grid_constant__ CUtensorMap tmO1, const __grid_constant__ CUtensorMap tmO2,
                 const GemmParams p) {
+  constexpr int STAGES = PAIR ? kPairStages : kStages;
+  constexpr int B_BYTES = PAIR ? kBBytes / 2 : kBBytes;  // B bytes per stage in this CTA
+  constexpr int TILE_M = PAIR ? 2 * kBM : kBM;           // output rows per tile
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
   uint8_t* sA = smem;
-  uint8_t* sB = smem + kStages * kABytes;
-  uint8_t* sOut = sB + kStages * kBBytes;  // 8 x 4 KB epilogue staging buffers
+  uint8_t* sB = smem + STAGES * kABytes;
+  uint8_t* sOut = sB + STAGES * B_BYTES;  // 8 x 4 KB epilogue staging buffers
   uint64_t* full = reinterpret_cast<uint64_t*>(sOut + 8 * kStageBytes);
-  uint64_t* empty = full + kStages;
-  uint64_t* tfull = empty + kStages;
+  uint64_t* empty = full + STAGES;
+  uint64_t* tfull = empty + STAGES;
   uint64_t* tempty = tfull + 2;
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(tempty + 2);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  // a pair (PAIR) or a CTA walks the units group, group + n_groups, ...
+  const int rank = PAIR ? (int)cluster_rank() : 0;
+  const int group = PAIR ? (int)(blockIdx.x >> 1) : (int)blockIdx.x;
+  const int n_groups = PAIR ? (int)(gridDim.x >> 1) : (int)gridDim.x;
 
   int M_eff = p.M;
   if (p.m_dev) M_eff = min(M_eff, *p.m_dev);
   int K_eff = p.K;
   if (p.k_dev) K_eff = min(K_eff, *p.k_dev);
-  const int m_tiles = (M_eff + kBM - 1) / kBM;
+  const int m_tiles = (M_eff + TILE_M - 1) / TILE_M;
   const int kb_pass = (K_eff + kBK - 1) / kBK;
   const int num_kb = (A_MN && p.a_seg_off > 0) ? 2 * kb_pass : kb_pass;
   const int tiles = m_tiles * p.n_tiles;
   int splits = 1, kps = num_kb;
-  const int cluster_k = (EPI == EPI_PACK && p.cluster_k > 1) ? p.cluster_k : 1;
+  const int cluster_k = (!PAIR && EPI == EPI_PACK && p.cluster_k > 1) ? p.cluster_k : 1;
   if (cluster_k > 1) {
     splits = cluster_k;
     kps = (num_kb + cluster_k - 1) / cluster_k;
-  } else if (p.split_k_max > 1 && num_kb > 0 && M_eff > 0) {
+  } else if (!PAIR && p.split_k_max > 1 && num_kb > 0 && M_eff > 0) {
     splitk_plan(m_tiles * kBM, p.split_rows > 0 ? p.split_rows : p.M, num_kb, p.split_k_max,
                 splits, kps);
   }
   const int total = (num_kb > 0 && M_eff > 0) ? tiles * splits : 0;
-  // nothing to do (e.g. no routed rows): leave before touching TMEM or barriers
-  if (total == 0 || (int)blockIdx.x >= total) return;
+  // nothing to do (e.g. no routed rows): leave before touching TMEM or
+  // barriers (uniform over a pair: both ranks have the same group)
+  if (total == 0 || group >= total) return;
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kStages; ++s) {
+    for (int s = 0; s < STAGES; ++s) {
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(&tfull[a], 1);
-      mbar_init(&tempty[a], kEpiThreads);
+      // PAIR: one arrival per epilogue warp of both ranks, on rank 0's barrier
+      mbar_init(&tempty[a], PAIR ? 2 * (kEpiThreads / 32) : kEpiThreads);
     }
     *abort_flag = 0;
     fence_mbar_init();
   }
   if (warp == 2) {
-    tmem_alloc(tmem_holder, kTmemCols);
-    tmem_relinquish();
+    if constexpr (PAIR) {
+      tmem_alloc_pair(tmem_holder, kTmemCols);
+      tmem_relinquish_pair();
+    } else {
+      tmem_alloc(tmem_holder, kTmemCols);
+      tmem_relinquish();
+    }
   }
   tc_fence_before();
-  __syncthreads();
+  if constexpr (PAIR)
+    cluster_sync_all();  // the peer's barriers are initialised before any remote arrival
+  else
+    __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_holder;
 
@@ -634,10 +741,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       tma_prefetch_desc(&tmA);
       tma_prefetch_desc(&tmB);
       tma_prefetch_desc(&tmB2);
+      // PAIR: both ranks' loads complete on rank 0's full barriers
+      const uint32_t full0 = PAIR ? cluster_addr(&full[0], 0) : 0u;
       int stage = 0;
       uint32_t phase = 0;
       bool ok = true;
-      for (int unit = blockIdx.x; unit < total && ok; unit += gridDim.x) {
+      for (int unit = group; unit < total && ok; unit += n_groups) {
         int mb, nb, tile, ks;
         unit_coords(unit, tiles, cluster_k, tile, ks);
         tile_coords(tile, m_tiles, p.n_tiles, mb, nb);
@@ -647,35 +756,78 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             ok = false;
             break;
           }
-          mbar_arrive_expect_tx(&full[stage], kABytes + kBBytes);
           uint8_t* a_dst = sA + stage * kABytes;
-          uint8_t* b_dst = sB + stage * kBBytes;
-          if (!A_MN) {
-            tma_load_2d(a_dst, &tmA, &full[stage], kb * kBK, mb * kBM);
-          } else {
-            const bool second = kb >= kb_pass;
-            const int ka = (second ? kb - kb_pass : kb) * kBK;
-            const int ma = mb * kBM + (second ? p.a_seg_off : 0);
-            tma_load_2d(a_dst, &tmA, &full[stage], ma, ka);
-            tma_load_2d(a_dst + 8192, &tmA, &full[stage], ma + 64, ka);
-          }
-          if (EPI == EPI_GATED) {
-            tma_load_2d(b_dst, &tmB, &full[stage], kb * kBK, nb * 128);
-            tma_load_2d(b_dst + 16384, &tmB2, &full[stage], kb * kBK, nb * 128);
-          } else {
-            const int kbb = (A_MN && kb >= kb_pass) ? kb - kb_pass : kb;  // B rows repeat
-            const int seg = kbb / p.k_split;
-            const CUtensorMap* mp = (seg & 1) ? &tmB2 : &tmB;
-            const int kk = kbb - seg * p.k_split;
-            if (!B_MN) {
-              tma_load_2d(b_dst, mp, &full[stage], kk * kBK, nb * kBN);
+          uint8_t* b_dst = sB + stage * B_BYTES;
+          if constexpr (PAIR) {
+            if (rank == 0) mbar_arrive_expect_tx(&full[stage], 2 * (kABytes + B_BYTES));
+            const uint32_t fb = full0 + 8u * (uint32_t)stage;
+            const int m0 = mb * TILE_M + rank * kBM;  // this rank's A rows
+            if (!A_MN) {
+              tma_load_2d_pair(a_dst, &tmA, fb, kb * kBK, m0);
             } else {
+              const bool second = kb >= kb_pass;
+              const int ka = (second ? kb - kb_pass : kb) * kBK;
+              const int ma = m0 + (second ? p.a_seg_off : 0);
+              tma_load_2d_pair(a_dst, &tmA, fb, ma, ka);
+              tma_load_2d_pair(a_dst + 8192, &tmA, fb, ma + 64, ka);
+            }
+            if (EPI == EPI_GATED) {
+              // rank 0 holds the tile's 128 gate rows, rank 1 its 128 up rows
+              tma_load_2d_pair(b_dst, rank ? &tmB2 : &tmB, fb, kb * kBK, nb * 128);
+            } else {
+              const int kbb = (A_MN && kb >= kb_pass) ? kb - kb_pass : kb;  // B rows repeat
+              const int seg = kbb / p.k_split;
+              const CUtensorMap* mp = (seg & 1) ? &tmB2 : &tmB;
+              const int kk = kbb - seg * p.k_split;
+              const int n0 = nb * kBN + rank * (kBN / 2);  // this rank's B rows
+              if (!B_MN) {
+                tma_load_2d_pair(b_dst, mp, fb, kk * kBK, n0);
+              } else {
+                tma_load_2d_pair(b_dst, mp, fb, n0, kk * kBK);
+                tma_load_2d_pair(b_dst + 8192, mp, fb, n0 + 64, kk * kBK);
+              }
+            }
+          } else {
+            mbar_arrive_expect_tx(&full[stage], kABytes + kBBytes);
+            if (!A_MN) {
+              tma_load_2d(a_dst, &tmA, &full[stage], kb * kBK, mb * kBM);
+            } else {
+              const bool second = kb >= kb_pass;
+              const int ka = (second ? kb - kb_pass : kb) * kBK;
+              const int ma = mb * kBM + (second ? p.a_seg_off : 0);
+              tma_load_2d(a_dst, &tmA, &full[stage], ma, ka);
+              tma_load_2d(a_dst + 8192, &tmA, &full[stage], ma + 64, ka);
+            }
+            if (EPI == EPI_GATED) {
+              tma_load_2d(b_dst, &tmB, &full[stage], kb * kBK, nb * 128);
+              tma_load_2d(b_dst + 16384, &tmB2, &full[stage], kb * kBK, nb * 128);
+            } else {
+              const int kbb = (A_MN && kb >= kb_pass) ? kb - kb_pass : kb;  // B rows repeat
+              const int seg = kbb / p.k_split;
+              const CUtensorMap* mp = (seg & 1) ? &tmB2 : &tmB;
+              const int kk = kbb - seg * p.k_split;
+              if (!B_MN) {
+                tma_load_2d(b_dst, mp, &full[stage], kk * kBK, nb * kBN);
+              } else {
 #pragma unroll
-              for (int i = 0; i < 4; ++i)
-                tma_load_2d(b_dst + i * 8192, mp, &full[stage], nb * kBN + 64 * i, kk * kBK);
+                for (int i = 0; i < 4; ++i)
+                  tma_load_2d(b_dst + i * 8192, mp, &full[stage], nb * kBN + 64 * i, kk * kBK);
+              }
             }
           }
-          if (++stage == kStages) {
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      if constexpr (PAIR) {
+        // rank 0's MMA warp signals this CTA's empty barriers from the other
+        // SM: wait for the release of the last STAGES fills, so no arrival
+        // is still on its way when the CTA leaves
+        for (int i = 0; i < STAGES && ok; ++i) {
+          if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag)) ok = false;
+          if (++stage == STAGES) {
             stage = 0;
             phase ^= 1u;
           }
@@ -689,13 +841,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     __syncwarp();
   } else if (warp == 1) {
     // ---------------------------------------------------------------- MMA issuer
-    if (lane == 0 && total > 0) {
-      constexpr uint32_t idesc = idesc_bf16(kBM, kBN, A_MN, B_MN);
+    if (lane == 0 && total > 0 && rank == 0) {
+      constexpr uint32_t idesc = idesc_bf16(TILE_M, kBN, A_MN, B_MN);
       int stage = 0;
       uint32_t phase = 0;
       int it = 0;
       bool ok = true;
-      for (int unit = blockIdx.x; unit < total && ok; unit += gridDim.x, ++it) {
+      for (int unit = group; unit < total && ok; unit += n_groups, ++it) {
         const int acc = it & 1;
         const uint32_t acc_phase = (uint32_t)(it >> 1) & 1u;
         if (!mbar_wait(&tempty[acc], acc_phase ^ 1u, abort_flag)) {
@@ -714,22 +866,33 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           }
           tc_fence_after();
           const uint32_t a0 = smem_u32(sA + stage * kABytes);
-          const uint32_t b0 = smem_u32(sB + stage * kBBytes);
+          const uint32_t b0 = smem_u32(sB + stage * B_BYTES);
 #pragma unroll
           for (int k = 0; k < kBK / 16; ++k) {
             const uint64_t ad = A_MN ? sdesc_sw128(a0 + k * 2048, 8192, 1024)
                                      : sdesc_sw128(a0 + k * 32, 16, 1024);
             const uint64_t bd = B_MN ? sdesc_sw128(b0 + k * 2048, 8192, 1024)
                                      : sdesc_sw128(b0 + k * 32, 16, 1024);
-            tc_mma_bf16(d_tmem, ad, bd, idesc, (kb != kb0 || k != 0) ? 1u : 0u);
+            if constexpr (PAIR)
+              tc_mma_bf16_pair(d_tmem, ad, bd, idesc, (kb != kb0 || k != 0) ? 1u : 0u);
+            else
+              tc_mma_bf16(d_tmem, ad, bd, idesc, (kb != kb0 || k != 0) ? 1u : 0u);
           }
-          tc_commit(&empty[stage]);
-          if (++stage == kStages) {
+          if constexpr (PAIR)
+            tc_commit_pair(&empty[stage], 0x3);
+          else
+            tc_commit(&empty[stage]);
+          if (++stage == STAGES) {
             stage = 0;
             phase ^= 1u;
           }
         }
-        if (ok) tc_commit(&tfull[acc]);
+        if (ok) {
+          if constexpr (PAIR)
+            tc_commit_pair(&tfull[acc], 0x3);
+          else
+            tc_commit(&tfull[acc]);
+        }
       }
       if (!ok) {
         set_status(p.status, TWELL_ERR_DEVICE_TIMEOUT);
@@ -744,8 +907,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     const int r_local = quarter * 32 + lane;
     Stager st{sOut + (warp - 4) * kStageBytes, lane, 0, false};
     const OutMaps om{&tmO0, &tmO1, &tmO2};
+    const uint32_t tempty0 = PAIR ? cluster_addr(&tempty[0], 0) : 0u;
     int it = 0;
-    for (int unit = blockIdx.x; unit < total; unit += gridDim.x, ++it) {
+    for (int unit = group; unit < total; unit += n_groups, ++it) {
       int mb, nb, tile, ks;
       unit_coords(unit, tiles, cluster_k, tile, ks);
       tile_coords(tile, m_tiles, p.n_tiles, mb, nb);
@@ -758,7 +922,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         break;
       }
       tc_fence_after();
-      const int row = mb * kBM + r_local;
+      const int m_row0 = mb * TILE_M + rank * kBM;  // this CTA's first output row of the tile
+      const int row = m_row0 + r_local;
       const bool row_ok = p.pad_rows ? (row < p.M) : (row < M_eff);
       const uint32_t tacc = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * kBN);
       const int n0 = (EPI == EPI_GATED) ? nb * 128 : nb * kBN;
@@ -780,9 +945,14 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         continue;
       }
       Epilogue<EPI>::run(p, tacc, row, row_ok, n0, p.N, half, st, om,
-                         row_off + mb * kBM + quarter * 32);
+                         row_off + m_row0 + quarter * 32);
       tc_fence_before();
-      mbar_arrive(&tempty[acc]);
+      if constexpr (PAIR) {
+        __syncwarp();
+        if (lane == 0) mbar_arrive_cluster(tempty0 + 8u * (uint32_t)acc);
+      } else {
+        mbar_arrive(&tempty[acc]);
+      }
     }
     st.drain();  // staged stores finish reading shared memory before the CTA exits
   }
@@ -848,9 +1018,19 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   }
 
   __syncthreads();
-  if (warp == 2) {
-    tc_fence_after();
-    tmem_dealloc(tmem_base, kTmemCols);
+  if constexpr (PAIR) {
+    // neither rank leaves (or frees TMEM) while the other may still signal
+    // its barriers or have its shared memory read by the pair's MMAs
+    cluster_sync_all();
+    if (warp == 2) {
+      tc_fence_after();
+      tmem_dealloc_pair(tmem_base, kTmemCols);
+    }
+  } else {
+    if (warp == 2) {
+      tc_fence_after();
+      tmem_dealloc(tmem_base, kTmemCols);
+    }
   }
 }
 

@@ -44,6 +44,10 @@ double l2_bytes();
 // Rows wider than 1024 take the split gathers (true, the default) or the
 // fused kernels (twell_set_split_gathers).
 bool split_gathers();
+// Large GEMMs run as CTA pairs with 256 x 256 tiles (true, the default) or
+// as single CTAs with 128 x 256 tiles (twell_set_pair_gemm).
+bool pair_gemm();
+int current_device();
 // Passes over the neuron axis for a gather whose weight rows total
 // `gathered_bytes`: 1 while they fit in the fraction `fit` of L2, else
 // enough chunks of at most the fraction `chunk` of L2 each.

@@ -30,7 +30,8 @@ STATUS = {
 EXPORTS = (
     "twell_pack", "twell_pack_dense", "hybrid_route", "twell_workspace_bytes",
     "twell_workspace_bytes_capped",
-    "twell_tiles_workspace_bytes", "twell_set_split_gathers", "twell_ffn_fwd",
+    "twell_tiles_workspace_bytes", "twell_set_split_gathers", "twell_set_pair_gemm",
+    "twell_ffn_fwd",
     "twell_ffn_bwd", "twell_dense_workspace_bytes", "twell_dense_ffn_fwd", "twell_dense_ffn_bwd",
     "twell_dense_ffn_fwd_act", "twell_dense_ffn_bwd_act",
     "twell_gemm_bf16", "twell_get_device_status", "twell_status_string", "twell_num_sms",
@@ -88,6 +89,7 @@ def load():
         "twell_workspace_bytes_capped": (SZ, [SP, I32, I32, I32]),
         "twell_tiles_workspace_bytes": (SZ, [SP]),
         "twell_set_split_gathers": (I32, [I32]),
+        "twell_set_pair_gemm": (I32, [I32]),
         "twell_ffn_fwd": (I32, [P, P, P, P, SP, TP, HP, P, P, SZ, P]),
         "twell_ffn_bwd": (I32, [P, P, P, P, P, SP, HP, F, P, P, P, P, P, SZ, P]),
         "twell_ffn_fwd_noalloc": (I32, [P, P, P, P, SP, HP, P, P]),
@@ -250,6 +252,12 @@ def twell_set_split_gathers(enable: bool) -> bool:
     """Split (True, the default) or fused (False) gathers for rows wider than
     1024; returns the previous setting."""
     return bool(load().twell_set_split_gathers(int(bool(enable))))
+
+
+def twell_set_pair_gemm(enable: bool) -> bool:
+    """CTA-pair 256 x 256 GEMM tiles (True, the default) or single-CTA
+    128 x 256 tiles (False); returns the previous setting."""
+    return bool(load().twell_set_pair_gemm(int(bool(enable))))
 
 
 def twell_ffn_fwd(x, wgT, wuT, wd, shape: Shape, y, tiles: Optional[TwellTiles] = None,

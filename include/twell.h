@@ -179,6 +179,16 @@ size_t twell_tiles_workspace_bytes(const twell_shape* shape);
  * synchronised with work in flight: change it between calls. */
 int32_t twell_set_split_gathers(int32_t enable);
 
+/* Choice of the tensor-core GEMM form, process-wide; returns the previous
+ * setting.  enable = 1 (the default): GEMMs without a K split run as 2-CTA
+ * clusters (tcgen05 cta_group::2) on 256 x 256 output tiles, each CTA
+ * staging half of the tile's A rows and half of its B rows, unless that
+ * would take more waves of tiles than the single-CTA form.  enable = 0:
+ * every GEMM runs one CTA per 128 x 256 tile.  The products and the fp32
+ * accumulation order over K are the same in both forms.  Not synchronised
+ * with work in flight: change it between calls. */
+int32_t twell_set_pair_gemm(int32_t enable);
+
 /* Fused sparse up + down projection.  Source: page 2, "¿Qué hace distinto a
  * TwELL frente a ELL clásico?" (one kernel reads the packed activations and
  * does both projections; the intermediate never reaches global memory) and,

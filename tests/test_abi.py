@@ -85,6 +85,12 @@ def test_host_validation_before_launch(lib):
                                        16, 16, 8, None) == 7
 
 
+def test_pair_gemm_switch(lib):
+    assert twell.twell_set_pair_gemm(False) is True   # the default is on
+    assert twell.twell_set_pair_gemm(True) is False
+    assert twell.twell_set_pair_gemm(True) is True
+
+
 def test_split_gathers_switch(lib):
     assert twell.twell_set_split_gathers(False) is True   # the default is on
     assert twell.twell_set_split_gathers(True) is False

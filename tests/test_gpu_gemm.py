@@ -1,5 +1,7 @@
 """tcgen05 GEMM engine through the C ABI (twell_gemm_bf16): all four operand
-majorness combinations, ragged tails, bf16 / fp32 outputs and accumulation.
+majorness combinations, ragged tails, bf16 / fp32 outputs and accumulation,
+each in both GEMM forms (CTA-pair 256 x 256 tiles and single-CTA 128 x 256
+tiles, twell_set_pair_gemm).
 
 Integer-valued operands make every product and partial sum exact in fp32, so
 those cases must match bit for bit; random operands are checked against a
@@ -13,6 +15,14 @@ from activation_sparse_gated_tcgen05_gb300 import twell
 from helpers import assert_close
 
 pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(params=[True, False], ids=["pair", "single"], autouse=True)
+def gemm_form(request):
+    """Every case runs with CTA-pair tiles (the default) and single-CTA tiles."""
+    prev = twell.twell_set_pair_gemm(request.param)
+    yield request.param
+    twell.twell_set_pair_gemm(prev)
 
 
 def _operands(M, N, K, a_mn, b_mn, integer, seed):
@@ -69,3 +79,20 @@ def test_gemm_many_tiles_persistent_wraparound():
     assert twell.twell_get_device_status() == 0
     ref = (A.cuda() @ B.cuda().t()).cpu().numpy()  # exact integers in fp64
     np.testing.assert_array_equal(C.cpu().numpy().astype(np.float64), ref)
+
+
+def test_pair_and_single_forms_agree_bit_for_bit():
+    # random bf16 operands: both forms accumulate the same products over K in
+    # the same order, so their fp32 outputs are identical
+    M, N, K = 2048, 1536, 1024
+    _, _, a, b = _operands(M, N, K, 0, 1, False, 4)
+    out = {}
+    for pair in (True, False):
+        prev = twell.twell_set_pair_gemm(pair)
+        C = torch.empty(M, N, dtype=torch.float32, device="cuda")
+        twell.twell_gemm_bf16(a, b, C, M, N, K, 0, 1)
+        torch.cuda.synchronize()
+        twell.twell_set_pair_gemm(prev)
+        out[pair] = C
+    assert twell.twell_get_device_status() == 0
+    assert torch.equal(out[True].view(torch.int32), out[False].view(torch.int32))
