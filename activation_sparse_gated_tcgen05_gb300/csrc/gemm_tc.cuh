@@ -509,8 +509,25 @@ struct Epilogue<EPI_GATED> {
 
 // acc = dh = dY Wd^T for 256 neurons.  du = dh * g, da = (dh * u + lambda) if
 // g > 0 else 0 (SiLU: see below); both stored bf16 into dd = [du | da].
+TW_DEV void prefetch_l2(const void* p) {
+  asm volatile("prefetch.global.L2 [%0];" ::"l"(reinterpret_cast<uint64_t>(p)));
+}
+
 template <>
 struct Epilogue<EPI_BWD_GATE> {
+  // Issued before the tile's accumulator is ready: pulls this thread's g and
+  // u (its row, its 128 columns: two 128-byte lines each) into L2, so the
+  // epilogue's loads do not wait on DRAM.
+  static __device__ __forceinline__ void prefetch(const GemmParams& p, int row, int n0, int half,
+                                                  int N) {
+    const int c = n0 + half * (kBN / 2);
+    if (row >= p.M || c >= N) return;
+    const long long gu = (long long)row * p.ldgu + c;
+    prefetch_l2(p.g_in + gu);
+    prefetch_l2(p.g_in + gu + 64);
+    prefetch_l2(p.u_in + gu);
+    prefetch_l2(p.u_in + gu + 64);
+  }
   static __device__ __forceinline__ void run(const GemmParams& p, uint32_t tacc, int row,
                                              bool row_ok, int n0, int N, int half, Stager& st,
                                              const OutMaps& om, int row0) {
@@ -571,6 +588,17 @@ struct Epilogue<EPI_BWD_GATE> {
 // epilogue stays lean): g bf16, u fp32, and dd = [du | da | du lo | da lo].
 template <>
 struct Epilogue<EPI_BWD_GATE_RT> {
+  // as for EPI_BWD_GATE; u is fp32 here (four lines)
+  static __device__ __forceinline__ void prefetch(const GemmParams& p, int row, int n0, int half,
+                                                  int N) {
+    const int c = n0 + half * (kBN / 2);
+    if (row >= p.M || c >= N) return;
+    const long long gu = (long long)row * p.ldgu + c;
+    prefetch_l2(p.g_in + gu);
+    prefetch_l2(p.g_in + gu + 64);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) prefetch_l2(p.u_f32_in + gu + 32 * i);
+  }
   // du, da from dh and the saved g, u (ReLU: da = dh u + lambda on live
   // entries; SiLU: g holds a, du = dh silu(a), da = dh u silu'(a))
   static __device__ __forceinline__ void grads(const GemmParams& p, float dh, float g, float u,
@@ -916,17 +944,19 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       const int row_off = cluster_k > 1 ? 0 : ks * m_tiles * kBM;  // split-K partial rows
       const int acc = it & 1;
       const uint32_t acc_phase = (uint32_t)(it >> 1) & 1u;
+      const int m_row0 = mb * TILE_M + rank * kBM;  // this CTA's first output row of the tile
+      const int row = m_row0 + r_local;
+      const int n0 = (EPI == EPI_GATED) ? nb * 128 : nb * kBN;
+      if constexpr (EPI == EPI_BWD_GATE || EPI == EPI_BWD_GATE_RT)
+        Epilogue<EPI>::prefetch(p, row, n0, half, p.N);
       if (!mbar_wait(&tfull[acc], acc_phase, abort_flag)) {
         set_status(p.status, TWELL_ERR_DEVICE_TIMEOUT);
         *abort_flag = 1;
         break;
       }
       tc_fence_after();
-      const int m_row0 = mb * TILE_M + rank * kBM;  // this CTA's first output row of the tile
-      const int row = m_row0 + r_local;
       const bool row_ok = p.pad_rows ? (row < p.M) : (row < M_eff);
       const uint32_t tacc = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(acc * kBN);
-      const int n0 = (EPI == EPI_GATED) ? nb * 128 : nb * kBN;
       if (cluster_k > 1) {
         // one unit per block: split 0 packs after the cluster barrier below;
         // the other splits stage their accumulator [column][row] in the
