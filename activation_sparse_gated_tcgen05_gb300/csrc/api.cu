@@ -232,8 +232,7 @@ SparseWs carve_sparse(void* ws, const twell_shape& s, int W, int dense_cap, int 
     w.gr = c.take<uint16_t>(Mr * f);
     w.ur = c.take<float>(Mr * f);
     w.ddr = c.take<uint16_t>(Mr * 4 * f);
-    const long long NG = (NB + 31) / 32;
-    w.mask_off = c.take<int>((2 * NB + (NG > 0 ? NG : 1)) * f);
+    w.mask_off = c.take<int>(32 + 2 * NB * f + f);  // counter, masks, offsets, totals
     w.csc_ptr = c.take<int>(f + 1);
     w.csc_row = c.take<int>(E > 0 ? E : 1);
     w.slot_pos = c.take<int>(E > 0 ? E : 1);

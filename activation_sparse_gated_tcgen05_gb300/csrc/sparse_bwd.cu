@@ -57,93 +57,97 @@ __global__ void __launch_bounds__(kWarps * 32)
   }
 }
 
-// Column scan of the row masks, in groups of 32 row blocks.  CTA (jb, g)
-// handles neurons [32 jb, 32 jb + 32) and row blocks [32 g, 32 g + 32):
-// off[b][j] = live rows of neuron j in the blocks of group g before b;
-// gtot[g][j] = live rows of neuron j in group g.
-constexpr int kScanG = 32;
+// Column scan of the row masks.  CTA c handles neurons [32 c, 32 c + 32)
+// over every row block, 32 blocks at a time (warp w: block 32 g + w; lane:
+// neuron), with a running count per neuron:
+//   off[b][j] = live rows of neuron j in the blocks before b
+//   tot[j]    = live rows of neuron j
+// The CTA that finishes last (a ticket on the zeroed counter `done`) forms
+// csc_ptr[0..f] = exclusive prefix of tot.
 __global__ void __launch_bounds__(1024)
-    csc_colscan_kernel(const unsigned* __restrict__ mask, int NB, int f, int* __restrict__ off,
-                       int* __restrict__ gtot) {
-  __shared__ int c[kScanG][33];
-  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;  // w: block in group, lane: neuron
+    csc_scan_kernel(const unsigned* __restrict__ mask, int NB, int f, int* __restrict__ off,
+                    int* __restrict__ tot, unsigned* __restrict__ done, int* __restrict__ csc_ptr) {
+  __shared__ int c[32][33];
+  __shared__ int carry[32];
+  __shared__ int warp_tot[32];
+  __shared__ int chunk_carry;
+  __shared__ bool last;
+  const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
   const int j = blockIdx.x * 32 + lane;
-  const int b = blockIdx.y * kScanG + w;
-  const bool ok = j < f && b < NB;
-  c[w][lane] = ok ? __popc(mask[(long long)b * f + j]) : 0;  // coalesced over neurons
-  __syncthreads();
-  {  // warp w scans neuron w of the block over the group's 32 row blocks (lane)
-    const int v = c[lane][w];
-    const int incl = warp_incl_scan(v);
-    c[lane][w] = incl - v;
-    const int jw = blockIdx.x * 32 + w;
-    if (lane == 31 && jw < f) gtot[(long long)blockIdx.y * f + jw] = incl;
+  const int NG = (NB + 31) / 32;
+  if (tid < 32) carry[tid] = 0;
+  for (int g0 = 0; g0 < NG; g0 += 8) {
+    // eight groups' mask words in flight before the first is scanned
+    int v[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      const int b = (g0 + k) * 32 + w;
+      v[k] = (j < f && b < NB) ? __popc(mask[(long long)b * f + j]) : 0;  // coalesced over j
+    }
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      if (g0 + k >= NG) break;  // uniform over the CTA
+      __syncthreads();          // the previous group's reads of c (and carry's init) are done
+      c[w][lane] = v[k];
+      __syncthreads();
+      {  // warp w scans neuron 32 c + w over the group's blocks (lane)
+        const int x = c[lane][w];
+        const int incl = warp_incl_scan(x);
+        c[lane][w] = carry[w] + incl - x;
+        __syncwarp();
+        if (lane == 31) carry[w] += incl;
+      }
+      __syncthreads();
+      const int b = (g0 + k) * 32 + w;
+      if (j < f && b < NB) off[(long long)b * f + j] = c[w][lane];
+    }
   }
   __syncthreads();
-  if (ok) off[(long long)b * f + j] = c[w][lane];
-}
-
-// Per neuron: exclusive prefix over the groups (gpre[g][j], written over
-// gtot) and the neuron's total; then csc_ptr[0..f] = exclusive prefix of the
-// totals (one block).
-__global__ void __launch_bounds__(1024)
-    csc_ptr_kernel(int* __restrict__ gtot, int NG, int f, int* __restrict__ csc_ptr) {
-  __shared__ int warp_tot[32];
-  __shared__ int carry;
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  if (tid == 0) carry = 0;
+  if (tid < 32 && blockIdx.x * 32 + tid < f) tot[blockIdx.x * 32 + tid] = carry[tid];
+  __threadfence();
+  __syncthreads();
+  if (tid == 0) last = atomicAdd(done, 1u) == gridDim.x - 1;
+  __syncthreads();
+  if (!last) return;
+  __threadfence();
+  if (tid == 0) chunk_carry = 0;
   __syncthreads();
   for (int base = 0; base < f; base += 1024) {
-    const int j = base + tid;
-    int c = 0;
-    if (j < f) {
-      // eight group totals are loaded before any is overwritten, so the
-      // loads overlap instead of alternating with the stores
-      for (int g0 = 0; g0 < NG; g0 += 8) {
-        int v[8];
-#pragma unroll
-        for (int k = 0; k < 8; ++k) v[k] = g0 + k < NG ? gtot[(long long)(g0 + k) * f + j] : 0;
-#pragma unroll
-        for (int k = 0; k < 8; ++k) {
-          if (g0 + k < NG) gtot[(long long)(g0 + k) * f + j] = c;
-          c += v[k];
-        }
-      }
-    }
-    const int incl = warp_incl_scan(c);
-    if (lane == 31) warp_tot[warp] = incl;
+    const int jj = base + tid;
+    const int t = jj < f ? __ldcg(tot + jj) : 0;  // other CTAs' totals: from L2
+    const int incl = warp_incl_scan(t);
+    if (lane == 31) warp_tot[w] = incl;
     __syncthreads();
-    if (warp == 0) {
-      const int v = warp_tot[lane];
-      warp_tot[lane] = warp_incl_scan(v) - v;
+    if (w == 0) {
+      const int x = warp_tot[lane];
+      warp_tot[lane] = warp_incl_scan(x) - x;
     }
     __syncthreads();
-    const int ex = carry + warp_tot[warp] + incl - c;
-    if (j < f) csc_ptr[j] = ex;
+    const int ex = chunk_carry + warp_tot[w] + incl - t;
+    if (jj < f) csc_ptr[jj] = ex;
     __syncthreads();
-    if (tid == 1023) carry = ex + c;
+    if (tid == 1023) chunk_carry = ex + t;
     __syncthreads();
   }
-  if (tid == 0) csc_ptr[f] = carry;
+  if (tid == 0) csc_ptr[f] = chunk_carry;
 }
 
 __global__ void __launch_bounds__(kWarps * 32)
     csc_place_kernel(const uint16_t* __restrict__ ell_col, const int* __restrict__ ell_nnz, int M,
                      int W, int f, const unsigned* __restrict__ mask, const int* __restrict__ off,
-                     const int* __restrict__ gpre, const int* __restrict__ csc_ptr,
-                     int* __restrict__ csc_row, int* __restrict__ slot_pos) {
+                     const int* __restrict__ csc_ptr, int* __restrict__ csc_row,
+                     int* __restrict__ slot_pos) {
   const int lane = threadIdx.x & 31;
   const int m = blockIdx.x * kWarps + (threadIdx.x >> 5);
   if (m >= M) return;
   int n = ell_nnz[m];
   TW_CHECK_INDEX(n, n >= 0 && n <= W);
   const long long blk = (long long)(m >> 5) * f;
-  const long long grp = (long long)((m >> 5) / kScanG) * f;
   const unsigned below = (1u << (m & 31)) - 1u;
   for (int s = lane; s < n; s += 32) {
     int j = ell_col[(long long)m * W + s];
     TW_CHECK_INDEX(j, j < f);
-    const int pos = csc_ptr[j] + gpre[grp + j] + off[blk + j] + __popc(mask[blk + j] & below);
+    const int pos = csc_ptr[j] + off[blk + j] + __popc(mask[blk + j] & below);
     csc_row[pos] = m;
     slot_pos[(long long)m * W + s] = pos;
   }
@@ -496,54 +500,43 @@ cudaError_t neurons_team(const void* x, const void* dy, int M, int d, int f, con
 
 }  // namespace
 
-// blk_counts holds the row masks and block offsets ([ceil(M/32)][f] ints each)
-// followed by the group totals / prefixes ([ceil(M/1024)][f] ints).
+// blk_counts holds the scan's finish counter (32 ints), the row masks and
+// the block offsets ([ceil(M/32)][f] ints each) and the neuron totals (f).
 cudaError_t launch_csc_build(const twell_hybrid& r, int M, int f, int* blk_counts, int* csc_ptr,
                              int* csc_row, int* slot_pos, cudaStream_t s) {
   const int NB = (M + 31) / 32;
-  const int NG = (NB + kScanG - 1) / kScanG;
-  unsigned* mask = reinterpret_cast<unsigned*>(blk_counts);
+  unsigned* done = reinterpret_cast<unsigned*>(blk_counts);
+  unsigned* mask = done + 32;
   {
     const cudaError_t ce = checked_setup();
     if (ce != cudaSuccess) return ce;
   }
-  int* off = blk_counts + (long long)NB * f;
-  int* gtot = off + (long long)NB * f;
-  cudaError_t e = cudaMemsetAsync(mask, 0, sizeof(unsigned) * (size_t)NB * f, s);
+  int* off = blk_counts + 32 + (long long)NB * f;
+  int* tot = off + (long long)NB * f;
+  // the counter and the masks start at zero
+  cudaError_t e = cudaMemsetAsync(done, 0, sizeof(unsigned) * (32 + (size_t)NB * f), s);
   if (e != cudaSuccess) return e;
-  if (M > 0) {
-    {
-      ProfScope prof("csc_mark", s);
-      csc_mark_kernel<<<(M + kWarps - 1) / kWarps, kWarps * 32, 0, s>>>(r.ell_col, r.ell_nnz, M,
-                                                                        r.ell_width, f, mask);
-    }
-    count_launch();
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    {
-      ProfScope prof("csc_colscan", s);
-      csc_colscan_kernel<<<dim3((f + 31) / 32, NG), 1024, 0, s>>>(mask, NB, f, off, gtot);
-    }
-    count_launch();
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  } else {
-    if ((e = cudaMemsetAsync(gtot, 0, sizeof(int) * (size_t)f, s)) != cudaSuccess) return e;
-  }
+  if (M == 0) return cudaMemsetAsync(csc_ptr, 0, sizeof(int) * ((size_t)f + 1), s);
   {
-    ProfScope prof("csc_ptr", s);
-    csc_ptr_kernel<<<1, 1024, 0, s>>>(gtot, M > 0 ? NG : 1, f, csc_ptr);
+    ProfScope prof("csc_mark", s);
+    csc_mark_kernel<<<(M + kWarps - 1) / kWarps, kWarps * 32, 0, s>>>(r.ell_col, r.ell_nnz, M,
+                                                                      r.ell_width, f, mask);
   }
   count_launch();
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  if (M > 0) {
-    {
-      ProfScope prof("csc_place", s);
-      csc_place_kernel<<<(M + kWarps - 1) / kWarps, kWarps * 32, 0, s>>>(
-          r.ell_col, r.ell_nnz, M, r.ell_width, f, mask, off, gtot, csc_ptr, csc_row, slot_pos);
-    }
-    count_launch();
-    e = cudaGetLastError();
+  {
+    ProfScope prof("csc_scan", s);
+    csc_scan_kernel<<<(f + 31) / 32, 1024, 0, s>>>(mask, NB, f, off, tot, done, csc_ptr);
   }
-  return e;
+  count_launch();
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  {
+    ProfScope prof("csc_place", s);
+    csc_place_kernel<<<(M + kWarps - 1) / kWarps, kWarps * 32, 0, s>>>(
+        r.ell_col, r.ell_nnz, M, r.ell_width, f, mask, off, csc_ptr, csc_row, slot_pos);
+  }
+  count_launch();
+  return cudaGetLastError();
 }
 
 namespace {

@@ -342,7 +342,7 @@ uint64_t twell_launch_count(void);
  * Families: gemm_gate_pack (also the small-batch gate), gemm_gated,
  * gemm_dgate, gemm_store_kk/mk/km/mm, pack_dense, route_rows, route_list,
  * gather_rows, splitk_scatter, sparse_fwd, sparse_fwd_up, sparse_fwd_down,
- * csc_mark, csc_colscan, csc_ptr, csc_place, bwd_rows, bwd_dh, bwd_grad_dx,
+ * csc_mark, csc_scan, csc_place, bwd_rows, bwd_dh, bwd_grad_dx,
  * bwd_neurons, bwd_neurons_dy, bwd_neurons_x.  Host-side state,
  * process-wide; not for use while another thread launches. */
 twell_status twell_profile_begin(const char* kernel);
