@@ -155,6 +155,50 @@ def test_backward_is_deterministic():
         assert torch.equal(u, v)
 
 
+def _bits(t):
+    """The tensor's bytes as integers, so equality is bitwise (NaN included)."""
+    t = t.contiguous()
+    if t.element_size() == 1:
+        return t
+    return t.view(torch.int16 if t.element_size() == 2 else torch.int32)
+
+
+@pytest.mark.parametrize("M,d,f", [(700, 512, 2048), (1000, 2048, 1024)])
+def test_pair_and_single_gemm_forms_agree(M, d, f):
+    """The CTA-pair GEMM form (the default) and the single-CTA form
+    (twell_set_pair_gemm(0)) give the same bytes through every epilogue: the
+    pack of the gate GEMM, the routed rows' gated / backward-gate / store
+    GEMMs, and the dense comparator's forward and backward; each run is also
+    checked against the oracle."""
+    r = Run(M, d, f, 128, 32, density=0.02, seed=7, exact=True, mixed=True)
+    out = {}
+    for pair in (True, False):
+        prev = twell.twell_set_pair_gemm(pair)
+        try:
+            t = r.pack()
+            W = _quantile_width(t, r.shape, 0.7)
+            h = r.route(t, W)
+            y = r.fwd(route=h, W=W)
+            dx, dws = r.bwd(h, W)
+            ws = torch.empty(twell.twell_dense_workspace_bytes(r.shape, True),
+                             dtype=torch.uint8, device="cuda")
+            yd = torch.empty(r.M, r.d, dtype=torch.bfloat16, device="cuda")
+            twell.twell_dense_ffn_fwd(r.x, r.wg, r.wu, r.wd, r.shape, yd, True, ws)
+            dxd = torch.empty_like(yd)
+            dwsd = [torch.empty(r.f, r.d, device="cuda") for _ in range(3)]
+            twell.twell_dense_ffn_bwd(r.x, r.wg, r.wu, r.wd, r.dy, r.shape, LAM, dxd, *dwsd, ws)
+            torch.cuda.synchronize()
+            assert twell.twell_get_device_status() == 0
+        finally:
+            twell.twell_set_pair_gemm(prev)
+        n_dense = int(h.n_dense[0].item())
+        assert n_dense > 0  # the routed rows' GEMMs ran
+        out[pair] = [twell.tiles_view(t, r.shape)[2], y, dx, *dws, yd, dxd, *dwsd]
+        _check_step(r, y, dx, *dws, allow=False)
+    for a, b in zip(out[True], out[False]):
+        assert torch.equal(_bits(a), _bits(b))
+
+
 @pytest.mark.parametrize("M", [300, 1])
 def test_dense_comparator_matches_oracle(M):
     r = Run(M, 256, 1024, 64, 16, density=0.05, seed=3, exact=True)
