@@ -11,7 +11,9 @@
 //               owns one accumulator row and half of its 256 columns
 // Two 256-column accumulators let the epilogue of tile i overlap the
 // mainloop of tile i+1.  Tiles are visited in a grouped raster so CTAs that
-// run together share A rows and B columns in L2.
+// run together share A rows and B columns in L2.  The CTA-pair form of the
+// same kernel (PAIR, see "kernel" below) runs 2-CTA clusters on 256 x 256
+// tiles with tcgen05.mma.cta_group::2.
 //
 // Operands: A (M x K) and B (N x K), each K-major ([rows][K], K contiguous) or
 // MN-major ([K][rows]).  Epilogues:
@@ -28,8 +30,8 @@
 namespace tw {
 
 // ---- CTA-pair forms (cta_group::2).  A kernel uses either these or the
-// single-CTA forms above for alloc / dealloc / relinquish / mma / commit,
-// never both.  The pair is the two CTAs of a 2-CTA cluster: rank 0 issues the
+// single-CTA forms of common.cuh for alloc / dealloc / relinquish / mma /
+// commit, never both.  The pair is the two CTAs of a 2-CTA cluster: rank 0 issues the
 // MMAs, which read A and B from both CTAs' shared memory (same offsets) and
 // write each CTA's own accumulator rows into that CTA's TMEM.
 
