@@ -162,6 +162,21 @@ def test_dense_fwd_bwd_match_torch_autograd(density):
         assert (a > 0).all()
 
 
+def test_gate_preact_matches_fp64_matmul_and_a_hand_case():
+    # the gate pre-activation a = x Wg (Wg stored neuron-major as Wg^T) on
+    # its own: a 2 x 3 case worked by hand, then random inputs against
+    # torch's fp64 matmul (a library routine the C++ oracle does not use)
+    x = np.array([[1.0, 2.0, -1.0], [0.5, 0.0, 4.0]])
+    wgT = np.array([[1.0, 0.0, 0.0], [2.0, -1.0, 3.0], [0.0, 0.25, 0.5], [-1.0, -1.0, -1.0]])
+    want = np.array([[1.0, -3.0, 0.0, -2.0], [0.5, 13.0, 2.0, -4.5]])
+    np.testing.assert_array_equal(oracle.gate_preact(x, wgT), want)
+    rng = np.random.default_rng(21)
+    x = rng.standard_normal((37, 48))
+    wgT = rng.standard_normal((70, 48))
+    ref = (torch.from_numpy(x) @ torch.from_numpy(wgT).t()).numpy()
+    np.testing.assert_allclose(oracle.gate_preact(x, wgT), ref, rtol=1e-13, atol=1e-13)
+
+
 def test_all_dead_gate_gives_exact_zeros():
     rng = np.random.default_rng(3)
     M, d, f = 8, 16, 32
